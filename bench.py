@@ -1,0 +1,445 @@
+#!/usr/bin/env python3
+"""Benchmark of the SmoothQuant W8A8 INT8 linear block on one GB300.
+
+One step = one forward pass of a workload's linear blocks: for every linear
+layer, smoothing + dynamic per-token quantisation of its activations
+(sq_quantize_act) and the INT8 GEMM with its fused dequantising epilogue
+(sq_linear_i8).  Weights are packed once (offline, as the method prescribes)
+before the timed region.  Default workload: BERT-large, 24 layers x
+{QKV, attention out-proj, FFN up + GELU, FFN down + residual} at batch 32 x
+sequence 256 (M = 8192).  Inputs are seeded synthetic data resident in HBM;
+every GEMM reads its own activations (5.4 GB per step, far above the 129 MB
+L2), so no step re-reads another's data from L2.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle
+instead, on a bounded row sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from smoothquant_w8a8_int8_gb300 import roofline as R  # noqa: E402
+from smoothquant_w8a8_int8_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "INT8 linear-block TOPS on BERT GEMM shapes; % of GB300 INT8 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            out = {}
+            for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                v = d.get(k)
+                if isinstance(v, dict):
+                    v = v.get("value")
+                if v is not None:
+                    out[k] = float(v)
+            if "hbm_gbs" in out and "bf16_tflops" in out:
+                out.setdefault("bf16_tflops_sustained", out["bf16_tflops"])
+                return out, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"sq_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------- our arm
+
+class Layer:
+    __slots__ = ("lin", "X", "s", "Wop", "Wq", "sw", "bias", "residual", "Y", "Xhost", "Yhost")
+
+
+def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool):
+    from smoothquant_w8a8_int8_gb300 import binding as sq
+    dev = torch.device("cuda")
+    layers = []
+    maxMK = max(w.M * lin.K for lin in w.linears)
+    Xop_buf = torch.empty(maxMK, dtype=torch.bfloat16, device=dev)
+    Xq_buf = torch.empty(maxMK, dtype=torch.int8, device=dev)
+    sx_buf = torch.empty(w.M, dtype=torch.float32, device=dev)
+    for layer, idx in [(l, i) for l in range(w.layers) for i in range(len(w.linears))]:
+        lin = w.linears[idx]
+        seed = wl.gemm_seed(w, layer, idx) + 7 * rank
+        c = wl.make_case(w.M, lin.K, lin.N, lin.mode, seed, w.outlier_frac, w.outlier_scale,
+                         lin.gelu_input, w.alpha, device=dev)
+        L = Layer()
+        L.lin = lin
+        L.X = c.X
+        # smoothing factor from this batch's own statistics (calibration = the input)
+        s = sq.smooth_factor(sq.channel_absmax(c.X), sq.channel_absmax(c.W), w.alpha)
+        L.s = s
+        Wq, sw, Wop = sq.pack_weight(c.W, s, want_q=(gemm == "mma_sync"), want_op=(gemm == "tc"))
+        L.Wq, L.sw, L.Wop = Wq, sw, Wop
+        L.bias, L.residual = c.bias, c.residual
+        L.Y = torch.empty(w.M, lin.N, dtype=torch.float32, device=dev)
+        L.Xhost = L.Yhost = None
+        if want_host:
+            L.Xhost = torch.empty(c.X.shape, dtype=torch.float32, pin_memory=True)
+            L.Xhost.copy_(c.X)
+            L.Yhost = torch.empty(L.Y.shape, dtype=torch.float32, pin_memory=True)
+        del c.W
+        layers.append(L)
+    torch.cuda.synchronize()
+    return layers, (Xq_buf, sx_buf, Xop_buf)
+
+
+def run_layer(sq, gemm, L, bufs, M, X=None, ev=None):
+    Xq_buf, sx_buf, Xop_buf = bufs
+    K, N = L.lin.K, L.lin.N
+    X = L.X if X is None else X
+    if gemm == "tc":
+        Xop = Xop_buf[: M * K].view(M, K)
+        if ev is not None:
+            ev[0].record()
+        sq.quantize_act(X, L.s, out=(None, sx_buf, Xop))
+        if ev is not None:
+            ev[1].record()
+        sq.linear_i8(Xop, sx_buf, L.Wop, L.sw, L.bias, L.residual, L.lin.mode, out=L.Y)
+        if ev is not None:
+            ev[2].record()
+    else:
+        Xq = Xq_buf[: M * K].view(M, K)
+        if ev is not None:
+            ev[0].record()
+        sq.quantize_act(X, L.s, out=(Xq, sx_buf, None))
+        if ev is not None:
+            ev[1].record()
+        sq.linear_i8_mma_sync(Xq, sx_buf, L.Wq, L.sw, L.bias, L.residual, L.lin.mode, out=L.Y)
+        if ev is not None:
+            ev[2].record()
+
+
+def bench_ours(args, w: wl.Workload, rank: int, world: int):
+    from smoothquant_w8a8_int8_gb300 import binding as sq
+    sq.load()
+    peaks, peak_src = load_peaks()
+    layers, bufs = setup_workload(w, args.gemm, rank, want_host=args.e2e_steps > 0)
+    M = w.M
+    n_gemm = len(layers)
+
+    def step(ev_list=None):
+        for i, L in enumerate(layers):
+            run_layer(sq, args.gemm, L, bufs, M, ev=None if ev_list is None else ev_list[i])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    rc = sq.device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status after warm-up: {sq.status_string(rc)}")
+
+    # per-launch events for every kernel in the timed region
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_gemm)]
+           for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for k in range(args.steps):
+        step(evs[k])
+    t1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clock_info = clocks.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    rc = sq.device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status after timed run: {sq.status_string(rc)}")
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    ops_per_step = w.ops()
+    ms_per_step = elapsed_ms / args.steps
+    tops = ops_per_step * world / (ms_per_step * 1e-3) / 1e12
+
+    # per-kernel durations from the live events
+    q_ms = g_ms = 0.0
+    for k in range(args.steps):
+        for i in range(n_gemm):
+            e = evs[k][i]
+            q_ms += e[0].elapsed_time(e[1])
+            g_ms += e[1].elapsed_time(e[2])
+    n_launch = args.steps * n_gemm
+    gemm_ops = args.steps * ops_per_step
+    gemm_tops = gemm_ops / (g_ms * 1e-3) / 1e12
+    peak_tensor = peaks["bf16_tflops_sustained"]
+    q_bytes = args.steps * sum(R.quantize_bytes(M, L.lin.K) for L in layers)
+    q_gbs = q_bytes / (q_ms * 1e-3) / 1e9
+    g_bytes = args.steps * sum(R.linear_bytes(M, L.lin.K, L.lin.N, L.lin.mode) for L in layers)
+
+    # e2e through the public API with host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        dev_X = torch.empty(max(M * L.lin.K for L in layers), dtype=torch.float32, device="cuda")
+        h2d = sum(L.Xhost.numel() * 4 for L in layers)
+        d2h = sum(L.Yhost.numel() * 4 for L in layers)
+
+        def e2e_step():
+            for L in layers:
+                X = dev_X[: M * L.lin.K].view(M, L.lin.K)
+                X.copy_(L.Xhost, non_blocking=True)
+                run_layer(sq, args.gemm, L, bufs, M, X=X)
+                L.Yhost.copy_(L.Y, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(b) / args.e2e_steps
+        if world > 1:
+            t = torch.tensor([e_ms], device="cuda")
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": round(ops_per_step * world / (e_ms * 1e-3) / 1e12, 3), "unit": "TOPS",
+               "ms_per_step": round(e_ms, 3), "steps": args.e2e_steps,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "path": "pinned host X -> device, quantise + GEMM via the C-ABI, Y -> pinned host"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, target_s=args.cpu_seconds)
+
+    gemm_kernel = ("tcgen05.mma kind::f16 (int8 codes as exact bf16, fp32 TMEM chunks of "
+                   "K<=1024 summed in int32)" if args.gemm == "tc"
+                   else "mma.sync m16n8k32 s8 (legacy warp MMA)")
+    result = {
+        "metric": METRIC, "value": round(tops, 3), "unit": "TOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+        "data": "synthetic (seeded N(0,1) activations with outlier channels, N(0,0.02) weights)",
+        "config": {"workload": w.name, "description": w.description, "M": M,
+                   "layers": w.layers, "gemms_per_step": n_gemm,
+                   "ops_per_step": ops_per_step, "gemm_kernel": gemm_kernel,
+                   "l2": "inputs larger than L2: every GEMM reads its own activations "
+                         f"({sum(L.X.numel() * 4 for L in layers) / 1e9:.1f} GB per step)",
+                   "weights": "packed once before the timed region",
+                   "parallelism": f"replicas x{world} (rows shard, no collective)"},
+        "roofline": {"bound": "tensor", "kernel": "gemm+epilogue",
+                     "achieved": round(gemm_tops, 2), "peak": peak_tensor,
+                     "unit": "TFLOP/s", "frac": round(gemm_tops / peak_tensor, 4),
+                     "traffic": None,
+                     "peak_source": f"bf16 dense sustained, {peak_src}",
+                     "avg_launch_us": round(g_ms * 1e3 / n_launch, 2),
+                     "algorithmic_bytes_per_step": g_bytes // args.steps},
+        "quantiser_roofline": {"bound": "hbm", "achieved": round(q_gbs, 1),
+                               "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                               "frac": round(q_gbs / peaks["hbm_gbs"], 4),
+                               "peak_source": peak_src,
+                               "avg_launch_us": round(q_ms * 1e3 / n_launch, 2),
+                               "algorithmic_bytes_per_step": q_bytes // args.steps},
+        "kernel_ms_per_step": {"quantize": round(q_ms / args.steps, 4),
+                               "gemm": round(g_ms / args.steps, 4)},
+        "gpu_launches": 2 * n_gemm * args.steps,
+        "clocks": clock_info,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    return result
+
+
+# ------------------------------------------------------------ oracle timing
+
+def _oracle_sample(w: wl.Workload, rows: int):
+    """Inputs of one layer's linears with `rows` tokens, plus packed weights
+    and the smoothing factor (computed by the oracle, untimed)."""
+    import oracle
+    items = []
+    for idx, lin in enumerate(w.linears):
+        c = wl.workload_case(w, 0, idx, rows=rows)
+        X, W = c.X.numpy(), c.W.numpy()
+        s = oracle.smooth_factor(oracle.channel_absmax(X), oracle.channel_absmax(W), w.alpha)
+        wq, sw = oracle.quantize_rows(W, s, "weight")
+        items.append((X, s, wq, sw, None if c.bias is None else c.bias.numpy(),
+                      None if c.residual is None else c.residual.numpy(), lin.mode))
+    return items
+
+
+def _oracle_step(items):
+    import oracle
+    for X, s, wq, sw, b, r, mode in items:
+        oracle.linear_block(X, s, wq, sw, b, r, mode)
+
+
+def _sample_ops(w, rows):
+    return sum(2 * rows * lin.K * lin.N for lin in w.linears)
+
+
+def _calibrate_rows(w: wl.Workload, target_s: float):
+    rows = 16
+    items = _oracle_sample(w, rows)
+    t = time.perf_counter()
+    _oracle_step(items)
+    dt = max(time.perf_counter() - t, 1e-4)
+    return int(max(16, min(w.M, rows * target_s / dt)))
+
+
+def cpu_baseline(w: wl.Workload, target_s: float = 15.0):
+    """The oracle as it stands, on the host cores, on a bounded row sample of
+    one layer of the workload (quantise + integer GEMM + epilogue)."""
+    import oracle
+    rows = _calibrate_rows(w, target_s)
+    items = _oracle_sample(w, rows)
+    t = time.perf_counter()
+    _oracle_step(items)
+    dt = time.perf_counter() - t
+    ops = _sample_ops(w, rows)
+    return {"value": round(ops / dt / 1e12, 6), "unit": "TOPS", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"layer 0 of {w.name}: {len(w.linears)} linears x {rows} of {w.M} rows "
+                      f"({ops / 1e9:.1f} GOP), quantise + int64 GEMM + double epilogue"}
+
+
+def bench_reference(args, w: wl.Workload):
+    """The CPU oracle timed as the reference arm (each step a bounded sample)."""
+    import oracle
+    rows = _calibrate_rows(w, args.reference_step_seconds)
+    items = _oracle_sample(w, rows)
+    for _ in range(args.warmup):
+        _oracle_step(items)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(items)
+    dt = (time.perf_counter() - t) / args.steps
+    ops = _sample_ops(w, rows)
+    value = ops / dt / 1e12
+    cores = oracle.num_threads()
+    sample = (f"layer 0 of {w.name}: {len(w.linears)} linears x {rows} of {w.M} rows "
+              f"({ops / 1e9:.2f} GOP per step)")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TOPS",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int64 (exact integer sums), fp32 quantiser",
+            "data": "synthetic", "config": {"workload": w.name, "M": w.M, "layers": w.layers},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TOPS", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="bert_large_encoder_b32_s256",
+                    choices=list(wl.WORKLOADS))
+    ap.add_argument("--gemm", choices=["tc", "mma_sync"], default="tc")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--reference-step-seconds", type=float, default=2.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    w = wl.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(bench_reference(args, w)), flush=True)
+        return
+
+    if world > 1:
+        local = int(os.environ.get("LOCAL_RANK", rank))
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    res = bench_ours(args, w, rank, world)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

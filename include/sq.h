@@ -1,0 +1,160 @@
+/*
+ * sq.h -- C ABI of the SmoothQuant W8A8 INT8 linear block for NVIDIA GB300
+ * (sm_103a).
+ *
+ * The operation is the linear block of BERT-family encoder inference analysed
+ * in "Efficient INT8 Inference of Small NLP Models on Server CPUs with PyTorch
+ * Native Stack" (Xia, Cui, Cao): SmoothQuant smoothing, dynamic per-token
+ * activation quantisation (Table 10, "Smooth-Dynamic"), an int8 x int8 -> int32
+ * GEMM, and the GEMM's fused post-operations -- bias, activation, residual
+ * addition (Table 3 caption).  The smoothing factor follows SmoothQuant (cited
+ * in the pages' reference list), with the migration strength alpha that
+ * Table 15 sets per model; GELU is the erf form ("Gaussian Error Linear Units",
+ * same reference list).
+ *
+ * Conventions for every entry point:
+ *  - All array pointers are DEVICE pointers (cudaMalloc'd or equivalent), owned
+ *    by the caller, row-major and densely packed, and must be 16-byte aligned
+ *    unless stated otherwise.  The library allocates no device memory.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *    enqueued asynchronously; no entry point synchronises except
+ *    sq_device_status().
+ *  - Arguments are checked on the host before anything is enqueued; a non-OK
+ *    status means nothing was launched.  A failed launch returns SQ_ERR_CUDA.
+ *    No entry point aborts, traps or throws.
+ *  - Sizes are int64_t.  A zero row count (M or N = 0) is a valid empty call
+ *    and returns SQ_OK without launching.  K must be a positive multiple of 16.
+ *  - Inputs must be finite; results for NaN or Inf inputs are unspecified.
+ */
+#ifndef SQ_GB300_H
+#define SQ_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SQ_OK = 0,
+    SQ_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad mode/alpha      */
+    SQ_ERR_ALIGNMENT = 2,   /* K not a multiple of 16 or pointer not 16-B aligned */
+    SQ_ERR_UNSUPPORTED = 3, /* size beyond a documented limit, or no sm_103 GPU */
+    SQ_ERR_CUDA = 4,        /* a CUDA runtime/driver call or launch failed      */
+    SQ_ERR_TIMEOUT = 5      /* a kernel's bounded wait ran out (device status)  */
+} sq_status;
+
+/* Epilogue of sq_linear_i8 (the linear block's fused post-operations,
+ * Table 3 caption).  With d = acc[m][n] * x_scale[m] * w_scale[n]:
+ *   SQ_EPI_NONE          Y = d
+ *   SQ_EPI_BIAS          Y = d + bias[n]
+ *   SQ_EPI_BIAS_GELU     Y = GELU(d + bias[n]),  GELU(t) = 0.5 t (1 + erf(t/sqrt 2))
+ *   SQ_EPI_BIAS_RESIDUAL Y = d + bias[n] + residual[m][n]
+ *   SQ_EPI_RAW_I32       Y = acc (int32; the scales, bias and residual are unused)
+ * Y is fp32 [M][N] for the first four modes and int32 [M][N] for the last. */
+typedef enum {
+    SQ_EPI_NONE = 0,
+    SQ_EPI_BIAS = 1,
+    SQ_EPI_BIAS_GELU = 2,
+    SQ_EPI_BIAS_RESIDUAL = 3,
+    SQ_EPI_RAW_I32 = 4
+} sq_epilogue;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *sq_status_string(int status);
+
+/* ABI version of this library: (major << 16) | minor. */
+int sq_version(void);
+
+/* Bytes of a GEMM-operand buffer for a rows x K matrix of int8 codes.
+ * The operand format is the tensor-core operand of sq_linear_i8: each int8
+ * code stored as the bf16 number of the same integer value (exact: every
+ * integer in [-127, 127] is a bf16), row-major [rows][K], K contiguous.
+ * Returns 0 for negative sizes. */
+size_t sq_operand_bytes(int64_t rows, int64_t K);
+
+/* ---- Smoothing factor (SmoothQuant; alpha per model in Table 15) ---------- */
+
+/* Running channel maxima for the smoothing factor:
+ *   amax[j] = max(amax[j], max_i |A[i][j]|),   A fp32 [rows][cols].
+ * The caller initialises amax (zeros for a fresh statistic); calling it once
+ * per calibration batch accumulates the maximum over all batches.  Use it on
+ * activations X [tokens][K] for max|X_j| and on weights W [N][K] for max|W_j|.
+ * amax need only be 4-byte aligned.  cols > 0 required; rows = 0 is a no-op. */
+sq_status sq_channel_absmax(const float *A, int64_t rows, int64_t cols, float *amax,
+                            void *stream);
+
+/* Smoothing factor per input channel:
+ *   s[j] = x_amax[j]^alpha / w_amax[j]^(1 - alpha),
+ * computed in double and rounded once to fp32; s[j] = 1 where either maximum
+ * is 0.  0 <= alpha <= 1.  Pointers need only be 4-byte aligned. */
+sq_status sq_smooth_factor(const float *x_amax, const float *w_amax, int64_t K, float alpha,
+                           float *s, void *stream);
+
+/* ---- Weight packing (once per layer, offline) ----------------------------- */
+
+/* Folds the smoothing factor into the weights and quantises each output
+ * channel symmetrically (per-channel int8 weights):
+ *   W'[n][j]   = W[n][j] * s[j]                                  (fp32)
+ *   w_scale[n] = max_j |W'[n][j]| / 127   (IEEE fp32 division; 1 if the row is 0)
+ *   Wq[n][j]   = clamp(round_half_even(W'[n][j] / w_scale[n]), -127, 127)
+ * W fp32 [N][K] (nn.Linear layout), s fp32 [K].  Outputs: w_scale fp32 [N]
+ * (required, 4-byte aligned), Wq int8 [N][K] (may be NULL), Wop GEMM operand
+ * of sq_operand_bytes(N, K) bytes (may be NULL); at least one of Wq / Wop. */
+sq_status sq_pack_weight(const float *W, const float *s, int64_t N, int64_t K, int8_t *Wq,
+                         float *w_scale, void *Wop, void *stream);
+
+/* ---- Activation smoothing + dynamic per-token quantisation (Table 10) ----- */
+
+/* Per token (row) m of X fp32 [M][K]:
+ *   v[j]       = X[m][j] / s[j]                                  (IEEE fp32 division)
+ *   x_scale[m] = max_j |v[j]| / 127       (IEEE fp32 division; 1 if the row is 0)
+ *   Xq[m][j]   = clamp(round_half_even(v[j] / x_scale[m]), -127, 127)
+ * Outputs: x_scale fp32 [M] (required, 4-byte aligned), Xq int8 [M][K] (may be
+ * NULL), Xop GEMM operand of sq_operand_bytes(M, K) bytes (may be NULL); at
+ * least one of Xq / Xop.  Any K that is a positive multiple of 16 works; rows
+ * of up to 8192 elements are held in registers (one HBM read), longer rows
+ * are read twice. */
+sq_status sq_quantize_act(const float *X, const float *s, int64_t M, int64_t K, int8_t *Xq,
+                          float *x_scale, void *Xop, void *stream);
+
+/* ---- INT8 GEMM + fused dequantising epilogue ------------------------------ */
+
+/* acc[m][n] = sum_k Xq[m][k] * Wq[n][k], exact in int32, then the epilogue
+ * `mode` (sq_epilogue) writes Y.  Operands are GEMM-operand buffers written by
+ * sq_quantize_act (Xop, [M][K]) and sq_pack_weight (Wop, [N][K]).  Runs on the
+ * tcgen05 tensor cores: the integer codes are multiplied exactly as bf16 and
+ * summed exactly in fp32 over chunks of at most 1024 of K (every partial sum
+ * stays below 2^24), the chunks being added in int32.  x_scale fp32 [M],
+ * w_scale fp32 [N], bias fp32 [N] (modes 1-3), residual fp32 [M][N] (mode 3);
+ * Y fp32 or int32 [M][N].  Y must not overlap any input; residual may equal Y
+ * only if it is exactly the same buffer.  Requires K <= 133144 (so that
+ * |acc| < 2^31 for any codes) and a GB300-class (sm_103) device. */
+sq_status sq_linear_i8(const void *Xop, const float *x_scale, const void *Wop,
+                       const float *w_scale, const float *bias, const float *residual,
+                       int64_t M, int64_t N, int64_t K, int mode, void *Y, void *stream);
+
+/* The same GEMM + epilogue on the legacy warp-level integer MMA path
+ * (mma.sync m16n8k32 s8 x s8 -> s32), reading int8 codes directly:
+ * Xq int8 [M][K] and Wq int8 [N][K] from sq_quantize_act / sq_pack_weight.
+ * Exact by construction; kept as the comparison point for sq_linear_i8.
+ * K <= 133144 (|acc| < 2^31 for any codes). */
+sq_status sq_linear_i8_mma_sync(const int8_t *Xq, const float *x_scale, const int8_t *Wq,
+                                const float *w_scale, const float *bias, const float *residual,
+                                int64_t M, int64_t N, int64_t K, int mode, void *Y,
+                                void *stream);
+
+/* ---- Device status --------------------------------------------------------- */
+
+/* Synchronises `stream`, then reports and clears the library's device error
+ * word for the current device: SQ_ERR_TIMEOUT if a kernel's bounded
+ * pipeline wait ran out since the last call (that kernel's output is then
+ * incomplete), SQ_ERR_CUDA if the stream reported an error, else SQ_OK. */
+sq_status sq_device_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SQ_GB300_H */

@@ -58,14 +58,12 @@ enum { ORC_EPI_NONE = 0, ORC_EPI_BIAS = 1, ORC_EPI_BIAS_GELU = 2, ORC_EPI_BIAS_R
 int oracle_channel_absmax(const float *A, int64_t rows, int64_t cols, float *out)
 {
     if (rows < 0 || cols < 0) return ORC_ERR_ARG;
-    for (int64_t j = 0; j < cols; ++j) {
-        float m = 0.0f;
-        for (int64_t i = 0; i < rows; ++i) {
+    for (int64_t j = 0; j < cols; ++j) out[j] = 0.0f;
+    for (int64_t i = 0; i < rows; ++i)
+        for (int64_t j = 0; j < cols; ++j) {
             float a = fabsf(A[i * cols + j]);
-            if (a > m) m = a;
+            if (a > out[j]) out[j] = a;
         }
-        out[j] = m;
-    }
     return ORC_OK;
 }
 

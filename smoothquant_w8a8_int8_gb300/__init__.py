@@ -1,16 +1,25 @@
 """SmoothQuant W8A8 INT8 linear block for GB300 (sm_103a).
 
 The compute runs in the C-ABI library ``libsq_gb300.so`` (hand-written CUDA);
-this package is a thin ctypes binding with the same entry-point names, plus the
-seeded workload generator and the roofline arithmetic.  The library is loaded
-on first use; if it is missing, that call raises.
+``binding`` is a thin ctypes layer with the same entry-point names.
+``workloads`` draws the seeded synthetic inputs and ``roofline`` holds the
+metric arithmetic.  The library is loaded on first use; if it is missing,
+that call raises.
 """
+import importlib
+
 from . import roofline, workloads  # noqa: F401
+
+_SUBMODULES = ("binding", "build", "roofline", "workloads")
 
 
 def __getattr__(name):
-    # the ctypes binding loads the CUDA library; defer it to first use
-    from . import binding
-    if hasattr(binding, name):
+    if name in _SUBMODULES:
+        return importlib.import_module(f"{__name__}.{name}")
+    if name.startswith("_"):
+        raise AttributeError(name)
+    binding = importlib.import_module(f"{__name__}.binding")
+    try:
         return getattr(binding, name)
-    raise AttributeError(name)
+    except AttributeError:
+        raise AttributeError(name) from None

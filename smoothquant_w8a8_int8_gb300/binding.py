@@ -1,0 +1,194 @@
+"""ctypes binding of libsq_gb300.so: the C-ABI entry points under the same
+names, taking torch CUDA tensors.  Argument marshalling only -- every step
+runs in the library's CUDA kernels, on the caller's current torch stream.
+
+There is no fallback: if the library is missing or fails to load, the first
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsq_gb300.so")
+
+SQ_OK, SQ_ERR_INVALID_ARG, SQ_ERR_ALIGNMENT, SQ_ERR_UNSUPPORTED, SQ_ERR_CUDA, SQ_ERR_TIMEOUT = range(6)
+EPI_NONE, EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESIDUAL, EPI_RAW_I32 = range(5)
+
+EXPORTS = ("sq_status_string", "sq_version", "sq_operand_bytes", "sq_channel_absmax",
+           "sq_smooth_factor", "sq_pack_weight", "sq_quantize_act", "sq_linear_i8",
+           "sq_linear_i8_mma_sync", "sq_device_status")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SQError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load the library (once).  Raises OSError if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise OSError(f"{p} is missing: build it with "
+                              "`python -m smoothquant_w8a8_int8_gb300.build`")
+            lib = ctypes.CDLL(p)
+            vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+            sig = {
+                "sq_status_string": ([i32], ctypes.c_char_p),
+                "sq_version": ([], i32),
+                "sq_operand_bytes": ([i64, i64], ctypes.c_size_t),
+                "sq_channel_absmax": ([vp, i64, i64, vp, vp], i32),
+                "sq_smooth_factor": ([vp, vp, i64, f32, vp, vp], i32),
+                "sq_pack_weight": ([vp, vp, i64, i64, vp, vp, vp, vp], i32),
+                "sq_quantize_act": ([vp, vp, i64, i64, vp, vp, vp, vp], i32),
+                "sq_linear_i8": ([vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp], i32),
+                "sq_linear_i8_mma_sync": ([vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp], i32),
+                "sq_device_status": ([vp], i32),
+            }
+            for name, (args, res) in sig.items():
+                f = getattr(lib, name)
+                f.argtypes = args
+                f.restype = res
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().sq_status_string(int(status)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != SQ_OK:
+        raise SQError(rc, what)
+
+
+def _p(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str, shape=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def operand_bytes(rows: int, K: int) -> int:
+    return int(load().sq_operand_bytes(rows, K))
+
+
+def empty_operand(rows: int, K: int, device="cuda") -> torch.Tensor:
+    """A GEMM-operand buffer (int8 codes held as exact bf16 values)."""
+    return torch.empty(rows, K, dtype=torch.bfloat16, device=device)
+
+
+def channel_absmax(A: torch.Tensor, amax: Optional[torch.Tensor] = None, stream=None):
+    """amax[j] = max(amax[j], max_i |A[i, j]|); a fresh zero statistic if None."""
+    _need(A, torch.float32, "A")
+    rows, cols = A.shape
+    if amax is None:
+        amax = torch.zeros(cols, dtype=torch.float32, device=A.device)
+    _need(amax, torch.float32, "amax", (cols,))
+    _check(load().sq_channel_absmax(_p(A), rows, cols, _p(amax), _stream(stream)),
+           "sq_channel_absmax")
+    return amax
+
+
+def smooth_factor(x_amax: torch.Tensor, w_amax: torch.Tensor, alpha: float, stream=None):
+    _need(x_amax, torch.float32, "x_amax")
+    _need(w_amax, torch.float32, "w_amax", x_amax.shape)
+    s = torch.empty_like(x_amax)
+    _check(load().sq_smooth_factor(_p(x_amax), _p(w_amax), x_amax.numel(), float(alpha), _p(s),
+                                   _stream(stream)), "sq_smooth_factor")
+    return s
+
+
+def pack_weight(W: torch.Tensor, s: torch.Tensor, want_q: bool = True, want_op: bool = True,
+                stream=None):
+    """Returns (Wq int8 or None, w_scale fp32, Wop operand or None)."""
+    _need(W, torch.float32, "W")
+    N, K = W.shape
+    _need(s, torch.float32, "s", (K,))
+    Wq = torch.empty(N, K, dtype=torch.int8, device=W.device) if want_q else None
+    Wop = empty_operand(N, K, W.device) if want_op else None
+    sw = torch.empty(N, dtype=torch.float32, device=W.device)
+    _check(load().sq_pack_weight(_p(W), _p(s), N, K, _p(Wq), _p(sw), _p(Wop), _stream(stream)),
+           "sq_pack_weight")
+    return Wq, sw, Wop
+
+
+def quantize_act(X: torch.Tensor, s: torch.Tensor, want_q: bool = True, want_op: bool = True,
+                 out=None, stream=None):
+    """Returns (Xq int8 or None, x_scale fp32, Xop operand or None).  `out`
+    may give preallocated (Xq, x_scale, Xop) buffers."""
+    _need(X, torch.float32, "X")
+    M, K = X.shape
+    _need(s, torch.float32, "s", (K,))
+    if out is not None:
+        Xq, sx, Xop = out
+    else:
+        Xq = torch.empty(M, K, dtype=torch.int8, device=X.device) if want_q else None
+        Xop = empty_operand(M, K, X.device) if want_op else None
+        sx = torch.empty(M, dtype=torch.float32, device=X.device)
+    _check(load().sq_quantize_act(_p(X), _p(s), M, K, _p(Xq), _p(sx), _p(Xop), _stream(stream)),
+           "sq_quantize_act")
+    return Xq, sx, Xop
+
+
+def _linear(fn, what, Xa, sx, Wa, sw, bias, residual, mode, out, stream):
+    M, K = Xa.shape
+    N = Wa.shape[0]
+    if Wa.shape[1] != K:
+        raise ValueError("operand K mismatch")
+    if out is None:
+        dt = torch.int32 if mode == EPI_RAW_I32 else torch.float32
+        out = torch.empty(M, N, dtype=dt, device=Xa.device)
+    _check(fn(_p(Xa), _p(sx), _p(Wa), _p(sw), _p(bias), _p(residual), M, N, K, int(mode),
+              _p(out), _stream(stream)), what)
+    return out
+
+
+def linear_i8(Xop, x_scale, Wop, w_scale, bias=None, residual=None, mode=EPI_BIAS, out=None,
+              stream=None):
+    """tcgen05 INT8 GEMM + epilogue on GEMM-operand buffers."""
+    _need(Xop, torch.bfloat16, "Xop")
+    _need(Wop, torch.bfloat16, "Wop")
+    return _linear(load().sq_linear_i8, "sq_linear_i8", Xop, x_scale, Wop, w_scale, bias,
+                   residual, mode, out, stream)
+
+
+def linear_i8_mma_sync(Xq, x_scale, Wq, w_scale, bias=None, residual=None, mode=EPI_BIAS,
+                       out=None, stream=None):
+    """Legacy mma.sync INT8 GEMM + epilogue on int8 codes."""
+    _need(Xq, torch.int8, "Xq")
+    _need(Wq, torch.int8, "Wq")
+    return _linear(load().sq_linear_i8_mma_sync, "sq_linear_i8_mma_sync", Xq, x_scale, Wq,
+                   w_scale, bias, residual, mode, out, stream)
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status."""
+    return int(load().sq_device_status(_stream(stream)))

@@ -1,0 +1,174 @@
+// C-ABI boundary: argument checks, then one launch per call on the caller's
+// stream.  Declarations and the contract of every entry point are in sq.h.
+#include "common.cuh"
+
+#include <mutex>
+
+namespace sq {
+
+sq_status device_info(DeviceInfo *out) {
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SQ_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return SQ_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(mu);
+    DeviceInfo &c = cache[dev];
+    if (c.device != dev) {
+        cudaDeviceProp p;
+        if (cudaGetDeviceProperties(&p, dev) != cudaSuccess) return SQ_ERR_CUDA;
+        c.sms = p.multiProcessorCount;
+        c.major = p.major;
+        c.minor = p.minor;
+        c.smem_optin = p.sharedMemPerBlockOptin;
+        c.device = dev;
+    }
+    *out = c;
+    return SQ_OK;
+}
+
+}  // namespace sq
+
+using namespace sq;
+
+namespace {
+
+inline cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
+
+// The kernels are built for sm_103a only.
+sq_status require_sm103() {
+    DeviceInfo di;
+    sq_status rc = device_info(&di);
+    if (rc != SQ_OK) return rc;
+    if (di.major != 10 || di.minor != 3) return SQ_ERR_UNSUPPORTED;
+    return SQ_OK;
+}
+
+constexpr int64_t kMaxK = 133144;  // K * 127^2 < 2^31
+
+sq_status check_linear_args(const void *X, const float *sx, const void *W, const float *sw,
+                            const float *bias, const float *residual, int64_t M, int64_t N,
+                            int64_t K, int mode, const void *Y) {
+    if (!X || !W || !Y) return SQ_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K <= 0) return SQ_ERR_INVALID_ARG;
+    if (mode < SQ_EPI_NONE || mode > SQ_EPI_RAW_I32) return SQ_ERR_INVALID_ARG;
+    if (mode != SQ_EPI_RAW_I32 && (!sx || !sw)) return SQ_ERR_INVALID_ARG;
+    if ((mode == SQ_EPI_BIAS || mode == SQ_EPI_BIAS_GELU || mode == SQ_EPI_BIAS_RESIDUAL) &&
+        !bias)
+        return SQ_ERR_INVALID_ARG;
+    if (mode == SQ_EPI_BIAS_RESIDUAL && !residual) return SQ_ERR_INVALID_ARG;
+    if (K % 16 != 0) return SQ_ERR_ALIGNMENT;
+    if (K > kMaxK) return SQ_ERR_UNSUPPORTED;
+    if (!aligned16(X) || !aligned16(W) || !aligned16(Y)) return SQ_ERR_ALIGNMENT;
+    if (mode != SQ_EPI_RAW_I32 && (!aligned4(sx) || !aligned4(sw))) return SQ_ERR_ALIGNMENT;
+    if (bias && !aligned4(bias)) return SQ_ERR_ALIGNMENT;
+    if (mode == SQ_EPI_BIAS_RESIDUAL && !aligned16(residual)) return SQ_ERR_ALIGNMENT;
+    return SQ_OK;
+}
+
+sq_status check_quant_args(const float *A, const float *s, int64_t rows, int64_t K,
+                           const int8_t *q, const float *scale, const void *op) {
+    if (!A || !s || !scale) return SQ_ERR_INVALID_ARG;
+    if (!q && !op) return SQ_ERR_INVALID_ARG;
+    if (rows < 0 || K <= 0) return SQ_ERR_INVALID_ARG;
+    if (K % 16 != 0) return SQ_ERR_ALIGNMENT;
+    if (K > (int64_t)1 << 30) return SQ_ERR_UNSUPPORTED;
+    if (!aligned16(A) || !aligned16(s) || (q && !aligned16(q)) || (op && !aligned16(op)))
+        return SQ_ERR_ALIGNMENT;
+    if (!aligned4(scale)) return SQ_ERR_ALIGNMENT;
+    return SQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *sq_status_string(int status) {
+    switch (status) {
+    case SQ_OK: return "SQ_OK";
+    case SQ_ERR_INVALID_ARG: return "SQ_ERR_INVALID_ARG: invalid argument";
+    case SQ_ERR_ALIGNMENT: return "SQ_ERR_ALIGNMENT: K not a multiple of 16 or misaligned pointer";
+    case SQ_ERR_UNSUPPORTED: return "SQ_ERR_UNSUPPORTED: size limit exceeded or device not sm_103";
+    case SQ_ERR_CUDA: return "SQ_ERR_CUDA: CUDA call or kernel launch failed";
+    case SQ_ERR_TIMEOUT: return "SQ_ERR_TIMEOUT: a kernel's bounded pipeline wait ran out";
+    default: return "unknown sq_status";
+    }
+}
+
+int sq_version(void) { return (1 << 16) | 0; }
+
+size_t sq_operand_bytes(int64_t rows, int64_t K) {
+    if (rows < 0 || K < 0) return 0;
+    return (size_t)rows * (size_t)K * sizeof(__nv_bfloat16);
+}
+
+sq_status sq_channel_absmax(const float *A, int64_t rows, int64_t cols, float *amax,
+                            void *stream) {
+    if (!A || !amax || rows < 0 || cols <= 0) return SQ_ERR_INVALID_ARG;
+    if (!aligned4(A) || !aligned4(amax)) return SQ_ERR_ALIGNMENT;
+    if (rows == 0) return SQ_OK;
+    sq_status rc = require_sm103();
+    if (rc != SQ_OK) return rc;
+    return launch_channel_absmax(A, rows, cols, amax, as_stream(stream));
+}
+
+sq_status sq_smooth_factor(const float *x_amax, const float *w_amax, int64_t K, float alpha,
+                           float *s, void *stream) {
+    if (!x_amax || !w_amax || !s || K <= 0) return SQ_ERR_INVALID_ARG;
+    if (!(alpha >= 0.0f && alpha <= 1.0f)) return SQ_ERR_INVALID_ARG;
+    if (!aligned4(x_amax) || !aligned4(w_amax) || !aligned4(s)) return SQ_ERR_ALIGNMENT;
+    sq_status rc = require_sm103();
+    if (rc != SQ_OK) return rc;
+    return launch_smooth_factor(x_amax, w_amax, K, alpha, s, as_stream(stream));
+}
+
+sq_status sq_pack_weight(const float *W, const float *s, int64_t N, int64_t K, int8_t *Wq,
+                         float *w_scale, void *Wop, void *stream) {
+    sq_status rc = check_quant_args(W, s, N, K, Wq, w_scale, Wop);
+    if (rc != SQ_OK) return rc;
+    if (N == 0) return SQ_OK;
+    if ((rc = require_sm103()) != SQ_OK) return rc;
+    return launch_quantize_rows(1, W, s, N, K, Wq, w_scale, static_cast<__nv_bfloat16 *>(Wop),
+                                as_stream(stream));
+}
+
+sq_status sq_quantize_act(const float *X, const float *s, int64_t M, int64_t K, int8_t *Xq,
+                          float *x_scale, void *Xop, void *stream) {
+    sq_status rc = check_quant_args(X, s, M, K, Xq, x_scale, Xop);
+    if (rc != SQ_OK) return rc;
+    if (M == 0) return SQ_OK;
+    if ((rc = require_sm103()) != SQ_OK) return rc;
+    return launch_quantize_rows(0, X, s, M, K, Xq, x_scale, static_cast<__nv_bfloat16 *>(Xop),
+                                as_stream(stream));
+}
+
+sq_status sq_linear_i8(const void *Xop, const float *x_scale, const void *Wop,
+                       const float *w_scale, const float *bias, const float *residual,
+                       int64_t M, int64_t N, int64_t K, int mode, void *Y, void *stream) {
+    sq_status rc = check_linear_args(Xop, x_scale, Wop, w_scale, bias, residual, M, N, K, mode, Y);
+    if (rc != SQ_OK) return rc;
+    if (M == 0 || N == 0) return SQ_OK;
+    if ((rc = require_sm103()) != SQ_OK) return rc;
+    return launch_gemm_tc(static_cast<const __nv_bfloat16 *>(Xop), x_scale,
+                          static_cast<const __nv_bfloat16 *>(Wop), w_scale, bias, residual, M, N,
+                          K, mode, Y, as_stream(stream));
+}
+
+sq_status sq_linear_i8_mma_sync(const int8_t *Xq, const float *x_scale, const int8_t *Wq,
+                                const float *w_scale, const float *bias, const float *residual,
+                                int64_t M, int64_t N, int64_t K, int mode, void *Y,
+                                void *stream) {
+    sq_status rc = check_linear_args(Xq, x_scale, Wq, w_scale, bias, residual, M, N, K, mode, Y);
+    if (rc != SQ_OK) return rc;
+    if (M == 0 || N == 0) return SQ_OK;
+    if ((rc = require_sm103()) != SQ_OK) return rc;
+    return launch_gemm_mma_sync(Xq, x_scale, Wq, w_scale, bias, residual, M, N, K, mode, Y,
+                                as_stream(stream));
+}
+
+sq_status sq_device_status(void *stream) {
+    if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return SQ_ERR_CUDA;
+    return gemm_tc_take_error(as_stream(stream));
+}
+
+}  // extern "C"

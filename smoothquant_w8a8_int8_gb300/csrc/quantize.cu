@@ -1,0 +1,235 @@
+// Smoothing statistics, smoothing factor, and the per-row symmetric int8
+// quantiser used for both activations (dynamic, per token) and weights
+// (offline, per output channel).
+//
+// "Efficient INT8 Inference of Small NLP Models on Server CPUs with PyTorch
+// Native Stack": Table 10 (Smooth-Dynamic: SmoothQuant + dynamic activation
+// quantisation), with per-token activation / per-channel weight scales; the
+// smoothing factor and its migration strength alpha follow SmoothQuant (the
+// pages' reference list; alpha per model in Table 15).
+//
+// The quantiser is HBM-bound (4 B read + 1-3 B written per element, a few
+// flops), so it is written as a coalesced row reduction: a group of TPR
+// threads owns a row, each thread holds up to VPT float4 of it in registers,
+// the row maximum is a warp-shuffle (and, for TPR > 32, a shared-memory)
+// reduction, and the codes are produced from the registers, so every input
+// byte is read from HBM exactly once.  Blocks loop over rows so that the
+// per-channel smoothing factors stay in registers across rows.
+#include "common.cuh"
+
+#include <algorithm>
+
+namespace sq {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kVPT = 8;  // float4 per thread held in registers (K <= 256*8*4)
+
+__device__ __forceinline__ float smooth_one(float x, float s, int direction) {
+    // activations: x / s (IEEE division); weights: x * s
+    return direction == 0 ? __fdiv_rn(x, s) : __fmul_rn(x, s);
+}
+
+__device__ __forceinline__ int code_of(float v, float scale) {
+    int c = __float2int_rn(__fdiv_rn(v, scale));  // round half to even
+    return max(-127, min(127, c));
+}
+
+__device__ __forceinline__ void store_codes(float4 v, float scale, int64_t off4, int8_t *q,
+                                            __nv_bfloat16 *op) {
+    int c0 = code_of(v.x, scale), c1 = code_of(v.y, scale);
+    int c2 = code_of(v.z, scale), c3 = code_of(v.w, scale);
+    if (q) {
+        uint32_t packed = (uint32_t)(c0 & 0xff) | ((uint32_t)(c1 & 0xff) << 8) |
+                          ((uint32_t)(c2 & 0xff) << 16) | ((uint32_t)(c3 & 0xff) << 24);
+        reinterpret_cast<uint32_t *>(q)[off4] = packed;
+    }
+    if (op) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn((float)c0, (float)c1);
+        __nv_bfloat162 hi = __floats2bfloat162_rn((float)c2, (float)c3);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t *>(&lo);
+        u.y = *reinterpret_cast<uint32_t *>(&hi);
+        reinterpret_cast<uint2 *>(op)[off4] = u;
+    }
+}
+
+// Row maximum across the TPR threads of a row group.  red: [rows_per_block][8].
+__device__ __forceinline__ float group_max(float m, int tpr, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (tpr > 32) {
+        const int warp = threadIdx.x >> 5;
+        const int wpg = tpr >> 5;           // warps per group
+        const int g = warp / wpg;
+        if ((threadIdx.x & 31) == 0) red[warp] = m;
+        __syncthreads();
+        m = 0.0f;
+        for (int w = 0; w < wpg; ++w) m = fmaxf(m, red[g * wpg + w]);
+        __syncthreads();
+    }
+    return m;
+}
+
+// Registers path: K4 = K/4 <= tpr * kVPT.
+template <int DIR>
+__global__ void __launch_bounds__(kThreads) quantize_rows_reg(
+    const float *__restrict__ A, const float *__restrict__ s, int64_t rows, int K4, int tpr,
+    int8_t *__restrict__ q, float *__restrict__ scale, __nv_bfloat16 *__restrict__ op) {
+    __shared__ float red[kThreads / 32];
+    const int rpb = kThreads / tpr;
+    const int g = threadIdx.x / tpr;
+    const int t = threadIdx.x % tpr;
+    const float4 *s4 = reinterpret_cast<const float4 *>(s);
+    float4 sv[kVPT];
+#pragma unroll
+    for (int i = 0; i < kVPT; ++i) {
+        int j = t + i * tpr;
+        sv[i] = j < K4 ? __ldg(s4 + j) : make_float4(1.f, 1.f, 1.f, 1.f);
+    }
+    const int64_t tiles = (rows + rpb - 1) / rpb;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const int64_t row = tile * rpb + g;
+        const bool valid = row < rows;
+        const float4 *a4 = reinterpret_cast<const float4 *>(A) + (valid ? row : 0) * K4;
+        float4 v[kVPT];
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kVPT; ++i) {
+            int j = t + i * tpr;
+            if (valid && j < K4) {
+                float4 x = __ldcs(a4 + j);
+                v[i].x = smooth_one(x.x, sv[i].x, DIR);
+                v[i].y = smooth_one(x.y, sv[i].y, DIR);
+                v[i].z = smooth_one(x.z, sv[i].z, DIR);
+                v[i].w = smooth_one(x.w, sv[i].w, DIR);
+                m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)),
+                                   fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+            } else {
+                v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        m = group_max(m, tpr, red);
+        const float sc = m == 0.0f ? 1.0f : __fdiv_rn(m, 127.0f);
+        if (valid) {
+            if (t == 0) scale[row] = sc;
+#pragma unroll
+            for (int i = 0; i < kVPT; ++i) {
+                int j = t + i * tpr;
+                if (j < K4) store_codes(v[i], sc, row * K4 + j, q, op);
+            }
+        }
+    }
+}
+
+// Long rows (K4 > kThreads * kVPT): one block per row, the row is read twice.
+template <int DIR>
+__global__ void __launch_bounds__(kThreads) quantize_rows_loop(
+    const float *__restrict__ A, const float *__restrict__ s, int64_t rows, int K4,
+    int8_t *__restrict__ q, float *__restrict__ scale, __nv_bfloat16 *__restrict__ op) {
+    __shared__ float red[kThreads / 32];
+    const float4 *s4 = reinterpret_cast<const float4 *>(s);
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const float4 *a4 = reinterpret_cast<const float4 *>(A) + row * K4;
+        float m = 0.0f;
+        for (int j = threadIdx.x; j < K4; j += kThreads) {
+            float4 x = __ldg(a4 + j), sv = __ldg(s4 + j);
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(smooth_one(x.x, sv.x, DIR)),
+                                     fabsf(smooth_one(x.y, sv.y, DIR))),
+                               fmaxf(fabsf(smooth_one(x.z, sv.z, DIR)),
+                                     fabsf(smooth_one(x.w, sv.w, DIR)))));
+        }
+        m = group_max(m, kThreads, red);
+        const float sc = m == 0.0f ? 1.0f : __fdiv_rn(m, 127.0f);
+        if (threadIdx.x == 0) scale[row] = sc;
+        for (int j = threadIdx.x; j < K4; j += kThreads) {
+            float4 x = __ldcs(a4 + j), sv = __ldg(s4 + j);
+            float4 v = make_float4(smooth_one(x.x, sv.x, DIR), smooth_one(x.y, sv.y, DIR),
+                                   smooth_one(x.z, sv.z, DIR), smooth_one(x.w, sv.w, DIR));
+            store_codes(v, sc, row * K4 + j, q, op);
+        }
+    }
+}
+
+// Column maxima, merged into amax with an integer atomicMax (the bit patterns
+// of non-negative floats order like the floats).
+__global__ void __launch_bounds__(kThreads) channel_absmax_kernel(
+    const float *__restrict__ A, int64_t rows, int64_t cols, int64_t rows_per_block,
+    float *__restrict__ amax) {
+    const int64_t j = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    if (j >= cols) return;
+    const int64_t r0 = (int64_t)blockIdx.y * rows_per_block;
+    const int64_t r1 = min(rows, r0 + rows_per_block);
+    float m = 0.0f;
+    for (int64_t i = r0; i < r1; ++i) m = fmaxf(m, fabsf(__ldg(A + i * cols + j)));
+    atomicMax(reinterpret_cast<int *>(amax) + j, __float_as_int(m));
+}
+
+__global__ void smooth_factor_kernel(const float *__restrict__ ax, const float *__restrict__ aw,
+                                     int64_t K, double alpha, float *__restrict__ s) {
+    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= K) return;
+    double x = (double)ax[j], w = (double)aw[j];
+    s[j] = (x == 0.0 || w == 0.0) ? 1.0f : (float)(pow(x, alpha) / pow(w, 1.0 - alpha));
+}
+
+template <typename Kern>
+int resident_blocks(Kern k) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, 0) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    return per_sm;
+}
+
+}  // namespace
+
+sq_status launch_quantize_rows(int direction, const float *A, const float *s, int64_t rows,
+                               int64_t K, int8_t *q, float *scale, __nv_bfloat16 *op,
+                               cudaStream_t st) {
+    DeviceInfo di;
+    sq_status rc = device_info(&di);
+    if (rc != SQ_OK) return rc;
+    const int K4 = (int)(K / 4);
+    if (K4 <= kThreads * kVPT) {
+        int tpr = 32;
+        while (tpr * kVPT < K4) tpr <<= 1;
+        const int rpb = kThreads / tpr;
+        const int64_t tiles = (rows + rpb - 1) / rpb;
+        auto kern = direction == 0 ? quantize_rows_reg<0> : quantize_rows_reg<1>;
+        static int per_sm[2] = {0, 0};
+        if (!per_sm[direction]) per_sm[direction] = resident_blocks(kern);
+        const int64_t grid = std::min<int64_t>(tiles, (int64_t)di.sms * per_sm[direction]);
+        kern<<<(unsigned)grid, kThreads, 0, st>>>(A, s, rows, K4, tpr, q, scale, op);
+    } else {
+        auto kern = direction == 0 ? quantize_rows_loop<0> : quantize_rows_loop<1>;
+        const int64_t grid = std::min<int64_t>(rows, (int64_t)di.sms * 8);
+        kern<<<(unsigned)grid, kThreads, 0, st>>>(A, s, rows, K4, q, scale, op);
+    }
+    return cuda_status(cudaGetLastError());
+}
+
+sq_status launch_channel_absmax(const float *A, int64_t rows, int64_t cols, float *amax,
+                                cudaStream_t st) {
+    DeviceInfo di;
+    sq_status rc = device_info(&di);
+    if (rc != SQ_OK) return rc;
+    const int64_t gx = (cols + kThreads - 1) / kThreads;
+    int64_t gy = std::max<int64_t>(1, ((int64_t)di.sms * 8 + gx - 1) / gx);
+    gy = std::min<int64_t>(gy, std::min<int64_t>(rows, 65535));
+    const int64_t rpb = (rows + gy - 1) / gy;
+    gy = (rows + rpb - 1) / rpb;
+    if (gx > 0x7fffffff) return SQ_ERR_UNSUPPORTED;
+    channel_absmax_kernel<<<dim3((unsigned)gx, (unsigned)gy), kThreads, 0, st>>>(A, rows, cols,
+                                                                                 rpb, amax);
+    return cuda_status(cudaGetLastError());
+}
+
+sq_status launch_smooth_factor(const float *ax, const float *aw, int64_t K, float alpha,
+                               float *s, cudaStream_t st) {
+    const int64_t grid = (K + kThreads - 1) / kThreads;
+    smooth_factor_kernel<<<(unsigned)grid, kThreads, 0, st>>>(ax, aw, K, (double)alpha, s);
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace sq

@@ -1,0 +1,102 @@
+"""Host-side checks of the C-ABI library (no GPU needed): it builds, loads,
+exports every function include/sq.h declares, and rejects bad arguments with
+the documented status before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from smoothquant_w8a8_int8_gb300 import build as sqbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = sqbuild.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "sq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("sq_pack_weight", "sq_quantize_act", "sq_linear_i8", "sq_channel_absmax",
+              "sq_smooth_factor", "sq_device_status", "sq_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in sq.h but not exported"
+
+
+def test_binding_covers_every_declared_symbol():
+    from smoothquant_w8a8_int8_gb300 import binding
+    assert sorted(binding.EXPORTS) == declared_functions()
+
+
+def test_status_strings_and_sizes(lib):
+    lib.sq_status_string.restype = ctypes.c_char_p
+    lib.sq_status_string.argtypes = [ctypes.c_int]
+    assert lib.sq_status_string(0) == b"SQ_OK"
+    for code in range(1, 6):
+        assert lib.sq_status_string(code).startswith(b"SQ_ERR_")
+    assert b"unknown" in lib.sq_status_string(99)
+    lib.sq_operand_bytes.restype = ctypes.c_size_t
+    lib.sq_operand_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
+    assert lib.sq_operand_bytes(8192, 1024) == 8192 * 1024 * 2
+    assert lib.sq_operand_bytes(-1, 16) == 0
+    assert lib.sq_version() >> 16 == 1
+
+
+def _fake(addr):
+    # a non-null, 16-byte aligned address that is never dereferenced: every
+    # call below fails its host-side argument check before any CUDA call
+    return ctypes.c_void_p(addr)
+
+
+def test_argument_checks_fail_before_any_launch(lib):
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.sq_quantize_act.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp]
+    lib.sq_pack_weight.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp]
+    lib.sq_linear_i8.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp]
+    lib.sq_linear_i8_mma_sync.argtypes = lib.sq_linear_i8.argtypes
+    lib.sq_smooth_factor.argtypes = [vp, vp, i64, ctypes.c_float, vp, vp]
+    lib.sq_channel_absmax.argtypes = [vp, i64, i64, vp, vp]
+    a = _fake(0x10000)
+    INVALID, ALIGN, UNSUP = 1, 2, 3
+    # quantiser
+    assert lib.sq_quantize_act(None, a, 4, 32, a, a, None, None) == INVALID
+    assert lib.sq_quantize_act(a, a, 4, 32, None, a, None, None) == INVALID   # no output
+    assert lib.sq_quantize_act(a, a, 4, 32, a, None, None, None) == INVALID   # no scale
+    assert lib.sq_quantize_act(a, a, -1, 32, a, a, None, None) == INVALID
+    assert lib.sq_quantize_act(a, a, 4, 0, a, a, None, None) == INVALID
+    assert lib.sq_quantize_act(a, a, 4, 24, a, a, None, None) == ALIGN       # K % 16
+    assert lib.sq_quantize_act(_fake(0x10004), a, 4, 32, a, a, None, None) == ALIGN
+    assert lib.sq_quantize_act(a, a, 0, 32, a, a, None, None) == 0           # empty: no launch
+    assert lib.sq_pack_weight(a, a, 4, 40, a, a, None, None) == ALIGN
+    assert lib.sq_pack_weight(a, a, 0, 32, None, a, a, None) == 0
+    # GEMM
+    for fn in (lib.sq_linear_i8, lib.sq_linear_i8_mma_sync):
+        assert fn(None, a, a, a, a, None, 8, 8, 32, 1, a, None) == INVALID
+        assert fn(a, a, a, a, None, None, 8, 8, 32, 1, a, None) == INVALID   # bias missing
+        assert fn(a, a, a, a, a, None, 8, 8, 32, 3, a, None) == INVALID      # residual missing
+        assert fn(a, a, a, a, a, a, 8, 8, 32, 5, a, None) == INVALID         # bad mode
+        assert fn(a, a, a, a, a, a, 8, 8, 32, -1, a, None) == INVALID
+        assert fn(a, a, a, a, a, None, 8, 8, 40, 1, a, None) == ALIGN
+        assert fn(a, a, a, a, a, None, 8, 8, 133152, 1, a, None) == UNSUP  # |acc| could overflow
+        assert fn(a, a, a, a, a, None, 8, 8, 32, 1, _fake(0x10008), None) == ALIGN
+        assert fn(a, a, a, a, a, None, 0, 8, 32, 1, a, None) == 0          # empty
+        assert fn(a, a, a, a, a, None, 8, 0, 32, 1, a, None) == 0
+    # smoothing factor
+    assert lib.sq_smooth_factor(a, a, 8, 1.5, a, None) == INVALID
+    assert lib.sq_smooth_factor(a, a, 8, -0.1, a, None) == INVALID
+    assert lib.sq_smooth_factor(a, None, 8, 0.5, a, None) == INVALID
+    assert lib.sq_channel_absmax(a, 4, 0, a, None) == INVALID
+    assert lib.sq_channel_absmax(a, 0, 4, a, None) == 0

@@ -1,0 +1,282 @@
+"""GPU parity: every kernel through the C-ABI against the CPU oracle on the
+same seeded inputs.  Codes, scale bit patterns and int32 accumulators must
+match exactly; fp32 outputs within max|err| <= 1e-5 max|ref| + 1e-6."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paritylib import (assert_bits_equal, assert_close_fp32, assert_codes_equal, op_as_int,
+                       oracle_smoothing, to_dev)
+from smoothquant_w8a8_int8_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+PATHS = ["tc", "mma_sync"]
+
+
+@pytest.fixture(scope="session")
+def sq():
+    from smoothquant_w8a8_int8_gb300 import binding, build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    binding.load()
+    return binding
+
+
+def gpu_pack(sq, W, s):
+    Wq, sw, Wop = sq.pack_weight(to_dev(W), to_dev(s))
+    return Wq, sw, Wop
+
+
+def gpu_linear(sq, path, Xq, Xop, sx, Wq, Wop, sw, bias=None, residual=None,
+               mode=wl.EPI_BIAS):
+    if path == "tc":
+        return sq.linear_i8(Xop, sx, Wop, sw, bias, residual, mode)
+    return sq.linear_i8_mma_sync(Xq, sx, Wq, sw, bias, residual, mode)
+
+
+# ------------------------------------------------------------------ quantiser
+
+QUANT_SHAPES = [(1, 16), (7, 48), (37, 1024), (130, 768), (64, 4096), (300, 3072), (3, 8192),
+                (5, 8208), (2, 16384)]
+
+
+@pytest.mark.parametrize("M,K", QUANT_SHAPES)
+def test_quantize_act_parity(sq, M, K):
+    c = wl.make_case(M, K, 8, wl.EPI_BIAS, seed=M * 31 + K)
+    X, W = c.X.numpy(), c.W.numpy()
+    s = oracle_smoothing(X, W, 0.5)
+    q_ref, sx_ref = oracle.quantize_rows(X, s, "act")
+    Xq, sx, Xop = sq.quantize_act(to_dev(X), to_dev(s))
+    torch.cuda.synchronize()
+    assert_codes_equal(Xq.cpu().numpy(), q_ref, "Xq")
+    assert_bits_equal(sx.cpu().numpy(), sx_ref, "x_scale")
+    assert_codes_equal(op_as_int(Xop), q_ref, "Xop")
+    # each output alone
+    _, sx2, Xop2 = sq.quantize_act(to_dev(X), to_dev(s), want_q=False)
+    Xq3, sx3, _ = sq.quantize_act(to_dev(X), to_dev(s), want_op=False)
+    assert_codes_equal(op_as_int(Xop2), q_ref, "Xop only")
+    assert_codes_equal(Xq3.cpu().numpy(), q_ref, "Xq only")
+    assert_bits_equal(sx2.cpu().numpy(), sx_ref, "x_scale (op only)")
+
+
+def test_quantize_degenerate_rows(sq):
+    K = 64
+    X = np.zeros((6, K), np.float32)
+    X[1, 3] = -2.5                      # one-hot row
+    X[2, :] = 1.0                       # constant row -> all 127
+    X[3, ::2], X[3, 1::2] = 3.0, -3.0   # alternating signs
+    X[4, :] = np.float32(1e-30)         # tiny values
+    X[5, 0], X[5, 1] = 127.0, -63.5     # ties: -63.5 -> -64
+    s = np.ones(K, np.float32)
+    q_ref, sx_ref = oracle.quantize_rows(X, s, "act")
+    Xq, sx, Xop = sq.quantize_act(to_dev(X), to_dev(s))
+    assert_codes_equal(Xq.cpu().numpy(), q_ref, "Xq")
+    assert_bits_equal(sx.cpu().numpy(), sx_ref, "x_scale")
+    assert sx.cpu().numpy()[0] == 1.0 and not Xq.cpu().numpy()[0].any()
+
+
+@pytest.mark.parametrize("N,K", [(1, 16), (5, 48), (1024, 1024), (3072, 1024), (768, 3072),
+                                 (9, 8208)])
+def test_pack_weight_parity(sq, N, K):
+    c = wl.make_case(16, K, N, wl.EPI_BIAS, seed=N + K)
+    X, W = c.X.numpy(), c.W.numpy()
+    s = oracle_smoothing(X, W, 0.5)
+    q_ref, sw_ref = oracle.quantize_rows(W, s, "weight")
+    Wq, sw, Wop = gpu_pack(sq, W, s)
+    torch.cuda.synchronize()
+    assert_codes_equal(Wq.cpu().numpy(), q_ref, "Wq")
+    assert_bits_equal(sw.cpu().numpy(), sw_ref, "w_scale")
+    assert_codes_equal(op_as_int(Wop), q_ref, "Wop")
+
+
+# ------------------------------------------------------------ smoothing factor
+
+@pytest.mark.parametrize("rows,cols", [(1, 16), (33, 100), (8192, 1024), (3, 4096)])
+def test_channel_absmax_parity(sq, rows, cols):
+    rng = np.random.default_rng(rows + cols)
+    A = rng.standard_normal((rows, cols)).astype(np.float32)
+    B = (rng.standard_normal((rows, cols)) * 3).astype(np.float32)
+    amax = sq.channel_absmax(to_dev(A))
+    np.testing.assert_array_equal(amax.cpu().numpy(), oracle.channel_absmax(A))
+    sq.channel_absmax(to_dev(B), amax)           # running max over two batches
+    want = np.maximum(oracle.channel_absmax(A), oracle.channel_absmax(B))
+    np.testing.assert_array_equal(amax.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("alpha", [0.5, 0.6, 0.75, 0.0, 1.0])
+def test_smooth_factor_parity(sq, alpha):
+    rng = np.random.default_rng(11)
+    ax = np.abs(rng.standard_normal(4096) * 5).astype(np.float32)
+    aw = np.abs(rng.standard_normal(4096) * 0.05).astype(np.float32)
+    ax[:3] = 0.0
+    aw[10:12] = 0.0
+    s = sq.smooth_factor(to_dev(ax), to_dev(aw), alpha).cpu().numpy()
+    ref = oracle.smooth_factor(ax, aw, np.float32(alpha))
+    # double pow on both sides, one rounding to fp32: equal up to 1 ulp
+    ulp = np.abs(s.view(np.int32).astype(np.int64) - ref.view(np.int32).astype(np.int64))
+    assert ulp.max() <= 1
+    if alpha in (0.5, 0.0, 1.0):
+        assert ulp.max() == 0
+
+
+# ----------------------------------------------------------------- GEMM
+
+GEMM_SHAPES = [(1, 1, 16), (5, 7, 48), (129, 130, 1040), (200, 300, 2064), (128, 256, 1024),
+               (256, 1024, 4096), (300, 260, 3072), (64, 96, 5008)]
+
+
+def _quantised_case(sq, M, K, N, mode, seed):
+    c = wl.make_case(M, K, N, mode, seed=seed)
+    X, W = c.X.numpy(), c.W.numpy()
+    s = oracle_smoothing(X, W, 0.5)
+    wq, sw = oracle.quantize_rows(W, s, "weight")
+    xq, sx = oracle.quantize_rows(X, s, "act")
+    dev = dict(Xq=to_dev(xq), sx=to_dev(sx), Wq=to_dev(wq), sw=to_dev(sw),
+               Xop=to_dev(xq.astype(np.float32), torch.bfloat16),
+               Wop=to_dev(wq.astype(np.float32), torch.bfloat16))
+    return c, xq, sx, wq, sw, dev
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+def test_gemm_raw_int32_exact(sq, path, M, N, K):
+    _, xq, _, wq, _, d = _quantised_case(sq, M, K, N, wl.EPI_NONE, seed=M + N + K)
+    acc = gpu_linear(sq, path, d["Xq"], d["Xop"], None, d["Wq"], d["Wop"], None,
+                     mode=sq.EPI_RAW_I32)
+    assert_codes_equal(acc.cpu().numpy(), oracle.gemm_i32(xq, wq), "acc")
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("K", [1024, 1040, 2048, 4096, 8192])
+def test_gemm_adversarial_exactness(sq, path, K):
+    """Worst-case sums: all +127 (K * 16129, above 2^24 once K > 1024),
+    alternating signs that cancel, and random +-127."""
+    M, N = 160, 136
+    rng = np.random.default_rng(K)
+    xq = np.full((M, K), 127, np.int8)
+    wq = np.full((N, K), 127, np.int8)
+    xq[1::3, 1::2] = -127
+    wq[2::5, :] = -127
+    xq[100:] = rng.choice(np.array([-127, 127], np.int8), (M - 100, K))
+    wq[100:] = rng.choice(np.array([-127, 127], np.int8), (N - 100, K))
+    xq[50, :] = 0
+    acc = gpu_linear(sq, path, to_dev(xq), to_dev(xq.astype(np.float32), torch.bfloat16), None,
+                     to_dev(wq), to_dev(wq.astype(np.float32), torch.bfloat16), None,
+                     mode=sq.EPI_RAW_I32)
+    ref = oracle.gemm_i32(xq, wq)
+    assert ref[0, 0] == K * 16129
+    assert_codes_equal(acc.cpu().numpy(), ref, "acc")
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("mode", [wl.EPI_NONE, wl.EPI_BIAS, wl.EPI_BIAS_GELU,
+                                  wl.EPI_BIAS_RESIDUAL])
+@pytest.mark.parametrize("M,N,K", [(77, 136, 1024), (256, 512, 3072)])
+def test_epilogue_modes(sq, path, mode, M, N, K):
+    c, xq, sx, wq, sw, d = _quantised_case(sq, M, K, N, wl.EPI_BIAS_RESIDUAL, seed=mode + M)
+    acc = oracle.gemm_i32(xq, wq)
+    b, r = c.bias.numpy(), c.residual.numpy()
+    ref = oracle.epilogue(acc, sx, sw, b, r, mode)
+    y = gpu_linear(sq, path, d["Xq"], d["Xop"], d["sx"], d["Wq"], d["Wop"], d["sw"],
+                   to_dev(b), to_dev(r), mode)
+    assert_close_fp32(y.cpu().numpy(), ref, f"mode {mode}")
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_residual_in_place(sq, path):
+    c, xq, sx, wq, sw, d = _quantised_case(sq, 96, 1024, 160, wl.EPI_BIAS_RESIDUAL, seed=3)
+    ref = oracle.epilogue(oracle.gemm_i32(xq, wq), sx, sw, c.bias.numpy(), c.residual.numpy(),
+                          wl.EPI_BIAS_RESIDUAL)
+    r = to_dev(c.residual.numpy())
+    fn = sq.linear_i8 if path == "tc" else sq.linear_i8_mma_sync
+    a, w = (d["Xop"], d["Wop"]) if path == "tc" else (d["Xq"], d["Wq"])
+    fn(a, d["sx"], w, d["sw"], to_dev(c.bias.numpy()), r, wl.EPI_BIAS_RESIDUAL, out=r)
+    assert_close_fp32(r.cpu().numpy(), ref, "in-place residual")
+
+
+def test_zero_input_gives_bias_and_residual(sq):
+    M, N, K = 40, 72, 256
+    X = np.zeros((M, K), np.float32)
+    W = np.random.default_rng(0).standard_normal((N, K)).astype(np.float32)
+    s = np.ones(K, np.float32)
+    b = np.linspace(-1, 1, N).astype(np.float32)
+    r = np.random.default_rng(1).standard_normal((M, N)).astype(np.float32)
+    _, sx, Xop = sq.quantize_act(to_dev(X), to_dev(s), want_q=False)
+    _, sw, Wop = sq.pack_weight(to_dev(W), to_dev(s), want_q=False)
+    y = sq.linear_i8(Xop, sx, Wop, sw, to_dev(b), None, wl.EPI_BIAS)
+    np.testing.assert_array_equal(y.cpu().numpy(), np.broadcast_to(b, (M, N)))
+    y = sq.linear_i8(Xop, sx, Wop, sw, to_dev(b), to_dev(r), wl.EPI_BIAS_RESIDUAL)
+    np.testing.assert_array_equal(y.cpu().numpy(), (r + b).astype(np.float32))
+
+
+def test_empty_calls(sq):
+    s = torch.ones(32, device="cuda")
+    X = torch.empty(0, 32, device="cuda")
+    Xq, sx, Xop = sq.quantize_act(X, s)
+    assert Xq.shape == (0, 32) and sx.shape == (0,)
+    W = torch.randn(8, 32, device="cuda")
+    _, sw, Wop = sq.pack_weight(W, s)
+    y = sq.linear_i8(Xop, sx, Wop, sw, torch.zeros(8, device="cuda"), None, wl.EPI_BIAS)
+    assert y.shape == (0, 8)
+    assert sq.device_status() == 0
+
+
+# ------------------------------------------------ full pipeline on workloads
+
+def _pipeline_gpu(sq, case, s, path):
+    """The hot path as the benchmark runs it: pack once, then quantise the
+    activations to the GEMM operand and run the fused GEMM."""
+    X, W = case.X.cuda(), case.W.cuda()
+    sd = to_dev(s)
+    Wq, sw, Wop = sq.pack_weight(W, sd, want_q=(path != "tc"), want_op=(path == "tc"))
+    Xq, sx, Xop = sq.quantize_act(X, sd, want_q=(path != "tc"), want_op=(path == "tc"))
+    b = case.bias.cuda() if case.bias is not None else None
+    r = case.residual.cuda() if case.residual is not None else None
+    y = gpu_linear(sq, path, Xq, Xop, sx, Wq, Wop, sw, b, r, case.mode)
+    return sx, y
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("name", ["bert_large_qkv_slice_m256", "bert_large_ffn_up_m256",
+                                  "bert_large_ffn_down_m256"])
+def test_small_workloads_full(sq, path, name):
+    w = wl.WORKLOADS[name]
+    case = wl.workload_case(w, 0, 0)
+    X, W = case.X.numpy(), case.W.numpy()
+    s = oracle_smoothing(X, W, w.alpha)
+    wq, sw = oracle.quantize_rows(W, s, "weight")
+    xq, sx_ref, acc, y_ref = oracle.linear_block(
+        X, s, wq, sw, None if case.bias is None else case.bias.numpy(),
+        None if case.residual is None else case.residual.numpy(), case.mode)
+    sx, y = _pipeline_gpu(sq, case, s, path)
+    assert_bits_equal(sx.cpu().numpy(), sx_ref, "x_scale")
+    assert_close_fp32(y.cpu().numpy(), y_ref, name)
+
+
+@pytest.mark.parametrize("path", ["tc"])
+@pytest.mark.parametrize("name,index", [("bert_large_encoder_b32_s256", i) for i in range(4)] +
+                         [("xlmr_base_b64_s512", i) for i in range(4)])
+def test_large_workloads_sampled(sq, path, name, index):
+    """Full-size M on the GPU, checked on a seeded sample of rows (rows are
+    independent through quantisation, GEMM and epilogue)."""
+    w = wl.WORKLOADS[name]
+    case = wl.workload_case(w, 0, index)
+    X, W = case.X.numpy(), case.W.numpy()
+    # the smoothing factor from the oracle, computed on the full calibration X
+    s = oracle_smoothing(X, W, w.alpha)
+    wq, sw = oracle.quantize_rows(W, s, "weight")
+    rng = np.random.default_rng(index)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, w.M - 1],
+                                     rng.choice(w.M, 59, replace=False)]))
+    b = None if case.bias is None else case.bias.numpy()
+    r = None if case.residual is None else case.residual.numpy()[rows]
+    _, sx_ref, _, y_ref = oracle.linear_block(X[rows], s, wq, sw, b, r, case.mode)
+    sx, y = _pipeline_gpu(sq, case, s, path)
+    assert_bits_equal(sx.cpu().numpy()[rows], sx_ref, "x_scale sample")
+    assert_close_fp32(y[torch.from_numpy(rows).cuda()].cpu().numpy(), y_ref, f"{name}[{index}]")
+    # all rows: the scales are the per-row maxima / 127 of the smoothed input
+    sx_all = sx.cpu().numpy()
+    v = X / s
+    np.testing.assert_allclose(sx_all, np.abs(v).max(axis=1) / 127.0, rtol=2.5e-7)
