@@ -17,6 +17,7 @@ instead, on a bounded row sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -415,6 +416,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-step-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="run only the first N layers (small cases for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -422,6 +425,8 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     w = wl.WORKLOADS[args.workload]
+    if args.layers is not None:
+        w = dataclasses.replace(w, layers=max(1, min(args.layers, w.layers)))
 
     if args.impl == "reference":
         if rank == 0:

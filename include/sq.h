@@ -22,8 +22,10 @@
  *  - Arguments are checked on the host before anything is enqueued; a non-OK
  *    status means nothing was launched.  A failed launch returns SQ_ERR_CUDA.
  *    No entry point aborts, traps or throws.
- *  - Sizes are int64_t.  A zero row count (M or N = 0) is a valid empty call
- *    and returns SQ_OK without launching.  K must be a positive multiple of 16.
+ *  - Sizes are int64_t.  A zero row count (M or N = 0) is a valid empty call:
+ *    once the sizes and mode are valid it returns SQ_OK without looking at
+ *    the pointers (which may be NULL) and without launching.  K must be a
+ *    positive multiple of 16.
  *  - Inputs must be finite; results for NaN or Inf inputs are unspecified.
  */
 #ifndef SQ_GB300_H

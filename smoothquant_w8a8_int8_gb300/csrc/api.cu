@@ -49,16 +49,17 @@ constexpr int64_t kMaxK = 133144;  // K * 127^2 < 2^31
 sq_status check_linear_args(const void *X, const float *sx, const void *W, const float *sw,
                             const float *bias, const float *residual, int64_t M, int64_t N,
                             int64_t K, int mode, const void *Y) {
-    if (!X || !W || !Y) return SQ_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K <= 0) return SQ_ERR_INVALID_ARG;
     if (mode < SQ_EPI_NONE || mode > SQ_EPI_RAW_I32) return SQ_ERR_INVALID_ARG;
+    if (K % 16 != 0) return SQ_ERR_ALIGNMENT;
+    if (K > kMaxK) return SQ_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return SQ_OK;  // empty: pointers may be NULL, nothing is launched
+    if (!X || !W || !Y) return SQ_ERR_INVALID_ARG;
     if (mode != SQ_EPI_RAW_I32 && (!sx || !sw)) return SQ_ERR_INVALID_ARG;
     if ((mode == SQ_EPI_BIAS || mode == SQ_EPI_BIAS_GELU || mode == SQ_EPI_BIAS_RESIDUAL) &&
         !bias)
         return SQ_ERR_INVALID_ARG;
     if (mode == SQ_EPI_BIAS_RESIDUAL && !residual) return SQ_ERR_INVALID_ARG;
-    if (K % 16 != 0) return SQ_ERR_ALIGNMENT;
-    if (K > kMaxK) return SQ_ERR_UNSUPPORTED;
     if (!aligned16(X) || !aligned16(W) || !aligned16(Y)) return SQ_ERR_ALIGNMENT;
     if (mode != SQ_EPI_RAW_I32 && (!aligned4(sx) || !aligned4(sw))) return SQ_ERR_ALIGNMENT;
     if (bias && !aligned4(bias)) return SQ_ERR_ALIGNMENT;
@@ -68,11 +69,12 @@ sq_status check_linear_args(const void *X, const float *sx, const void *W, const
 
 sq_status check_quant_args(const float *A, const float *s, int64_t rows, int64_t K,
                            const int8_t *q, const float *scale, const void *op) {
-    if (!A || !s || !scale) return SQ_ERR_INVALID_ARG;
-    if (!q && !op) return SQ_ERR_INVALID_ARG;
     if (rows < 0 || K <= 0) return SQ_ERR_INVALID_ARG;
     if (K % 16 != 0) return SQ_ERR_ALIGNMENT;
     if (K > (int64_t)1 << 30) return SQ_ERR_UNSUPPORTED;
+    if (rows == 0) return SQ_OK;  // empty: pointers may be NULL, nothing is launched
+    if (!A || !s || !scale) return SQ_ERR_INVALID_ARG;
+    if (!q && !op) return SQ_ERR_INVALID_ARG;
     if (!aligned16(A) || !aligned16(s) || (q && !aligned16(q)) || (op && !aligned16(op)))
         return SQ_ERR_ALIGNMENT;
     if (!aligned4(scale)) return SQ_ERR_ALIGNMENT;
@@ -104,9 +106,10 @@ size_t sq_operand_bytes(int64_t rows, int64_t K) {
 
 sq_status sq_channel_absmax(const float *A, int64_t rows, int64_t cols, float *amax,
                             void *stream) {
-    if (!A || !amax || rows < 0 || cols <= 0) return SQ_ERR_INVALID_ARG;
-    if (!aligned4(A) || !aligned4(amax)) return SQ_ERR_ALIGNMENT;
+    if (rows < 0 || cols <= 0) return SQ_ERR_INVALID_ARG;
     if (rows == 0) return SQ_OK;
+    if (!A || !amax) return SQ_ERR_INVALID_ARG;
+    if (!aligned4(A) || !aligned4(amax)) return SQ_ERR_ALIGNMENT;
     sq_status rc = require_sm103();
     if (rc != SQ_OK) return rc;
     return launch_channel_absmax(A, rows, cols, amax, as_stream(stream));

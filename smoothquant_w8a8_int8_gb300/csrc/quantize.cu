@@ -93,21 +93,21 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_reg(
         const bool valid = row < rows;
         const float4 *a4 = reinterpret_cast<const float4 *>(A) + (valid ? row : 0) * K4;
         float4 v[kVPT];
-        float m = 0.0f;
+        // issue every load of the row before any arithmetic (all in flight at once)
 #pragma unroll
         for (int i = 0; i < kVPT; ++i) {
             int j = t + i * tpr;
-            if (valid && j < K4) {
-                float4 x = __ldcs(a4 + j);
-                v[i].x = smooth_one(x.x, sv[i].x, DIR);
-                v[i].y = smooth_one(x.y, sv[i].y, DIR);
-                v[i].z = smooth_one(x.z, sv[i].z, DIR);
-                v[i].w = smooth_one(x.w, sv[i].w, DIR);
-                m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)),
-                                   fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
-            } else {
-                v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+            v[i] = (valid && j < K4) ? __ldcs(a4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kVPT; ++i) {
+            v[i].x = smooth_one(v[i].x, sv[i].x, DIR);
+            v[i].y = smooth_one(v[i].y, sv[i].y, DIR);
+            v[i].z = smooth_one(v[i].z, sv[i].z, DIR);
+            v[i].w = smooth_one(v[i].w, sv[i].w, DIR);
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)),
+                               fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
         }
         m = group_max(m, tpr, red);
         const float sc = m == 0.0f ? 1.0f : __fdiv_rn(m, 127.0f);

@@ -80,6 +80,8 @@ def test_argument_checks_fail_before_any_launch(lib):
     assert lib.sq_quantize_act(a, a, 4, 24, a, a, None, None) == ALIGN       # K % 16
     assert lib.sq_quantize_act(_fake(0x10004), a, 4, 32, a, a, None, None) == ALIGN
     assert lib.sq_quantize_act(a, a, 0, 32, a, a, None, None) == 0           # empty: no launch
+    assert lib.sq_quantize_act(None, None, 0, 32, None, None, None, None) == 0
+    assert lib.sq_quantize_act(None, None, 0, 24, None, None, None, None) == ALIGN
     assert lib.sq_pack_weight(a, a, 4, 40, a, a, None, None) == ALIGN
     assert lib.sq_pack_weight(a, a, 0, 32, None, a, a, None) == 0
     # GEMM
@@ -94,9 +96,11 @@ def test_argument_checks_fail_before_any_launch(lib):
         assert fn(a, a, a, a, a, None, 8, 8, 32, 1, _fake(0x10008), None) == ALIGN
         assert fn(a, a, a, a, a, None, 0, 8, 32, 1, a, None) == 0          # empty
         assert fn(a, a, a, a, a, None, 8, 0, 32, 1, a, None) == 0
+        assert fn(None, None, None, None, None, None, 0, 0, 32, 3, None, None) == 0
     # smoothing factor
     assert lib.sq_smooth_factor(a, a, 8, 1.5, a, None) == INVALID
     assert lib.sq_smooth_factor(a, a, 8, -0.1, a, None) == INVALID
     assert lib.sq_smooth_factor(a, None, 8, 0.5, a, None) == INVALID
     assert lib.sq_channel_absmax(a, 4, 0, a, None) == INVALID
     assert lib.sq_channel_absmax(a, 0, 4, a, None) == 0
+    assert lib.sq_channel_absmax(None, 0, 4, None, None) == 0
