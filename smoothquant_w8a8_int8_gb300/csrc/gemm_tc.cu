@@ -1,6 +1,6 @@
 // INT8 GEMM + fused dequantising epilogue on the 5th-generation tensor cores
 // (tcgen05, sm_103a): TMA-fed shared-memory ring, accumulators in tensor
-// memory, warp-specialised persistent CTAs.
+// memory, warp-specialised persistent CTAs, TMA-staged epilogue stores.
 //
 // "Efficient INT8 Inference of Small NLP Models on Server CPUs with PyTorch
 // Native Stack": the linear block is the int8 x int8 -> int32 GEMM plus its
@@ -20,11 +20,22 @@
 // Roles (320 threads, one CTA per SM, persistent over 128 x 256 output tiles):
 //   warp 0, lane 0  TMA producer: A [128 x 64] and B [256 x 64] bf16 tiles,
 //                   128-byte swizzle, into a 4-stage ring (48 KB per stage)
-//   warp 1, lane 0  MMA issuer: tcgen05.mma kind::f16, M=128 N=256 K=16,
-//                   one chunk into one of two 256-column TMEM accumulators
-//   warps 2..9      epilogue: warp w reads TMEM lanes 32*(w%4).. (its rows)
-//                   and columns 128*((w-2)/4).. (its half), int32 partials in
-//                   registers, then scales, bias, GELU / residual, stores.
+//   warp 1, lane 0  MMA issuer: tcgen05.mma kind::f16, M=128 N=256 K=16
+//   warps 2..9      epilogue: warp w owns TMEM lanes 32*(w%4).. (32 rows of
+//                   the tile) and columns 128*((w-2)/4).. (half of its width)
+// Tensor memory (512 columns):
+//   K <= 1024: two 256-column accumulators; the MMA fills one while the
+//              epilogue drains the other.
+//   K >  1024: one 256-column chunk accumulator A and a 256-column int32
+//              partial P; after each chunk the epilogue adds A into P (in
+//              tensor memory) and frees A, so the MMA of the next chunk only
+//              waits for that short pass, and the final pass (scales, bias,
+//              GELU / residual, stores) overlaps the next tile's first chunk.
+// Epilogue I/O per 32 x 32 slice: results are written to a per-warp 4 KB
+// staging tile in shared memory (128-byte swizzle, conflict-free) and stored
+// with one TMA bulk tensor store; the residual slice arrives by TMA load into
+// the same tile.  Shapes whose rows are not 16-byte multiples (N % 4 != 0)
+// take plain per-element loads and stores instead.
 // Every wait is bounded (about 4 s of %globaltimer); on expiry the kernel
 // records SQ_ERR_TIMEOUT in a device word, lets its issued copies and MMAs
 // drain, frees its tensor memory and returns.
@@ -47,9 +58,14 @@ constexpr int THREADS = 64 + NUM_EPI_WARPS * 32;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int TMEM_COLS = 2 * BN;           // two accumulators
+constexpr int SLICE = 32;                   // epilogue slice: 32 rows x 32 columns
+constexpr int COLS_PER_WARP = BN / 2;       // 128
+constexpr int SLICES = COLS_PER_WARP / SLICE;
+constexpr int STG_BYTES = SLICE * SLICE * 4;  // 4 KB staging tile per epilogue warp
+constexpr int TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
+constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+constexpr int SMEM_BYTES = RING_BYTES + NUM_EPI_WARPS * STG_BYTES + BAR_BYTES + 1024;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;
 
 // instruction descriptor, kind::f16: D fp32, A/B bf16, both K-major, N, M
@@ -139,6 +155,27 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// the staging tile may be overwritten once the previous store has read it
+__device__ __forceinline__ void bulk_wait_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait0() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -188,6 +225,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+        "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+        "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ kernel
 
 struct Smem {
@@ -195,35 +248,122 @@ struct Smem {
     uint64_t empty[STAGES];
     uint64_t tfull[2];
     uint64_t tempty[2];
+    uint64_t rfull[NUM_EPI_WARPS];  // residual slice landed in a warp's staging tile
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
 };
 static_assert(sizeof(Smem) <= BAR_BYTES, "barrier block");
 
-__device__ __forceinline__ void store4(float *y, int64_t off, int64_t n, int64_t N, bool vec_ok,
-                                       float a, float b, float c, float d) {
-    if (vec_ok && n + 3 < N) {
-        *reinterpret_cast<float4 *>(y + off) = make_float4(a, b, c, d);
-    } else {
-        if (n < N) y[off] = a;
-        if (n + 1 < N) y[off + 1] = b;
-        if (n + 2 < N) y[off + 2] = c;
-        if (n + 3 < N) y[off + 3] = d;
+struct EpiArgs {
+    const float *sx, *sw, *bias, *residual;
+    void *Y;
+    int M, N;
+    int tma_io;  // 1: TMA staging for Y (and the residual); 0: plain per-element I/O
+};
+
+// Turns one 32 x 32 slice of exact int32 sums (this thread's row, 32
+// consecutive columns starting at n) into the epilogue's outputs and stores
+// them, four columns at a time.  `stg` is the warp's staging tile (row
+// `lane` holds this thread's 32 values, 16-byte chunk c at c ^ (lane & 7));
+// `rbar`/`rph` are its residual barrier and parity.
+template <int MODE>
+__device__ __forceinline__ void epilogue_slice(const uint32_t (&acc)[32], int64_t m, int64_t n,
+                                               int row0, int lane, const EpiArgs &a,
+                                               const CUtensorMap *tmY, const CUtensorMap *tmR,
+                                               uint8_t *stg, uint32_t rbar, uint32_t &rph,
+                                               volatile int *abort_flag) {
+    if (n >= a.N || row0 >= a.M) return;  // slice wholly outside Y: nothing to do
+    const uint32_t stg_u32 = smem_u32(stg);
+    if (a.tma_io) {
+        // the previous TMA store of this warp must have finished reading the tile
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+        if (MODE == SQ_EPI_BIAS_RESIDUAL) {
+            if (lane == 0) {
+                mbar_expect_tx(rbar, STG_BYTES);
+                tma_load_2d(stg_u32, tmR, rbar, (int)n, row0);
+            }
+            const bool ok = mbar_wait(rbar, rph, abort_flag);
+            rph ^= 1;
+            if (!ok) mbar_drain(rbar, rph ^ 1);  // the copy may still land: let it
+        }
+    }
+    const bool row_ok = m < a.M;
+    const bool vec = a.tma_io && n + 31 < a.N;  // whole slice in range, 16-byte aligned
+    const float xs = (MODE != SQ_EPI_RAW_I32 && row_ok) ? __ldg(a.sx + m) : 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const int64_t n4 = n + 4 * c;
+        uint8_t *chunk = stg + lane * 128 + ((c ^ (lane & 7)) << 4);
+        uint32_t o[4];
+        if (MODE == SQ_EPI_RAW_I32) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[e] = acc[4 * c + e];
+        } else {
+            float w[4], b[4] = {0.f, 0.f, 0.f, 0.f}, r[4] = {0.f, 0.f, 0.f, 0.f};
+            if (vec) {
+                const float4 wv = __ldg(reinterpret_cast<const float4 *>(a.sw + n4));
+                w[0] = wv.x; w[1] = wv.y; w[2] = wv.z; w[3] = wv.w;
+                if (MODE != SQ_EPI_NONE) {
+                    const float4 bv = __ldg(reinterpret_cast<const float4 *>(a.bias + n4));
+                    b[0] = bv.x; b[1] = bv.y; b[2] = bv.z; b[3] = bv.w;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const bool ok = n4 + e < a.N;
+                    w[e] = ok ? __ldg(a.sw + n4 + e) : 0.f;
+                    if (MODE != SQ_EPI_NONE) b[e] = ok ? __ldg(a.bias + n4 + e) : 0.f;
+                }
+            }
+            if (MODE == SQ_EPI_BIAS_RESIDUAL) {
+                if (a.tma_io) {
+                    const float4 rv = *reinterpret_cast<const float4 *>(chunk);
+                    r[0] = rv.x; r[1] = rv.y; r[2] = rv.z; r[3] = rv.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        r[e] = (row_ok && n4 + e < a.N) ? a.residual[m * a.N + n4 + e] : 0.f;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                o[e] = __float_as_uint(
+                    epilogue_value((int32_t)acc[4 * c + e], xs, w[e], b[e], r[e], MODE));
+        }
+        if (a.tma_io) {
+            *reinterpret_cast<uint4 *>(chunk) = make_uint4(o[0], o[1], o[2], o[3]);
+        } else if (row_ok) {
+            uint32_t *y = static_cast<uint32_t *>(a.Y) + m * a.N;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (n4 + e < a.N) y[n4 + e] = o[e];
+        }
+    }
+    if (a.tma_io) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmY, stg_u32, (int)n, row0);
+            bulk_commit();
+        }
     }
 }
 
+template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const float *__restrict__ sx, const float *__restrict__ sw,
-                   const float *__restrict__ bias, const float *residual, int M, int N, int K,
-                   int mode, int vec_ok, void *Y) {
+                   const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmR,
+                   const EpiArgs args, int K) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    Smem &S = *reinterpret_cast<Smem *>(smem + STAGES * STAGE_BYTES);
+    uint8_t *staging = smem + RING_BYTES;
+    Smem &S = *reinterpret_cast<Smem *>(staging + NUM_EPI_WARPS * STG_BYTES);
     const uint32_t ring = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int M = args.M, N = args.N;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -234,6 +374,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(smem_u32(&S.tfull[b]), 1);
             mbar_init(smem_u32(&S.tempty[b]), NUM_EPI_WARPS);
         }
+        for (int e = 0; e < NUM_EPI_WARPS; ++e) mbar_init(smem_u32(&S.rfull[e]), 1);
         mbar_init(smem_u32(&S.mma_done), 1);
         S.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -289,12 +430,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
             int stage = 0;
-            uint32_t phase = 0, item = 0;
+            uint32_t phase = 0, tph = 0;  // tph: per-buffer use parity bits
             bool issued_any = false;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-                for (int c = 0; c < nchunks; ++c, ++item) {
-                    const uint32_t b = item & 1, use = (item >> 1) & 1;
-                    if (!mbar_wait(smem_u32(&S.tempty[b]), use ^ 1, abort_flag)) goto done_m;
+            int it = 0;
+            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+                for (int c = 0; c < nchunks; ++c) {
+                    const uint32_t b = nchunks == 1 ? (uint32_t)(it & 1) : 0u;
+                    const uint32_t par = (tph >> b) & 1u;
+                    if (!mbar_wait(smem_u32(&S.tempty[b]), par ^ 1, abort_flag)) goto done_m;
+                    tph ^= 1u << b;
                     tc_fence_after();
                     const uint32_t d = tmem_base + b * BN;
                     const int kb0 = c * KB_PER_CHUNK;
@@ -330,93 +474,81 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else {
         // ---------------------------------------------------- epilogue
-        const int q = warp & 3;              // TMEM lane quarter this warp may access
-        const int half = (warp - 2) >> 2;    // which 128 of the 256 columns
-        const int row_in_tile = q * 32 + lane;
-        uint32_t item = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        const int ew = warp - 2;
+        const int q = warp & 3;            // TMEM lane quarter this warp may access
+        const int half = ew >> 2;          // which 128 of the 256 columns
+        uint8_t *stg = staging + ew * STG_BYTES;
+        const uint32_t rbar = smem_u32(&S.rfull[ew]);
+        uint32_t rph = 0, fph = 0;         // residual / accumulator-full parities
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const uint32_t colP = BN;          // int32 partial (multi-chunk shapes)
+        int it = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
             const int m0 = (tile % m_tiles) * BM, n0 = (tile / m_tiles) * BN;
-            int32_t part[128];
-            for (int c = 0; c < nchunks; ++c, ++item) {
-                const uint32_t b = item & 1, use = (item >> 1) & 1;
-                if (!mbar_wait(smem_u32(&S.tfull[b]), use, abort_flag)) goto done_e;
+            const int row0 = m0 + q * 32;
+            const int64_t m = (int64_t)row0 + lane;
+            const int nb = n0 + half * COLS_PER_WARP;
+            if (nchunks == 1) {
+                const uint32_t b = (uint32_t)(it & 1);
+                if (!mbar_wait(smem_u32(&S.tfull[b]), (fph >> b) & 1u, abort_flag)) goto done_e;
+                fph ^= 1u << b;
                 tc_fence_after();
-                const uint32_t taddr =
-                    tmem_base + ((uint32_t)(q * 32) << 16) + b * BN + (uint32_t)(half * 128);
-#pragma unroll
-                for (int s = 0; s < 4; ++s) {
+                const uint32_t tA = tmem_base + lane_off + b * BN + half * COLS_PER_WARP;
+#pragma unroll 1
+                for (int s = 0; s < SLICES; ++s) {
                     uint32_t v[32];
-                    tmem_ld32(taddr + s * 32, v);
+                    tmem_ld32(tA + s * SLICE, v);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        // an exact integer below 2^24 in magnitude
-                        const int32_t a = __float2int_rn(__uint_as_float(v[i]));
-                        part[s * 32 + i] = c == 0 ? a : part[s * 32 + i] + a;
-                    }
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = (uint32_t)__float2int_rn(__uint_as_float(v[j]));
+                    epilogue_slice<MODE>(v, m, nb + s * SLICE, row0, lane, args, &tmY, &tmR, stg,
+                                         rbar, rph, abort_flag);
+                    if (*abort_flag) goto done_e;
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.tempty[b]));
-            }
-            const int64_t m = (int64_t)m0 + row_in_tile;
-            if (m < M) {
-                const int64_t nb = (int64_t)n0 + half * 128;
-                const int64_t rowoff = m * (int64_t)N;
-                if (mode == SQ_EPI_RAW_I32) {
-                    int32_t *y = static_cast<int32_t *>(Y);
+            } else {
+                const uint32_t tA = tmem_base + lane_off + half * COLS_PER_WARP;
+                const uint32_t tP = tmem_base + lane_off + colP + half * COLS_PER_WARP;
+                for (int c = 0; c < nchunks; ++c) {
+                    if (!mbar_wait(smem_u32(&S.tfull[0]), fph & 1u, abort_flag)) goto done_e;
+                    fph ^= 1u;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int s = 0; s < SLICES; ++s) {
+                        uint32_t v[32];
+                        tmem_ld32(tA + s * SLICE, v);
 #pragma unroll
-                    for (int j = 0; j < 128; j += 4) {
-                        const int64_t n = nb + j;
-                        if (vec_ok && n + 3 < N) {
-                            *reinterpret_cast<int4 *>(y + rowoff + n) =
-                                make_int4(part[j], part[j + 1], part[j + 2], part[j + 3]);
-                        } else {
+                        for (int j = 0; j < 32; ++j)
+                            v[j] = (uint32_t)__float2int_rn(__uint_as_float(v[j]));
+                        if (c > 0) {
+                            uint32_t p[32];
+                            tmem_ld32(tP + s * SLICE, p);
 #pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                if (n + e < N) y[rowoff + n + e] = part[j + e];
+                            for (int j = 0; j < 32; ++j) v[j] = (uint32_t)((int32_t)v[j] + (int32_t)p[j]);
                         }
+                        tmem_st32(tP + s * SLICE, v);
                     }
-                } else {
-                    float *y = static_cast<float *>(Y);
-                    const float xs = __ldg(sx + m);
-#pragma unroll
-                    for (int j = 0; j < 128; j += 4) {
-                        const int64_t n = nb + j;
-                        if (n >= N) break;
-                        float r[4] = {0.f, 0.f, 0.f, 0.f}, bb[4] = {0.f, 0.f, 0.f, 0.f};
-                        float ws[4];
-                        if (vec_ok && n + 3 < N) {
-                            const float4 w4 = __ldg(reinterpret_cast<const float4 *>(sw + n));
-                            ws[0] = w4.x; ws[1] = w4.y; ws[2] = w4.z; ws[3] = w4.w;
-                            if (mode != SQ_EPI_NONE) {
-                                const float4 b4 = __ldg(reinterpret_cast<const float4 *>(bias + n));
-                                bb[0] = b4.x; bb[1] = b4.y; bb[2] = b4.z; bb[3] = b4.w;
-                            }
-                            if (mode == SQ_EPI_BIAS_RESIDUAL) {
-                                const float4 r4 =
-                                    *reinterpret_cast<const float4 *>(residual + rowoff + n);
-                                r[0] = r4.x; r[1] = r4.y; r[2] = r4.z; r[3] = r4.w;
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const bool ok = n + e < N;
-                                ws[e] = ok ? __ldg(sw + n + e) : 0.f;
-                                if (mode != SQ_EPI_NONE) bb[e] = ok ? __ldg(bias + n + e) : 0.f;
-                                if (mode == SQ_EPI_BIAS_RESIDUAL)
-                                    r[e] = ok ? residual[rowoff + n + e] : 0.f;
-                            }
-                        }
-                        float o[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            o[e] = epilogue_value(part[j + e], xs, ws[e], bb[e], r[e], mode);
-                        store4(y, rowoff + n, n, N, vec_ok, o[0], o[1], o[2], o[3]);
-                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&S.tempty[0]));
+                }
+                // final pass from the int32 partial; overlaps the next tile's MMAs
+#pragma unroll 1
+                for (int s = 0; s < SLICES; ++s) {
+                    uint32_t v[32];
+                    tmem_ld32(tP + s * SLICE, v);
+                    epilogue_slice<MODE>(v, m, nb + s * SLICE, row0, lane, args, &tmY, &tmR, stg,
+                                         rbar, rph, abort_flag);
+                    if (*abort_flag) goto done_e;
                 }
             }
         }
-    done_e:;
+    done_e:
+        if (lane == 0) bulk_wait0();  // stores complete before the CTA exits
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -450,17 +582,33 @@ sq_status get_encoder() {
     return rc;
 }
 
-// rows x K bf16, K contiguous; box = box_rows x 64 with 128-byte swizzle
-sq_status make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t K, int box_rows) {
-    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+// 2-D row-major tensor of `rows` x `cols` elements, box box_rows x box_cols,
+// 128-byte swizzle (the box's inner extent is 128 bytes).
+sq_status make_map(CUtensorMap *map, CUtensorMapDataType dt, int esize, const void *base,
+                   int64_t rows, int64_t cols, int box_rows, int box_cols) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * esize};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = g_encode(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? SQ_OK : SQ_ERR_CUDA;
+}
+
+template <int MODE>
+sq_status launch_mode(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty,
+                      const CUtensorMap &tr, const EpiArgs &args, int K, int grid, int device,
+                      cudaStream_t st) {
+    static int attr_dev = -1;
+    if (attr_dev != device) {
+        if (cudaFuncSetAttribute(gemm_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_BYTES) != cudaSuccess)
+            return SQ_ERR_CUDA;
+        attr_dev = device;
+    }
+    gemm_tc_kernel<MODE><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, ty, tr, args, K);
+    return cuda_status(cudaGetLastError());
 }
 
 }  // namespace
@@ -473,27 +621,47 @@ sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const __nv_b
     if (rc != SQ_OK) return rc;
     DeviceInfo di;
     if ((rc = device_info(&di)) != SQ_OK) return rc;
-    static int attr_dev = -1;
-    if (attr_dev != di.device) {
-        if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES) != cudaSuccess)
-            return SQ_ERR_CUDA;
-        attr_dev = di.device;
+    EpiArgs args;
+    args.sx = sx;
+    args.sw = sw;
+    args.bias = bias;
+    args.residual = residual;
+    args.Y = Y;
+    args.M = (int)M;
+    args.N = (int)N;
+    // TMA staging for Y (and the residual) needs 16-byte rows and aligned bases;
+    // the vector loads of the scales and bias need them aligned too
+    args.tma_io = (N % 4 == 0) && aligned16(Y) && (mode == SQ_EPI_RAW_I32 || aligned16(sw)) &&
+                  (bias == nullptr || aligned16(bias)) &&
+                  (residual == nullptr || aligned16(residual));
+    CUtensorMap ta, tb, ty, tr;
+    if ((rc = make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Xop, M, K, BM, BK)) != SQ_OK)
+        return rc;
+    if ((rc = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wop, N, K, BN, BK)) != SQ_OK)
+        return rc;
+    ty = ta;  // unused placeholders unless tma_io
+    tr = ta;
+    if (args.tma_io) {
+        const CUtensorMapDataType yt = mode == SQ_EPI_RAW_I32 ? CU_TENSOR_MAP_DATA_TYPE_INT32
+                                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+        if ((rc = make_map(&ty, yt, 4, Y, M, N, SLICE, SLICE)) != SQ_OK) return rc;
+        if (mode == SQ_EPI_BIAS_RESIDUAL &&
+            (rc = make_map(&tr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, residual, M, N, SLICE,
+                           SLICE)) != SQ_OK)
+            return rc;
     }
-    CUtensorMap ta, tb;
-    if ((rc = make_map(&ta, Xop, M, K, BM)) != SQ_OK) return rc;
-    if ((rc = make_map(&tb, Wop, N, K, BN)) != SQ_OK) return rc;
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     if (tiles > 0x7fffffff) return SQ_ERR_UNSUPPORTED;
     const int grid = (int)std::min<int64_t>(tiles, di.sms);
-    // 16-byte vector loads/stores of the epilogue need N % 4 == 0 and aligned vectors
-    const int vec_ok = (N % 4 == 0) && aligned16(Y) &&
-                       (mode == SQ_EPI_RAW_I32 || aligned16(sw)) &&
-                       (bias == nullptr || aligned16(bias)) &&
-                       (residual == nullptr || aligned16(residual));
-    gemm_tc_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, sx, sw, bias, residual, (int)M,
-                                                      (int)N, (int)K, mode, vec_ok, Y);
-    return cuda_status(cudaGetLastError());
+    switch (mode) {
+    case SQ_EPI_NONE: return launch_mode<SQ_EPI_NONE>(ta, tb, ty, tr, args, (int)K, grid, di.device, st);
+    case SQ_EPI_BIAS: return launch_mode<SQ_EPI_BIAS>(ta, tb, ty, tr, args, (int)K, grid, di.device, st);
+    case SQ_EPI_BIAS_GELU:
+        return launch_mode<SQ_EPI_BIAS_GELU>(ta, tb, ty, tr, args, (int)K, grid, di.device, st);
+    case SQ_EPI_BIAS_RESIDUAL:
+        return launch_mode<SQ_EPI_BIAS_RESIDUAL>(ta, tb, ty, tr, args, (int)K, grid, di.device, st);
+    default: return launch_mode<SQ_EPI_RAW_I32>(ta, tb, ty, tr, args, (int)K, grid, di.device, st);
+    }
 }
 
 sq_status gemm_tc_take_error(cudaStream_t st) {

@@ -23,22 +23,38 @@ namespace sq {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kVPT = 8;  // float4 per thread held in registers (K <= 256*8*4)
+constexpr int kMaxVPT = 8;  // float4 per thread held in registers: K <= 256 * 8 * 4
 
 __device__ __forceinline__ float smooth_one(float x, float s, int direction) {
     // activations: x / s (IEEE division); weights: x * s
     return direction == 0 ? __fdiv_rn(x, s) : __fmul_rn(x, s);
 }
 
-__device__ __forceinline__ int code_of(float v, float scale) {
-    int c = __float2int_rn(__fdiv_rn(v, scale));  // round half to even
+// round_half_even(fl(v / scale)), clamped to [-127, 127], with the division
+// replaced by a multiplication where that provably gives the same integer.
+// With r = fl(1/scale) (correctly rounded) and p = fl(v * r), p differs from
+// the exact quotient v/scale by a relative 2^-23 + 2^-48 at most, and so does
+// fl(v/scale) by 2^-24: for |v/scale| <= 128 the two lie within 2.3e-5 of each
+// other.  Their integer roundings can differ only if a half-integer lies
+// between them, so when p is farther than 2^-14 from every half-integer the
+// rounded p is the answer; otherwise (rare) the IEEE division decides.
+__device__ __forceinline__ int code_of(float v, float scale, float rscale) {
+    const float p = __fmul_rn(v, rscale);
+    const float k = rintf(p);
+    const float d = fabsf(__fsub_rn(p, k));  // exact (Sterbenz)
+    int c;
+    if (fabsf(d - 0.5f) > 6.103515625e-05f) {
+        c = (int)k;
+    } else {
+        c = __float2int_rn(__fdiv_rn(v, scale));  // round half to even
+    }
     return max(-127, min(127, c));
 }
 
-__device__ __forceinline__ void store_codes(float4 v, float scale, int64_t off4, int8_t *q,
-                                            __nv_bfloat16 *op) {
-    int c0 = code_of(v.x, scale), c1 = code_of(v.y, scale);
-    int c2 = code_of(v.z, scale), c3 = code_of(v.w, scale);
+__device__ __forceinline__ void store_codes(float4 v, float scale, float rscale, int64_t off4,
+                                            int8_t *q, __nv_bfloat16 *op) {
+    int c0 = code_of(v.x, scale, rscale), c1 = code_of(v.y, scale, rscale);
+    int c2 = code_of(v.z, scale, rscale), c3 = code_of(v.w, scale, rscale);
     if (q) {
         uint32_t packed = (uint32_t)(c0 & 0xff) | ((uint32_t)(c1 & 0xff) << 8) |
                           ((uint32_t)(c2 & 0xff) << 16) | ((uint32_t)(c3 & 0xff) << 24);
@@ -72,7 +88,7 @@ __device__ __forceinline__ float group_max(float m, int tpr, float *red) {
 }
 
 // Registers path: K4 = K/4 <= tpr * kVPT.
-template <int DIR>
+template <int DIR, int kVPT>
 __global__ void __launch_bounds__(kThreads) quantize_rows_reg(
     const float *__restrict__ A, const float *__restrict__ s, int64_t rows, int K4, int tpr,
     int8_t *__restrict__ q, float *__restrict__ scale, __nv_bfloat16 *__restrict__ op) {
@@ -111,18 +127,19 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_reg(
         }
         m = group_max(m, tpr, red);
         const float sc = m == 0.0f ? 1.0f : __fdiv_rn(m, 127.0f);
+        const float rsc = __frcp_rn(sc);
         if (valid) {
             if (t == 0) scale[row] = sc;
 #pragma unroll
             for (int i = 0; i < kVPT; ++i) {
                 int j = t + i * tpr;
-                if (j < K4) store_codes(v[i], sc, row * K4 + j, q, op);
+                if (j < K4) store_codes(v[i], sc, rsc, row * K4 + j, q, op);
             }
         }
     }
 }
 
-// Long rows (K4 > kThreads * kVPT): one block per row, the row is read twice.
+// Long rows (K4 > kThreads * kMaxVPT): one block per row, the row is read twice.
 template <int DIR>
 __global__ void __launch_bounds__(kThreads) quantize_rows_loop(
     const float *__restrict__ A, const float *__restrict__ s, int64_t rows, int K4,
@@ -141,12 +158,13 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_loop(
         }
         m = group_max(m, kThreads, red);
         const float sc = m == 0.0f ? 1.0f : __fdiv_rn(m, 127.0f);
+        const float rsc = __frcp_rn(sc);
         if (threadIdx.x == 0) scale[row] = sc;
         for (int j = threadIdx.x; j < K4; j += kThreads) {
             float4 x = __ldcs(a4 + j), sv = __ldg(s4 + j);
             float4 v = make_float4(smooth_one(x.x, sv.x, DIR), smooth_one(x.y, sv.y, DIR),
                                    smooth_one(x.z, sv.z, DIR), smooth_one(x.w, sv.w, DIR));
-            store_codes(v, sc, row * K4 + j, q, op);
+            store_codes(v, sc, rsc, row * K4 + j, q, op);
         }
     }
 }
@@ -191,15 +209,23 @@ sq_status launch_quantize_rows(int direction, const float *A, const float *s, in
     sq_status rc = device_info(&di);
     if (rc != SQ_OK) return rc;
     const int K4 = (int)(K / 4);
-    if (K4 <= kThreads * kVPT) {
+    if (K4 <= kThreads * kMaxVPT) {
+        // 4 float4 per thread when that covers the row with one block (more
+        // resident warps), else 8
+        const bool small = K4 <= kThreads * 4;
+        const int vpt = small ? 4 : 8;
         int tpr = 32;
-        while (tpr * kVPT < K4) tpr <<= 1;
+        while (tpr * vpt < K4) tpr <<= 1;
         const int rpb = kThreads / tpr;
         const int64_t tiles = (rows + rpb - 1) / rpb;
-        auto kern = direction == 0 ? quantize_rows_reg<0> : quantize_rows_reg<1>;
-        static int per_sm[2] = {0, 0};
-        if (!per_sm[direction]) per_sm[direction] = resident_blocks(kern);
-        const int64_t grid = std::min<int64_t>(tiles, (int64_t)di.sms * per_sm[direction]);
+        void (*kern)(const float *, const float *, int64_t, int, int, int8_t *, float *,
+                     __nv_bfloat16 *);
+        if (direction == 0) kern = small ? quantize_rows_reg<0, 4> : quantize_rows_reg<0, 8>;
+        else kern = small ? quantize_rows_reg<1, 4> : quantize_rows_reg<1, 8>;
+        static int per_sm[2][2] = {{0, 0}, {0, 0}};
+        int &occ = per_sm[direction][small ? 0 : 1];
+        if (!occ) occ = resident_blocks(kern);
+        const int64_t grid = std::min<int64_t>(tiles, (int64_t)di.sms * occ);
         kern<<<(unsigned)grid, kThreads, 0, st>>>(A, s, rows, K4, tpr, q, scale, op);
     } else {
         auto kern = direction == 0 ? quantize_rows_loop<0> : quantize_rows_loop<1>;

@@ -77,6 +77,36 @@ def test_quantize_degenerate_rows(sq):
     assert sx.cpu().numpy()[0] == 1.0 and not Xq.cpu().numpy()[0].any()
 
 
+def test_quantize_ties_and_near_ties(sq):
+    """Codes whose quotient is a half-integer or within a few ulp of one:
+    the cases where round-half-to-even decides and a rounding slip shows."""
+    K = 256
+    ties = np.concatenate([np.arange(-127, 127) + 0.5, [127.0, 0.0]]).astype(np.float32)
+    rows = [ties,                                   # scale 1: exact ties
+            ties * np.float32(2.0 ** -7),           # scale 2^-7: exact ties
+            ties * np.float32(1 + 2.0 ** -20),      # just above the ties
+            ties * np.float32(1 - 2.0 ** -20)]      # just below
+    rng = np.random.default_rng(5)
+    sc = np.float32(0.7531)
+    k = rng.integers(-126, 126, K).astype(np.float32)
+    r = ((k + np.float32(0.5)) * sc).astype(np.float32)
+    r[0] = np.float32(127) * sc                     # amax -> scale close to sc
+    rows.append(r)
+    for ulps in (-2, -1, 1, 2):                     # quotients within ulps of a tie
+        rows.append(np.nextafter(r, np.float32(np.inf) if ulps > 0 else np.float32(-np.inf))
+                    if abs(ulps) == 1 else
+                    np.nextafter(np.nextafter(r, np.float32(np.sign(ulps) * np.inf)),
+                                 np.float32(np.sign(ulps) * np.inf)))
+    X = np.stack(rows).astype(np.float32)
+    s = np.ones(K, np.float32)
+    q_ref, sx_ref = oracle.quantize_rows(X, s, "act")
+    Xq, sx, Xop = sq.quantize_act(to_dev(X), to_dev(s))
+    assert_codes_equal(Xq.cpu().numpy(), q_ref, "Xq")
+    assert_bits_equal(sx.cpu().numpy(), sx_ref, "x_scale")
+    assert_codes_equal(op_as_int(Xop), q_ref, "Xop")
+    np.testing.assert_array_equal(q_ref[0, :254], np.round(ties[:254]).astype(np.int8))
+
+
 @pytest.mark.parametrize("N,K", [(1, 16), (5, 48), (1024, 1024), (3072, 1024), (768, 3072),
                                  (9, 8208)])
 def test_pack_weight_parity(sq, N, K):
