@@ -33,9 +33,8 @@
 //              GELU / residual, stores) overlaps the next tile's first chunk.
 // Epilogue I/O per 32 x 32 slice: results are written to a per-warp 4 KB
 // staging tile in shared memory (128-byte swizzle, conflict-free) and stored
-// with one TMA bulk tensor store; the residual slice arrives by TMA load into
-// the same tile.  Shapes whose rows are not 16-byte multiples (N % 4 != 0)
-// take plain per-element loads and stores instead.
+// with one TMA bulk tensor store.  Shapes whose rows are not 16-byte
+// multiples (N % 4 != 0) take plain per-element stores instead.
 // Every wait is bounded (about 4 s of %globaltimer); on expiry the kernel
 // records SQ_ERR_TIMEOUT in a device word, lets its issued copies and MMAs
 // drain, frees its tensor memory and returns.
@@ -248,7 +247,6 @@ struct Smem {
     uint64_t empty[STAGES];
     uint64_t tfull[2];
     uint64_t tempty[2];
-    uint64_t rfull[NUM_EPI_WARPS];  // residual slice landed in a warp's staging tile
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -262,100 +260,159 @@ struct EpiArgs {
     int tma_io;  // 1: TMA staging for Y (and the residual); 0: plain per-element I/O
 };
 
-// Turns one 32 x 32 slice of exact int32 sums (this thread's row, 32
-// consecutive columns starting at n) into the epilogue's outputs and stores
-// them, four columns at a time.  `stg` is the warp's staging tile (row
-// `lane` holds this thread's 32 values, 16-byte chunk c at c ^ (lane & 7));
-// `rbar`/`rph` are its residual barrier and parity.
+// erf by Abramowitz & Stegun, Handbook of Mathematical Functions, formula
+// 7.1.26 (after Hastings): erf(x) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5))))
+// exp(-x^2), t = 1 / (1 + p x), x >= 0, odd extension for x < 0; absolute
+// error <= 1.5e-7.  Branch-free, so a warp never splits across ranges.
+__device__ __forceinline__ float erf_as7126(float x) {
+    const float ax = fabsf(x);
+    const float t = __fdividef(1.0f, fmaf(0.3275911f, ax, 1.0f));
+    float poly = fmaf(1.061405429f, t, -1.453152027f);
+    poly = fmaf(poly, t, 1.421413741f);
+    poly = fmaf(poly, t, -0.284496736f);
+    poly = fmaf(poly, t, 0.254829592f);
+    poly *= t;
+    const float r = fmaf(-poly, __expf(-ax * ax), 1.0f);
+    return copysignf(r, x);
+}
+
+// Per-column epilogue operands of one tile half, spread over the warp: lane j
+// holds column (nb + 32 s + j) for slice s; a slice broadcasts them with
+// shuffles.  Loaded before the accumulator wait, so their latency hides.
+struct ColParams {
+    float w[SLICES];
+    float b[SLICES];
+};
+
 template <int MODE>
-__device__ __forceinline__ void epilogue_slice(const uint32_t (&acc)[32], int64_t m, int64_t n,
-                                               int row0, int lane, const EpiArgs &a,
-                                               const CUtensorMap *tmY, const CUtensorMap *tmR,
-                                               uint8_t *stg, uint32_t rbar, uint32_t &rph,
-                                               volatile int *abort_flag) {
-    if (n >= a.N || row0 >= a.M) return;  // slice wholly outside Y: nothing to do
-    const uint32_t stg_u32 = smem_u32(stg);
+__device__ __forceinline__ void load_col_params(ColParams &cp, const EpiArgs &a, int nb,
+                                                int lane) {
+#pragma unroll
+    for (int s = 0; s < SLICES; ++s) {
+        const int n = nb + s * SLICE + lane;
+        const bool ok = n < a.N;
+        cp.w[s] = (MODE != SQ_EPI_RAW_I32 && ok) ? __ldg(a.sw + n) : 0.f;
+        cp.b[s] = (MODE != SQ_EPI_RAW_I32 && MODE != SQ_EPI_NONE && ok) ? __ldg(a.bias + n) : 0.f;
+    }
+}
+
+// residual row segment of one slice: 32 floats of this thread's row
+__device__ __forceinline__ void load_residual(float4 (&r)[8], const EpiArgs &a, int64_t m,
+                                              int64_t n) {
+    const bool row_ok = m < a.M;
+    const float *rrow = a.residual + (row_ok ? m : 0) * (int64_t)a.N;
+    const bool vec = a.tma_io && n + 31 < a.N;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const int64_t n4 = n + 4 * c;
+        if (vec && row_ok) {
+            r[c] = *reinterpret_cast<const float4 *>(rrow + n4);
+        } else {
+            r[c].x = (row_ok && n4 < a.N) ? rrow[n4] : 0.f;
+            r[c].y = (row_ok && n4 + 1 < a.N) ? rrow[n4 + 1] : 0.f;
+            r[c].z = (row_ok && n4 + 2 < a.N) ? rrow[n4 + 2] : 0.f;
+            r[c].w = (row_ok && n4 + 3 < a.N) ? rrow[n4 + 3] : 0.f;
+        }
+    }
+}
+
+// Dequantise one 32 x 32 slice and store it: this thread's row m, the 32
+// consecutive columns from n.  `v` holds the exact integer sums, as fp32
+// (single-chunk accumulators straight from tensor memory) or as int32
+// (INT_IN: the partial of multi-chunk shapes).  The wait for this warp's
+// previous TMA store to release the staging tile comes after the arithmetic,
+// so the store's latency hides behind it.  Staging tile row `lane` holds this
+// thread's 32 values, 16-byte chunk c at c ^ (lane & 7) (the TMA 128-byte
+// swizzle: conflict-free for the warp).
+template <int MODE, bool INT_IN>
+__device__ __forceinline__ void epilogue_slice(uint32_t (&v)[32], int64_t m, int64_t n,
+                                               int row0, int lane, const EpiArgs &a, float xs,
+                                               float wl, float bl, const float4 (&r4)[8],
+                                               const CUtensorMap *tmY, uint8_t *stg) {
+    if (n >= a.N || row0 >= a.M) return;  // slice wholly outside Y
+    if (MODE == SQ_EPI_RAW_I32) {
+        if (!INT_IN) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = (uint32_t)__float2int_rn(__uint_as_float(v[j]));
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float w = __shfl_sync(0xffffffffu, wl, j);
+            // the exact integer sum as fp32 (|acc| < 2^31: one rounding at most)
+            const float x = INT_IN ? __int2float_rn((int32_t)v[j]) : __uint_as_float(v[j]);
+            const float sc = __fmul_rn(xs, w);
+            float o;
+            if (MODE == SQ_EPI_NONE) {
+                o = __fmul_rn(x, sc);
+            } else {
+                const float b = __shfl_sync(0xffffffffu, bl, j);
+                const float t = __fmaf_rn(x, sc, b);
+                if (MODE == SQ_EPI_BIAS) {
+                    o = t;
+                } else if (MODE == SQ_EPI_BIAS_GELU) {
+                    const float h = 0.5f * t;
+                    o = __fmaf_rn(h, erf_as7126(t * 0.70710678118654752f), h);
+                } else {
+                    const float rr = (j & 3) == 0 ? r4[j >> 2].x
+                                   : (j & 3) == 1 ? r4[j >> 2].y
+                                   : (j & 3) == 2 ? r4[j >> 2].z : r4[j >> 2].w;
+                    o = __fadd_rn(t, rr);
+                }
+            }
+            v[j] = __float_as_uint(o);
+        }
+    }
     if (a.tma_io) {
         // the previous TMA store of this warp must have finished reading the tile
         if (lane == 0) bulk_wait_read0();
         __syncwarp();
-        if (MODE == SQ_EPI_BIAS_RESIDUAL) {
-            if (lane == 0) {
-                mbar_expect_tx(rbar, STG_BYTES);
-                tma_load_2d(stg_u32, tmR, rbar, (int)n, row0);
-            }
-            const bool ok = mbar_wait(rbar, rph, abort_flag);
-            rph ^= 1;
-            if (!ok) mbar_drain(rbar, rph ^ 1);  // the copy may still land: let it
-        }
-    }
-    const bool row_ok = m < a.M;
-    const bool vec = a.tma_io && n + 31 < a.N;  // whole slice in range, 16-byte aligned
-    const float xs = (MODE != SQ_EPI_RAW_I32 && row_ok) ? __ldg(a.sx + m) : 0.f;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const int64_t n4 = n + 4 * c;
-        uint8_t *chunk = stg + lane * 128 + ((c ^ (lane & 7)) << 4);
-        uint32_t o[4];
-        if (MODE == SQ_EPI_RAW_I32) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) o[e] = acc[4 * c + e];
-        } else {
-            float w[4], b[4] = {0.f, 0.f, 0.f, 0.f}, r[4] = {0.f, 0.f, 0.f, 0.f};
-            if (vec) {
-                const float4 wv = __ldg(reinterpret_cast<const float4 *>(a.sw + n4));
-                w[0] = wv.x; w[1] = wv.y; w[2] = wv.z; w[3] = wv.w;
-                if (MODE != SQ_EPI_NONE) {
-                    const float4 bv = __ldg(reinterpret_cast<const float4 *>(a.bias + n4));
-                    b[0] = bv.x; b[1] = bv.y; b[2] = bv.z; b[3] = bv.w;
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const bool ok = n4 + e < a.N;
-                    w[e] = ok ? __ldg(a.sw + n4 + e) : 0.f;
-                    if (MODE != SQ_EPI_NONE) b[e] = ok ? __ldg(a.bias + n4 + e) : 0.f;
-                }
-            }
-            if (MODE == SQ_EPI_BIAS_RESIDUAL) {
-                if (a.tma_io) {
-                    const float4 rv = *reinterpret_cast<const float4 *>(chunk);
-                    r[0] = rv.x; r[1] = rv.y; r[2] = rv.z; r[3] = rv.w;
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        r[e] = (row_ok && n4 + e < a.N) ? a.residual[m * a.N + n4 + e] : 0.f;
-                }
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                o[e] = __float_as_uint(
-                    epilogue_value((int32_t)acc[4 * c + e], xs, w[e], b[e], r[e], MODE));
-        }
-        if (a.tma_io) {
-            *reinterpret_cast<uint4 *>(chunk) = make_uint4(o[0], o[1], o[2], o[3]);
-        } else if (row_ok) {
-            uint32_t *y = static_cast<uint32_t *>(a.Y) + m * a.N;
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (n4 + e < a.N) y[n4 + e] = o[e];
-        }
-    }
-    if (a.tma_io) {
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4 *>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            tma_store_2d(tmY, stg_u32, (int)n, row0);
+            tma_store_2d(tmY, smem_u32(stg), (int)n, row0);
             bulk_commit();
         }
+    } else if (m < a.M) {
+        uint32_t *y = static_cast<uint32_t *>(a.Y) + m * a.N;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (n + j < a.N) y[n + j] = v[j];
+    }
+}
+
+// The four slices of this warp's part of a tile, reading tensor memory at
+// `taddr` (fp32 sums, or int32 with INT_IN).
+template <int MODE, bool INT_IN>
+__device__ __forceinline__ void epilogue_tile(uint32_t taddr, int64_t m, int nb, int row0,
+                                              int lane, const EpiArgs &a, float xs,
+                                              const ColParams &cp, float4 (&rnext)[8],
+                                              const CUtensorMap *tmY, uint8_t *stg) {
+#pragma unroll 1
+    for (int s = 0; s < SLICES; ++s) {
+        float4 rcur[8];
+        if (MODE == SQ_EPI_BIAS_RESIDUAL) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) rcur[c] = rnext[c];
+            if (s + 1 < SLICES) load_residual(rnext, a, m, nb + (s + 1) * SLICE);
+        }
+        const float wl = s == 0 ? cp.w[0] : s == 1 ? cp.w[1] : s == 2 ? cp.w[2] : cp.w[3];
+        const float bl = s == 0 ? cp.b[0] : s == 1 ? cp.b[1] : s == 2 ? cp.b[2] : cp.b[3];
+        uint32_t v[32];
+        tmem_ld32(taddr + s * SLICE, v);
+        epilogue_slice<MODE, INT_IN>(v, m, nb + s * SLICE, row0, lane, a, xs, wl, bl, rcur, tmY,
+                                     stg);
     }
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmR,
-                   const EpiArgs args, int K) {
+                   const __grid_constant__ CUtensorMap tmY, const EpiArgs args, int K) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -374,7 +431,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(smem_u32(&S.tfull[b]), 1);
             mbar_init(smem_u32(&S.tempty[b]), NUM_EPI_WARPS);
         }
-        for (int e = 0; e < NUM_EPI_WARPS; ++e) mbar_init(smem_u32(&S.rfull[e]), 1);
         mbar_init(smem_u32(&S.mma_done), 1);
         S.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -478,8 +534,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int q = warp & 3;            // TMEM lane quarter this warp may access
         const int half = ew >> 2;          // which 128 of the 256 columns
         uint8_t *stg = staging + ew * STG_BYTES;
-        const uint32_t rbar = smem_u32(&S.rfull[ew]);
-        uint32_t rph = 0, fph = 0;         // residual / accumulator-full parities
+        uint32_t fph = 0;                  // accumulator-full parities
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const uint32_t colP = BN;          // int32 partial (multi-chunk shapes)
         int it = 0;
@@ -488,23 +543,19 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int row0 = m0 + q * 32;
             const int64_t m = (int64_t)row0 + lane;
             const int nb = n0 + half * COLS_PER_WARP;
+            // operands that do not depend on the accumulators: fetch them now
+            ColParams cp;
+            load_col_params<MODE>(cp, args, nb, lane);
+            const float xs = (MODE != SQ_EPI_RAW_I32 && m < M) ? __ldg(args.sx + m) : 0.f;
+            float4 rnext[8];
+            if (MODE == SQ_EPI_BIAS_RESIDUAL) load_residual(rnext, args, m, nb);
             if (nchunks == 1) {
                 const uint32_t b = (uint32_t)(it & 1);
                 if (!mbar_wait(smem_u32(&S.tfull[b]), (fph >> b) & 1u, abort_flag)) goto done_e;
                 fph ^= 1u << b;
                 tc_fence_after();
                 const uint32_t tA = tmem_base + lane_off + b * BN + half * COLS_PER_WARP;
-#pragma unroll 1
-                for (int s = 0; s < SLICES; ++s) {
-                    uint32_t v[32];
-                    tmem_ld32(tA + s * SLICE, v);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        v[j] = (uint32_t)__float2int_rn(__uint_as_float(v[j]));
-                    epilogue_slice<MODE>(v, m, nb + s * SLICE, row0, lane, args, &tmY, &tmR, stg,
-                                         rbar, rph, abort_flag);
-                    if (*abort_flag) goto done_e;
-                }
+                epilogue_tile<MODE, false>(tA, m, nb, row0, lane, args, xs, cp, rnext, &tmY, stg);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.tempty[b]));
@@ -536,14 +587,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (lane == 0) mbar_arrive(smem_u32(&S.tempty[0]));
                 }
                 // final pass from the int32 partial; overlaps the next tile's MMAs
-#pragma unroll 1
-                for (int s = 0; s < SLICES; ++s) {
-                    uint32_t v[32];
-                    tmem_ld32(tP + s * SLICE, v);
-                    epilogue_slice<MODE>(v, m, nb + s * SLICE, row0, lane, args, &tmY, &tmR, stg,
-                                         rbar, rph, abort_flag);
-                    if (*abort_flag) goto done_e;
-                }
+                epilogue_tile<MODE, true>(tP, m, nb, row0, lane, args, xs, cp, rnext, &tmY, stg);
             }
         }
     done_e:
@@ -598,8 +642,7 @@ sq_status make_map(CUtensorMap *map, CUtensorMapDataType dt, int esize, const vo
 
 template <int MODE>
 sq_status launch_mode(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty,
-                      const CUtensorMap &tr, const EpiArgs &args, int K, int grid, int device,
-                      cudaStream_t st) {
+                      const EpiArgs &args, int K, int grid, int device, cudaStream_t st) {
     static int attr_dev = -1;
     if (attr_dev != device) {
         if (cudaFuncSetAttribute(gemm_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -607,7 +650,7 @@ sq_status launch_mode(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
             return SQ_ERR_CUDA;
         attr_dev = device;
     }
-    gemm_tc_kernel<MODE><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, ty, tr, args, K);
+    gemm_tc_kernel<MODE><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, ty, args, K);
     return cuda_status(cudaGetLastError());
 }
 
@@ -634,33 +677,28 @@ sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const __nv_b
     args.tma_io = (N % 4 == 0) && aligned16(Y) && (mode == SQ_EPI_RAW_I32 || aligned16(sw)) &&
                   (bias == nullptr || aligned16(bias)) &&
                   (residual == nullptr || aligned16(residual));
-    CUtensorMap ta, tb, ty, tr;
+    CUtensorMap ta, tb, ty;
     if ((rc = make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Xop, M, K, BM, BK)) != SQ_OK)
         return rc;
     if ((rc = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wop, N, K, BN, BK)) != SQ_OK)
         return rc;
-    ty = ta;  // unused placeholders unless tma_io
-    tr = ta;
+    ty = ta;  // unused placeholder unless tma_io
     if (args.tma_io) {
         const CUtensorMapDataType yt = mode == SQ_EPI_RAW_I32 ? CU_TENSOR_MAP_DATA_TYPE_INT32
                                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
         if ((rc = make_map(&ty, yt, 4, Y, M, N, SLICE, SLICE)) != SQ_OK) return rc;
-        if (mode == SQ_EPI_BIAS_RESIDUAL &&
-            (rc = make_map(&tr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, residual, M, N, SLICE,
-                           SLICE)) != SQ_OK)
-            return rc;
     }
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     if (tiles > 0x7fffffff) return SQ_ERR_UNSUPPORTED;
     const int grid = (int)std::min<int64_t>(tiles, di.sms);
     switch (mode) {
-    case SQ_EPI_NONE: return launch_mode<SQ_EPI_NONE>(ta, tb, ty, tr, args, (int)K, grid, di.device, st);
-    case SQ_EPI_BIAS: return launch_mode<SQ_EPI_BIAS>(ta, tb, ty, tr, args, (int)K, grid, di.device, st);
+    case SQ_EPI_NONE: return launch_mode<SQ_EPI_NONE>(ta, tb, ty, args, (int)K, grid, di.device, st);
+    case SQ_EPI_BIAS: return launch_mode<SQ_EPI_BIAS>(ta, tb, ty, args, (int)K, grid, di.device, st);
     case SQ_EPI_BIAS_GELU:
-        return launch_mode<SQ_EPI_BIAS_GELU>(ta, tb, ty, tr, args, (int)K, grid, di.device, st);
+        return launch_mode<SQ_EPI_BIAS_GELU>(ta, tb, ty, args, (int)K, grid, di.device, st);
     case SQ_EPI_BIAS_RESIDUAL:
-        return launch_mode<SQ_EPI_BIAS_RESIDUAL>(ta, tb, ty, tr, args, (int)K, grid, di.device, st);
-    default: return launch_mode<SQ_EPI_RAW_I32>(ta, tb, ty, tr, args, (int)K, grid, di.device, st);
+        return launch_mode<SQ_EPI_BIAS_RESIDUAL>(ta, tb, ty, args, (int)K, grid, di.device, st);
+    default: return launch_mode<SQ_EPI_RAW_I32>(ta, tb, ty, args, (int)K, grid, di.device, st);
     }
 }
 

@@ -30,39 +30,40 @@ __device__ __forceinline__ float smooth_one(float x, float s, int direction) {
     return direction == 0 ? __fdiv_rn(x, s) : __fmul_rn(x, s);
 }
 
-// round_half_even(fl(v / scale)), clamped to [-127, 127], with the division
-// replaced by a multiplication where that provably gives the same integer.
-// With r = fl(1/scale) (correctly rounded) and p = fl(v * r), p differs from
-// the exact quotient v/scale by a relative 2^-23 + 2^-48 at most, and so does
-// fl(v/scale) by 2^-24: for |v/scale| <= 128 the two lie within 2.3e-5 of each
-// other.  Their integer roundings can differ only if a half-integer lies
-// between them, so when p is farther than 2^-14 from every half-integer the
-// rounded p is the answer; otherwise (rare) the IEEE division decides.
-__device__ __forceinline__ int code_of(float v, float scale, float rscale) {
+// round_half_even(fl(v / scale)), clamped to [-127, 127], returned as an
+// integer-valued float, with the division replaced by a multiplication where
+// that provably gives the same integer.  With r = fl(1/scale) (correctly
+// rounded) and p = fl(v * r), p differs from the exact quotient v/scale by a
+// relative 2^-23 + 2^-48 at most, and fl(v/scale) by 2^-24: for
+// |v/scale| <= 128 the two lie within 2.3e-5 of each other.  Their integer
+// roundings can differ only if a half-integer lies between them, so when p is
+// farther than 2^-14 from every half-integer the rounded p is the answer;
+// otherwise (rare) the IEEE division decides.  (|v| <= amax and
+// scale = fl(amax/127) keep every quotient within 127 * (1 + 2^-23), so the
+// clamp never acts on the fast path.)
+__device__ __forceinline__ float code_of(float v, float scale, float rscale) {
     const float p = __fmul_rn(v, rscale);
     const float k = rintf(p);
-    const float d = fabsf(__fsub_rn(p, k));  // exact (Sterbenz)
-    int c;
-    if (fabsf(d - 0.5f) > 6.103515625e-05f) {
-        c = (int)k;
-    } else {
-        c = __float2int_rn(__fdiv_rn(v, scale));  // round half to even
-    }
-    return max(-127, min(127, c));
+    if (fabsf(__fsub_rn(p, k)) <= 0.49993896484375f) return k;  // 0.5 - 2^-14
+    const float e = rintf(__fdiv_rn(v, scale));                 // round half to even
+    return fminf(127.0f, fmaxf(-127.0f, e));
 }
 
 __device__ __forceinline__ void store_codes(float4 v, float scale, float rscale, int64_t off4,
                                             int8_t *q, __nv_bfloat16 *op) {
-    int c0 = code_of(v.x, scale, rscale), c1 = code_of(v.y, scale, rscale);
-    int c2 = code_of(v.z, scale, rscale), c3 = code_of(v.w, scale, rscale);
+    const float c0 = code_of(v.x, scale, rscale), c1 = code_of(v.y, scale, rscale);
+    const float c2 = code_of(v.z, scale, rscale), c3 = code_of(v.w, scale, rscale);
     if (q) {
-        uint32_t packed = (uint32_t)(c0 & 0xff) | ((uint32_t)(c1 & 0xff) << 8) |
-                          ((uint32_t)(c2 & 0xff) << 16) | ((uint32_t)(c3 & 0xff) << 24);
+        const uint32_t packed = (uint32_t)(__float2int_rn(c0) & 0xff) |
+                                ((uint32_t)(__float2int_rn(c1) & 0xff) << 8) |
+                                ((uint32_t)(__float2int_rn(c2) & 0xff) << 16) |
+                                ((uint32_t)(__float2int_rn(c3) & 0xff) << 24);
         reinterpret_cast<uint32_t *>(q)[off4] = packed;
     }
     if (op) {
-        __nv_bfloat162 lo = __floats2bfloat162_rn((float)c0, (float)c1);
-        __nv_bfloat162 hi = __floats2bfloat162_rn((float)c2, (float)c3);
+        // integers |c| <= 127 are exact in bf16
+        __nv_bfloat162 lo = __floats2bfloat162_rn(c0, c1);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(c2, c3);
         uint2 u;
         u.x = *reinterpret_cast<uint32_t *>(&lo);
         u.y = *reinterpret_cast<uint32_t *>(&hi);

@@ -215,6 +215,25 @@ def test_epilogue_modes(sq, path, mode, M, N, K):
 
 
 @pytest.mark.parametrize("path", PATHS)
+def test_gelu_sweep(sq, path):
+    """GELU(erf) over pre-activations spanning [-10, 10], against the oracle's
+    double-precision erf."""
+    M, N, K = 128, 256, 16
+    xq = np.zeros((M, K), np.int8)
+    wq = np.zeros((N, K), np.int8)
+    xq[:, 0] = np.arange(M) - 64                    # -64 .. 63
+    wq[:, 0] = (np.arange(N) % 127) - 63            # -63 .. 63
+    sx = np.ones(M, np.float32)
+    sw = np.full(N, 1.0 / 400.0, np.float32)        # d in about [-10, 10]
+    b = np.linspace(-0.5, 0.5, N).astype(np.float32)
+    ref = oracle.epilogue(oracle.gemm_i32(xq, wq), sx, sw, b, mode=oracle.EPI_BIAS_GELU)
+    y = gpu_linear(sq, path, to_dev(xq), to_dev(xq.astype(np.float32), torch.bfloat16),
+                   to_dev(sx), to_dev(wq), to_dev(wq.astype(np.float32), torch.bfloat16),
+                   to_dev(sw), to_dev(b), None, wl.EPI_BIAS_GELU)
+    assert_close_fp32(y.cpu().numpy(), ref, "gelu sweep")
+
+
+@pytest.mark.parametrize("path", PATHS)
 def test_residual_in_place(sq, path):
     c, xq, sx, wq, sw, d = _quantised_case(sq, 96, 1024, 160, wl.EPI_BIAS_RESIDUAL, seed=3)
     ref = oracle.epilogue(oracle.gemm_i32(xq, wq), sx, sw, c.bias.numpy(), c.residual.numpy(),
