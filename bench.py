@@ -38,6 +38,25 @@ METRIC = "INT8 linear-block TOPS on BERT GEMM shapes; % of GB300 INT8 roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def kernel_traffic():
+    """Per-launch DRAM traffic of the GEMM kernel from the committed ncu
+    capture, if that capture was taken of the kernel source as it is now."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "gemm_tc_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        h = hashlib.sha256()
+        for src in d["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest()[:16] != d["source_sha256_16"]:
+            return None, "kernel changed since the capture"
+        return float(d["mean_traffic_bytes_per_launch"]), d["capture"]
+    except (OSError, KeyError, ValueError):
+        return None, "no capture"
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -286,6 +305,7 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, target_s=args.cpu_seconds)
 
+    traffic, traffic_src = kernel_traffic() if args.gemm == "tc" else (None, "not captured")
     gemm_kernel = ("tcgen05.mma kind::f16 (int8 codes as exact bf16, fp32 TMEM chunks of "
                    "K<=1024 summed in int32)" if args.gemm == "tc"
                    else "mma.sync m16n8k32 s8 (legacy warp MMA)")
@@ -304,7 +324,8 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
         "roofline": {"bound": "tensor", "kernel": "gemm+epilogue",
                      "achieved": round(gemm_tops, 2), "peak": peak_tensor,
                      "unit": "TFLOP/s", "frac": round(gemm_tops / peak_tensor, 4),
-                     "traffic": None,
+                     "traffic": traffic,
+                     "traffic_source": traffic_src,
                      "peak_source": f"bf16 dense sustained, {peak_src}",
                      "avg_launch_us": round(g_ms * 1e3 / n_launch, 2),
                      "algorithmic_bytes_per_step": g_bytes // args.steps},
