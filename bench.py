@@ -138,7 +138,8 @@ class ClockSampler:
 # ------------------------------------------------------------------- our arm
 
 class Layer:
-    __slots__ = ("lin", "X", "s", "Wop", "Wq", "sw", "bias", "residual", "Y", "Xhost", "Yhost")
+    __slots__ = ("lin", "X", "s", "Wop", "Wq", "sw", "wl1", "bias", "residual", "Y", "Xhost",
+                 "Yhost")
 
 
 def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool):
@@ -149,6 +150,7 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool):
     Xop_buf = torch.empty(maxMK, dtype=torch.bfloat16, device=dev)
     Xq_buf = torch.empty(maxMK, dtype=torch.int8, device=dev)
     sx_buf = torch.empty(w.M, dtype=torch.float32, device=dev)
+    l1_buf = torch.empty(w.M, dtype=torch.int32, device=dev)
     for layer, idx in [(l, i) for l in range(w.layers) for i in range(len(w.linears))]:
         lin = w.linears[idx]
         seed = wl.gemm_seed(w, layer, idx) + 7 * rank
@@ -160,8 +162,9 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool):
         # smoothing factor from this batch's own statistics (calibration = the input)
         s = sq.smooth_factor(sq.channel_absmax(c.X), sq.channel_absmax(c.W), w.alpha)
         L.s = s
-        Wq, sw, Wop = sq.pack_weight(c.W, s, want_q=(gemm == "mma_sync"), want_op=(gemm == "tc"))
-        L.Wq, L.sw, L.Wop = Wq, sw, Wop
+        Wq, sw, Wop, wl1 = sq.pack_weight(c.W, s, want_q=(gemm == "mma_sync"),
+                                          want_op=(gemm == "tc"), want_l1=True)
+        L.Wq, L.sw, L.Wop, L.wl1 = Wq, sw, Wop, wl1
         L.bias, L.residual = c.bias, c.residual
         L.Y = torch.empty(w.M, lin.N, dtype=torch.float32, device=dev)
         L.Xhost = L.Yhost = None
@@ -172,11 +175,11 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool):
         del c.W
         layers.append(L)
     torch.cuda.synchronize()
-    return layers, (Xq_buf, sx_buf, Xop_buf)
+    return layers, (Xq_buf, sx_buf, Xop_buf, l1_buf)
 
 
 def run_layer(sq, gemm, L, bufs, M, X=None, ev=None):
-    Xq_buf, sx_buf, Xop_buf = bufs
+    Xq_buf, sx_buf, Xop_buf, l1_buf = bufs
     K, N = L.lin.K, L.lin.N
     X = L.X if X is None else X
     if gemm == "tc":
@@ -186,7 +189,9 @@ def run_layer(sq, gemm, L, bufs, M, X=None, ev=None):
         sq.quantize_act(X, L.s, out=(None, sx_buf, Xop))
         if ev is not None:
             ev[1].record()
-        sq.linear_i8(Xop, sx_buf, L.Wop, L.sw, L.bias, L.residual, L.lin.mode, out=L.Y)
+        # the packed weights' row L1 norms let the GEMM prove single-pass exactness
+        sq.linear_i8(Xop, sx_buf, L.Wop, L.sw, L.bias, L.residual, L.lin.mode, out=L.Y,
+                     w_l1=L.wl1)
         if ev is not None:
             ev[2].record()
     else:

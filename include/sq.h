@@ -103,9 +103,11 @@ sq_status sq_smooth_factor(const float *x_amax, const float *w_amax, int64_t K, 
  *   Wq[n][j]   = clamp(round_half_even(W'[n][j] / w_scale[n]), -127, 127)
  * W fp32 [N][K] (nn.Linear layout), s fp32 [K].  Outputs: w_scale fp32 [N]
  * (required, 4-byte aligned), Wq int8 [N][K] (may be NULL), Wop GEMM operand
- * of sq_operand_bytes(N, K) bytes (may be NULL); at least one of Wq / Wop. */
+ * of sq_operand_bytes(N, K) bytes (may be NULL); at least one of Wq / Wop;
+ * w_row_l1 int32 [N] (may be NULL): sum_j |Wq[n][j]| per row, which lets
+ * sq_linear_i8 prove single-pass exactness (see there). */
 sq_status sq_pack_weight(const float *W, const float *s, int64_t N, int64_t K, int8_t *Wq,
-                         float *w_scale, void *Wop, void *stream);
+                         float *w_scale, void *Wop, int32_t *w_row_l1, void *stream);
 
 /* ---- Activation smoothing + dynamic per-token quantisation (Table 10) ----- */
 
@@ -115,11 +117,12 @@ sq_status sq_pack_weight(const float *W, const float *s, int64_t N, int64_t K, i
  *   Xq[m][j]   = clamp(round_half_even(v[j] / x_scale[m]), -127, 127)
  * Outputs: x_scale fp32 [M] (required, 4-byte aligned), Xq int8 [M][K] (may be
  * NULL), Xop GEMM operand of sq_operand_bytes(M, K) bytes (may be NULL); at
- * least one of Xq / Xop.  Any K that is a positive multiple of 16 works; rows
- * of up to 8192 elements are held in registers (one HBM read), longer rows
- * are read twice. */
+ * least one of Xq / Xop; x_row_l1 int32 [M] (may be NULL): sum_j |Xq[m][j]|
+ * per token, for sq_linear_i8.  Any K that is a positive multiple of 16 works;
+ * rows of up to 8192 elements are held in registers (one HBM read), longer
+ * rows are read twice. */
 sq_status sq_quantize_act(const float *X, const float *s, int64_t M, int64_t K, int8_t *Xq,
-                          float *x_scale, void *Xop, void *stream);
+                          float *x_scale, void *Xop, int32_t *x_row_l1, void *stream);
 
 /* ---- INT8 GEMM + fused dequantising epilogue ------------------------------ */
 
@@ -128,14 +131,19 @@ sq_status sq_quantize_act(const float *X, const float *s, int64_t M, int64_t K, 
  * sq_quantize_act (Xop, [M][K]) and sq_pack_weight (Wop, [N][K]).  Runs on the
  * tcgen05 tensor cores: the integer codes are multiplied exactly as bf16 and
  * summed exactly in fp32 over chunks of at most 1024 of K (every partial sum
- * stays below 2^24), the chunks being added in int32.  x_scale fp32 [M],
- * w_scale fp32 [N], bias fp32 [N] (modes 1-3), residual fp32 [M][N] (mode 3);
- * Y fp32 or int32 [M][N].  Y must not overlap any input; residual may equal Y
- * only if it is exactly the same buffer.  Requires K <= 133144 (so that
- * |acc| < 2^31 for any codes) and a GB300-class (sm_103) device. */
-sq_status sq_linear_i8(const void *Xop, const float *x_scale, const void *Wop,
-                       const float *w_scale, const float *bias, const float *residual,
-                       int64_t M, int64_t N, int64_t K, int mode, void *Y, void *stream);
+ * stays below 2^24), the chunks being added in int32.  x_row_l1 [M] and
+ * w_row_l1 [N] (int32, each may be NULL) are the row sums of |code| written by
+ * sq_quantize_act / sq_pack_weight: if 127 * max(row L1) < 2^24 for either
+ * operand, no partial sum can reach 2^24 and all of K is summed in one pass
+ * (faster for K > 1024, same exact result).  x_scale fp32 [M], w_scale fp32
+ * [N], bias fp32 [N] (modes 1-3), residual fp32 [M][N] (mode 3); Y fp32 or
+ * int32 [M][N].  Y must not overlap any input; residual may equal Y only if it
+ * is exactly the same buffer.  Requires K <= 133144 (so that |acc| < 2^31 for
+ * any codes) and a GB300-class (sm_103) device. */
+sq_status sq_linear_i8(const void *Xop, const float *x_scale, const int32_t *x_row_l1,
+                       const void *Wop, const float *w_scale, const int32_t *w_row_l1,
+                       const float *bias, const float *residual, int64_t M, int64_t N, int64_t K,
+                       int mode, void *Y, void *stream);
 
 /* The same GEMM + epilogue on the legacy warp-level integer MMA path
  * (mma.sync m16n8k32 s8 x s8 -> s32), reading int8 codes directly:

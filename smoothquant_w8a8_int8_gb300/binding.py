@@ -51,9 +51,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                 "sq_operand_bytes": ([i64, i64], ctypes.c_size_t),
                 "sq_channel_absmax": ([vp, i64, i64, vp, vp], i32),
                 "sq_smooth_factor": ([vp, vp, i64, f32, vp, vp], i32),
-                "sq_pack_weight": ([vp, vp, i64, i64, vp, vp, vp, vp], i32),
-                "sq_quantize_act": ([vp, vp, i64, i64, vp, vp, vp, vp], i32),
-                "sq_linear_i8": ([vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp], i32),
+                "sq_pack_weight": ([vp, vp, i64, i64, vp, vp, vp, vp, vp], i32),
+                "sq_quantize_act": ([vp, vp, i64, i64, vp, vp, vp, vp, vp], i32),
+                "sq_linear_i8": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp],
+                                 i32),
                 "sq_linear_i8_mma_sync": ([vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp], i32),
                 "sq_device_status": ([vp], i32),
             }
@@ -127,38 +128,45 @@ def smooth_factor(x_amax: torch.Tensor, w_amax: torch.Tensor, alpha: float, stre
 
 
 def pack_weight(W: torch.Tensor, s: torch.Tensor, want_q: bool = True, want_op: bool = True,
-                stream=None):
-    """Returns (Wq int8 or None, w_scale fp32, Wop operand or None)."""
+                want_l1: bool = False, stream=None):
+    """Returns (Wq int8 or None, w_scale fp32, Wop operand or None), plus the
+    per-row code L1 norms (int32) as a fourth item when want_l1."""
     _need(W, torch.float32, "W")
     N, K = W.shape
     _need(s, torch.float32, "s", (K,))
     Wq = torch.empty(N, K, dtype=torch.int8, device=W.device) if want_q else None
     Wop = empty_operand(N, K, W.device) if want_op else None
     sw = torch.empty(N, dtype=torch.float32, device=W.device)
-    _check(load().sq_pack_weight(_p(W), _p(s), N, K, _p(Wq), _p(sw), _p(Wop), _stream(stream)),
-           "sq_pack_weight")
-    return Wq, sw, Wop
+    l1 = torch.empty(N, dtype=torch.int32, device=W.device) if want_l1 else None
+    _check(load().sq_pack_weight(_p(W), _p(s), N, K, _p(Wq), _p(sw), _p(Wop), _p(l1),
+                                 _stream(stream)), "sq_pack_weight")
+    return (Wq, sw, Wop, l1) if want_l1 else (Wq, sw, Wop)
 
 
 def quantize_act(X: torch.Tensor, s: torch.Tensor, want_q: bool = True, want_op: bool = True,
-                 out=None, stream=None):
-    """Returns (Xq int8 or None, x_scale fp32, Xop operand or None).  `out`
-    may give preallocated (Xq, x_scale, Xop) buffers."""
+                 want_l1: bool = False, out=None, stream=None):
+    """Returns (Xq int8 or None, x_scale fp32, Xop operand or None), plus the
+    per-token code L1 norms (int32) as a fourth item when want_l1.  `out` may
+    give preallocated (Xq, x_scale, Xop[, x_l1]) buffers."""
     _need(X, torch.float32, "X")
     M, K = X.shape
     _need(s, torch.float32, "s", (K,))
     if out is not None:
-        Xq, sx, Xop = out
+        Xq, sx, Xop = out[:3]
+        l1 = out[3] if len(out) > 3 else None
     else:
         Xq = torch.empty(M, K, dtype=torch.int8, device=X.device) if want_q else None
         Xop = empty_operand(M, K, X.device) if want_op else None
         sx = torch.empty(M, dtype=torch.float32, device=X.device)
-    _check(load().sq_quantize_act(_p(X), _p(s), M, K, _p(Xq), _p(sx), _p(Xop), _stream(stream)),
-           "sq_quantize_act")
+        l1 = torch.empty(M, dtype=torch.int32, device=X.device) if want_l1 else None
+    _check(load().sq_quantize_act(_p(X), _p(s), M, K, _p(Xq), _p(sx), _p(Xop), _p(l1),
+                                  _stream(stream)), "sq_quantize_act")
+    if want_l1 or (out is not None and len(out) > 3):
+        return Xq, sx, Xop, l1
     return Xq, sx, Xop
 
 
-def _linear(fn, what, Xa, sx, Wa, sw, bias, residual, mode, out, stream):
+def _out(Xa, Wa, mode, out):
     M, K = Xa.shape
     N = Wa.shape[0]
     if Wa.shape[1] != K:
@@ -166,18 +174,20 @@ def _linear(fn, what, Xa, sx, Wa, sw, bias, residual, mode, out, stream):
     if out is None:
         dt = torch.int32 if mode == EPI_RAW_I32 else torch.float32
         out = torch.empty(M, N, dtype=dt, device=Xa.device)
-    _check(fn(_p(Xa), _p(sx), _p(Wa), _p(sw), _p(bias), _p(residual), M, N, K, int(mode),
-              _p(out), _stream(stream)), what)
-    return out
+    return M, N, K, out
 
 
 def linear_i8(Xop, x_scale, Wop, w_scale, bias=None, residual=None, mode=EPI_BIAS, out=None,
-              stream=None):
-    """tcgen05 INT8 GEMM + epilogue on GEMM-operand buffers."""
+              x_l1=None, w_l1=None, stream=None):
+    """tcgen05 INT8 GEMM + epilogue on GEMM-operand buffers.  x_l1 / w_l1:
+    optional per-row code L1 norms from quantize_act / pack_weight."""
     _need(Xop, torch.bfloat16, "Xop")
     _need(Wop, torch.bfloat16, "Wop")
-    return _linear(load().sq_linear_i8, "sq_linear_i8", Xop, x_scale, Wop, w_scale, bias,
-                   residual, mode, out, stream)
+    M, N, K, out = _out(Xop, Wop, mode, out)
+    _check(load().sq_linear_i8(_p(Xop), _p(x_scale), _p(x_l1), _p(Wop), _p(w_scale), _p(w_l1),
+                               _p(bias), _p(residual), M, N, K, int(mode), _p(out),
+                               _stream(stream)), "sq_linear_i8")
+    return out
 
 
 def linear_i8_mma_sync(Xq, x_scale, Wq, w_scale, bias=None, residual=None, mode=EPI_BIAS,
@@ -185,8 +195,11 @@ def linear_i8_mma_sync(Xq, x_scale, Wq, w_scale, bias=None, residual=None, mode=
     """Legacy mma.sync INT8 GEMM + epilogue on int8 codes."""
     _need(Xq, torch.int8, "Xq")
     _need(Wq, torch.int8, "Wq")
-    return _linear(load().sq_linear_i8_mma_sync, "sq_linear_i8_mma_sync", Xq, x_scale, Wq,
-                   w_scale, bias, residual, mode, out, stream)
+    M, N, K, out = _out(Xq, Wq, mode, out)
+    _check(load().sq_linear_i8_mma_sync(_p(Xq), _p(x_scale), _p(Wq), _p(w_scale), _p(bias),
+                                        _p(residual), M, N, K, int(mode), _p(out),
+                                        _stream(stream)), "sq_linear_i8_mma_sync")
+    return out
 
 
 def device_status(stream=None) -> int:

@@ -126,35 +126,40 @@ sq_status sq_smooth_factor(const float *x_amax, const float *w_amax, int64_t K, 
 }
 
 sq_status sq_pack_weight(const float *W, const float *s, int64_t N, int64_t K, int8_t *Wq,
-                         float *w_scale, void *Wop, void *stream) {
+                         float *w_scale, void *Wop, int32_t *w_row_l1, void *stream) {
     sq_status rc = check_quant_args(W, s, N, K, Wq, w_scale, Wop);
     if (rc != SQ_OK) return rc;
     if (N == 0) return SQ_OK;
     if ((rc = require_sm103()) != SQ_OK) return rc;
+    if (w_row_l1 && !aligned4(w_row_l1)) return SQ_ERR_ALIGNMENT;
     return launch_quantize_rows(1, W, s, N, K, Wq, w_scale, static_cast<__nv_bfloat16 *>(Wop),
-                                as_stream(stream));
+                                w_row_l1, as_stream(stream));
 }
 
 sq_status sq_quantize_act(const float *X, const float *s, int64_t M, int64_t K, int8_t *Xq,
-                          float *x_scale, void *Xop, void *stream) {
+                          float *x_scale, void *Xop, int32_t *x_row_l1, void *stream) {
     sq_status rc = check_quant_args(X, s, M, K, Xq, x_scale, Xop);
     if (rc != SQ_OK) return rc;
     if (M == 0) return SQ_OK;
     if ((rc = require_sm103()) != SQ_OK) return rc;
+    if (x_row_l1 && !aligned4(x_row_l1)) return SQ_ERR_ALIGNMENT;
     return launch_quantize_rows(0, X, s, M, K, Xq, x_scale, static_cast<__nv_bfloat16 *>(Xop),
-                                as_stream(stream));
+                                x_row_l1, as_stream(stream));
 }
 
-sq_status sq_linear_i8(const void *Xop, const float *x_scale, const void *Wop,
-                       const float *w_scale, const float *bias, const float *residual,
-                       int64_t M, int64_t N, int64_t K, int mode, void *Y, void *stream) {
+sq_status sq_linear_i8(const void *Xop, const float *x_scale, const int32_t *x_row_l1,
+                       const void *Wop, const float *w_scale, const int32_t *w_row_l1,
+                       const float *bias, const float *residual, int64_t M, int64_t N, int64_t K,
+                       int mode, void *Y, void *stream) {
     sq_status rc = check_linear_args(Xop, x_scale, Wop, w_scale, bias, residual, M, N, K, mode, Y);
     if (rc != SQ_OK) return rc;
     if (M == 0 || N == 0) return SQ_OK;
+    if ((x_row_l1 && !aligned4(x_row_l1)) || (w_row_l1 && !aligned4(w_row_l1)))
+        return SQ_ERR_ALIGNMENT;
     if ((rc = require_sm103()) != SQ_OK) return rc;
-    return launch_gemm_tc(static_cast<const __nv_bfloat16 *>(Xop), x_scale,
-                          static_cast<const __nv_bfloat16 *>(Wop), w_scale, bias, residual, M, N,
-                          K, mode, Y, as_stream(stream));
+    return launch_gemm_tc(static_cast<const __nv_bfloat16 *>(Xop), x_scale, x_row_l1,
+                          static_cast<const __nv_bfloat16 *>(Wop), w_scale, w_row_l1, bias,
+                          residual, M, N, K, mode, Y, as_stream(stream));
 }
 
 sq_status sq_linear_i8_mma_sync(const int8_t *Xq, const float *x_scale, const int8_t *Wq,

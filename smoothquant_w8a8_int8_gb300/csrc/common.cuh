@@ -29,14 +29,15 @@ sq_status launch_smooth_factor(const float *ax, const float *aw, int64_t K, floa
                                float *s, cudaStream_t st);
 sq_status launch_quantize_rows(int direction, const float *A, const float *s, int64_t rows,
                                int64_t K, int8_t *q, float *scale, __nv_bfloat16 *op,
-                               cudaStream_t st);
+                               int32_t *l1, cudaStream_t st);
 sq_status launch_gemm_mma_sync(const int8_t *Xq, const float *sx, const int8_t *Wq,
                                const float *sw, const float *bias, const float *residual,
                                int64_t M, int64_t N, int64_t K, int mode, void *Y,
                                cudaStream_t st);
-sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const __nv_bfloat16 *Wop,
-                         const float *sw, const float *bias, const float *residual,
-                         int64_t M, int64_t N, int64_t K, int mode, void *Y, cudaStream_t st);
+sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_t *x_l1,
+                         const __nv_bfloat16 *Wop, const float *sw, const int32_t *w_l1,
+                         const float *bias, const float *residual, int64_t M, int64_t N,
+                         int64_t K, int mode, void *Y, cudaStream_t st);
 // Reads and clears the tcgen05 GEMM's device error word (synchronous).
 sq_status gemm_tc_take_error(cudaStream_t st);
 

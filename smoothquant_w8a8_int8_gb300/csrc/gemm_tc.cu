@@ -31,6 +31,9 @@
 //              tensor memory) and frees A, so the MMA of the next chunk only
 //              waits for that short pass, and the final pass (scales, bias,
 //              GELU / residual, stores) overlaps the next tile's first chunk.
+//              When the caller passes the row L1 norms of the codes and
+//              127 * max L1 < 2^24 for either operand, no partial sum can
+//              reach 2^24 and all of K is one exact pass (the K <= 1024 case).
 // Epilogue I/O per 32 x 32 slice: results are written to a per-warp 4 KB
 // staging tile in shared memory (128-byte swizzle, conflict-free) and stored
 // with one TMA bulk tensor store.  Shapes whose rows are not 16-byte
@@ -62,7 +65,7 @@ constexpr int COLS_PER_WARP = BN / 2;       // 128
 constexpr int SLICES = COLS_PER_WARP / SLICE;
 constexpr int STG_BYTES = SLICE * SLICE * 4;  // 4 KB staging tile per epilogue warp
 constexpr int TMEM_COLS = 512;
-constexpr int BAR_BYTES = 256;
+constexpr int BAR_BYTES = 512;
 constexpr int RING_BYTES = STAGES * STAGE_BYTES;
 constexpr int SMEM_BYTES = RING_BYTES + NUM_EPI_WARPS * STG_BYTES + BAR_BYTES + 1024;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;
@@ -250,15 +253,22 @@ struct Smem {
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
+    int32_t l1max[9][2];  // per-warp maxima of the row L1 norms (warps 1..9)
 };
 static_assert(sizeof(Smem) <= BAR_BYTES, "barrier block");
 
 struct EpiArgs {
     const float *sx, *sw, *bias, *residual;
+    const int32_t *x_l1, *w_l1;  // per-row sums of |code| (nullable)
     void *Y;
     int M, N;
     int tma_io;  // 1: TMA staging for Y (and the residual); 0: plain per-element I/O
 };
+
+// Largest row L1 norm of int8 codes for which 127 * L1 < 2^24: then every
+// partial sum of that row's products with any codes stays below 2^24 in
+// magnitude and the whole K accumulates exactly in one fp32 pass.
+constexpr int32_t kSinglePassL1 = 132104;
 
 // erf by Abramowitz & Stegun, Handbook of Mathematical Functions, formula
 // 7.1.26 (after Hastings): erf(x) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5))))
@@ -452,7 +462,36 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int n_tiles = (N + BN - 1) / BN;
     const int num_tiles = m_tiles * n_tiles;
     const int nkb = (K + BK - 1) / BK;
-    const int nchunks = (nkb + KB_PER_CHUNK - 1) / KB_PER_CHUNK;
+    // K per exact fp32 pass: 1024, or all of K when the row L1 norms of either
+    // operand bound every partial sum below 2^24.  Decided by warps 1..9 (the
+    // MMA issuer and the epilogue); the producer does not need it.
+    int chunk_kb = KB_PER_CHUNK;
+    if (warp != 0 && nkb > KB_PER_CHUNK && (args.x_l1 || args.w_l1)) {
+        const int tid = threadIdx.x - 32;
+        int32_t mx = args.x_l1 ? 0 : 0x7fffffff, mw = args.w_l1 ? 0 : 0x7fffffff;
+        if (args.x_l1)
+            for (int i = tid; i < M; i += THREADS - 32) mx = max(mx, __ldg(args.x_l1 + i));
+        if (args.w_l1)
+            for (int i = tid; i < N; i += THREADS - 32) mw = max(mw, __ldg(args.w_l1 + i));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            mw = max(mw, __shfl_xor_sync(0xffffffffu, mw, o));
+        }
+        if (lane == 0) {
+            S.l1max[warp - 1][0] = mx;
+            S.l1max[warp - 1][1] = mw;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(THREADS - 32) : "memory");
+        mx = 0;
+        mw = 0;
+        for (int w = 0; w < 9; ++w) {
+            mx = max(mx, S.l1max[w][0]);
+            mw = max(mw, S.l1max[w][1]);
+        }
+        if (min(mx, mw) <= kSinglePassL1) chunk_kb = nkb;
+    }
+    const int nchunks = (nkb + chunk_kb - 1) / chunk_kb;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -497,8 +536,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tph ^= 1u << b;
                     tc_fence_after();
                     const uint32_t d = tmem_base + b * BN;
-                    const int kb0 = c * KB_PER_CHUNK;
-                    const int kb1 = min(nkb, kb0 + KB_PER_CHUNK);
+                    const int kb0 = c * chunk_kb;
+                    const int kb1 = min(nkb, kb0 + chunk_kb);
                     for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait(smem_u32(&S.full[stage]), phase, abort_flag)) goto done_m;
                         tc_fence_after();
@@ -656,9 +695,10 @@ sq_status launch_mode(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
 
 }  // namespace
 
-sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const __nv_bfloat16 *Wop,
-                         const float *sw, const float *bias, const float *residual, int64_t M,
-                         int64_t N, int64_t K, int mode, void *Y, cudaStream_t st) {
+sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_t *x_l1,
+                         const __nv_bfloat16 *Wop, const float *sw, const int32_t *w_l1,
+                         const float *bias, const float *residual, int64_t M, int64_t N,
+                         int64_t K, int mode, void *Y, cudaStream_t st) {
     if (M > 0x7fffffff || N > 0x7fffffff) return SQ_ERR_UNSUPPORTED;
     sq_status rc = get_encoder();
     if (rc != SQ_OK) return rc;
@@ -669,6 +709,8 @@ sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const __nv_b
     args.sw = sw;
     args.bias = bias;
     args.residual = residual;
+    args.x_l1 = x_l1;
+    args.w_l1 = w_l1;
     args.Y = Y;
     args.M = (int)M;
     args.N = (int)N;

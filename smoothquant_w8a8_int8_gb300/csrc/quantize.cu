@@ -49,10 +49,9 @@ __device__ __forceinline__ float code_of(float v, float scale, float rscale) {
     return fminf(127.0f, fmaxf(-127.0f, e));
 }
 
-__device__ __forceinline__ void store_codes(float4 v, float scale, float rscale, int64_t off4,
-                                            int8_t *q, __nv_bfloat16 *op) {
-    const float c0 = code_of(v.x, scale, rscale), c1 = code_of(v.y, scale, rscale);
-    const float c2 = code_of(v.z, scale, rscale), c3 = code_of(v.w, scale, rscale);
+// four integer-valued codes to the int8 and/or bf16 outputs (float4 index off4)
+__device__ __forceinline__ void store_code_values(float c0, float c1, float c2, float c3,
+                                                  int64_t off4, int8_t *q, __nv_bfloat16 *op) {
     if (q) {
         const uint32_t packed = (uint32_t)(__float2int_rn(c0) & 0xff) |
                                 ((uint32_t)(__float2int_rn(c1) & 0xff) << 8) |
@@ -69,6 +68,15 @@ __device__ __forceinline__ void store_codes(float4 v, float scale, float rscale,
         u.y = *reinterpret_cast<uint32_t *>(&hi);
         reinterpret_cast<uint2 *>(op)[off4] = u;
     }
+}
+
+// Writes four codes; returns the sum of their magnitudes (for the row L1 norm).
+__device__ __forceinline__ float store_codes(float4 v, float scale, float rscale, int64_t off4,
+                                             int8_t *q, __nv_bfloat16 *op) {
+    const float c0 = code_of(v.x, scale, rscale), c1 = code_of(v.y, scale, rscale);
+    const float c2 = code_of(v.z, scale, rscale), c3 = code_of(v.w, scale, rscale);
+    store_code_values(c0, c1, c2, c3, off4, q, op);
+    return (fabsf(c0) + fabsf(c1)) + (fabsf(c2) + fabsf(c3));
 }
 
 // Row maximum across the TPR threads of a row group.  red: [rows_per_block][8].
@@ -88,11 +96,29 @@ __device__ __forceinline__ float group_max(float m, int tpr, float *red) {
     return m;
 }
 
+// Row sum across the TPR threads of a row group (as group_max).
+__device__ __forceinline__ float group_sum(float v, int tpr, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (tpr > 32) {
+        const int warp = threadIdx.x >> 5;
+        const int wpg = tpr >> 5;
+        const int g = warp / wpg;
+        if ((threadIdx.x & 31) == 0) red[warp] = v;
+        __syncthreads();
+        v = 0.0f;
+        for (int w = 0; w < wpg; ++w) v += red[g * wpg + w];
+        __syncthreads();
+    }
+    return v;
+}
+
 // Registers path: K4 = K/4 <= tpr * kVPT.
 template <int DIR, int kVPT>
 __global__ void __launch_bounds__(kThreads) quantize_rows_reg(
     const float *__restrict__ A, const float *__restrict__ s, int64_t rows, int K4, int tpr,
-    int8_t *__restrict__ q, float *__restrict__ scale, __nv_bfloat16 *__restrict__ op) {
+    int8_t *__restrict__ q, float *__restrict__ scale, __nv_bfloat16 *__restrict__ op,
+    int32_t *__restrict__ l1) {
     __shared__ float red[kThreads / 32];
     const int rpb = kThreads / tpr;
     const int g = threadIdx.x / tpr;
@@ -129,13 +155,18 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_reg(
         m = group_max(m, tpr, red);
         const float sc = m == 0.0f ? 1.0f : __fdiv_rn(m, 127.0f);
         const float rsc = __frcp_rn(sc);
+        float a1 = 0.0f;  // sum of |code| (exact: at most 127 * 8192 < 2^24)
         if (valid) {
             if (t == 0) scale[row] = sc;
 #pragma unroll
             for (int i = 0; i < kVPT; ++i) {
                 int j = t + i * tpr;
-                if (j < K4) store_codes(v[i], sc, rsc, row * K4 + j, q, op);
+                if (j < K4) a1 += store_codes(v[i], sc, rsc, row * K4 + j, q, op);
             }
+        }
+        if (l1) {
+            a1 = group_sum(a1, tpr, red);
+            if (valid && t == 0) l1[row] = (int32_t)a1;
         }
     }
 }
@@ -144,7 +175,8 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_reg(
 template <int DIR>
 __global__ void __launch_bounds__(kThreads) quantize_rows_loop(
     const float *__restrict__ A, const float *__restrict__ s, int64_t rows, int K4,
-    int8_t *__restrict__ q, float *__restrict__ scale, __nv_bfloat16 *__restrict__ op) {
+    int8_t *__restrict__ q, float *__restrict__ scale, __nv_bfloat16 *__restrict__ op,
+    int32_t *__restrict__ l1) {
     __shared__ float red[kThreads / 32];
     const float4 *s4 = reinterpret_cast<const float4 *>(s);
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
@@ -161,11 +193,24 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_loop(
         const float sc = m == 0.0f ? 1.0f : __fdiv_rn(m, 127.0f);
         const float rsc = __frcp_rn(sc);
         if (threadIdx.x == 0) scale[row] = sc;
+        int a1 = 0;  // integer: long rows may exceed 2^24
         for (int j = threadIdx.x; j < K4; j += kThreads) {
             float4 x = __ldcs(a4 + j), sv = __ldg(s4 + j);
             float4 v = make_float4(smooth_one(x.x, sv.x, DIR), smooth_one(x.y, sv.y, DIR),
                                    smooth_one(x.z, sv.z, DIR), smooth_one(x.w, sv.w, DIR));
-            store_codes(v, sc, rsc, row * K4 + j, q, op);
+            a1 += (int)store_codes(v, sc, rsc, row * K4 + j, q, op);
+        }
+        if (l1) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+            if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = __int_as_float(a1);
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                long long tot = 0;
+                for (int w = 0; w < kThreads / 32; ++w) tot += __float_as_int(red[w]);
+                l1[row] = tot > 0x7fffffffLL ? 0x7fffffff : (int32_t)tot;
+            }
+            __syncthreads();
         }
     }
 }
@@ -205,7 +250,7 @@ int resident_blocks(Kern k) {
 
 sq_status launch_quantize_rows(int direction, const float *A, const float *s, int64_t rows,
                                int64_t K, int8_t *q, float *scale, __nv_bfloat16 *op,
-                               cudaStream_t st) {
+                               int32_t *l1, cudaStream_t st) {
     DeviceInfo di;
     sq_status rc = device_info(&di);
     if (rc != SQ_OK) return rc;
@@ -220,18 +265,18 @@ sq_status launch_quantize_rows(int direction, const float *A, const float *s, in
         const int rpb = kThreads / tpr;
         const int64_t tiles = (rows + rpb - 1) / rpb;
         void (*kern)(const float *, const float *, int64_t, int, int, int8_t *, float *,
-                     __nv_bfloat16 *);
+                     __nv_bfloat16 *, int32_t *);
         if (direction == 0) kern = small ? quantize_rows_reg<0, 4> : quantize_rows_reg<0, 8>;
         else kern = small ? quantize_rows_reg<1, 4> : quantize_rows_reg<1, 8>;
         static int per_sm[2][2] = {{0, 0}, {0, 0}};
         int &occ = per_sm[direction][small ? 0 : 1];
         if (!occ) occ = resident_blocks(kern);
         const int64_t grid = std::min<int64_t>(tiles, (int64_t)di.sms * occ);
-        kern<<<(unsigned)grid, kThreads, 0, st>>>(A, s, rows, K4, tpr, q, scale, op);
+        kern<<<(unsigned)grid, kThreads, 0, st>>>(A, s, rows, K4, tpr, q, scale, op, l1);
     } else {
         auto kern = direction == 0 ? quantize_rows_loop<0> : quantize_rows_loop<1>;
         const int64_t grid = std::min<int64_t>(rows, (int64_t)di.sms * 8);
-        kern<<<(unsigned)grid, kThreads, 0, st>>>(A, s, rows, K4, q, scale, op);
+        kern<<<(unsigned)grid, kThreads, 0, st>>>(A, s, rows, K4, q, scale, op, l1);
     }
     return cuda_status(cudaGetLastError());
 }

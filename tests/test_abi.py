@@ -63,29 +63,33 @@ def _fake(addr):
 
 def test_argument_checks_fail_before_any_launch(lib):
     vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
-    lib.sq_quantize_act.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp]
-    lib.sq_pack_weight.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp]
-    lib.sq_linear_i8.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp]
-    lib.sq_linear_i8_mma_sync.argtypes = lib.sq_linear_i8.argtypes
+    lib.sq_quantize_act.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp, vp]
+    lib.sq_pack_weight.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp, vp]
+    lib.sq_linear_i8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp]
+    lib.sq_linear_i8_mma_sync.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp]
     lib.sq_smooth_factor.argtypes = [vp, vp, i64, ctypes.c_float, vp, vp]
     lib.sq_channel_absmax.argtypes = [vp, i64, i64, vp, vp]
     a = _fake(0x10000)
     INVALID, ALIGN, UNSUP = 1, 2, 3
     # quantiser
-    assert lib.sq_quantize_act(None, a, 4, 32, a, a, None, None) == INVALID
-    assert lib.sq_quantize_act(a, a, 4, 32, None, a, None, None) == INVALID   # no output
-    assert lib.sq_quantize_act(a, a, 4, 32, a, None, None, None) == INVALID   # no scale
-    assert lib.sq_quantize_act(a, a, -1, 32, a, a, None, None) == INVALID
-    assert lib.sq_quantize_act(a, a, 4, 0, a, a, None, None) == INVALID
-    assert lib.sq_quantize_act(a, a, 4, 24, a, a, None, None) == ALIGN       # K % 16
-    assert lib.sq_quantize_act(_fake(0x10004), a, 4, 32, a, a, None, None) == ALIGN
-    assert lib.sq_quantize_act(a, a, 0, 32, a, a, None, None) == 0           # empty: no launch
-    assert lib.sq_quantize_act(None, None, 0, 32, None, None, None, None) == 0
-    assert lib.sq_quantize_act(None, None, 0, 24, None, None, None, None) == ALIGN
-    assert lib.sq_pack_weight(a, a, 4, 40, a, a, None, None) == ALIGN
-    assert lib.sq_pack_weight(a, a, 0, 32, None, a, a, None) == 0
-    # GEMM
-    for fn in (lib.sq_linear_i8, lib.sq_linear_i8_mma_sync):
+    assert lib.sq_quantize_act(None, a, 4, 32, a, a, None, None, None) == INVALID
+    assert lib.sq_quantize_act(a, a, 4, 32, None, a, None, None, None) == INVALID   # no output
+    assert lib.sq_quantize_act(a, a, 4, 32, a, None, None, None, None) == INVALID   # no scale
+    assert lib.sq_quantize_act(a, a, -1, 32, a, a, None, None, None) == INVALID
+    assert lib.sq_quantize_act(a, a, 4, 0, a, a, None, None, None) == INVALID
+    assert lib.sq_quantize_act(a, a, 4, 24, a, a, None, None, None) == ALIGN       # K % 16
+    assert lib.sq_quantize_act(_fake(0x10004), a, 4, 32, a, a, None, None, None) == ALIGN
+    assert lib.sq_quantize_act(a, a, 0, 32, a, a, None, None, None) == 0           # empty: no launch
+    assert lib.sq_quantize_act(None, None, 0, 32, None, None, None, None, None) == 0
+    assert lib.sq_quantize_act(None, None, 0, 24, None, None, None, None, None) == ALIGN
+    assert lib.sq_pack_weight(a, a, 4, 40, a, a, None, None, None) == ALIGN
+    assert lib.sq_pack_weight(a, a, 0, 32, None, a, a, None, None) == 0
+    # GEMM (the tcgen05 entry point also takes the two optional row-L1 arrays)
+    def tc(X, sx, W, sw, b, r, M, N, K, mode, Y, st):
+        return lib.sq_linear_i8(X, sx, None, W, sw, None, b, r, M, N, K, mode, Y, st)
+    bad_l1 = lib.sq_linear_i8(a, a, _fake(0x10002), a, a, None, a, None, 8, 8, 32, 1, a, None)
+    assert bad_l1 == ALIGN
+    for fn in (tc, lib.sq_linear_i8_mma_sync):
         assert fn(None, a, a, a, a, None, 8, 8, 32, 1, a, None) == INVALID
         assert fn(a, a, a, a, None, None, 8, 8, 32, 1, a, None) == INVALID   # bias missing
         assert fn(a, a, a, a, a, None, 8, 8, 32, 3, a, None) == INVALID      # residual missing

@@ -48,11 +48,12 @@ def test_quantize_act_parity(sq, M, K):
     X, W = c.X.numpy(), c.W.numpy()
     s = oracle_smoothing(X, W, 0.5)
     q_ref, sx_ref = oracle.quantize_rows(X, s, "act")
-    Xq, sx, Xop = sq.quantize_act(to_dev(X), to_dev(s))
+    Xq, sx, Xop, l1 = sq.quantize_act(to_dev(X), to_dev(s), want_l1=True)
     torch.cuda.synchronize()
     assert_codes_equal(Xq.cpu().numpy(), q_ref, "Xq")
     assert_bits_equal(sx.cpu().numpy(), sx_ref, "x_scale")
     assert_codes_equal(op_as_int(Xop), q_ref, "Xop")
+    np.testing.assert_array_equal(l1.cpu().numpy(), np.abs(q_ref.astype(np.int64)).sum(axis=1))
     # each output alone
     _, sx2, Xop2 = sq.quantize_act(to_dev(X), to_dev(s), want_q=False)
     Xq3, sx3, _ = sq.quantize_act(to_dev(X), to_dev(s), want_op=False)
@@ -107,6 +108,31 @@ def test_quantize_ties_and_near_ties(sq):
     np.testing.assert_array_equal(q_ref[0, :254], np.round(ties[:254]).astype(np.int8))
 
 
+def test_quantize_row_max_near_ties(sq):
+    """Rows whose smoothed values x/s are all within a few ulp of each other,
+    so that only exact division finds the row maximum; rows of tiny and of
+    very large values (where reciprocal estimates lose their error bound)."""
+    rng = np.random.default_rng(9)
+    K = 1024
+    s = (rng.uniform(0.05, 20.0, K)).astype(np.float32)
+    rows = []
+    for target in (1.0, 3.7, 1e-3, 250.0):
+        x = (np.float32(target) * s).astype(np.float32)           # x/s = target +- 1 ulp
+        x *= rng.choice(np.array([-1, 1], np.float32), K)
+        rows.append(x)
+    rows.append((rng.standard_normal(K) * 1e-36).astype(np.float32))  # tiny / subnormal
+    rows.append((rng.standard_normal(K) * 1e35).astype(np.float32))   # large
+    big = np.zeros(K, np.float32)
+    big[7] = np.float32(1.5e37 * float(s[7]))                       # quotient near 1.5e37
+    rows.append(big)
+    X = np.stack(rows).astype(np.float32)
+    q_ref, sx_ref = oracle.quantize_rows(X, s, "act")
+    Xq, sx, Xop = sq.quantize_act(to_dev(X), to_dev(s))
+    assert_bits_equal(sx.cpu().numpy(), sx_ref, "x_scale")
+    assert_codes_equal(Xq.cpu().numpy(), q_ref, "Xq")
+    assert_codes_equal(op_as_int(Xop), q_ref, "Xop")
+
+
 @pytest.mark.parametrize("N,K", [(1, 16), (5, 48), (1024, 1024), (3072, 1024), (768, 3072),
                                  (9, 8208)])
 def test_pack_weight_parity(sq, N, K):
@@ -114,11 +140,12 @@ def test_pack_weight_parity(sq, N, K):
     X, W = c.X.numpy(), c.W.numpy()
     s = oracle_smoothing(X, W, 0.5)
     q_ref, sw_ref = oracle.quantize_rows(W, s, "weight")
-    Wq, sw, Wop = gpu_pack(sq, W, s)
+    Wq, sw, Wop, l1 = sq.pack_weight(to_dev(W), to_dev(s), want_l1=True)
     torch.cuda.synchronize()
     assert_codes_equal(Wq.cpu().numpy(), q_ref, "Wq")
     assert_bits_equal(sw.cpu().numpy(), sw_ref, "w_scale")
     assert_codes_equal(op_as_int(Wop), q_ref, "Wop")
+    np.testing.assert_array_equal(l1.cpu().numpy(), np.abs(q_ref.astype(np.int64)).sum(axis=1))
 
 
 # ------------------------------------------------------------ smoothing factor
@@ -197,6 +224,41 @@ def test_gemm_adversarial_exactness(sq, path, K):
                      mode=sq.EPI_RAW_I32)
     ref = oracle.gemm_i32(xq, wq)
     assert ref[0, 0] == K * 16129
+    assert_codes_equal(acc.cpu().numpy(), ref, "acc")
+    if path == "tc":
+        # with the row L1 norms passed: these rows exceed the single-pass bound
+        xl1 = to_dev(np.abs(xq.astype(np.int64)).sum(1).astype(np.int32))
+        wl1 = to_dev(np.abs(wq.astype(np.int64)).sum(1).astype(np.int32))
+        acc = sq.linear_i8(to_dev(xq.astype(np.float32), torch.bfloat16), None,
+                           to_dev(wq.astype(np.float32), torch.bfloat16), None,
+                           mode=sq.EPI_RAW_I32, x_l1=xl1, w_l1=wl1)
+        assert_codes_equal(acc.cpu().numpy(), ref, "acc (row L1 given)")
+
+
+@pytest.mark.parametrize("limit_ok", [True, False])
+@pytest.mark.parametrize("K", [2048, 4096])
+def test_gemm_single_pass_bound(sq, limit_ok, K):
+    """At the single-pass limit (127 * L1 < 2^24) the whole K is summed in one
+    fp32 pass; one more unit of L1 forces chunks.  Both must be exact: the
+    boundary rows make the sum 127 * 132104 = 16,777,208 = 2^24 - 8."""
+    M, N = 130, 144
+    L1 = 132104 if limit_ok else 132105
+    xq = np.zeros((M, K), np.int8)
+    full, rest = divmod(L1, 127)
+    xq[:, :full] = 127
+    xq[:, full] = rest
+    xq[1::2] = -xq[1::2]
+    rng = np.random.default_rng(K + L1)
+    xq[64:] = np.clip(rng.integers(-3, 4, (M - 64, K)), -127, 127).astype(np.int8)
+    xq[64:, :4] = 127                                   # keep every row's max code 127
+    wq = np.full((N, K), 127, np.int8)
+    wq[N // 2:] = rng.choice(np.array([-127, 127], np.int8), (N - N // 2, K))
+    xl1 = np.abs(xq.astype(np.int64)).sum(1).astype(np.int32)
+    assert xl1.max() == L1
+    ref = oracle.gemm_i32(xq, wq)
+    acc = sq.linear_i8(to_dev(xq.astype(np.float32), torch.bfloat16), None,
+                       to_dev(wq.astype(np.float32), torch.bfloat16), None, mode=sq.EPI_RAW_I32,
+                       x_l1=to_dev(xl1))
     assert_codes_equal(acc.cpu().numpy(), ref, "acc")
 
 
@@ -279,11 +341,16 @@ def _pipeline_gpu(sq, case, s, path):
     activations to the GEMM operand and run the fused GEMM."""
     X, W = case.X.cuda(), case.W.cuda()
     sd = to_dev(s)
-    Wq, sw, Wop = sq.pack_weight(W, sd, want_q=(path != "tc"), want_op=(path == "tc"))
-    Xq, sx, Xop = sq.quantize_act(X, sd, want_q=(path != "tc"), want_op=(path == "tc"))
     b = case.bias.cuda() if case.bias is not None else None
     r = case.residual.cuda() if case.residual is not None else None
-    y = gpu_linear(sq, path, Xq, Xop, sx, Wq, Wop, sw, b, r, case.mode)
+    if path == "tc":
+        _, sw, Wop, wl1 = sq.pack_weight(W, sd, want_q=False, want_l1=True)
+        _, sx, Xop, xl1 = sq.quantize_act(X, sd, want_q=False, want_l1=True)
+        y = sq.linear_i8(Xop, sx, Wop, sw, b, r, case.mode, x_l1=xl1, w_l1=wl1)
+        return sx, y
+    Wq, sw, _ = sq.pack_weight(W, sd, want_op=False)
+    Xq, sx, _ = sq.quantize_act(X, sd, want_op=False)
+    y = gpu_linear(sq, path, Xq, None, sx, Wq, None, sw, b, r, case.mode)
     return sx, y
 
 
