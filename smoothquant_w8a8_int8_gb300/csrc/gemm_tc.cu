@@ -270,20 +270,70 @@ struct EpiArgs {
 // magnitude and the whole K accumulates exactly in one fp32 pass.
 constexpr int32_t kSinglePassL1 = 132104;
 
-// erf by Abramowitz & Stegun, Handbook of Mathematical Functions, formula
-// 7.1.26 (after Hastings): erf(x) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5))))
-// exp(-x^2), t = 1 / (1 + p x), x >= 0, odd extension for x < 0; absolute
-// error <= 1.5e-7.  Branch-free, so a warp never splits across ranges.
-__device__ __forceinline__ float erf_as7126(float x) {
-    const float ax = fabsf(x);
-    const float t = __fdividef(1.0f, fmaf(0.3275911f, ax, 1.0f));
-    float poly = fmaf(1.061405429f, t, -1.453152027f);
-    poly = fmaf(poly, t, 1.421413741f);
-    poly = fmaf(poly, t, -0.284496736f);
-    poly = fmaf(poly, t, 0.254829592f);
-    poly *= t;
-    const float r = fmaf(-poly, __expf(-ax * ax), 1.0f);
-    return copysignf(r, x);
+// ---- packed fp32 pairs (f32x2: two lanes of arithmetic per instruction) ----
+
+__device__ __forceinline__ unsigned long long pk(float a, float b) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void upk(unsigned long long r, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// GELU(t) = 0.5 t (1 + erf(t / sqrt 2)) on a pair.  erf by Abramowitz &
+// Stegun, Handbook of Mathematical Functions, formula 7.1.26 (after Hastings):
+// erf(x) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-x^2),
+// t = 1 / (1 + p x), x >= 0, odd extension for x < 0, absolute error <=
+// 1.5e-7 (the hardware reciprocal and exp2 approximations add a few ulp).
+// Branch-free, so a warp never splits across ranges.
+__device__ __forceinline__ unsigned long long gelu2(unsigned long long t2) {
+    const unsigned long long h2 = mul2(t2, pk(0.5f, 0.5f));
+    const unsigned long long u2 = mul2(t2, pk(0.70710678118654752f, 0.70710678118654752f));
+    float u0, u1;
+    upk(u2, u0, u1);
+    const unsigned long long a2 = pk(fabsf(u0), fabsf(u1));
+    float d0, d1;
+    upk(fma2(a2, pk(0.3275911f, 0.3275911f), pk(1.0f, 1.0f)), d0, d1);
+    const unsigned long long tt = pk(rcp_approx(d0), rcp_approx(d1));
+    // -poly(t) by Horner with negated coefficients, then 1 + (-poly) e
+    unsigned long long p2 = fma2(pk(-1.061405429f, -1.061405429f), tt,
+                                 pk(1.453152027f, 1.453152027f));
+    p2 = fma2(p2, tt, pk(-1.421413741f, -1.421413741f));
+    p2 = fma2(p2, tt, pk(0.284496736f, 0.284496736f));
+    p2 = fma2(p2, tt, pk(-0.254829592f, -0.254829592f));
+    p2 = mul2(p2, tt);
+    float e0, e1;
+    upk(mul2(mul2(a2, a2), pk(-1.4426950408889634f, -1.4426950408889634f)), e0, e1);
+    float r0, r1;
+    upk(fma2(p2, pk(ex2_approx(e0), ex2_approx(e1)), pk(1.0f, 1.0f)), r0, r1);
+    return fma2(h2, pk(copysignf(r0, u0), copysignf(r1, u1)), h2);
 }
 
 // Per-column epilogue operands of one tile half, spread over the warp: lane j
@@ -346,31 +396,37 @@ __device__ __forceinline__ void epilogue_slice(uint32_t (&v)[32], int64_t m, int
             for (int j = 0; j < 32; ++j) v[j] = (uint32_t)__float2int_rn(__uint_as_float(v[j]));
         }
     } else {
+        // two columns per step on packed fp32 pairs
+        const unsigned long long xs2 = pk(xs, xs);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const float w = __shfl_sync(0xffffffffu, wl, j);
-            // the exact integer sum as fp32 (|acc| < 2^31: one rounding at most)
-            const float x = INT_IN ? __int2float_rn((int32_t)v[j]) : __uint_as_float(v[j]);
-            const float sc = __fmul_rn(xs, w);
-            float o;
+        for (int j = 0; j < 32; j += 2) {
+            const unsigned long long w2 =
+                pk(__shfl_sync(0xffffffffu, wl, j), __shfl_sync(0xffffffffu, wl, j + 1));
+            // the exact integer sums as fp32 (|acc| < 2^31: one rounding at most)
+            const unsigned long long x2 =
+                INT_IN ? pk(__int2float_rn((int32_t)v[j]), __int2float_rn((int32_t)v[j + 1]))
+                       : pk(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+            const unsigned long long sc2 = mul2(xs2, w2);
+            unsigned long long o2;
             if (MODE == SQ_EPI_NONE) {
-                o = __fmul_rn(x, sc);
+                o2 = mul2(x2, sc2);
             } else {
-                const float b = __shfl_sync(0xffffffffu, bl, j);
-                const float t = __fmaf_rn(x, sc, b);
+                const unsigned long long b2 =
+                    pk(__shfl_sync(0xffffffffu, bl, j), __shfl_sync(0xffffffffu, bl, j + 1));
+                const unsigned long long t2 = fma2(x2, sc2, b2);
                 if (MODE == SQ_EPI_BIAS) {
-                    o = t;
+                    o2 = t2;
                 } else if (MODE == SQ_EPI_BIAS_GELU) {
-                    const float h = 0.5f * t;
-                    o = __fmaf_rn(h, erf_as7126(t * 0.70710678118654752f), h);
+                    o2 = gelu2(t2);
                 } else {
-                    const float rr = (j & 3) == 0 ? r4[j >> 2].x
-                                   : (j & 3) == 1 ? r4[j >> 2].y
-                                   : (j & 3) == 2 ? r4[j >> 2].z : r4[j >> 2].w;
-                    o = __fadd_rn(t, rr);
+                    const float4 rq = r4[j >> 2];
+                    o2 = add2(t2, (j & 2) ? pk(rq.z, rq.w) : pk(rq.x, rq.y));
                 }
             }
-            v[j] = __float_as_uint(o);
+            float o0, o1;
+            upk(o2, o0, o1);
+            v[j] = __float_as_uint(o0);
+            v[j + 1] = __float_as_uint(o1);
         }
     }
     if (a.tma_io) {
