@@ -396,3 +396,33 @@ def test_large_workloads_sampled(sq, path, name, index):
     sx_all = sx.cpu().numpy()
     v = X / s
     np.testing.assert_allclose(sx_all, np.abs(v).max(axis=1) / 127.0, rtol=2.5e-7)
+
+
+def test_host_pipeline_matches_direct_calls(sq):
+    """The host-streaming pipeline (copies overlapped with kernels on three
+    streams) returns exactly what the direct device calls return."""
+    from smoothquant_w8a8_int8_gb300.pipeline import HostLinearPipeline, LinearLayer
+    M = 300
+    shapes = [(256, 384, wl.EPI_BIAS), (384, 256, wl.EPI_BIAS_GELU), (256, 256, wl.EPI_BIAS_RESIDUAL),
+              (1040, 272, wl.EPI_BIAS_RESIDUAL), (272, 128, wl.EPI_NONE)]
+    layers, xh, yh, ref = [], [], [], []
+    for i, (K, N, mode) in enumerate(shapes):
+        c = wl.make_case(M, K, N, mode, seed=700 + i)
+        X, W = c.X.cuda(), c.W.cuda()
+        s = sq.smooth_factor(sq.channel_absmax(X), sq.channel_absmax(W), 0.5)
+        _, sw, Wop, wl1 = sq.pack_weight(W, s, want_q=False, want_l1=True)
+        b = c.bias.cuda() if c.bias is not None else None
+        r = c.residual.cuda() if c.residual is not None else None
+        _, sx, Xop = sq.quantize_act(X, s, want_q=False)
+        ref.append(sq.linear_i8(Xop, sx, Wop, sw, b, r, mode, w_l1=wl1).cpu())
+        layers.append(LinearLayer(s, Wop, sw, mode, b, r, wl1))
+        xh.append(c.X.pin_memory())
+        yh.append(torch.empty(M, N, dtype=torch.float32).pin_memory())
+    pipe = HostLinearPipeline(M, max(k for k, _, _ in shapes), max(n for _, n, _ in shapes))
+    for _ in range(2):
+        for y in yh:
+            y.zero_()
+        pipe.run(layers, xh, yh)
+        torch.cuda.synchronize()
+        for y, r in zip(yh, ref):
+            assert torch.equal(y, r)
