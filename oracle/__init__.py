@@ -16,6 +16,8 @@ Parity status per function (what pins each one, see ``tests/test_oracle.py``):
   smooth           exact invariant X W^T == (X/s)(W*s)^T for power-of-two s
   quantize_rows    hand-worked round-half-even example (golden file),
                    error bound |v - q*scale| <= scale/2, max code = 127
+  act_absmax /     hand-worked saturating example (golden file); a one-row
+  quantize_static  calibration set reproduces the dynamic codes
   gemm_i32         brute force in an outer-product order, closed forms
                    (all 127, cancelling signs, one-hot rows), overflow check
   epilogue         textbook normal-CDF values for GELU, zero-input cases
@@ -68,10 +70,13 @@ def _load():
             lib.oracle_linear_block.argtypes = [p, p, p, p, p, p, i64, i64, i64, i32,
                                                 p, p, p, p]
             lib.oracle_num_threads.argtypes = []
+            lib.oracle_act_absmax.argtypes = [p, p, i64, i64, p]
+            lib.oracle_quantize_static.argtypes = [p, p, i64, i64, ctypes.c_float, p]
             for f in (lib.oracle_channel_absmax, lib.oracle_smooth_factor,
                       lib.oracle_smooth, lib.oracle_quantize_rows,
                       lib.oracle_gemm_i32, lib.oracle_epilogue,
-                      lib.oracle_linear_block, lib.oracle_num_threads):
+                      lib.oracle_linear_block, lib.oracle_num_threads,
+                      lib.oracle_act_absmax, lib.oracle_quantize_static):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -140,6 +145,33 @@ def quantize_rows(A, s, direction):
     _check(_load().oracle_quantize_rows(_ptr(A), _ptr(s), rows, K, d, _ptr(q),
                                         _ptr(scale)), "quantize_rows")
     return q, scale
+
+
+def act_absmax(X, s, amax=0.0):
+    """Per-tensor running max of |X / s| (Smooth-Static calibration, Table 10)."""
+    X = _c(X, np.float32)
+    s = _c(s, np.float32)
+    rows, K = X.shape
+    out = np.array([amax], np.float32)
+    _check(_load().oracle_act_absmax(_ptr(X), _ptr(s), rows, K, _ptr(out)), "act_absmax")
+    return out[0]
+
+
+def static_scale(amax):
+    """fl32(amax / 127), or 1 for a zero maximum."""
+    amax = np.float32(amax)
+    return np.float32(1.0) if amax == 0 else np.float32(amax / np.float32(127.0))
+
+
+def quantize_static(X, s, scale):
+    """Smooth-Static codes with one offline per-tensor scale (saturating)."""
+    X = _c(X, np.float32)
+    s = _c(s, np.float32)
+    rows, K = X.shape
+    q = np.empty((rows, K), np.int8)
+    _check(_load().oracle_quantize_static(_ptr(X), _ptr(s), rows, K, float(np.float32(scale)),
+                                          _ptr(q)), "quantize_static")
+    return q
 
 
 def gemm_i32(xq, wq):

@@ -135,6 +135,43 @@ int oracle_quantize_rows(const float *A, const float *s, int64_t rows, int64_t K
     return ORC_OK;
 }
 
+/* Smooth-Static calibration (Table 10, "SmoothQuant, static quantization"):
+ * the per-tensor running maximum of the smoothed activations,
+ *   amax = max(amax, max_{i,j} |fl(X[i][j] / s[j])|),
+ * over one calibration batch.  The static scale is fl(amax / 127), or 1 when
+ * amax is 0. */
+int oracle_act_absmax(const float *X, const float *s, int64_t rows, int64_t K, float *amax)
+{
+    if (rows < 0 || K < 0) return ORC_ERR_ARG;
+    float m = *amax;
+    for (int64_t i = 0; i < rows; ++i)
+        for (int64_t j = 0; j < K; ++j) {
+            float v = fabsf(X[i * K + j] / s[j]);
+            if (v > m) m = v;
+        }
+    *amax = m;
+    return ORC_OK;
+}
+
+/* Smooth-Static quantisation with one per-tensor scale fixed offline:
+ *   q[i][j] = clamp(round_half_even(fl(fl(X[i][j] / s[j]) / scale)), -127, 127)
+ * Values beyond the calibrated range saturate at +-127. */
+int oracle_quantize_static(const float *X, const float *s, int64_t rows, int64_t K,
+                           float scale, int8_t *q)
+{
+    if (rows < 0 || K < 0 || !(scale > 0.0f)) return ORC_ERR_ARG;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < rows; ++i)
+        for (int64_t j = 0; j < K; ++j) {
+            float v = X[i * K + j] / s[j];
+            float n = nearbyintf(v / scale);
+            if (n > 127.0f) n = 127.0f;
+            if (n < -127.0f) n = -127.0f;
+            q[i * K + j] = (int8_t)n;
+        }
+    return ORC_OK;
+}
+
 /* Exact integer contraction acc[m][n] = sum_k xq[m][k] * wq[n][k]
  * (both operands K-contiguous: X is tokens x K, W is the nn.Linear
  * out x in layout).  Summed in int64; any result outside int32 is an error. */

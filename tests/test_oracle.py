@@ -242,3 +242,40 @@ def test_linear_block_matches_steps():
     # the quantised block approximates the fp64 linear layer
     ref = X.astype(np.float64) @ W.astype(np.float64).T + c.bias.numpy() + c.residual.numpy()
     assert np.max(np.abs(y - ref)) < 0.05 * np.max(np.abs(ref))
+
+
+# --------------------------------------------------------------- Smooth-Static
+
+def test_static_hand_example(golden_dir):
+    for scale, vals, codes in parse_golden(os.path.join(golden_dir, "quantize_static_example.txt")):
+        X = np.array([[float(v) for v in vals.split()]], np.float32)
+        q = oracle.quantize_static(X, np.ones(X.shape[1], np.float32), np.float32(float(scale)))
+        np.testing.assert_array_equal(q[0], np.array([int(c) for c in codes.split()], np.int8))
+
+
+def test_static_calibration_on_one_row_equals_dynamic():
+    """Calibrating the static scale on a single row gives that row's dynamic
+    scale and therefore the dynamic codes."""
+    c = workloads.make_case(6, 64, 8, workloads.EPI_BIAS, seed=21)
+    X = c.X.numpy()
+    s = (np.abs(np.random.default_rng(3).standard_normal(64)) + 0.5).astype(np.float32)
+    qd, sd = oracle.quantize_rows(X, s, "act")
+    for i in range(X.shape[0]):
+        amax = oracle.act_absmax(X[i:i + 1], s)
+        sc = oracle.static_scale(amax)
+        assert sc.view(np.uint32) == sd[i].view(np.uint32)
+        np.testing.assert_array_equal(oracle.quantize_static(X[i:i + 1], s, sc)[0], qd[i])
+
+
+def test_static_absmax_running_and_brute_force():
+    rng = np.random.default_rng(4)
+    A = rng.standard_normal((5, 16)).astype(np.float32)
+    B = (rng.standard_normal((3, 16)) * 4).astype(np.float32)
+    s = (rng.uniform(0.5, 2.0, 16)).astype(np.float32)
+    want = max(abs(float(np.float32(A[i, j]) / np.float32(s[j]))) for i in range(5) for j in range(16))
+    a = oracle.act_absmax(A, s)
+    assert a == np.float32(want)
+    want2 = max(want, max(abs(float(np.float32(B[i, j]) / np.float32(s[j])))
+                          for i in range(3) for j in range(16)))
+    assert oracle.act_absmax(B, s, a) == np.float32(want2)
+    assert oracle.static_scale(0.0) == 1.0
