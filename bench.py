@@ -139,10 +139,11 @@ class ClockSampler:
 
 class Layer:
     __slots__ = ("lin", "X", "s", "Wop", "Wq", "sw", "wl1", "bias", "residual", "Y", "Xhost",
-                 "Yhost")
+                 "Yhost", "static_scale")
 
 
-def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool):
+def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
+                   quant: str = "dynamic"):
     from smoothquant_w8a8_int8_gb300 import binding as sq
     dev = torch.device("cuda")
     layers = []
@@ -166,6 +167,13 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool):
                                           want_op=(gemm == "tc"), want_l1=True)
         L.Wq, L.sw, L.Wop, L.wl1 = Wq, sw, Wop, wl1
         L.bias, L.residual = c.bias, c.residual
+        L.static_scale = None
+        if quant == "static":
+            # Smooth-Static: the per-tensor scale is calibrated offline on a
+            # separate batch drawn from the same distribution
+            calib = wl.make_activation(512, lin.K, seed + 555, w.outlier_frac, w.outlier_scale,
+                                       lin.gelu_input, device=dev, channel_seed=seed)
+            L.static_scale = sq.static_scale(sq.act_absmax(calib, s).item())
         L.Y = torch.empty(w.M, lin.N, dtype=torch.float32, device=dev)
         L.Xhost = L.Yhost = None
         if want_host:
@@ -186,7 +194,10 @@ def run_layer(sq, gemm, L, bufs, M, X=None, ev=None):
         Xop = Xop_buf[: M * K].view(M, K)
         if ev is not None:
             ev[0].record()
-        sq.quantize_act(X, L.s, out=(None, sx_buf, Xop))
+        if L.static_scale is not None:
+            sq.quantize_act_static(X, L.s, L.static_scale, out=(None, sx_buf, Xop))
+        else:
+            sq.quantize_act(X, L.s, out=(None, sx_buf, Xop))
         if ev is not None:
             ev[1].record()
         # the packed weights' row L1 norms let the GEMM prove single-pass exactness
@@ -210,7 +221,8 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
     from smoothquant_w8a8_int8_gb300 import binding as sq
     sq.load()
     peaks, peak_src = load_peaks()
-    layers, bufs = setup_workload(w, args.gemm, rank, want_host=args.e2e_steps > 0)
+    layers, bufs = setup_workload(w, args.gemm, rank, want_host=args.e2e_steps > 0,
+                                  quant=args.quant)
     M = w.M
     n_gemm = len(layers)
 
@@ -278,8 +290,8 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
     if args.e2e_steps > 0:
         from smoothquant_w8a8_int8_gb300.pipeline import HostLinearPipeline, LinearLayer
         pipe = HostLinearPipeline(M, max(L.lin.K for L in layers), max(L.lin.N for L in layers))
-        specs = [LinearLayer(L.s, L.Wop, L.sw, L.lin.mode, L.bias, L.residual, L.wl1)
-                 for L in layers]
+        specs = [LinearLayer(L.s, L.Wop, L.sw, L.lin.mode, L.bias, L.residual, L.wl1,
+                             L.static_scale) for L in layers]
         xh = [L.Xhost for L in layers]
         yh = [L.Yhost for L in layers]
         h2d = sum(L.Xhost.numel() * 4 for L in layers)
@@ -327,6 +339,10 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
                    "l2": "inputs larger than L2: every GEMM reads its own activations "
                          f"({sum(L.X.numel() * 4 for L in layers) / 1e9:.1f} GB per step)",
                    "weights": "packed once before the timed region",
+                   "quantisation": ("Smooth-Static (per-tensor scale calibrated offline on a "
+                                    "separate 512-token batch of the same distribution)"
+                                    if args.quant == "static"
+                                    else "Smooth-Dynamic (per-token scales at run time)"),
                    "parallelism": f"replicas x{world} (rows shard, no collective)"},
         "roofline": {"bound": "tensor", "kernel": "gemm+epilogue",
                      "achieved": round(gemm_tops, 2), "peak": peak_tensor,
@@ -440,6 +456,9 @@ def main():
     ap.add_argument("--workload", default="bert_large_encoder_b32_s256",
                     choices=list(wl.WORKLOADS))
     ap.add_argument("--gemm", choices=["tc", "mma_sync"], default="tc")
+    ap.add_argument("--quant", choices=["dynamic", "static"], default="dynamic",
+                    help="activation quantisation: per-token dynamic (Smooth-Dynamic, the "
+                         "default) or per-tensor static (Smooth-Static)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-step-seconds", type=float, default=2.0)

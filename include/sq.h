@@ -124,6 +124,26 @@ sq_status sq_pack_weight(const float *W, const float *s, int64_t N, int64_t K, i
 sq_status sq_quantize_act(const float *X, const float *s, int64_t M, int64_t K, int8_t *Xq,
                           float *x_scale, void *Xop, int32_t *x_row_l1, void *stream);
 
+/* ---- Smooth-Static: per-tensor activation scale fixed offline (Table 10) --- */
+
+/* Calibration statistic for Smooth-Static:
+ *   *amax = max(*amax, max_{m,j} |X[m][j] / s[j]|)     (IEEE fp32 division)
+ * X fp32 [M][K], s fp32 [K]; amax one float (4-byte aligned), initialised by
+ * the caller (0 for a fresh statistic) and accumulated over calibration
+ * batches.  The static scale is then fl32(amax / 127) (1 if amax is 0),
+ * computed by the caller in fp32. */
+sq_status sq_act_absmax(const float *X, const float *s, int64_t M, int64_t K, float *amax,
+                        void *stream);
+
+/* Smooth-Static quantisation with one per-tensor scale `scale` (> 0, finite):
+ *   Xq[m][j] = clamp(round_half_even(fl(fl(X[m][j] / s[j]) / scale)), -127, 127)
+ * (values beyond the calibrated range saturate).  Outputs as sq_quantize_act;
+ * x_scale[m] is set to `scale` for every token, so sq_linear_i8 applies the
+ * per-tensor dequantisation unchanged. */
+sq_status sq_quantize_act_static(const float *X, const float *s, int64_t M, int64_t K,
+                                 float scale, int8_t *Xq, float *x_scale, void *Xop,
+                                 int32_t *x_row_l1, void *stream);
+
 /* ---- INT8 GEMM + fused dequantising epilogue ------------------------------ */
 
 /* acc[m][n] = sum_k Xq[m][k] * Wq[n][k], exact in int32, then the epilogue

@@ -21,8 +21,9 @@ SQ_OK, SQ_ERR_INVALID_ARG, SQ_ERR_ALIGNMENT, SQ_ERR_UNSUPPORTED, SQ_ERR_CUDA, SQ
 EPI_NONE, EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESIDUAL, EPI_RAW_I32 = range(5)
 
 EXPORTS = ("sq_status_string", "sq_version", "sq_operand_bytes", "sq_channel_absmax",
-           "sq_smooth_factor", "sq_pack_weight", "sq_quantize_act", "sq_linear_i8",
-           "sq_linear_i8_mma_sync", "sq_device_status")
+           "sq_smooth_factor", "sq_pack_weight", "sq_quantize_act", "sq_act_absmax",
+           "sq_quantize_act_static", "sq_linear_i8", "sq_linear_i8_mma_sync",
+           "sq_device_status")
 
 _lock = threading.Lock()
 _lib = None
@@ -53,6 +54,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                 "sq_smooth_factor": ([vp, vp, i64, f32, vp, vp], i32),
                 "sq_pack_weight": ([vp, vp, i64, i64, vp, vp, vp, vp, vp], i32),
                 "sq_quantize_act": ([vp, vp, i64, i64, vp, vp, vp, vp, vp], i32),
+                "sq_act_absmax": ([vp, vp, i64, i64, vp, vp], i32),
+                "sq_quantize_act_static": ([vp, vp, i64, i64, f32, vp, vp, vp, vp, vp], i32),
                 "sq_linear_i8": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp],
                                  i32),
                 "sq_linear_i8_mma_sync": ([vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp], i32),
@@ -163,6 +166,44 @@ def quantize_act(X: torch.Tensor, s: torch.Tensor, want_q: bool = True, want_op:
                                   _stream(stream)), "sq_quantize_act")
     if want_l1 or (out is not None and len(out) > 3):
         return Xq, sx, Xop, l1
+    return Xq, sx, Xop
+
+
+def act_absmax(X: torch.Tensor, s: torch.Tensor, amax: Optional[torch.Tensor] = None,
+               stream=None):
+    """Smooth-Static calibration: amax = max(amax, max |X / s|) (one float)."""
+    _need(X, torch.float32, "X")
+    M, K = X.shape
+    _need(s, torch.float32, "s", (K,))
+    if amax is None:
+        amax = torch.zeros(1, dtype=torch.float32, device=X.device)
+    _check(load().sq_act_absmax(_p(X), _p(s), M, K, _p(amax), _stream(stream)), "sq_act_absmax")
+    return amax
+
+
+def static_scale(amax: float) -> float:
+    """The per-tensor static scale fl32(amax / 127) (1 for a zero maximum)."""
+    import numpy as np
+    a = np.float32(amax)
+    return float(np.float32(1.0) if a == 0 else np.float32(a / np.float32(127.0)))
+
+
+def quantize_act_static(X: torch.Tensor, s: torch.Tensor, scale: float, want_q: bool = True,
+                        want_op: bool = True, out=None, stream=None):
+    """Smooth-Static quantisation with a fixed per-tensor scale; returns
+    (Xq or None, x_scale [M] filled with scale, Xop or None)."""
+    _need(X, torch.float32, "X")
+    M, K = X.shape
+    _need(s, torch.float32, "s", (K,))
+    if out is not None:
+        Xq, sx, Xop = out
+    else:
+        Xq = torch.empty(M, K, dtype=torch.int8, device=X.device) if want_q else None
+        Xop = empty_operand(M, K, X.device) if want_op else None
+        sx = torch.empty(M, dtype=torch.float32, device=X.device)
+    _check(load().sq_quantize_act_static(_p(X), _p(s), M, K, float(scale), _p(Xq), _p(sx),
+                                         _p(Xop), None, _stream(stream)),
+           "sq_quantize_act_static")
     return Xq, sx, Xop
 
 

@@ -133,7 +133,7 @@ sq_status sq_pack_weight(const float *W, const float *s, int64_t N, int64_t K, i
     if ((rc = require_sm103()) != SQ_OK) return rc;
     if (w_row_l1 && !aligned4(w_row_l1)) return SQ_ERR_ALIGNMENT;
     return launch_quantize_rows(1, W, s, N, K, Wq, w_scale, static_cast<__nv_bfloat16 *>(Wop),
-                                w_row_l1, as_stream(stream));
+                                w_row_l1, 0.0f, as_stream(stream));
 }
 
 sq_status sq_quantize_act(const float *X, const float *s, int64_t M, int64_t K, int8_t *Xq,
@@ -144,7 +144,32 @@ sq_status sq_quantize_act(const float *X, const float *s, int64_t M, int64_t K, 
     if ((rc = require_sm103()) != SQ_OK) return rc;
     if (x_row_l1 && !aligned4(x_row_l1)) return SQ_ERR_ALIGNMENT;
     return launch_quantize_rows(0, X, s, M, K, Xq, x_scale, static_cast<__nv_bfloat16 *>(Xop),
-                                x_row_l1, as_stream(stream));
+                                x_row_l1, 0.0f, as_stream(stream));
+}
+
+sq_status sq_act_absmax(const float *X, const float *s, int64_t M, int64_t K, float *amax,
+                        void *stream) {
+    if (M < 0 || K <= 0) return SQ_ERR_INVALID_ARG;
+    if (K % 16 != 0) return SQ_ERR_ALIGNMENT;
+    if (M == 0) return SQ_OK;
+    if (!X || !s || !amax) return SQ_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(s) || !aligned4(amax)) return SQ_ERR_ALIGNMENT;
+    sq_status rc = require_sm103();
+    if (rc != SQ_OK) return rc;
+    return launch_act_absmax(X, s, M, K, amax, as_stream(stream));
+}
+
+sq_status sq_quantize_act_static(const float *X, const float *s, int64_t M, int64_t K,
+                                 float scale, int8_t *Xq, float *x_scale, void *Xop,
+                                 int32_t *x_row_l1, void *stream) {
+    if (!(scale > 0.0f) || !(scale <= 3.4028234663852886e38f)) return SQ_ERR_INVALID_ARG;
+    sq_status rc = check_quant_args(X, s, M, K, Xq, x_scale, Xop);
+    if (rc != SQ_OK) return rc;
+    if (M == 0) return SQ_OK;
+    if (x_row_l1 && !aligned4(x_row_l1)) return SQ_ERR_ALIGNMENT;
+    if ((rc = require_sm103()) != SQ_OK) return rc;
+    return launch_quantize_rows(2, X, s, M, K, Xq, x_scale, static_cast<__nv_bfloat16 *>(Xop),
+                                x_row_l1, scale, as_stream(stream));
 }
 
 sq_status sq_linear_i8(const void *Xop, const float *x_scale, const int32_t *x_row_l1,

@@ -27,9 +27,12 @@ sq_status launch_channel_absmax(const float *A, int64_t rows, int64_t cols, floa
                                 cudaStream_t st);
 sq_status launch_smooth_factor(const float *ax, const float *aw, int64_t K, float alpha,
                                float *s, cudaStream_t st);
+// direction: 0 dynamic activations, 1 weights, 2 static activations (fixed_scale)
 sq_status launch_quantize_rows(int direction, const float *A, const float *s, int64_t rows,
                                int64_t K, int8_t *q, float *scale, __nv_bfloat16 *op,
-                               int32_t *l1, cudaStream_t st);
+                               int32_t *l1, float fixed_scale, cudaStream_t st);
+sq_status launch_act_absmax(const float *A, const float *s, int64_t rows, int64_t K,
+                            float *amax, cudaStream_t st);
 sq_status launch_gemm_mma_sync(const int8_t *Xq, const float *sx, const int8_t *Wq,
                                const float *sw, const float *bias, const float *residual,
                                int64_t M, int64_t N, int64_t K, int mode, void *Y,

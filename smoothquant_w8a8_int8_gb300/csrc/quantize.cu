@@ -25,9 +25,13 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kMaxVPT = 8;  // float4 per thread held in registers: K <= 256 * 8 * 4
 
-__device__ __forceinline__ float smooth_one(float x, float s, int direction) {
+// Row kinds: dynamic activations (per-token scale from the row maximum),
+// weights (per-output-channel scale), static activations (one given scale).
+constexpr int kActDynamic = 0, kWeight = 1, kActStatic = 2;
+
+__device__ __forceinline__ float smooth_one(float x, float s, int kind) {
     // activations: x / s (IEEE division); weights: x * s
-    return direction == 0 ? __fdiv_rn(x, s) : __fmul_rn(x, s);
+    return kind == kWeight ? __fmul_rn(x, s) : __fdiv_rn(x, s);
 }
 
 // round_half_even(fl(v / scale)), clamped to [-127, 127], returned as an
@@ -46,6 +50,21 @@ __device__ __forceinline__ float code_of(float v, float scale, float rscale) {
     const float k = rintf(p);
     if (fabsf(__fsub_rn(p, k)) <= 0.49993896484375f) return k;  // 0.5 - 2^-14
     const float e = rintf(__fdiv_rn(v, scale));                 // round half to even
+    return fminf(127.0f, fmaxf(-127.0f, e));
+}
+
+// Static-scale code: round_half_even(fl(v / scale)) clamped to [-127, 127]
+// for any finite v.  p = fl(v * fl(1/scale)) is within a relative 3u of the
+// quotient; |p| >= 128 means the quotient exceeds 127.5 in magnitude (the
+// code saturates); below that p is within 2.3e-5 of fl(v/scale), so its
+// rounding decides unless p lies within 2^-14 of a half-integer.
+__device__ __forceinline__ float static_code(float v, float scale, float rscale) {
+    const float p = __fmul_rn(v, rscale);
+    if (fabsf(p) >= 128.0f) return copysignf(127.0f, p);
+    const float k = rintf(p);
+    if (fabsf(__fsub_rn(p, k)) <= 0.49993896484375f)  // 0.5 - 2^-14
+        return fminf(127.0f, fmaxf(-127.0f, k));
+    const float e = rintf(__fdiv_rn(v, scale));
     return fminf(127.0f, fmaxf(-127.0f, e));
 }
 
@@ -71,10 +90,13 @@ __device__ __forceinline__ void store_code_values(float c0, float c1, float c2, 
 }
 
 // Writes four codes; returns the sum of their magnitudes (for the row L1 norm).
+template <int KIND>
 __device__ __forceinline__ float store_codes(float4 v, float scale, float rscale, int64_t off4,
                                              int8_t *q, __nv_bfloat16 *op) {
-    const float c0 = code_of(v.x, scale, rscale), c1 = code_of(v.y, scale, rscale);
-    const float c2 = code_of(v.z, scale, rscale), c3 = code_of(v.w, scale, rscale);
+    auto code = [&](float x) {
+        return KIND == kActStatic ? static_code(x, scale, rscale) : code_of(x, scale, rscale);
+    };
+    const float c0 = code(v.x), c1 = code(v.y), c2 = code(v.z), c3 = code(v.w);
     store_code_values(c0, c1, c2, c3, off4, q, op);
     return (fabsf(c0) + fabsf(c1)) + (fabsf(c2) + fabsf(c3));
 }
@@ -118,7 +140,7 @@ template <int DIR, int kVPT>
 __global__ void __launch_bounds__(kThreads) quantize_rows_reg(
     const float *__restrict__ A, const float *__restrict__ s, int64_t rows, int K4, int tpr,
     int8_t *__restrict__ q, float *__restrict__ scale, __nv_bfloat16 *__restrict__ op,
-    int32_t *__restrict__ l1) {
+    int32_t *__restrict__ l1, float fixed_scale) {
     __shared__ float red[kThreads / 32];
     const int rpb = kThreads / tpr;
     const int g = threadIdx.x / tpr;
@@ -149,11 +171,15 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_reg(
             v[i].y = smooth_one(v[i].y, sv[i].y, DIR);
             v[i].z = smooth_one(v[i].z, sv[i].z, DIR);
             v[i].w = smooth_one(v[i].w, sv[i].w, DIR);
-            m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)),
-                               fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+            if (DIR != kActStatic)
+                m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)),
+                                   fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
         }
-        m = group_max(m, tpr, red);
-        const float sc = m == 0.0f ? 1.0f : __fdiv_rn(m, 127.0f);
+        float sc = fixed_scale;
+        if (DIR != kActStatic) {
+            m = group_max(m, tpr, red);
+            sc = m == 0.0f ? 1.0f : __fdiv_rn(m, 127.0f);
+        }
         const float rsc = __frcp_rn(sc);
         float a1 = 0.0f;  // sum of |code| (exact: at most 127 * 8192 < 2^24)
         if (valid) {
@@ -161,7 +187,7 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_reg(
 #pragma unroll
             for (int i = 0; i < kVPT; ++i) {
                 int j = t + i * tpr;
-                if (j < K4) a1 += store_codes(v[i], sc, rsc, row * K4 + j, q, op);
+                if (j < K4) a1 += store_codes<DIR>(v[i], sc, rsc, row * K4 + j, q, op);
             }
         }
         if (l1) {
@@ -176,21 +202,24 @@ template <int DIR>
 __global__ void __launch_bounds__(kThreads) quantize_rows_loop(
     const float *__restrict__ A, const float *__restrict__ s, int64_t rows, int K4,
     int8_t *__restrict__ q, float *__restrict__ scale, __nv_bfloat16 *__restrict__ op,
-    int32_t *__restrict__ l1) {
+    int32_t *__restrict__ l1, float fixed_scale) {
     __shared__ float red[kThreads / 32];
     const float4 *s4 = reinterpret_cast<const float4 *>(s);
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
         const float4 *a4 = reinterpret_cast<const float4 *>(A) + row * K4;
-        float m = 0.0f;
-        for (int j = threadIdx.x; j < K4; j += kThreads) {
-            float4 x = __ldg(a4 + j), sv = __ldg(s4 + j);
-            m = fmaxf(m, fmaxf(fmaxf(fabsf(smooth_one(x.x, sv.x, DIR)),
-                                     fabsf(smooth_one(x.y, sv.y, DIR))),
-                               fmaxf(fabsf(smooth_one(x.z, sv.z, DIR)),
-                                     fabsf(smooth_one(x.w, sv.w, DIR)))));
+        float sc = fixed_scale;
+        if (DIR != kActStatic) {
+            float m = 0.0f;
+            for (int j = threadIdx.x; j < K4; j += kThreads) {
+                float4 x = __ldg(a4 + j), sv = __ldg(s4 + j);
+                m = fmaxf(m, fmaxf(fmaxf(fabsf(smooth_one(x.x, sv.x, DIR)),
+                                         fabsf(smooth_one(x.y, sv.y, DIR))),
+                                   fmaxf(fabsf(smooth_one(x.z, sv.z, DIR)),
+                                         fabsf(smooth_one(x.w, sv.w, DIR)))));
+            }
+            m = group_max(m, kThreads, red);
+            sc = m == 0.0f ? 1.0f : __fdiv_rn(m, 127.0f);
         }
-        m = group_max(m, kThreads, red);
-        const float sc = m == 0.0f ? 1.0f : __fdiv_rn(m, 127.0f);
         const float rsc = __frcp_rn(sc);
         if (threadIdx.x == 0) scale[row] = sc;
         int a1 = 0;  // integer: long rows may exceed 2^24
@@ -198,7 +227,7 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_loop(
             float4 x = __ldcs(a4 + j), sv = __ldg(s4 + j);
             float4 v = make_float4(smooth_one(x.x, sv.x, DIR), smooth_one(x.y, sv.y, DIR),
                                    smooth_one(x.z, sv.z, DIR), smooth_one(x.w, sv.w, DIR));
-            a1 += (int)store_codes(v, sc, rsc, row * K4 + j, q, op);
+            a1 += (int)store_codes<DIR>(v, sc, rsc, row * K4 + j, q, op);
         }
         if (l1) {
 #pragma unroll
@@ -213,6 +242,27 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_loop(
             __syncthreads();
         }
     }
+}
+
+// Smooth-Static calibration: per-tensor maximum of |fl(x / s)| (IEEE
+// division; offline), merged into *amax with an integer atomicMax.
+__global__ void __launch_bounds__(kThreads) act_absmax_kernel(const float *__restrict__ A,
+                                                              const float *__restrict__ s,
+                                                              int64_t rows, int K4,
+                                                              float *__restrict__ amax) {
+    const float4 *a4 = reinterpret_cast<const float4 *>(A);
+    const float4 *s4 = reinterpret_cast<const float4 *>(s);
+    const int64_t total = rows * (int64_t)K4;
+    float m = 0.0f;
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * kThreads) {
+        const float4 x = __ldcs(a4 + i), sv = __ldg(s4 + (int)(i % K4));
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(__fdiv_rn(x.x, sv.x)), fabsf(__fdiv_rn(x.y, sv.y))),
+                           fmaxf(fabsf(__fdiv_rn(x.z, sv.z)), fabsf(__fdiv_rn(x.w, sv.w)))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<int *>(amax), __float_as_int(m));
 }
 
 // Column maxima, merged into amax with an integer atomicMax (the bit patterns
@@ -250,7 +300,7 @@ int resident_blocks(Kern k) {
 
 sq_status launch_quantize_rows(int direction, const float *A, const float *s, int64_t rows,
                                int64_t K, int8_t *q, float *scale, __nv_bfloat16 *op,
-                               int32_t *l1, cudaStream_t st) {
+                               int32_t *l1, float fixed_scale, cudaStream_t st) {
     DeviceInfo di;
     sq_status rc = device_info(&di);
     if (rc != SQ_OK) return rc;
@@ -265,19 +315,38 @@ sq_status launch_quantize_rows(int direction, const float *A, const float *s, in
         const int rpb = kThreads / tpr;
         const int64_t tiles = (rows + rpb - 1) / rpb;
         void (*kern)(const float *, const float *, int64_t, int, int, int8_t *, float *,
-                     __nv_bfloat16 *, int32_t *);
-        if (direction == 0) kern = small ? quantize_rows_reg<0, 4> : quantize_rows_reg<0, 8>;
-        else kern = small ? quantize_rows_reg<1, 4> : quantize_rows_reg<1, 8>;
-        static int per_sm[2][2] = {{0, 0}, {0, 0}};
+                     __nv_bfloat16 *, int32_t *, float);
+        if (direction == kActDynamic)
+            kern = small ? quantize_rows_reg<kActDynamic, 4> : quantize_rows_reg<kActDynamic, 8>;
+        else if (direction == kWeight)
+            kern = small ? quantize_rows_reg<kWeight, 4> : quantize_rows_reg<kWeight, 8>;
+        else
+            kern = small ? quantize_rows_reg<kActStatic, 4> : quantize_rows_reg<kActStatic, 8>;
+        static int per_sm[3][2] = {{0, 0}, {0, 0}, {0, 0}};
         int &occ = per_sm[direction][small ? 0 : 1];
         if (!occ) occ = resident_blocks(kern);
         const int64_t grid = std::min<int64_t>(tiles, (int64_t)di.sms * occ);
-        kern<<<(unsigned)grid, kThreads, 0, st>>>(A, s, rows, K4, tpr, q, scale, op, l1);
+        kern<<<(unsigned)grid, kThreads, 0, st>>>(A, s, rows, K4, tpr, q, scale, op, l1,
+                                                  fixed_scale);
     } else {
-        auto kern = direction == 0 ? quantize_rows_loop<0> : quantize_rows_loop<1>;
+        auto kern = direction == kActDynamic ? quantize_rows_loop<kActDynamic>
+                    : direction == kWeight       ? quantize_rows_loop<kWeight>
+                                                 : quantize_rows_loop<kActStatic>;
         const int64_t grid = std::min<int64_t>(rows, (int64_t)di.sms * 8);
-        kern<<<(unsigned)grid, kThreads, 0, st>>>(A, s, rows, K4, q, scale, op, l1);
+        kern<<<(unsigned)grid, kThreads, 0, st>>>(A, s, rows, K4, q, scale, op, l1, fixed_scale);
     }
+    return cuda_status(cudaGetLastError());
+}
+
+sq_status launch_act_absmax(const float *A, const float *s, int64_t rows, int64_t K,
+                            float *amax, cudaStream_t st) {
+    DeviceInfo di;
+    sq_status rc = device_info(&di);
+    if (rc != SQ_OK) return rc;
+    const int64_t total4 = rows * (K / 4);
+    const int64_t grid = std::max<int64_t>(
+        1, std::min<int64_t>((total4 + kThreads - 1) / kThreads, (int64_t)di.sms * 8));
+    act_absmax_kernel<<<(unsigned)grid, kThreads, 0, st>>>(A, s, rows, (int)(K / 4), amax);
     return cuda_status(cudaGetLastError());
 }
 

@@ -30,6 +30,7 @@ class LinearLayer:
     bias: Optional[torch.Tensor] = None
     residual: Optional[torch.Tensor] = None   # [M, N] fp32, device
     w_l1: Optional[torch.Tensor] = None       # [N] int32 row L1 norms of the codes
+    static_scale: Optional[float] = None      # Smooth-Static per-tensor scale, else dynamic
 
 
 class HostLinearPipeline:
@@ -78,7 +79,11 @@ class HostLinearPipeline:
                 if y_free[slot] is not None:
                     self.comp.wait_event(y_free[slot])
                 xop = self.xop[: M * K].view(M, K)
-                sq.quantize_act(dX, L.s, out=(None, self.sx, xop), stream=self.comp)
+                if L.static_scale is not None:
+                    sq.quantize_act_static(dX, L.s, L.static_scale, out=(None, self.sx, xop),
+                                           stream=self.comp)
+                else:
+                    sq.quantize_act(dX, L.s, out=(None, self.sx, xop), stream=self.comp)
                 ev = torch.cuda.Event()
                 ev.record(self.comp)
                 x_free[slot] = ev

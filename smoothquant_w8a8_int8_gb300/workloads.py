@@ -118,13 +118,18 @@ def gemm_seed(w: Workload, layer: int, index: int) -> int:
 
 
 def make_activation(M: int, K: int, seed: int, outlier_frac: float, outlier_scale: float,
-                    gelu_input: bool = False, device="cpu") -> torch.Tensor:
-    """X [M, K] fp32: N(0,1) (or GELU(Z)), outlier channels multiplied."""
+                    gelu_input: bool = False, device="cpu",
+                    channel_seed: Optional[int] = None) -> torch.Tensor:
+    """X [M, K] fp32: N(0,1) (or GELU(Z)), outlier channels multiplied.  The
+    outlier channels come from `channel_seed` (default: `seed`) alone, so a
+    calibration batch drawn with another seed but the same channel seed has
+    the same outlier channels."""
+    ch = outlier_channels(K, outlier_frac, _gen(seed if channel_seed is None else channel_seed,
+                                                 device))
     g = _gen(seed, device)
     X = torch.randn(M, K, generator=g, device=device, dtype=torch.float32)
     if gelu_input:
         X = 0.5 * X * (1.0 + torch.erf(X * (1.0 / math.sqrt(2.0))))
-    ch = outlier_channels(K, outlier_frac, g)
     if ch.numel():
         X[:, ch] *= outlier_scale
     return X.contiguous()

@@ -101,6 +101,18 @@ def test_argument_checks_fail_before_any_launch(lib):
         assert fn(a, a, a, a, a, None, 0, 8, 32, 1, a, None) == 0          # empty
         assert fn(a, a, a, a, a, None, 8, 0, 32, 1, a, None) == 0
         assert fn(None, None, None, None, None, None, 0, 0, 32, 3, None, None) == 0
+    # Smooth-Static
+    lib.sq_act_absmax.argtypes = [vp, vp, i64, i64, vp, vp]
+    lib.sq_quantize_act_static.argtypes = [vp, vp, i64, i64, ctypes.c_float, vp, vp, vp, vp, vp]
+    assert lib.sq_act_absmax(None, a, 4, 32, a, None) == INVALID
+    assert lib.sq_act_absmax(a, a, 4, 24, a, None) == ALIGN
+    assert lib.sq_act_absmax(None, None, 0, 32, None, None) == 0
+    assert lib.sq_quantize_act_static(a, a, 4, 32, 0.0, a, a, None, None, None) == INVALID
+    assert lib.sq_quantize_act_static(a, a, 4, 32, -1.0, a, a, None, None, None) == INVALID
+    assert lib.sq_quantize_act_static(a, a, 4, 32, float("inf"), a, a, None, None, None) == INVALID
+    assert lib.sq_quantize_act_static(a, a, 4, 32, float("nan"), a, a, None, None, None) == INVALID
+    assert lib.sq_quantize_act_static(a, a, 4, 32, 1.0, None, a, None, None, None) == INVALID
+    assert lib.sq_quantize_act_static(a, a, 0, 32, 1.0, None, None, None, None, None) == 0
     # smoothing factor
     assert lib.sq_smooth_factor(a, a, 8, 1.5, a, None) == INVALID
     assert lib.sq_smooth_factor(a, a, 8, -0.1, a, None) == INVALID

@@ -1,6 +1,8 @@
 """GPU parity: every kernel through the C-ABI against the CPU oracle on the
 same seeded inputs.  Codes, scale bit patterns and int32 accumulators must
 match exactly; fp32 outputs within max|err| <= 1e-5 max|ref| + 1e-6."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -426,3 +428,64 @@ def test_host_pipeline_matches_direct_calls(sq):
         torch.cuda.synchronize()
         for y, r in zip(yh, ref):
             assert torch.equal(y, r)
+
+
+# ------------------------------------------------------------- Smooth-Static
+
+@pytest.mark.parametrize("M,K", [(5, 48), (300, 1024), (64, 4096), (3, 8208)])
+def test_static_calibration_and_quantize_parity(sq, M, K):
+    c = wl.make_case(M, K, 8, wl.EPI_BIAS, seed=K + 3 * M)
+    # a separate calibration batch from the same distribution (same outlier channels)
+    calib = wl.make_activation(2 * M + 7, K, seed=K + 3 * M + 1, outlier_frac=0.01,
+                               outlier_scale=20.0, channel_seed=K + 3 * M).numpy()
+    X = c.X.numpy()
+    s = oracle_smoothing(X, c.W.numpy(), 0.5)
+    amax_ref = oracle.act_absmax(calib[: M + 3], s)
+    amax_ref = oracle.act_absmax(calib[M + 3:], s, amax_ref)
+    amax = sq.act_absmax(to_dev(calib[: M + 3]), to_dev(s))
+    sq.act_absmax(to_dev(calib[M + 3:]), to_dev(s), amax)
+    assert np.float32(amax.item()).view(np.uint32) == np.float32(amax_ref).view(np.uint32)
+    for scale in (oracle.static_scale(amax_ref), oracle.static_scale(amax_ref) * np.float32(0.25)):
+        q_ref = oracle.quantize_static(X, s, scale)
+        Xq, sx, Xop = sq.quantize_act_static(to_dev(X), to_dev(s), float(scale))
+        assert_codes_equal(Xq.cpu().numpy(), q_ref, "static Xq")
+        assert_codes_equal(op_as_int(Xop), q_ref, "static Xop")
+        assert np.all(sx.cpu().numpy() == np.float32(scale))
+    # the quarter scale saturates: the clamp is exercised
+    assert np.abs(q_ref).max() == 127 and (np.abs(q_ref) == 127).sum() > M
+
+
+def test_static_saturation_and_ties(sq, golden_dir):
+    rows = []
+    with open(os.path.join(golden_dir, "quantize_static_example.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                rows.append([c.strip() for c in line.split("|")])
+    scale, vals, codes = rows[0]
+    K = 16
+    x = np.zeros((2, K), np.float32)
+    v = np.array([float(t) for t in vals.split()], np.float32)
+    x[0, :v.size] = v
+    x[1, :v.size] = -v
+    s = np.ones(K, np.float32)
+    Xq, _, _ = sq.quantize_act_static(to_dev(x), to_dev(s), float(scale))
+    want = np.array([int(t) for t in codes.split()], np.int8)
+    np.testing.assert_array_equal(Xq.cpu().numpy()[0, :v.size], want)
+    np.testing.assert_array_equal(Xq.cpu().numpy()[1, :v.size], -want)
+
+
+def test_static_linear_block(sq):
+    """Static codes through the tcgen05 GEMM + epilogue against the oracle."""
+    M, K, N = 256, 1024, 512
+    c = wl.make_case(M, K, N, wl.EPI_BIAS_GELU, seed=17)
+    X, W = c.X.numpy(), c.W.numpy()
+    s = oracle_smoothing(X, W, 0.5)
+    scale = oracle.static_scale(oracle.act_absmax(X, s))
+    wq, sw = oracle.quantize_rows(W, s, "weight")
+    xq = oracle.quantize_static(X, s, scale)
+    ref = oracle.epilogue(oracle.gemm_i32(xq, wq), np.full(M, scale, np.float32), sw,
+                          c.bias.numpy(), mode=wl.EPI_BIAS_GELU)
+    _, sw_d, Wop = sq.pack_weight(to_dev(W), to_dev(s), want_q=False)
+    _, sx_d, Xop = sq.quantize_act_static(to_dev(X), to_dev(s), float(scale), want_q=False)
+    y = sq.linear_i8(Xop, sx_d, Wop, sw_d, to_dev(c.bias.numpy()), None, wl.EPI_BIAS_GELU)
+    assert_close_fp32(y.cpu().numpy(), ref, "static linear block")
