@@ -189,21 +189,28 @@ def static_scale(amax: float) -> float:
 
 
 def quantize_act_static(X: torch.Tensor, s: torch.Tensor, scale: float, want_q: bool = True,
-                        want_op: bool = True, out=None, stream=None):
+                        want_op: bool = True, want_l1: bool = False, out=None, stream=None):
     """Smooth-Static quantisation with a fixed per-tensor scale; returns
-    (Xq or None, x_scale [M] filled with scale, Xop or None)."""
+    (Xq or None, x_scale [M] filled with scale, Xop or None), plus the
+    per-token code L1 norms as a fourth item when want_l1 (or a 4-tuple
+    `out`)."""
     _need(X, torch.float32, "X")
     M, K = X.shape
     _need(s, torch.float32, "s", (K,))
+    l1 = None
     if out is not None:
-        Xq, sx, Xop = out
+        Xq, sx, Xop = out[:3]
+        l1 = out[3] if len(out) > 3 else None
     else:
         Xq = torch.empty(M, K, dtype=torch.int8, device=X.device) if want_q else None
         Xop = empty_operand(M, K, X.device) if want_op else None
         sx = torch.empty(M, dtype=torch.float32, device=X.device)
+        l1 = torch.empty(M, dtype=torch.int32, device=X.device) if want_l1 else None
     _check(load().sq_quantize_act_static(_p(X), _p(s), M, K, float(scale), _p(Xq), _p(sx),
-                                         _p(Xop), None, _stream(stream)),
+                                         _p(Xop), _p(l1), _stream(stream)),
            "sq_quantize_act_static")
+    if want_l1 or (out is not None and len(out) > 3):
+        return Xq, sx, Xop, l1
     return Xq, sx, Xop
 
 

@@ -40,8 +40,10 @@ def gpu_linear(sq, path, Xq, Xop, sx, Wq, Wop, sw, bias=None, residual=None,
 
 # ------------------------------------------------------------------ quantiser
 
+# The last rows span many staged chunks per SM with a ragged final chunk (the
+# activation quantiser streams each SM's row range through a ring of stages).
 QUANT_SHAPES = [(1, 16), (7, 48), (37, 1024), (130, 768), (64, 4096), (300, 3072), (3, 8192),
-                (5, 8208), (2, 16384)]
+                (5, 8208), (2, 16384), (6847, 1024), (1900, 4096), (4000, 768), (777, 3072)]
 
 
 @pytest.mark.parametrize("M,K", QUANT_SHAPES)
@@ -133,6 +135,38 @@ def test_quantize_row_max_near_ties(sq):
     assert_bits_equal(sx.cpu().numpy(), sx_ref, "x_scale")
     assert_codes_equal(Xq.cpu().numpy(), q_ref, "Xq")
     assert_codes_equal(op_as_int(Xop), q_ref, "Xop")
+
+
+@pytest.mark.parametrize("K", [1024, 4096])
+def test_quantize_extreme_magnitudes(sq, K):
+    """Rows whose largest |x/s| sits at extreme magnitudes (2^-61 .. 2^101,
+    each a hair below, at and above a power of two), smoothing factors far
+    outside the usual range (1e-7, 3e7), and static scales from 2^-71 to
+    2^98: codes, scales and L1 norms bit for bit (dynamic and static)."""
+    rng = np.random.default_rng(K)
+    s = rng.uniform(0.05, 20.0, K).astype(np.float32)
+    base = rng.standard_normal(K).astype(np.float32)
+    base /= np.abs(base).max()
+    rows = []
+    for m in (2.0 ** -60, 2.0 ** -59, 2.0 ** -61, 2.0 ** 100, 2.0 ** 99, 2.0 ** 101):
+        for f in (np.float32(1 - 2.0 ** -20), np.float32(1), np.float32(1 + 2.0 ** -20)):
+            rows.append((base * np.float32(m) * f * s).astype(np.float32))
+    X = np.stack(rows).astype(np.float32)
+    for s_case in (s, np.where(np.arange(K) == 5, np.float32(1e-7), s).astype(np.float32),
+                   np.where(np.arange(K) == 9, np.float32(3e7), s).astype(np.float32)):
+        q_ref, sx_ref = oracle.quantize_rows(X, s_case, "act")
+        Xq, sx, Xop, l1 = sq.quantize_act(to_dev(X), to_dev(s_case), want_l1=True)
+        assert_bits_equal(sx.cpu().numpy(), sx_ref, "x_scale")
+        assert_codes_equal(Xq.cpu().numpy(), q_ref, "Xq")
+        assert_codes_equal(op_as_int(Xop), q_ref, "Xop")
+        np.testing.assert_array_equal(l1.cpu().numpy(),
+                                      np.abs(q_ref.astype(np.int64)).sum(axis=1))
+        for scale in (np.float32(2.0 ** -71), np.float32(2.0 ** -69), np.float32(3.0),
+                      np.float32(2.0 ** 98)):
+            q_ref = oracle.quantize_static(X, s_case, scale)
+            Xq, _, Xop = sq.quantize_act_static(to_dev(X), to_dev(s_case), float(scale))
+            assert_codes_equal(Xq.cpu().numpy(), q_ref, f"static Xq, scale {scale}")
+            assert_codes_equal(op_as_int(Xop), q_ref, f"static Xop, scale {scale}")
 
 
 @pytest.mark.parametrize("N,K", [(1, 16), (5, 48), (1024, 1024), (3072, 1024), (768, 3072),
@@ -432,7 +466,7 @@ def test_host_pipeline_matches_direct_calls(sq):
 
 # ------------------------------------------------------------- Smooth-Static
 
-@pytest.mark.parametrize("M,K", [(5, 48), (300, 1024), (64, 4096), (3, 8208)])
+@pytest.mark.parametrize("M,K", [(5, 48), (300, 1024), (64, 4096), (3, 8208), (5000, 1024)])
 def test_static_calibration_and_quantize_parity(sq, M, K):
     c = wl.make_case(M, K, 8, wl.EPI_BIAS, seed=K + 3 * M)
     # a separate calibration batch from the same distribution (same outlier channels)
@@ -447,10 +481,15 @@ def test_static_calibration_and_quantize_parity(sq, M, K):
     assert np.float32(amax.item()).view(np.uint32) == np.float32(amax_ref).view(np.uint32)
     for scale in (oracle.static_scale(amax_ref), oracle.static_scale(amax_ref) * np.float32(0.25)):
         q_ref = oracle.quantize_static(X, s, scale)
-        Xq, sx, Xop = sq.quantize_act_static(to_dev(X), to_dev(s), float(scale))
+        Xq, sx, Xop, l1 = sq.quantize_act_static(to_dev(X), to_dev(s), float(scale),
+                                                 want_l1=True)
         assert_codes_equal(Xq.cpu().numpy(), q_ref, "static Xq")
         assert_codes_equal(op_as_int(Xop), q_ref, "static Xop")
         assert np.all(sx.cpu().numpy() == np.float32(scale))
+        np.testing.assert_array_equal(l1.cpu().numpy(),
+                                      np.abs(q_ref.astype(np.int64)).sum(axis=1))
+        _, _, Xop2 = sq.quantize_act_static(to_dev(X), to_dev(s), float(scale), want_q=False)
+        assert_codes_equal(op_as_int(Xop2), q_ref, "static Xop only")
     # the quarter scale saturates: the clamp is exercised
     assert np.abs(q_ref).max() == 127 and (np.abs(q_ref) == 127).sum() > M
 
