@@ -71,8 +71,8 @@ constexpr int SMEM_BYTES = RING_BYTES + NUM_EPI_WARPS * STG_BYTES + BAR_BYTES + 
 constexpr unsigned long long kTimeoutNs = 4000000000ull;
 
 // instruction descriptor, kind::f16: D fp32, A/B bf16, both K-major, N, M
-constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                           ((uint32_t)(BM >> 4) << 24);
+constexpr uint32_t IDESC_BASE = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BM >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_for(int n) { return IDESC_BASE | ((uint32_t)(n >> 3) << 17); }
 
 __device__ unsigned int g_tc_error;
 
@@ -201,11 +201,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 }
 
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t accumulate) {
+                                          uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate)
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -248,6 +248,48 @@ __device__ __forceinline__ void tmem_wait_st() {
 }
 
 // ------------------------------------------------------------------ kernel
+
+// Work items of a launch.  The BM x BN tiles that fill whole waves of the
+// persistent grid are items as they are; when the last, partial wave holds at
+// most half a wave of tiles, each of them is cut into two 128-column halves
+// (MMA N = 128), so that the last round takes half as long.  (Quarters, N = 64,
+// measured slower: the A tile is loaded in full for a quarter of the work.)
+// Tiles are numbered m-fastest, so CTAs working at the same time share B tiles
+// in L2.
+struct Schedule {
+    int m_tiles, full_items, sub, items;
+};
+
+__host__ __device__ inline Schedule make_schedule(int m_tiles, int n_tiles, int grid) {
+    Schedule sc;
+    sc.m_tiles = m_tiles;
+    const int tiles = m_tiles * n_tiles;
+    const int waves = tiles / grid, rem = tiles - waves * grid;
+    sc.sub = (waves >= 1 && rem > 0 && 2 * rem <= grid) ? 2 : 1;
+    sc.full_items = sc.sub == 1 ? tiles : waves * grid;
+    sc.items = sc.full_items + (tiles - sc.full_items) * sc.sub;
+    return sc;
+}
+
+struct Item {
+    int m0, n0, bn;
+};
+
+__device__ __forceinline__ Item item_at(const Schedule &sc, int i) {
+    Item it;
+    if (i < sc.full_items) {
+        it.m0 = (i % sc.m_tiles) * BM;
+        it.n0 = (i / sc.m_tiles) * BN;
+        it.bn = BN;
+    } else {
+        const int j = i - sc.full_items;
+        const int t = sc.full_items + j / sc.sub;
+        it.bn = BN / sc.sub;
+        it.m0 = (t % sc.m_tiles) * BM;
+        it.n0 = (t / sc.m_tiles) * BN + (j % sc.sub) * it.bn;
+    }
+    return it;
+}
 
 struct Smem {
     uint64_t full[STAGES];
@@ -455,20 +497,21 @@ __device__ __forceinline__ void epilogue_slice(uint32_t (&v)[32], int64_t m, int
     }
 }
 
-// The four slices of this warp's part of a tile, reading tensor memory at
-// `taddr` (fp32 sums, or int32 with INT_IN).
+// The first `nsl` slices of this warp's part of a tile (all four for a full
+// tile, fewer for a column slice of one), reading tensor memory at `taddr`
+// (fp32 sums, or int32 with INT_IN).
 template <int MODE, bool INT_IN>
 __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int64_t m, int nb, int row0,
                                               int lane, const EpiArgs &a, float xs,
                                               const ColParams &cp, float4 (&rnext)[8],
-                                              const CUtensorMap *tmY, uint8_t *stg) {
+                                              const CUtensorMap *tmY, uint8_t *stg, int nsl) {
 #pragma unroll 1
-    for (int s = 0; s < SLICES; ++s) {
+    for (int s = 0; s < nsl; ++s) {
         float4 rcur[8];
         if (MODE == SQ_EPI_BIAS_RESIDUAL) {
 #pragma unroll
             for (int c = 0; c < 8; ++c) rcur[c] = rnext[c];
-            if (s + 1 < SLICES) load_residual(rnext, a, m, nb + (s + 1) * SLICE);
+            if (s + 1 < nsl) load_residual(rnext, a, m, nb + (s + 1) * SLICE);
         }
         const float wl = s == 0 ? cp.w[0] : s == 1 ? cp.w[1] : s == 2 ? cp.w[2] : cp.w[3];
         const float bl = s == 0 ? cp.b[0] : s == 1 ? cp.b[1] : s == 2 ? cp.b[2] : cp.b[3];
@@ -482,7 +525,8 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int64_t m, int nb,
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmY, const EpiArgs args, int K) {
+                   const __grid_constant__ CUtensorMap tmBs, const __grid_constant__ CUtensorMap tmY,
+                   const EpiArgs args, int K) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -520,7 +564,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int m_tiles = (M + BM - 1) / BM;
     const int n_tiles = (N + BN - 1) / BN;
-    const int num_tiles = m_tiles * n_tiles;
+    const Schedule sched = make_schedule(m_tiles, n_tiles, gridDim.x);
+    const int num_items = sched.items;
     const int nkb = (K + BK - 1) / BK;
     // K per exact fp32 pass: 1024, or all of K when the row L1 norms of either
     // operand bound every partial sum below 2^24.  Decided by warps 1..9 (the
@@ -559,15 +604,16 @@ __global__ void __launch_bounds__(THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued = 0, fill_parity = 0;  // per-stage bits: loads in flight
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-                const int m0 = (tile % m_tiles) * BM, n0 = (tile / m_tiles) * BN;
+            for (int i = blockIdx.x; i < num_items; i += gridDim.x) {
+                const Item t = item_at(sched, i);
+                const bool slice = t.bn < BN;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(smem_u32(&S.empty[stage]), phase ^ 1, abort_flag)) goto done_p;
                     const uint32_t full = smem_u32(&S.full[stage]);
-                    mbar_expect_tx(full, STAGE_BYTES);
+                    mbar_expect_tx(full, A_BYTES + t.bn * BK * 2);
                     const uint32_t sa = ring + stage * STAGE_BYTES;
-                    tma_load_2d(sa, &tmA, full, kb * BK, m0);
-                    tma_load_2d(sa + A_BYTES, &tmB, full, kb * BK, n0);
+                    tma_load_2d(sa, &tmA, full, kb * BK, t.m0);
+                    tma_load_2d(sa + A_BYTES, slice ? &tmBs : &tmB, full, kb * BK, t.n0);
                     issued |= 1u << stage;
                     fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -588,7 +634,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t phase = 0, tph = 0;  // tph: per-buffer use parity bits
             bool issued_any = false;
             int it = 0;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+            for (int i = blockIdx.x; i < num_items; i += gridDim.x, ++it) {
+                const uint32_t idesc = idesc_for(item_at(sched, i).bn);
                 for (int c = 0; c < nchunks; ++c) {
                     const uint32_t b = nchunks == 1 ? (uint32_t)(it & 1) : 0u;
                     const uint32_t par = (tph >> b) & 1u;
@@ -607,7 +654,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                         for (int k = 0; k < BK / UMMA_K; ++k) {
                             // advance 16 bf16 = 32 bytes along K inside the swizzled row
-                            umma_bf16(d, adesc + 2 * k, bdesc + 2 * k,
+                            umma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc,
                                       (kb > kb0 || k > 0) ? 1u : 0u);
                         }
                         issued_any = true;
@@ -637,24 +684,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const uint32_t colP = BN;          // int32 partial (multi-chunk shapes)
         int it = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
-            const int m0 = (tile % m_tiles) * BM, n0 = (tile / m_tiles) * BN;
-            const int row0 = m0 + q * 32;
+        for (int i = blockIdx.x; i < num_items; i += gridDim.x, ++it) {
+            const Item t = item_at(sched, i);
+            const int row0 = t.m0 + q * 32;
             const int64_t m = (int64_t)row0 + lane;
-            const int nb = n0 + half * COLS_PER_WARP;
+            const int nb = t.n0 + half * COLS_PER_WARP;
+            // 32-column slices of this warp's half that the item covers (0..4)
+            const int nsl = max(0, min(SLICES, (t.bn - half * COLS_PER_WARP) / SLICE));
             // operands that do not depend on the accumulators: fetch them now
             ColParams cp;
             load_col_params<MODE>(cp, args, nb, lane);
             const float xs = (MODE != SQ_EPI_RAW_I32 && m < M) ? __ldg(args.sx + m) : 0.f;
             float4 rnext[8];
-            if (MODE == SQ_EPI_BIAS_RESIDUAL) load_residual(rnext, args, m, nb);
+            if (MODE == SQ_EPI_BIAS_RESIDUAL && nsl > 0) load_residual(rnext, args, m, nb);
             if (nchunks == 1) {
                 const uint32_t b = (uint32_t)(it & 1);
                 if (!mbar_wait(smem_u32(&S.tfull[b]), (fph >> b) & 1u, abort_flag)) goto done_e;
                 fph ^= 1u << b;
                 tc_fence_after();
                 const uint32_t tA = tmem_base + lane_off + b * BN + half * COLS_PER_WARP;
-                epilogue_tile<MODE, false>(tA, m, nb, row0, lane, args, xs, cp, rnext, &tmY, stg);
+                epilogue_tile<MODE, false>(tA, m, nb, row0, lane, args, xs, cp, rnext, &tmY, stg,
+                                           nsl);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.tempty[b]));
@@ -666,7 +716,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     fph ^= 1u;
                     tc_fence_after();
 #pragma unroll 1
-                    for (int s = 0; s < SLICES; ++s) {
+                    for (int s = 0; s < nsl; ++s) {
                         uint32_t v[32];
                         tmem_ld32(tA + s * SLICE, v);
 #pragma unroll
@@ -686,7 +736,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (lane == 0) mbar_arrive(smem_u32(&S.tempty[0]));
                 }
                 // final pass from the int32 partial; overlaps the next tile's MMAs
-                epilogue_tile<MODE, true>(tP, m, nb, row0, lane, args, xs, cp, rnext, &tmY, stg);
+                epilogue_tile<MODE, true>(tP, m, nb, row0, lane, args, xs, cp, rnext, &tmY, stg, nsl);
             }
         }
     done_e:
@@ -740,8 +790,9 @@ sq_status make_map(CUtensorMap *map, CUtensorMapDataType dt, int esize, const vo
 }
 
 template <int MODE>
-sq_status launch_mode(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ty,
-                      const EpiArgs &args, int K, int grid, int device, cudaStream_t st) {
+sq_status launch_mode(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tbs,
+                      const CUtensorMap &ty, const EpiArgs &args, int K, int grid, int device,
+                      cudaStream_t st) {
     static int attr_dev = -1;
     if (attr_dev != device) {
         if (cudaFuncSetAttribute(gemm_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -749,7 +800,7 @@ sq_status launch_mode(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
             return SQ_ERR_CUDA;
         attr_dev = device;
     }
-    gemm_tc_kernel<MODE><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, ty, args, K);
+    gemm_tc_kernel<MODE><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, tbs, ty, args, K);
     return cuda_status(cudaGetLastError());
 }
 
@@ -779,10 +830,21 @@ sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_
     args.tma_io = (N % 4 == 0) && aligned16(Y) && (mode == SQ_EPI_RAW_I32 || aligned16(sw)) &&
                   (bias == nullptr || aligned16(bias)) &&
                   (residual == nullptr || aligned16(residual));
-    CUtensorMap ta, tb, ty;
+    CUtensorMap ta, tb, tbs, ty;
     if ((rc = make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Xop, M, K, BM, BK)) != SQ_OK)
         return rc;
     if ((rc = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wop, N, K, BN, BK)) != SQ_OK)
+        return rc;
+    const int64_t m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN - 1) / BN;
+    const int64_t tiles = m_tiles * n_tiles;
+    if (tiles > 0x7fffffff) return SQ_ERR_UNSUPPORTED;
+    const int grid = (int)std::min<int64_t>(tiles, di.sms);
+    // B box of the column slices of the last wave's tiles (see make_schedule)
+    const Schedule sched = make_schedule((int)m_tiles, (int)n_tiles, grid);
+    tbs = tb;
+    if (sched.sub > 1 &&
+        (rc = make_map(&tbs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wop, N, K, BN / sched.sub, BK)) !=
+            SQ_OK)
         return rc;
     ty = ta;  // unused placeholder unless tma_io
     if (args.tma_io) {
@@ -790,17 +852,14 @@ sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_
                                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
         if ((rc = make_map(&ty, yt, 4, Y, M, N, SLICE, SLICE)) != SQ_OK) return rc;
     }
-    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    if (tiles > 0x7fffffff) return SQ_ERR_UNSUPPORTED;
-    const int grid = (int)std::min<int64_t>(tiles, di.sms);
     switch (mode) {
-    case SQ_EPI_NONE: return launch_mode<SQ_EPI_NONE>(ta, tb, ty, args, (int)K, grid, di.device, st);
-    case SQ_EPI_BIAS: return launch_mode<SQ_EPI_BIAS>(ta, tb, ty, args, (int)K, grid, di.device, st);
+    case SQ_EPI_NONE: return launch_mode<SQ_EPI_NONE>(ta, tb, tbs, ty, args, (int)K, grid, di.device, st);
+    case SQ_EPI_BIAS: return launch_mode<SQ_EPI_BIAS>(ta, tb, tbs, ty, args, (int)K, grid, di.device, st);
     case SQ_EPI_BIAS_GELU:
-        return launch_mode<SQ_EPI_BIAS_GELU>(ta, tb, ty, args, (int)K, grid, di.device, st);
+        return launch_mode<SQ_EPI_BIAS_GELU>(ta, tb, tbs, ty, args, (int)K, grid, di.device, st);
     case SQ_EPI_BIAS_RESIDUAL:
-        return launch_mode<SQ_EPI_BIAS_RESIDUAL>(ta, tb, ty, args, (int)K, grid, di.device, st);
-    default: return launch_mode<SQ_EPI_RAW_I32>(ta, tb, ty, args, (int)K, grid, di.device, st);
+        return launch_mode<SQ_EPI_BIAS_RESIDUAL>(ta, tb, tbs, ty, args, (int)K, grid, di.device, st);
+    default: return launch_mode<SQ_EPI_RAW_I32>(ta, tb, tbs, ty, args, (int)K, grid, di.device, st);
     }
 }
 

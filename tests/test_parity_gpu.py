@@ -241,6 +241,32 @@ def test_gemm_raw_int32_exact(sq, path, M, N, K):
     assert_codes_equal(acc.cpu().numpy(), oracle.gemm_i32(xq, wq), "acc")
 
 
+# Shapes with more tiles (128 x 256) than a GB300 has SMs and a partial last
+# wave of at most half the SMs: the tcgen05 GEMM cuts that wave's tiles into
+# 128-column halves.
+#   (2560, 2304): 180 tiles, 28 in the last wave -> halves
+#   (2560, 2816): 220 tiles, 68 in the last wave -> halves
+#   (2560, 3328): 260 tiles, 108 in the last wave -> no split (control)
+# K = 1088 takes two exact fp32 chunks (no L1 bound passed); 4096 with
+# residual exercises the multi-chunk epilogue with the residual prefetch.
+SPLIT_SHAPES = [(2560, 2304, 1088, wl.EPI_NONE), (2560, 2816, 256, wl.EPI_BIAS_GELU),
+                (2560, 3328, 512, wl.EPI_BIAS), (2560, 2304, 4096, wl.EPI_BIAS_RESIDUAL)]
+
+
+@pytest.mark.parametrize("M,N,K,mode", SPLIT_SHAPES)
+def test_gemm_tail_wave_slices(sq, M, N, K, mode):
+    c, xq, sx, wq, sw, d = _quantised_case(sq, M, K, N, wl.EPI_BIAS_RESIDUAL, seed=M + N + K)
+    acc_ref = oracle.gemm_i32(xq, wq)
+    acc = sq.linear_i8(d["Xop"], None, d["Wop"], None, None, None, sq.EPI_RAW_I32)
+    assert_codes_equal(acc.cpu().numpy(), acc_ref, "acc")
+    if mode != wl.EPI_NONE:
+        b, r = c.bias.numpy(), c.residual.numpy()
+        ref = oracle.epilogue(acc_ref, sx, sw, b, r, mode)
+        y = sq.linear_i8(d["Xop"], d["sx"], d["Wop"], d["sw"], to_dev(b),
+                         to_dev(r) if mode == wl.EPI_BIAS_RESIDUAL else None, mode)
+        assert_close_fp32(y.cpu().numpy(), ref, f"mode {mode}")
+
+
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("K", [1024, 1040, 2048, 4096, 8192])
 def test_gemm_adversarial_exactness(sq, path, K):
