@@ -152,11 +152,11 @@ class ClockSampler:
 
 class Layer:
     __slots__ = ("lin", "X", "s", "Wop", "Wq", "sw", "wl1", "bias", "residual", "Y", "Xhost",
-                 "Yhost", "static_scale")
+                 "Yhost", "static_scale", "feeds", "fed_by")
 
 
 def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
-                   quant: str = "dynamic"):
+                   quant: str = "dynamic", ffn_chain: str = "off"):
     from smoothquant_w8a8_int8_gb300 import binding as sq
     dev = torch.device("cuda")
     layers = []
@@ -165,9 +165,46 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
     Xq_buf = torch.empty(maxMK, dtype=torch.int8, device=dev)
     sx_buf = torch.empty(w.M, dtype=torch.float32, device=dev)
     l1_buf = torch.empty(w.M, dtype=torch.int32, device=dev)
+    chained = ffn_chain != "off"
+    if chained:
+        # codes of a chained FFN-down input (written by FFN-up's requantising
+        # epilogue, or by the static quantiser from FFN-up's fp32 output)
+        maxN = max(lin.N for lin in w.linears)
+        bufs_chain = (torch.empty(w.M * maxN, dtype=torch.bfloat16, device=dev),
+                      torch.empty(w.M, dtype=torch.float32, device=dev))
     for layer, idx in [(l, i) for l in range(w.layers) for i in range(len(w.linears))]:
         lin = w.linears[idx]
         seed = wl.gemm_seed(w, layer, idx) + 7 * rank
+        up = layers[-1] if (chained and lin.gelu_input and layers) else None
+        if up is not None:
+            # FFN-down fed by this layer's FFN-up: its smoothing factor and
+            # Smooth-Static scale are calibrated offline on FFN-up's output for a
+            # separate 512-token batch
+            c = wl.make_case(w.M, lin.K, lin.N, lin.mode, seed, w.outlier_frac,
+                             w.outlier_scale, lin.gelu_input, w.alpha, device=dev)
+            calib_x = wl.make_activation(512, up.lin.K, seed + 555, w.outlier_frac,
+                                         w.outlier_scale, False, device=dev,
+                                         channel_seed=wl.gemm_seed(w, layer, idx - 1) + 7 * rank)
+            _, sxc, Xopc = sq.quantize_act(calib_x, up.s, want_q=False)
+            y_cal = sq.linear_i8(Xopc, sxc, up.Wop, up.sw, up.bias, None, up.lin.mode)
+            s = sq.smooth_factor(sq.channel_absmax(y_cal), sq.channel_absmax(c.W), w.alpha)
+            L = Layer()
+            L.lin = lin
+            L.X = None
+            L.s = s
+            Wq, sw, Wop, wl1 = sq.pack_weight(c.W, s, want_q=(gemm == "mma_sync"),
+                                              want_op=(gemm == "tc"), want_l1=True)
+            L.Wq, L.sw, L.Wop, L.wl1 = Wq, sw, Wop, wl1
+            L.bias, L.residual = c.bias, c.residual
+            L.static_scale = sq.static_scale(sq.act_absmax(y_cal, s).item())
+            L.Y = torch.empty(w.M, lin.N, dtype=torch.float32, device=dev)
+            L.Xhost = L.Yhost = None
+            L.feeds = None
+            L.fed_by = up
+            up.feeds = L
+            del c.W, c.X
+            layers.append(L)
+            continue
         c = wl.make_case(w.M, lin.K, lin.N, lin.mode, seed, w.outlier_frac, w.outlier_scale,
                          lin.gelu_input, w.alpha, device=dev)
         L = Layer()
@@ -189,6 +226,7 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
             L.static_scale = sq.static_scale(sq.act_absmax(calib, s).item())
         L.Y = torch.empty(w.M, lin.N, dtype=torch.float32, device=dev)
         L.Xhost = L.Yhost = None
+        L.feeds = L.fed_by = None
         if want_host:
             L.Xhost = torch.empty(c.X.shape, dtype=torch.float32, pin_memory=True)
             L.Xhost.copy_(c.X)
@@ -196,13 +234,51 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
         del c.W
         layers.append(L)
     torch.cuda.synchronize()
-    return layers, (Xq_buf, sx_buf, Xop_buf, l1_buf)
+    bufs = (Xq_buf, sx_buf, Xop_buf, l1_buf)
+    return layers, bufs + (bufs_chain if chained else (None, None))
 
 
-def run_layer(sq, gemm, L, bufs, M, X=None, ev=None):
-    Xq_buf, sx_buf, Xop_buf, l1_buf = bufs
+def run_layer(sq, gemm, L, bufs, M, X=None, ev=None, ffn_chain="off"):
+    """One linear of the step.  Returns whether an activation quantiser ran."""
+    Xq_buf, sx_buf, Xop_buf, l1_buf, Xop_chain, sx_chain = bufs
     K, N = L.lin.K, L.lin.N
     X = L.X if X is None else X
+    if ffn_chain != "off" and (L.feeds is not None or L.fed_by is not None):
+        # the chained FFN pair (tcgen05 path)
+        if L.fed_by is not None:
+            if ev is not None:
+                ev[0].record()
+            if ffn_chain == "unfused":
+                sq.quantize_act_static(L.fed_by.Y, L.s, L.static_scale,
+                                       out=(None, sx_chain, Xop_chain[: M * K].view(M, K)))
+            if ev is not None:
+                ev[1].record()
+            sq.linear_i8(Xop_chain[: M * K].view(M, K), sx_chain, L.Wop, L.sw, L.bias,
+                         L.residual, L.lin.mode, out=L.Y, w_l1=L.wl1)
+            if ev is not None:
+                ev[2].record()
+            return ffn_chain == "unfused"
+        Xop = Xop_buf[: M * K].view(M, K)
+        if ev is not None:
+            ev[0].record()
+        if L.static_scale is not None:
+            sq.quantize_act_static(X, L.s, L.static_scale, out=(None, sx_buf, Xop))
+        else:
+            sq.quantize_act(X, L.s, out=(None, sx_buf, Xop))
+        if ev is not None:
+            ev[1].record()
+        if ffn_chain == "fused":
+            nxt = L.feeds
+            sq.linear_i8_requant(Xop, sx_buf, L.Wop, L.sw, L.bias, L.residual, L.lin.mode,
+                                 nxt.s, nxt.static_scale,
+                                 out=(None, Xop_chain[: M * N].view(M, N), sx_chain),
+                                 w_l1=L.wl1)
+        else:
+            sq.linear_i8(Xop, sx_buf, L.Wop, L.sw, L.bias, L.residual, L.lin.mode, out=L.Y,
+                         w_l1=L.wl1)
+        if ev is not None:
+            ev[2].record()
+        return True
     if gemm == "tc":
         Xop = Xop_buf[: M * K].view(M, K)
         if ev is not None:
@@ -228,20 +304,28 @@ def run_layer(sq, gemm, L, bufs, M, X=None, ev=None):
         sq.linear_i8_mma_sync(Xq, sx_buf, L.Wq, L.sw, L.bias, L.residual, L.lin.mode, out=L.Y)
         if ev is not None:
             ev[2].record()
+    return True
 
 
 def bench_ours(args, w: wl.Workload, rank: int, world: int):
     from smoothquant_w8a8_int8_gb300 import binding as sq
     sq.load()
     peaks, peak_src = load_peaks()
-    layers, bufs = setup_workload(w, args.gemm, rank, want_host=args.e2e_steps > 0,
-                                  quant=args.quant)
+    chained = args.ffn_chain != "off"
+    if chained and args.gemm != "tc":
+        raise SystemExit("--ffn-chain needs the tcgen05 GEMM (--gemm tc)")
+    layers, bufs = setup_workload(w, args.gemm, rank,
+                                  want_host=args.e2e_steps > 0 and not chained,
+                                  quant=args.quant, ffn_chain=args.ffn_chain)
     M = w.M
     n_gemm = len(layers)
+    quantised = [True] * n_gemm  # which linears run an activation quantiser kernel
 
     def step(ev_list=None):
         for i, L in enumerate(layers):
-            run_layer(sq, args.gemm, L, bufs, M, ev=None if ev_list is None else ev_list[i])
+            quantised[i] = run_layer(sq, args.gemm, L, bufs, M,
+                                     ev=None if ev_list is None else ev_list[i],
+                                     ffn_chain=args.ffn_chain)
 
     for _ in range(args.warmup):
         step()
@@ -294,7 +378,9 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
     gemm_ops = args.steps * ops_per_step
     gemm_tops = gemm_ops / (g_ms * 1e-3) / 1e12
     peak_tensor = peaks["bf16_tflops_sustained"]
-    q_bytes = args.steps * sum(R.quantize_bytes(M, L.lin.K) for L in layers)
+    q_bytes = args.steps * sum(R.quantize_bytes(M, L.lin.K)
+                               for L, qd in zip(layers, quantised) if qd)
+    n_quant = args.steps * sum(quantised)
     q_gbs = q_bytes / (q_ms * 1e-3) / 1e9
     g_bytes = args.steps * sum(R.linear_bytes(M, L.lin.K, L.lin.N, L.lin.mode) for L in layers)
 
@@ -302,7 +388,7 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
     # host memory, copied in, the linear block, Y copied out, inside the timed
     # region (three streams overlap copies with the kernels)
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and not chained:
         from smoothquant_w8a8_int8_gb300.pipeline import HostLinearPipeline, LinearLayer
         pipe = HostLinearPipeline(M, max(L.lin.K for L in layers), max(L.lin.N for L in layers))
         specs = [LinearLayer(L.s, L.Wop, L.sw, L.lin.mode, L.bias, L.residual, L.wl1,
@@ -352,13 +438,19 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
                    "layers": w.layers, "gemms_per_step": n_gemm,
                    "ops_per_step": ops_per_step, "gemm_kernel": gemm_kernel,
                    "l2": "inputs larger than L2: every GEMM reads its own activations "
-                         f"({sum(L.X.numel() * 4 for L in layers) / 1e9:.1f} GB per step)",
+                         f"({sum(M * L.lin.K * 4 for L in layers) / 1e9:.1f} GB per step)",
                    "weights": "packed once before the timed region",
                    "quantisation": ("Smooth-Static (per-tensor scale calibrated offline on a "
                                     "separate 512-token batch of the same distribution)"
                                     if args.quant == "static"
                                     else "Smooth-Dynamic (per-token scales at run time)"),
-                   "parallelism": f"replicas x{world} (rows shard, no collective)"},
+                   "parallelism": f"replicas x{world} (rows shard, no collective)",
+                   "ffn_chain": {"off": "not chained: every linear has its own input",
+                                 "unfused": "FFN-down consumes FFN-up's output: fp32 Y, then "
+                                            "the Smooth-Static quantiser",
+                                 "fused": "FFN-down consumes FFN-up's output: FFN-up's "
+                                          "epilogue emits FFN-down's Smooth-Static codes "
+                                          "(sq_linear_i8_requant)"}[args.ffn_chain]},
         "roofline": {"bound": "tensor", "kernel": "gemm+epilogue",
                      "achieved": round(gemm_tops, 2), "peak": peak_tensor,
                      "unit": "TFLOP/s", "frac": round(gemm_tops / peak_tensor, 4),
@@ -371,11 +463,11 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
                                "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                "frac": round(q_gbs / peaks["hbm_gbs"], 4),
                                "peak_source": peak_src,
-                               "avg_launch_us": round(q_ms * 1e3 / n_launch, 2),
+                               "avg_launch_us": round(q_ms * 1e3 / max(1, n_quant), 2),
                                "algorithmic_bytes_per_step": q_bytes // args.steps},
         "kernel_ms_per_step": {"quantize": round(q_ms / args.steps, 4),
                                "gemm": round(g_ms / args.steps, 4)},
-        "gpu_launches": 2 * n_gemm * args.steps,
+        "gpu_launches": n_gemm * args.steps + n_quant,
         "clocks": clock_info,
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -482,6 +574,10 @@ def main():
     ap.add_argument("--quant", choices=["dynamic", "static"], default="dynamic",
                     help="activation quantisation: per-token dynamic (Smooth-Dynamic, the "
                          "default) or per-tensor static (Smooth-Static)")
+    ap.add_argument("--ffn-chain", choices=["off", "unfused", "fused"], default="off",
+                    help="chain each layer's FFN-down to its FFN-up (Smooth-Static input): "
+                         "through fp32 Y and the quantiser, or through the requantising "
+                         "epilogue")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-step-seconds", type=float, default=2.0)

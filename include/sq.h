@@ -165,6 +165,27 @@ sq_status sq_linear_i8(const void *Xop, const float *x_scale, const int32_t *x_r
                        const float *bias, const float *residual, int64_t M, int64_t N, int64_t K,
                        int mode, void *Y, void *stream);
 
+/* ---- Producer-fused Smooth-Static quantisation ------------------------------ */
+
+/* sq_linear_i8 whose epilogue hands its results straight to the NEXT linear
+ * layer's Smooth-Static quantiser (Table 10), the GPU counterpart of the
+ * pages' INT8 subgraph fusion: no fp32 output is written.  For every element
+ * the epilogue forms y[m][n], bit for bit the value sq_linear_i8 stores for
+ * the same inputs and mode (modes 0-3; not SQ_EPI_RAW_I32), then
+ *   code[m][n] = clamp(round_half_even(fl(fl(y[m][n] / s_next[n]) / scale)), -127, 127)
+ * (IEEE fp32 divisions), i.e. sq_quantize_act_static applied to Y with the
+ * next layer's smoothing factor s_next fp32 [N] and per-tensor scale
+ * (> 0, finite).  Outputs: Yop [M][N] codes as exact bf16 values (the next
+ * sq_linear_i8's activation operand; 2-byte aligned) and/or Yq int8 [M][N] --
+ * at least one; x_scale_next fp32 [M] (nullable) is set to `scale` for every
+ * token.  Rows of N a multiple of 16 and 16-byte aligned code arrays take
+ * vector stores.  Other arguments, limits and statuses as sq_linear_i8. */
+sq_status sq_linear_i8_requant(const void *Xop, const float *x_scale, const int32_t *x_row_l1,
+                               const void *Wop, const float *w_scale, const int32_t *w_row_l1,
+                               const float *bias, const float *residual, int64_t M, int64_t N,
+                               int64_t K, int mode, const float *s_next, float scale, int8_t *Yq,
+                               void *Yop, float *x_scale_next, void *stream);
+
 /* The same GEMM + epilogue on the legacy warp-level integer MMA path
  * (mma.sync m16n8k32 s8 x s8 -> s32), reading int8 codes directly:
  * Xq int8 [M][K] and Wq int8 [N][K] from sq_quantize_act / sq_pack_weight.
@@ -174,6 +195,27 @@ sq_status sq_linear_i8_mma_sync(const int8_t *Xq, const float *x_scale, const in
                                 const float *w_scale, const float *bias, const float *residual,
                                 int64_t M, int64_t N, int64_t K, int mode, void *Y,
                                 void *stream);
+
+/* ---- Self-check of the epilogue's division --------------------------------- */
+
+/* sq_linear_i8_requant divides its results by the next layer's smoothing
+ * factor (y / s_next[n], Table 10) with a per-column reciprocal
+ * y = RN(1/s) and one fused correction,
+ *   q0 = RN(x y),  r = RN(x - s q0),  q = RN(q0 + r y),
+ * which is the IEEE quotient RN(x / s) in the range it is used.  Scaling x or
+ * s by a power of two scales every step exactly, so correctness is a property
+ * of the 2^46 significand pairs.  This entry point runs the kernel's own
+ * routine against IEEE division on the pairs a = 1 + af 2^-23,
+ * b = 1 + bf 2^-23 with bf in [b_first, b_first + b_count) and af in
+ * [a_first, a_first + a_count) (fraction fields, each range within [0, 2^23)).
+ * corrected = 0 checks the uncorrected RN(x RN(1/s)) instead (a control that
+ * does differ on some pairs).  out: two unsigned 64-bit words in device
+ * memory (8-byte aligned), zeroed by the caller: out[0] += the number of pairs
+ * that differ; out[1] = 1 + (af << 32 | bf) of one differing pair (unchanged if
+ * none).  One thread per b; a call costs about b_count * a_count / 2e12 s. */
+sq_status sq_check_division(uint32_t b_first, uint32_t b_count, uint32_t a_first,
+                            uint32_t a_count, int corrected, unsigned long long *out,
+                            void *stream);
 
 /* ---- Device status --------------------------------------------------------- */
 

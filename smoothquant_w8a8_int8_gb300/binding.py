@@ -22,8 +22,9 @@ EPI_NONE, EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESIDUAL, EPI_RAW_I32 = range(5)
 
 EXPORTS = ("sq_status_string", "sq_version", "sq_operand_bytes", "sq_channel_absmax",
            "sq_smooth_factor", "sq_pack_weight", "sq_quantize_act", "sq_act_absmax",
-           "sq_quantize_act_static", "sq_linear_i8", "sq_linear_i8_mma_sync",
-           "sq_device_status")
+           "sq_quantize_act_static", "sq_linear_i8", "sq_linear_i8_requant",
+           "sq_linear_i8_mma_sync",
+           "sq_check_division", "sq_device_status")
 
 _lock = threading.Lock()
 _lib = None
@@ -58,7 +59,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                 "sq_quantize_act_static": ([vp, vp, i64, i64, f32, vp, vp, vp, vp, vp], i32),
                 "sq_linear_i8": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp],
                                  i32),
+                "sq_linear_i8_requant": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp,
+                                          f32, vp, vp, vp, vp], i32),
                 "sq_linear_i8_mma_sync": ([vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp], i32),
+                "sq_check_division": ([ctypes.c_uint32] * 4 + [i32, vp, vp], i32),
                 "sq_device_status": ([vp], i32),
             }
             for name, (args, res) in sig.items():
@@ -238,6 +242,33 @@ def linear_i8(Xop, x_scale, Wop, w_scale, bias=None, residual=None, mode=EPI_BIA
     return out
 
 
+def linear_i8_requant(Xop, x_scale, Wop, w_scale, bias, residual, mode, s_next, scale: float,
+                      want_q: bool = False, want_op: bool = True, want_x_scale: bool = True,
+                      out=None, x_l1=None, w_l1=None, stream=None):
+    """tcgen05 INT8 GEMM whose epilogue emits the next linear's Smooth-Static
+    codes (smoothing factor s_next [N], per-tensor scale) instead of fp32 Y.
+    Returns (Yq or None, Yop or None, x_scale_next or None); `out` may give
+    those three (each may be None)."""
+    _need(Xop, torch.bfloat16, "Xop")
+    _need(Wop, torch.bfloat16, "Wop")
+    M, K = Xop.shape
+    N = Wop.shape[0]
+    if Wop.shape[1] != K:
+        raise ValueError("operand K mismatch")
+    _need(s_next, torch.float32, "s_next", (N,))
+    if out is not None:
+        Yq, Yop, xs = out
+    else:
+        Yq = torch.empty(M, N, dtype=torch.int8, device=Xop.device) if want_q else None
+        Yop = empty_operand(M, N, Xop.device) if want_op else None
+        xs = torch.empty(M, dtype=torch.float32, device=Xop.device) if want_x_scale else None
+    _check(load().sq_linear_i8_requant(_p(Xop), _p(x_scale), _p(x_l1), _p(Wop), _p(w_scale),
+                                       _p(w_l1), _p(bias), _p(residual), M, N, K, int(mode),
+                                       _p(s_next), float(scale), _p(Yq), _p(Yop), _p(xs),
+                                       _stream(stream)), "sq_linear_i8_requant")
+    return Yq, Yop, xs
+
+
 def linear_i8_mma_sync(Xq, x_scale, Wq, w_scale, bias=None, residual=None, mode=EPI_BIAS,
                        out=None, stream=None):
     """Legacy mma.sync INT8 GEMM + epilogue on int8 codes."""
@@ -247,6 +278,19 @@ def linear_i8_mma_sync(Xq, x_scale, Wq, w_scale, bias=None, residual=None, mode=
     _check(load().sq_linear_i8_mma_sync(_p(Xq), _p(x_scale), _p(Wq), _p(w_scale), _p(bias),
                                         _p(residual), M, N, K, int(mode), _p(out),
                                         _stream(stream)), "sq_linear_i8_mma_sync")
+    return out
+
+
+def check_division(b_first: int, b_count: int, a_first: int, a_count: int,
+                   corrected: bool = True, out: Optional[torch.Tensor] = None,
+                   stream=None) -> torch.Tensor:
+    """Run the requantising epilogue's division against IEEE division on the
+    significand pairs (see sq_check_division); returns the int64[2] device
+    tensor (mismatch count, 1 + (af << 32 | bf) of one mismatch or 0)."""
+    if out is None:
+        out = torch.zeros(2, dtype=torch.int64, device="cuda")
+    _check(load().sq_check_division(b_first, b_count, a_first, a_count, int(bool(corrected)),
+                                    _p(out), _stream(stream)), "sq_check_division")
     return out
 
 

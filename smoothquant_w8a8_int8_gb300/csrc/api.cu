@@ -184,7 +184,38 @@ sq_status sq_linear_i8(const void *Xop, const float *x_scale, const int32_t *x_r
     if ((rc = require_sm103()) != SQ_OK) return rc;
     return launch_gemm_tc(static_cast<const __nv_bfloat16 *>(Xop), x_scale, x_row_l1,
                           static_cast<const __nv_bfloat16 *>(Wop), w_scale, w_row_l1, bias,
-                          residual, M, N, K, mode, Y, as_stream(stream));
+                          residual, M, N, K, mode, Y, nullptr, as_stream(stream));
+}
+
+sq_status sq_linear_i8_requant(const void *Xop, const float *x_scale, const int32_t *x_row_l1,
+                               const void *Wop, const float *w_scale, const int32_t *w_row_l1,
+                               const float *bias, const float *residual, int64_t M, int64_t N,
+                               int64_t K, int mode, const float *s_next, float scale, int8_t *Yq,
+                               void *Yop, float *x_scale_next, void *stream) {
+    if (mode == SQ_EPI_RAW_I32) return SQ_ERR_INVALID_ARG;
+    if (!(scale > 0.0f) || !(scale <= 3.4028234663852886e38f)) return SQ_ERR_INVALID_ARG;
+    const void *out = Yop ? Yop : static_cast<const void *>(Yq);
+    sq_status rc = check_linear_args(Xop, x_scale, Wop, w_scale, bias, residual, M, N, K, mode,
+                                     out);
+    if (rc != SQ_OK) return rc;
+    if (M == 0 || N == 0) return SQ_OK;
+    if (!s_next || (!Yq && !Yop)) return SQ_ERR_INVALID_ARG;
+    if (!aligned4(s_next) || (x_scale_next && !aligned4(x_scale_next)) ||
+        (Yop && (reinterpret_cast<uintptr_t>(Yop) & 1u)))
+        return SQ_ERR_ALIGNMENT;
+    if ((x_row_l1 && !aligned4(x_row_l1)) || (w_row_l1 && !aligned4(w_row_l1)))
+        return SQ_ERR_ALIGNMENT;
+    if ((rc = require_sm103()) != SQ_OK) return rc;
+    RequantOut rq;
+    rq.s_next = s_next;
+    rq.scale = scale;
+    rq.rscale = 1.0f / scale;  // IEEE division: the correctly rounded reciprocal
+    rq.Yq = Yq;
+    rq.Yop = static_cast<__nv_bfloat16 *>(Yop);
+    rq.x_scale = x_scale_next;
+    return launch_gemm_tc(static_cast<const __nv_bfloat16 *>(Xop), x_scale, x_row_l1,
+                          static_cast<const __nv_bfloat16 *>(Wop), w_scale, w_row_l1, bias,
+                          residual, M, N, K, mode, nullptr, &rq, as_stream(stream));
 }
 
 sq_status sq_linear_i8_mma_sync(const int8_t *Xq, const float *x_scale, const int8_t *Wq,
@@ -197,6 +228,21 @@ sq_status sq_linear_i8_mma_sync(const int8_t *Xq, const float *x_scale, const in
     if ((rc = require_sm103()) != SQ_OK) return rc;
     return launch_gemm_mma_sync(Xq, x_scale, Wq, w_scale, bias, residual, M, N, K, mode, Y,
                                 as_stream(stream));
+}
+
+sq_status sq_check_division(uint32_t b_first, uint32_t b_count, uint32_t a_first,
+                            uint32_t a_count, int corrected, unsigned long long *out,
+                            void *stream) {
+    const uint64_t lim = 1ull << 23;
+    if ((uint64_t)b_first + b_count > lim || (uint64_t)a_first + a_count > lim)
+        return SQ_ERR_INVALID_ARG;
+    if (b_count == 0 || a_count == 0) return SQ_OK;
+    if (!out) return SQ_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(out) & 7u) != 0) return SQ_ERR_ALIGNMENT;
+    sq_status rc = require_sm103();
+    if (rc != SQ_OK) return rc;
+    return launch_check_division(b_first, b_count, a_first, a_count, corrected ? 1 : 0, out,
+                                 as_stream(stream));
 }
 
 sq_status sq_device_status(void *stream) {

@@ -22,6 +22,54 @@ struct DeviceInfo {
 };
 sq_status device_info(DeviceInfo *out);
 
+// x / s with y = RN(1/s) computed once per column:
+//   q0 = RN(x y),  r = RN(x - s q0) (one fma),  q = RN(q0 + r y) (one fma).
+// q is the IEEE quotient RN(x / s) when no step leaves the normal range.  With
+// y = (1/s)(1 + d), |d| < 2^-24, and r exact, the value rounded last is
+// x/s + d (x/s - q0), a few 2^-48 ulp from x/s, while x/s -- never itself a
+// rounding midpoint -- lies at least ulp / 2^25 from every midpoint; q0 can be
+// more than an ulp off only for the largest few dividend significands.  Scaling
+// x or s by a power of two scales every step exactly, so correctness is a
+// property of the 2^46 significand pairs, and sq_check_division runs this very
+// function against IEEE division over all of them (or any subset).  Range used
+// by the callers: |s| in [2^-20, 2^20], |x| >= 2^-100 (then r is exact) and
+// |q0| <= 2^100; tinier x only matter as code 0.
+__device__ __forceinline__ float div_smooth(float x, float s, float y) {
+    const float q0 = __fmul_rn(x, y);
+    const float r = __fmaf_rn(-q0, s, x);
+    return __fmaf_rn(r, y, q0);
+}
+
+// Smooth-Static code of a smoothed value v (Table 10): round_half_even(fl(v /
+// scale)) saturated to [-127, 127], for any finite v, given rscale =
+// fl(1/scale).  p = fl(v * rscale) is within a relative 3u of the quotient;
+// |p| >= 128 means the quotient exceeds 127.5 in magnitude (the code
+// saturates); below that p is within 2.3e-5 of fl(v/scale), so its rounding
+// decides unless p lies within 2^-14 of a half-integer, where the IEEE
+// division does.  Shared by the activation quantiser and the GEMM epilogue
+// that emits the next linear's codes.
+__device__ __forceinline__ float static_code(float v, float scale, float rscale) {
+    const float p = __fmul_rn(v, rscale);
+    if (fabsf(p) >= 128.0f) return copysignf(127.0f, p);
+    const float k = rintf(p);
+    if (fabsf(__fsub_rn(p, k)) <= 0.49993896484375f)  // 0.5 - 2^-14
+        return fminf(127.0f, fmaxf(-127.0f, k));
+    const float e = rintf(__fdiv_rn(v, scale));
+    return fminf(127.0f, fmaxf(-127.0f, e));
+}
+
+// Outputs of the requantising epilogue (sq_linear_i8_requant): the codes of
+// the next linear's input, Smooth-Static with its smoothing factor s_next [N]
+// and per-tensor scale; either code array may be NULL (not both).
+struct RequantOut {
+    const float *s_next;
+    float scale, rscale;
+    int8_t *Yq;
+    __nv_bfloat16 *Yop;
+    float *x_scale;  // [M], set to `scale` (nullable)
+};
+
+
 // Launchers (internal): arguments were validated by the C-ABI layer.
 sq_status launch_channel_absmax(const float *A, int64_t rows, int64_t cols, float *amax,
                                 cudaStream_t st);
@@ -31,16 +79,21 @@ sq_status launch_smooth_factor(const float *ax, const float *aw, int64_t K, floa
 sq_status launch_quantize_rows(int direction, const float *A, const float *s, int64_t rows,
                                int64_t K, int8_t *q, float *scale, __nv_bfloat16 *op,
                                int32_t *l1, float fixed_scale, cudaStream_t st);
+sq_status launch_check_division(uint32_t b_first, uint32_t b_count, uint32_t a_first,
+                                uint32_t a_count, int corrected, unsigned long long *out,
+                                cudaStream_t st);
 sq_status launch_act_absmax(const float *A, const float *s, int64_t rows, int64_t K,
                             float *amax, cudaStream_t st);
 sq_status launch_gemm_mma_sync(const int8_t *Xq, const float *sx, const int8_t *Wq,
                                const float *sw, const float *bias, const float *residual,
                                int64_t M, int64_t N, int64_t K, int mode, void *Y,
                                cudaStream_t st);
+// rq == NULL: Y gets the epilogue's fp32 (or int32) values; otherwise the
+// epilogue's values are requantised into rq's code arrays and Y is unused.
 sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_t *x_l1,
                          const __nv_bfloat16 *Wop, const float *sw, const int32_t *w_l1,
                          const float *bias, const float *residual, int64_t M, int64_t N,
-                         int64_t K, int mode, void *Y, cudaStream_t st);
+                         int64_t K, int mode, void *Y, const RequantOut *rq, cudaStream_t st);
 // Reads and clears the tcgen05 GEMM's device error word (synchronous).
 sq_status gemm_tc_take_error(cudaStream_t st);
 

@@ -309,6 +309,9 @@ struct EpiArgs {
     void *Y;
     int M, N;
     int tma_io;  // 1: TMA staging for Y (and the residual); 0: plain per-element I/O
+    RequantOut rq;  // the requantising epilogue's outputs (QUANT kernels)
+    int rq_vec;     // 1: rows of the code arrays are 16-byte multiples (N % 16 == 0)
+    int rq_fast;    // 1: scale >= 2^-70, so the reciprocal division may be used
 };
 
 // Largest row L1 norm of int8 codes for which 127 * L1 < 2^24: then every
@@ -390,7 +393,7 @@ struct ColParams {
     float b[SLICES];
 };
 
-template <int MODE>
+template <int MODE, bool QUANT>
 __device__ __forceinline__ void load_col_params(ColParams &cp, const EpiArgs &a, int nb,
                                                 int lane) {
 #pragma unroll
@@ -399,6 +402,135 @@ __device__ __forceinline__ void load_col_params(ColParams &cp, const EpiArgs &a,
         const bool ok = n < a.N;
         cp.w[s] = (MODE != SQ_EPI_RAW_I32 && ok) ? __ldg(a.sw + n) : 0.f;
         cp.b[s] = (MODE != SQ_EPI_RAW_I32 && MODE != SQ_EPI_NONE && ok) ? __ldg(a.bias + n) : 0.f;
+    }
+}
+
+// The requantising epilogue's column parameters for this warp's 128 columns,
+// (-s_next, RN(1/s_next)) per column -- NaN for the reciprocal where s_next is
+// outside [2^-20, 2^20], which sends those columns to the exact path -- in the
+// warp's staging area (unused by the requantising kernels), read back by every
+// lane as broadcasts.
+__device__ __forceinline__ void stage_next_smoothing(uint8_t *stg, const EpiArgs &a, int nb,
+                                                     int lane) {
+    float2 *sy = reinterpret_cast<float2 *>(stg);
+#pragma unroll
+    for (int s = 0; s < SLICES; ++s) {
+        const int n = nb + s * SLICE + lane;
+        const float sn = n < a.N ? __ldg(a.rq.s_next + n) : 1.f;
+        const float as = fabsf(sn);
+        const float yn = (as >= 0x1p-20f && as <= 0x1p20f) ? __frcp_rn(sn)
+                                                           : __int_as_float(0x7fffffff);
+        sy[s * SLICE + lane] = make_float2(-sn, yn);
+    }
+    __syncwarp();
+}
+
+// max that propagates NaN
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+// Requantising epilogue: the slice's fp32 values y (this thread's row m, 32
+// columns from n) become the next linear's Smooth-Static codes,
+// clamp(round_half_even(fl(fl(y / s_next[n]) / scale)), +-127), written as
+// exact bf16 values and/or int8.  y / s_next takes the reciprocal division
+// (div_smooth, exact where |y| >= 2^-100 and |y / s| <= 2^100; tinier y give
+// code 0 either way since scale >= 2^-70), the code the 1.5 * 2^23 rounding;
+// a thread whose slice holds a value outside that range, a smoothing factor
+// outside [2^-20, 2^20] (NaN reciprocal) or a product within 2^-14 of a
+// half-integer takes the IEEE divisions for that element (static_code).
+__device__ __noinline__ float requant_exact(float y, float s, float scale, float rscale) {
+    return static_code(__fdiv_rn(y, s), scale, rscale);
+}
+
+__device__ __forceinline__ void requant_slice(const uint32_t (&v)[32], int64_t m, int64_t n,
+                                              const EpiArgs &a, const float4 *sy) {
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    const float lim = a.rq_fast ? 0.49993896484375f : -1.0f;  // 0.5 - 2^-14
+    const unsigned long long r2 = pk(a.rq.rscale, a.rq.rscale);
+    const unsigned long long mg2 = pk(kMagic, kMagic), nmg2 = pk(-kMagic, -kMagic);
+    const unsigned long long neg1 = pk(-1.0f, -1.0f);
+    float c[32];
+    float dm = 0.0f, qm = 0.0f;  // largest |p - k| and |q0| (NaN kept) of the slice
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        // columns j, j+1: (-s, RN(1/s)) pairs, the same for every lane
+        const float4 q = sy[j >> 1];
+        const unsigned long long y2 = pk(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+        const unsigned long long yn2 = pk(q.y, q.w), ns2 = pk(q.x, q.z);
+        const unsigned long long q0 = mul2(y2, yn2);
+        const unsigned long long v2 = fma2(fma2(q0, ns2, y2), yn2, q0);  // div_smooth
+        float p0, p1;
+        upk(mul2(v2, r2), p0, p1);
+        // clamping to +-127 before rounding yields the saturated code directly
+        p0 = fminf(fmaxf(p0, -127.0f), 127.0f);
+        p1 = fminf(fmaxf(p1, -127.0f), 127.0f);
+        const unsigned long long pp = pk(p0, p1);
+        const unsigned long long k2 = add2(add2(pp, mg2), nmg2);
+        float k0, k1, d0, d1, qa, qb;
+        upk(k2, k0, k1);
+        upk(fma2(k2, neg1, pp), d0, d1);
+        upk(q0, qa, qb);
+        c[j] = k0;
+        c[j + 1] = k1;
+        dm = fmaxf(dm, fmaxf(fabsf(d0), fabsf(d1)));
+        qm = max_nan(qm, max_nan(fabsf(qa), fabsf(qb)));
+    }
+    // a near-tie, a NaN or a |q0| above 2^100 somewhere in the slice: those
+    // elements take the exact path (rare; one branch per slice)
+    if (!(dm <= lim) || !(qm <= 0x1p100f)) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float2 q = reinterpret_cast<const float2 *>(sy)[j];
+            const float y = __uint_as_float(v[j]);
+            const float q0 = __fmul_rn(y, q.y);
+            const float vv = __fmaf_rn(__fmaf_rn(q0, q.x, y), q.y, q0);
+            const float p = fminf(fmaxf(__fmul_rn(vv, a.rq.rscale), -127.0f), 127.0f);
+            const float k = __fsub_rn(__fadd_rn(p, kMagic), kMagic);
+            if (!(fabsf(__fsub_rn(p, k)) <= lim) || !(fabsf(q0) <= 0x1p100f))
+                c[j] = requant_exact(y, -q.x, a.rq.scale, a.rq.rscale);
+        }
+    }
+    if (m >= a.M) return;
+    const int64_t off = m * a.N + n;
+    if (a.rq_vec && n + 31 < a.N) {
+        if (a.rq.Yop) {
+            uint4 *dst = reinterpret_cast<uint4 *>(a.rq.Yop + off);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)  // integers |c| <= 127: the high halves are exact bf16
+                    w[e] = __byte_perm(__float_as_uint(c[8 * q + 2 * e]),
+                                       __float_as_uint(c[8 * q + 2 * e + 1]), 0x7632);
+                dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+        if (a.rq.Yq) {
+            uint4 *dst = reinterpret_cast<uint4 *>(a.rq.Yq + off);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = 16 * q + 4 * e;
+                    w[e] = (uint32_t)(__float2int_rn(c[j]) & 0xff) |
+                           ((uint32_t)(__float2int_rn(c[j + 1]) & 0xff) << 8) |
+                           ((uint32_t)(__float2int_rn(c[j + 2]) & 0xff) << 16) |
+                           ((uint32_t)(__float2int_rn(c[j + 3]) & 0xff) << 24);
+                }
+                dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (n + j >= a.N) break;
+            if (a.rq.Yop) a.rq.Yop[off + j] = __float2bfloat16_rn(c[j]);
+            if (a.rq.Yq) a.rq.Yq[off + j] = (int8_t)__float2int_rn(c[j]);
+        }
     }
 }
 
@@ -430,11 +562,12 @@ __device__ __forceinline__ void load_residual(float4 (&r)[8], const EpiArgs &a, 
 // so the store's latency hides behind it.  Staging tile row `lane` holds this
 // thread's 32 values, 16-byte chunk c at c ^ (lane & 7) (the TMA 128-byte
 // swizzle: conflict-free for the warp).
-template <int MODE, bool INT_IN>
+template <int MODE, bool INT_IN, bool QUANT>
 __device__ __forceinline__ void epilogue_slice(uint32_t (&v)[32], int64_t m, int64_t n,
                                                int row0, int lane, const EpiArgs &a, float xs,
-                                               float wl, float bl, const float4 (&r4)[8],
-                                               const CUtensorMap *tmY, uint8_t *stg) {
+                                               float wl, float bl, int slice_index,
+                                               const float4 (&r4)[8], const CUtensorMap *tmY,
+                                               uint8_t *stg) {
     if (n >= a.N || row0 >= a.M) return;  // slice wholly outside Y
     if (MODE == SQ_EPI_RAW_I32) {
         if (!INT_IN) {
@@ -475,6 +608,11 @@ __device__ __forceinline__ void epilogue_slice(uint32_t (&v)[32], int64_t m, int
             v[j + 1] = __float_as_uint(o1);
         }
     }
+    if (QUANT) {
+        // this slice's columns in the warp's staging area (written per tile)
+        requant_slice(v, m, n, a, reinterpret_cast<const float4 *>(stg) + 16 * slice_index);
+        return;
+    }
     if (a.tma_io) {
         // the previous TMA store of this warp must have finished reading the tile
         if (lane == 0) bulk_wait_read0();
@@ -500,7 +638,7 @@ __device__ __forceinline__ void epilogue_slice(uint32_t (&v)[32], int64_t m, int
 // The first `nsl` slices of this warp's part of a tile (all four for a full
 // tile, fewer for a column slice of one), reading tensor memory at `taddr`
 // (fp32 sums, or int32 with INT_IN).
-template <int MODE, bool INT_IN>
+template <int MODE, bool INT_IN, bool QUANT>
 __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int64_t m, int nb, int row0,
                                               int lane, const EpiArgs &a, float xs,
                                               const ColParams &cp, float4 (&rnext)[8],
@@ -517,12 +655,12 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int64_t m, int nb,
         const float bl = s == 0 ? cp.b[0] : s == 1 ? cp.b[1] : s == 2 ? cp.b[2] : cp.b[3];
         uint32_t v[32];
         tmem_ld32(taddr + s * SLICE, v);
-        epilogue_slice<MODE, INT_IN>(v, m, nb + s * SLICE, row0, lane, a, xs, wl, bl, rcur, tmY,
-                                     stg);
+        epilogue_slice<MODE, INT_IN, QUANT>(v, m, nb + s * SLICE, row0, lane, a, xs, wl, bl, s,
+                                            rcur, tmY, stg);
     }
 }
 
-template <int MODE>
+template <int MODE, bool QUANT>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmBs, const __grid_constant__ CUtensorMap tmY,
@@ -693,7 +831,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int nsl = max(0, min(SLICES, (t.bn - half * COLS_PER_WARP) / SLICE));
             // operands that do not depend on the accumulators: fetch them now
             ColParams cp;
-            load_col_params<MODE>(cp, args, nb, lane);
+            load_col_params<MODE, QUANT>(cp, args, nb, lane);
+            if (QUANT) stage_next_smoothing(stg, args, nb, lane);
+            if (QUANT && args.rq.x_scale && t.n0 == 0 && half == 0 && m < M)
+                args.rq.x_scale[m] = args.rq.scale;  // the next linear's per-token scales
             const float xs = (MODE != SQ_EPI_RAW_I32 && m < M) ? __ldg(args.sx + m) : 0.f;
             float4 rnext[8];
             if (MODE == SQ_EPI_BIAS_RESIDUAL && nsl > 0) load_residual(rnext, args, m, nb);
@@ -703,8 +844,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 fph ^= 1u << b;
                 tc_fence_after();
                 const uint32_t tA = tmem_base + lane_off + b * BN + half * COLS_PER_WARP;
-                epilogue_tile<MODE, false>(tA, m, nb, row0, lane, args, xs, cp, rnext, &tmY, stg,
-                                           nsl);
+                epilogue_tile<MODE, false, QUANT>(tA, m, nb, row0, lane, args, xs, cp, rnext, &tmY,
+                                                  stg, nsl);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.tempty[b]));
@@ -736,7 +877,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (lane == 0) mbar_arrive(smem_u32(&S.tempty[0]));
                 }
                 // final pass from the int32 partial; overlaps the next tile's MMAs
-                epilogue_tile<MODE, true>(tP, m, nb, row0, lane, args, xs, cp, rnext, &tmY, stg, nsl);
+                epilogue_tile<MODE, true, QUANT>(tP, m, nb, row0, lane, args, xs, cp, rnext, &tmY, stg,
+                                                 nsl);
             }
         }
     done_e:
@@ -789,19 +931,28 @@ sq_status make_map(CUtensorMap *map, CUtensorMapDataType dt, int esize, const vo
     return r == CUDA_SUCCESS ? SQ_OK : SQ_ERR_CUDA;
 }
 
-template <int MODE>
-sq_status launch_mode(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tbs,
-                      const CUtensorMap &ty, const EpiArgs &args, int K, int grid, int device,
-                      cudaStream_t st) {
+template <int MODE, bool QUANT>
+sq_status launch_kernel(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tbs,
+                        const CUtensorMap &ty, const EpiArgs &args, int K, int grid, int device,
+                        cudaStream_t st) {
     static int attr_dev = -1;
     if (attr_dev != device) {
-        if (cudaFuncSetAttribute(gemm_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(gemm_tc_kernel<MODE, QUANT>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SMEM_BYTES) != cudaSuccess)
             return SQ_ERR_CUDA;
         attr_dev = device;
     }
-    gemm_tc_kernel<MODE><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, tbs, ty, args, K);
+    gemm_tc_kernel<MODE, QUANT><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, tbs, ty, args, K);
     return cuda_status(cudaGetLastError());
+}
+
+template <int MODE>
+sq_status launch_mode(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tbs,
+                      const CUtensorMap &ty, const EpiArgs &args, int K, int grid, int device,
+                      bool quant, cudaStream_t st) {
+    return quant ? launch_kernel<MODE, true>(ta, tb, tbs, ty, args, K, grid, device, st)
+                 : launch_kernel<MODE, false>(ta, tb, tbs, ty, args, K, grid, device, st);
 }
 
 }  // namespace
@@ -809,8 +960,9 @@ sq_status launch_mode(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
 sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_t *x_l1,
                          const __nv_bfloat16 *Wop, const float *sw, const int32_t *w_l1,
                          const float *bias, const float *residual, int64_t M, int64_t N,
-                         int64_t K, int mode, void *Y, cudaStream_t st) {
+                         int64_t K, int mode, void *Y, const RequantOut *rq, cudaStream_t st) {
     if (M > 0x7fffffff || N > 0x7fffffff) return SQ_ERR_UNSUPPORTED;
+    if (rq && mode == SQ_EPI_RAW_I32) return SQ_ERR_INVALID_ARG;
     sq_status rc = get_encoder();
     if (rc != SQ_OK) return rc;
     DeviceInfo di;
@@ -827,9 +979,14 @@ sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_
     args.N = (int)N;
     // TMA staging for Y (and the residual) needs 16-byte rows and aligned bases;
     // the vector loads of the scales and bias need them aligned too
-    args.tma_io = (N % 4 == 0) && aligned16(Y) && (mode == SQ_EPI_RAW_I32 || aligned16(sw)) &&
+    args.tma_io = (N % 4 == 0) && (rq || aligned16(Y)) &&
+                  (mode == SQ_EPI_RAW_I32 || aligned16(sw)) &&
                   (bias == nullptr || aligned16(bias)) &&
                   (residual == nullptr || aligned16(residual));
+    args.rq = rq ? *rq : RequantOut{};
+    args.rq_vec = rq && N % 16 == 0 && (!rq->Yq || aligned16(rq->Yq)) &&
+                  (!rq->Yop || aligned16(rq->Yop));
+    args.rq_fast = rq && rq->scale >= 0x1p-70f;
     CUtensorMap ta, tb, tbs, ty;
     if ((rc = make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Xop, M, K, BM, BK)) != SQ_OK)
         return rc;
@@ -846,20 +1003,23 @@ sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_
         (rc = make_map(&tbs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wop, N, K, BN / sched.sub, BK)) !=
             SQ_OK)
         return rc;
-    ty = ta;  // unused placeholder unless tma_io
-    if (args.tma_io) {
+    ty = ta;  // unused placeholder unless Y is stored through TMA
+    if (args.tma_io && !rq) {
         const CUtensorMapDataType yt = mode == SQ_EPI_RAW_I32 ? CU_TENSOR_MAP_DATA_TYPE_INT32
                                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
         if ((rc = make_map(&ty, yt, 4, Y, M, N, SLICE, SLICE)) != SQ_OK) return rc;
     }
+    const bool q = rq != nullptr;
+    const int k = (int)K, dev = di.device;
     switch (mode) {
-    case SQ_EPI_NONE: return launch_mode<SQ_EPI_NONE>(ta, tb, tbs, ty, args, (int)K, grid, di.device, st);
-    case SQ_EPI_BIAS: return launch_mode<SQ_EPI_BIAS>(ta, tb, tbs, ty, args, (int)K, grid, di.device, st);
+    case SQ_EPI_NONE: return launch_mode<SQ_EPI_NONE>(ta, tb, tbs, ty, args, k, grid, dev, q, st);
+    case SQ_EPI_BIAS: return launch_mode<SQ_EPI_BIAS>(ta, tb, tbs, ty, args, k, grid, dev, q, st);
     case SQ_EPI_BIAS_GELU:
-        return launch_mode<SQ_EPI_BIAS_GELU>(ta, tb, tbs, ty, args, (int)K, grid, di.device, st);
+        return launch_mode<SQ_EPI_BIAS_GELU>(ta, tb, tbs, ty, args, k, grid, dev, q, st);
     case SQ_EPI_BIAS_RESIDUAL:
-        return launch_mode<SQ_EPI_BIAS_RESIDUAL>(ta, tb, tbs, ty, args, (int)K, grid, di.device, st);
-    default: return launch_mode<SQ_EPI_RAW_I32>(ta, tb, tbs, ty, args, (int)K, grid, di.device, st);
+        return launch_mode<SQ_EPI_BIAS_RESIDUAL>(ta, tb, tbs, ty, args, k, grid, dev, q, st);
+    default:
+        return launch_kernel<SQ_EPI_RAW_I32, false>(ta, tb, tbs, ty, args, k, grid, dev, st);
     }
 }
 

@@ -53,21 +53,6 @@ __device__ __forceinline__ float code_of(float v, float scale, float rscale) {
     return fminf(127.0f, fmaxf(-127.0f, e));
 }
 
-// Static-scale code: round_half_even(fl(v / scale)) clamped to [-127, 127]
-// for any finite v.  p = fl(v * fl(1/scale)) is within a relative 3u of the
-// quotient; |p| >= 128 means the quotient exceeds 127.5 in magnitude (the
-// code saturates); below that p is within 2.3e-5 of fl(v/scale), so its
-// rounding decides unless p lies within 2^-14 of a half-integer.
-__device__ __forceinline__ float static_code(float v, float scale, float rscale) {
-    const float p = __fmul_rn(v, rscale);
-    if (fabsf(p) >= 128.0f) return copysignf(127.0f, p);
-    const float k = rintf(p);
-    if (fabsf(__fsub_rn(p, k)) <= 0.49993896484375f)  // 0.5 - 2^-14
-        return fminf(127.0f, fmaxf(-127.0f, k));
-    const float e = rintf(__fdiv_rn(v, scale));
-    return fminf(127.0f, fmaxf(-127.0f, e));
-}
-
 // four integer-valued codes to the int8 and/or bf16 outputs (float4 index off4)
 __device__ __forceinline__ void store_code_values(float c0, float c1, float c2, float c3,
                                                   int64_t off4, int8_t *q, __nv_bfloat16 *op) {

@@ -120,3 +120,26 @@ def test_argument_checks_fail_before_any_launch(lib):
     assert lib.sq_channel_absmax(a, 4, 0, a, None) == INVALID
     assert lib.sq_channel_absmax(a, 0, 4, a, None) == 0
     assert lib.sq_channel_absmax(None, 0, 4, None, None) == 0
+    # producer-fused requantisation
+    f = lib.sq_linear_i8_requant
+    f.argtypes = [vp] * 8 + [i64, i64, i64, ctypes.c_int, vp, ctypes.c_float, vp, vp, vp, vp]
+    assert f(a, a, None, a, a, None, a, None, 8, 8, 32, 4, a, 1.0, a, a, None, None) == INVALID
+    assert f(a, a, None, a, a, None, a, None, 8, 8, 32, 1, a, 0.0, a, a, None, None) == INVALID
+    assert f(a, a, None, a, a, None, a, None, 8, 8, 32, 1, a, float("inf"), a, a, None,
+             None) == INVALID
+    assert f(a, a, None, a, a, None, a, None, 8, 8, 32, 1, None, 1.0, a, a, None, None) == INVALID
+    assert f(a, a, None, a, a, None, a, None, 8, 8, 32, 1, a, 1.0, None, None, None,
+             None) == INVALID                                                # no code output
+    assert f(a, a, None, a, a, None, a, None, 8, 8, 32, 1, a, 1.0, None, _fake(0x10001), None,
+             None) == ALIGN                                                  # odd bf16 address
+    assert f(a, a, None, a, a, None, a, None, 0, 8, 32, 1, None, 1.0, None, None, None,
+             None) == 0                                                      # empty
+    # division self-check: ranges within the 2^23 fraction fields, output aligned
+    u32 = ctypes.c_uint32
+    lib.sq_check_division.argtypes = [u32, u32, u32, u32, ctypes.c_int, vp, vp]
+    F = 1 << 23
+    assert lib.sq_check_division(F - 1, 2, 0, 1, 1, a, None) == INVALID
+    assert lib.sq_check_division(0, 1, F, 1, 1, a, None) == INVALID
+    assert lib.sq_check_division(0, 1, 0, 1, 1, None, None) == INVALID
+    assert lib.sq_check_division(0, 1, 0, 1, 1, _fake(0x10004), None) == ALIGN
+    assert lib.sq_check_division(0, 0, 0, 1, 1, None, None) == 0        # empty

@@ -554,3 +554,67 @@ def test_static_linear_block(sq):
     _, sx_d, Xop = sq.quantize_act_static(to_dev(X), to_dev(s), float(scale), want_q=False)
     y = sq.linear_i8(Xop, sx_d, Wop, sw_d, to_dev(c.bias.numpy()), None, wl.EPI_BIAS_GELU)
     assert_close_fp32(y.cpu().numpy(), ref, "static linear block")
+
+
+# ------------------------------------------------ producer-fused requantisation
+
+@pytest.mark.parametrize("mode", [wl.EPI_NONE, wl.EPI_BIAS, wl.EPI_BIAS_GELU,
+                                  wl.EPI_BIAS_RESIDUAL])
+@pytest.mark.parametrize("M,N,K", [(77, 136, 1024), (256, 1024, 1024), (300, 4096, 1024),
+                                   (2560, 2304, 512), (130, 200, 2064)])
+def test_requant_epilogue_matches_static_quantiser(sq, mode, M, N, K):
+    """The requantising epilogue's codes equal the oracle's Smooth-Static
+    quantiser applied to the fp32 output the plain epilogue stores (the same
+    y, bit for bit), for a calibrated scale and for a quarter of it
+    (saturating codes); x_scale_next is the scale everywhere."""
+    c, xq, sx, wq, sw, d = _quantised_case(sq, M, K, N, wl.EPI_BIAS_RESIDUAL, seed=3 * M + N + mode)
+    b = to_dev(c.bias.numpy())
+    r = to_dev(c.residual.numpy()) if mode == wl.EPI_BIAS_RESIDUAL else None
+    y = sq.linear_i8(d["Xop"], d["sx"], d["Wop"], d["sw"], b, r, mode).cpu().numpy()
+    rng = np.random.default_rng(M + N)
+    s_next = rng.uniform(0.2, 6.0, N).astype(np.float32)
+    calib = oracle.static_scale(oracle.act_absmax(y, s_next))
+    for scale in (calib, calib * np.float32(0.25)):
+        Yq, Yop, xs = sq.linear_i8_requant(d["Xop"], d["sx"], d["Wop"], d["sw"], b, r, mode,
+                                           to_dev(s_next), float(scale), want_q=True)
+        ref = oracle.quantize_static(y, s_next, scale)
+        assert_codes_equal(Yq.cpu().numpy(), ref, "Yq")
+        assert_codes_equal(op_as_int(Yop), ref, "Yop")
+        assert np.all(xs.cpu().numpy() == np.float32(scale))
+    assert np.abs(ref).max() == 127  # the quarter scale saturates
+    # smoothing factors outside [2^-20, 2^20] and a scale below 2^-70 take the
+    # exact path (IEEE divisions)
+    s_odd = s_next.copy()
+    s_odd[min(3, N - 1)] = np.float32(1e-7)
+    s_odd[min(5, N - 1)] = np.float32(3e7)
+    for s_case, scale in ((s_odd, calib), (s_next, np.float32(2.0 ** -71))):
+        _, Yop, _ = sq.linear_i8_requant(d["Xop"], d["sx"], d["Wop"], d["sw"], b, r, mode,
+                                         to_dev(s_case), float(scale), want_x_scale=False)
+        assert_codes_equal(op_as_int(Yop), oracle.quantize_static(y, s_case, scale), "Yop")
+
+
+def test_requant_feeds_next_linear(sq):
+    """FFN-up with the requantising epilogue feeding FFN-down: the down
+    projection's output equals the unfused chain's (the same codes go in)."""
+    M, K1, N1, N2 = 512, 1024, 4096, 1024
+    c1 = wl.make_case(M, K1, N1, wl.EPI_BIAS_GELU, seed=11)
+    W2 = wl.make_weight(N2, N1, 12)
+    b2 = wl.make_bias(N2, 12)
+    r2 = wl.make_residual(M, N2, 12)
+    Xd, Wd = c1.X.cuda(), c1.W.cuda()
+    s1 = sq.smooth_factor(sq.channel_absmax(Xd), sq.channel_absmax(Wd), 0.5)
+    _, sw1, Wop1 = sq.pack_weight(Wd, s1, want_q=False)
+    _, sx1, Xop1 = sq.quantize_act(Xd, s1, want_q=False)
+    y1 = sq.linear_i8(Xop1, sx1, Wop1, sw1, c1.bias.cuda(), None, wl.EPI_BIAS_GELU)
+    s2 = sq.smooth_factor(sq.channel_absmax(y1), sq.channel_absmax(W2.cuda()), 0.5)
+    _, sw2, Wop2 = sq.pack_weight(W2.cuda(), s2, want_q=False)
+    scale = float(oracle.static_scale(oracle.act_absmax(y1.cpu().numpy(), s2.cpu().numpy())))
+    # unfused: fp32 y1, then the static quantiser
+    _, sx2, Xop2 = sq.quantize_act_static(y1, s2, scale, want_q=False)
+    y2 = sq.linear_i8(Xop2, sx2, Wop2, sw2, b2.cuda(), r2.cuda(), wl.EPI_BIAS_RESIDUAL)
+    # fused: FFN-up emits FFN-down's operand
+    _, Xop2f, sx2f = sq.linear_i8_requant(Xop1, sx1, Wop1, sw1, c1.bias.cuda(), None,
+                                          wl.EPI_BIAS_GELU, s2, scale)
+    y2f = sq.linear_i8(Xop2f, sx2f, Wop2, sw2, b2.cuda(), r2.cuda(), wl.EPI_BIAS_RESIDUAL)
+    assert torch.equal(Xop2f, Xop2) and torch.equal(sx2f, sx2)
+    assert torch.equal(y2f, y2)
