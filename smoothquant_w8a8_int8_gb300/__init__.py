@@ -3,14 +3,15 @@
 The compute runs in the C-ABI library ``libsq_gb300.so`` (hand-written CUDA);
 ``binding`` is a thin ctypes layer with the same entry-point names.
 ``workloads`` draws the seeded synthetic inputs and ``roofline`` holds the
-metric arithmetic.  The library is loaded on first use; if it is missing,
-that call raises.
+metric arithmetic; ``pipeline`` streams host-resident activations through the
+block and ``alpha_sweep`` calibrates the migration strength on synthetic data.
+The library is loaded on first use; if it is missing, that call raises.
 """
 import importlib
 
 from . import roofline, workloads  # noqa: F401
 
-_SUBMODULES = ("binding", "build", "roofline", "workloads")
+_SUBMODULES = ("alpha_sweep", "binding", "build", "pipeline", "roofline", "workloads")
 
 
 def __getattr__(name):
