@@ -21,6 +21,8 @@ Parity status per function (what pins each one, see ``tests/test_oracle.py``):
   gemm_i32         brute force in an outer-product order, closed forms
                    (all 127, cancelling signs, one-hot rows), overflow check
   epilogue         textbook normal-CDF values for GELU, zero-input cases
+  layernorm        closed forms (constant row -> beta, alternating +-a -> +-1),
+                   scale and shift invariance, zero mean / unit variance
 """
 from __future__ import annotations
 
@@ -72,11 +74,13 @@ def _load():
             lib.oracle_num_threads.argtypes = []
             lib.oracle_act_absmax.argtypes = [p, p, i64, i64, p]
             lib.oracle_quantize_static.argtypes = [p, p, i64, i64, ctypes.c_float, p]
+            lib.oracle_layernorm.argtypes = [p, p, p, dbl, i64, i64, p]
             for f in (lib.oracle_channel_absmax, lib.oracle_smooth_factor,
                       lib.oracle_smooth, lib.oracle_quantize_rows,
                       lib.oracle_gemm_i32, lib.oracle_epilogue,
                       lib.oracle_linear_block, lib.oracle_num_threads,
-                      lib.oracle_act_absmax, lib.oracle_quantize_static):
+                      lib.oracle_act_absmax, lib.oracle_quantize_static,
+                      lib.oracle_layernorm):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -172,6 +176,20 @@ def quantize_static(X, s, scale):
     _check(_load().oracle_quantize_static(_ptr(X), _ptr(s), rows, K, float(np.float32(scale)),
                                           _ptr(q)), "quantize_static")
     return q
+
+
+def layernorm(H, gamma, beta, eps=1e-12):
+    """Row LayerNorm in double, rounded once to fp32 (Table 3's LayerNorm; the
+    input the next linear quantises)."""
+    H = _c(H, np.float32)
+    gamma = _c(gamma, np.float32)
+    beta = _c(beta, np.float32)
+    rows, K = H.shape
+    assert gamma.shape == (K,) and beta.shape == (K,)
+    y = np.empty_like(H)
+    _check(_load().oracle_layernorm(_ptr(H), _ptr(gamma), _ptr(beta), float(eps), rows, K,
+                                    _ptr(y)), "layernorm")
+    return y
 
 
 def gemm_i32(xq, wq):

@@ -246,6 +246,37 @@ int oracle_linear_block(const float *X, const float *s, const int8_t *wq,
     return oracle_epilogue(acc, sx, sw, bias, residual, M, N, mode, y);
 }
 
+/* LayerNorm of each row, the encoder's normalisation that precedes the FFN
+ * and QKV linears (Table 3 lists it among BERT-large's operators; SmoothQuant
+ * folds the smoothing factor into it, so its output is what the next linear
+ * quantises):
+ *   y = (h - mean) / sqrt(var + eps) * gamma[j] + beta[j],
+ * mean and the biased variance over the row's K elements, all in double,
+ * rounded once to fp32. */
+int oracle_layernorm(const float *H, const float *gamma, const float *beta, double eps,
+                     int64_t rows, int64_t K, float *Y)
+{
+    if (!H || !gamma || !beta || !Y || rows < 0 || K <= 0 || !(eps >= 0.0))
+        return ORC_ERR_ARG;
+    #pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < rows; ++m) {
+        const float *h = H + m * K;
+        double sum = 0.0;
+        for (int64_t j = 0; j < K; ++j) sum += (double)h[j];
+        const double mean = sum / (double)K;
+        double sq = 0.0;
+        for (int64_t j = 0; j < K; ++j) {
+            const double d = (double)h[j] - mean;
+            sq += d * d;
+        }
+        const double rstd = 1.0 / sqrt(sq / (double)K + eps);
+        for (int64_t j = 0; j < K; ++j)
+            Y[m * K + j] = (float)(((double)h[j] - mean) * rstd * (double)gamma[j] +
+                                   (double)beta[j]);
+    }
+    return ORC_OK;
+}
+
 /* Number of OpenMP threads a parallel region of this library uses. */
 int oracle_num_threads(void)
 {

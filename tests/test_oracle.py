@@ -279,3 +279,38 @@ def test_static_absmax_running_and_brute_force():
                           for i in range(3) for j in range(16)))
     assert oracle.act_absmax(B, s, a) == np.float32(want2)
     assert oracle.static_scale(0.0) == 1.0
+
+
+# ---------------------------------------------------------------- LayerNorm
+
+def test_layernorm_closed_forms():
+    K = 64
+    g = np.ones(K, np.float32)
+    b = np.linspace(-1, 1, K).astype(np.float32)
+    # a constant row has zero deviation from its mean: the output is beta
+    y = oracle.layernorm(np.full((1, K), 3.25, np.float32), g, b, eps=1e-5)
+    np.testing.assert_array_equal(y[0], b)
+    # +-a alternating: mean 0, variance a^2, so with eps = 0 the output is +-1
+    a = np.float32(2.5)
+    h = np.tile(np.array([a, -a], np.float32), K // 2)[None]
+    y = oracle.layernorm(h, g, np.zeros(K, np.float32), eps=0.0)
+    np.testing.assert_array_equal(y[0], np.tile(np.array([1, -1], np.float32), K // 2))
+    # gamma and beta act per channel
+    y2 = oracle.layernorm(h, np.full(K, 2.0, np.float32), np.full(K, 0.5, np.float32), eps=0.0)
+    np.testing.assert_array_equal(y2[0], 2.0 * y[0] + 0.5)
+
+
+def test_layernorm_invariances():
+    rng = np.random.default_rng(3)
+    K = 256
+    h = rng.standard_normal((8, K)).astype(np.float32)
+    g, b = np.ones(K, np.float32), np.zeros(K, np.float32)
+    y = oracle.layernorm(h, g, b, eps=0.0)
+    # zero mean and unit (biased) variance per row
+    np.testing.assert_allclose(y.astype(np.float64).mean(axis=1), 0.0, atol=1e-6)
+    np.testing.assert_allclose(y.astype(np.float64).var(axis=1), 1.0, rtol=1e-6)
+    # invariant under scaling by a power of two and under a shift
+    y4 = oracle.layernorm(h * np.float32(4.0), g, b, eps=0.0)
+    np.testing.assert_array_equal(y4, y)
+    ys = oracle.layernorm(h + np.float32(0.75), g, b, eps=0.0)
+    np.testing.assert_allclose(ys, y, atol=2e-6)
