@@ -152,11 +152,14 @@ class ClockSampler:
 
 class Layer:
     __slots__ = ("lin", "X", "s", "Wop", "Wq", "sw", "wl1", "bias", "residual", "Y", "Xhost",
-                 "Yhost", "static_scale", "feeds", "fed_by")
+                 "Yhost", "static_scale", "feeds", "fed_by", "ln")
+
+
+LN_EPS = 1e-12
 
 
 def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
-                   quant: str = "dynamic", ffn_chain: str = "off"):
+                   quant: str = "dynamic", ffn_chain: str = "off", ln: bool = False):
     from smoothquant_w8a8_int8_gb300 import binding as sq
     dev = torch.device("cuda")
     layers = []
@@ -200,6 +203,7 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
             L.Y = torch.empty(w.M, lin.N, dtype=torch.float32, device=dev)
             L.Xhost = L.Yhost = None
             L.feeds = None
+            L.ln = None
             L.fed_by = up
             up.feeds = L
             del c.W, c.X
@@ -210,8 +214,22 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
         L = Layer()
         L.lin = lin
         L.X = c.X
+        L.ln = None
+        stats_src = c.X
+        if ln and idx in (0, 2):
+            # the QKV and FFN-up inputs come from the encoder's LayerNorms: X is
+            # the pre-normalisation hidden state, gamma ~ 1 + N(0, 0.05),
+            # beta ~ N(0, 0.05); the smoothing statistics are the LayerNorm's
+            g = torch.Generator(device=dev)
+            g.manual_seed(seed + 4242)
+            gamma = 1.0 + 0.05 * torch.randn(lin.K, generator=g, device=dev)
+            beta = 0.05 * torch.randn(lin.K, generator=g, device=dev)
+            L.ln = (gamma.contiguous(), beta.contiguous())
+            ones = torch.ones(lin.K, dtype=torch.float32, device=dev)
+            _, _, _, stats_src, _ = sq.layernorm_quant(c.X, L.ln[0], L.ln[1], LN_EPS, ones,
+                                                       want_q=False, want_y=True)
         # smoothing factor from this batch's own statistics (calibration = the input)
-        s = sq.smooth_factor(sq.channel_absmax(c.X), sq.channel_absmax(c.W), w.alpha)
+        s = sq.smooth_factor(sq.channel_absmax(stats_src), sq.channel_absmax(c.W), w.alpha)
         L.s = s
         Wq, sw, Wop, wl1 = sq.pack_weight(c.W, s, want_q=(gemm == "mma_sync"),
                                           want_op=(gemm == "tc"), want_l1=True)
@@ -223,6 +241,10 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
             # separate batch drawn from the same distribution
             calib = wl.make_activation(512, lin.K, seed + 555, w.outlier_frac, w.outlier_scale,
                                        lin.gelu_input, device=dev, channel_seed=seed)
+            if L.ln is not None:
+                ones = torch.ones(lin.K, dtype=torch.float32, device=dev)
+                _, _, _, calib, _ = sq.layernorm_quant(calib, L.ln[0], L.ln[1], LN_EPS, ones,
+                                                       want_q=False, want_y=True)
             L.static_scale = sq.static_scale(sq.act_absmax(calib, s).item())
         L.Y = torch.empty(w.M, lin.N, dtype=torch.float32, device=dev)
         L.Xhost = L.Yhost = None
@@ -236,6 +258,19 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
     torch.cuda.synchronize()
     bufs = (Xq_buf, sx_buf, Xop_buf, l1_buf)
     return layers, bufs + (bufs_chain if chained else (None, None))
+
+
+def quantise(sq, L, X, sx_buf, Xop):
+    """The activation quantiser of one linear: fused with its LayerNorm when
+    the input comes from one, Smooth-Static or Smooth-Dynamic."""
+    static = 0.0 if L.static_scale is None else L.static_scale
+    if L.ln is not None:
+        sq.layernorm_quant(X, L.ln[0], L.ln[1], LN_EPS, L.s, static,
+                           out=(None, sx_buf, Xop, None, None))
+    elif L.static_scale is not None:
+        sq.quantize_act_static(X, L.s, L.static_scale, out=(None, sx_buf, Xop))
+    else:
+        sq.quantize_act(X, L.s, out=(None, sx_buf, Xop))
 
 
 def run_layer(sq, gemm, L, bufs, M, X=None, ev=None, ffn_chain="off"):
@@ -261,10 +296,7 @@ def run_layer(sq, gemm, L, bufs, M, X=None, ev=None, ffn_chain="off"):
         Xop = Xop_buf[: M * K].view(M, K)
         if ev is not None:
             ev[0].record()
-        if L.static_scale is not None:
-            sq.quantize_act_static(X, L.s, L.static_scale, out=(None, sx_buf, Xop))
-        else:
-            sq.quantize_act(X, L.s, out=(None, sx_buf, Xop))
+        quantise(sq, L, X, sx_buf, Xop)
         if ev is not None:
             ev[1].record()
         if ffn_chain == "fused":
@@ -283,10 +315,7 @@ def run_layer(sq, gemm, L, bufs, M, X=None, ev=None, ffn_chain="off"):
         Xop = Xop_buf[: M * K].view(M, K)
         if ev is not None:
             ev[0].record()
-        if L.static_scale is not None:
-            sq.quantize_act_static(X, L.s, L.static_scale, out=(None, sx_buf, Xop))
-        else:
-            sq.quantize_act(X, L.s, out=(None, sx_buf, Xop))
+        quantise(sq, L, X, sx_buf, Xop)
         if ev is not None:
             ev[1].record()
         # the packed weights' row L1 norms let the GEMM prove single-pass exactness
@@ -314,9 +343,11 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
     chained = args.ffn_chain != "off"
     if chained and args.gemm != "tc":
         raise SystemExit("--ffn-chain needs the tcgen05 GEMM (--gemm tc)")
+    if args.ln and args.gemm != "tc":
+        raise SystemExit("--ln needs the tcgen05 GEMM (--gemm tc)")
     layers, bufs = setup_workload(w, args.gemm, rank,
-                                  want_host=args.e2e_steps > 0 and not chained,
-                                  quant=args.quant, ffn_chain=args.ffn_chain)
+                                  want_host=args.e2e_steps > 0 and not chained and not args.ln,
+                                  quant=args.quant, ffn_chain=args.ffn_chain, ln=args.ln)
     M = w.M
     n_gemm = len(layers)
     quantised = [True] * n_gemm  # which linears run an activation quantiser kernel
@@ -388,7 +419,7 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
     # host memory, copied in, the linear block, Y copied out, inside the timed
     # region (three streams overlap copies with the kernels)
     e2e = None
-    if args.e2e_steps > 0 and not chained:
+    if args.e2e_steps > 0 and not chained and not args.ln:
         from smoothquant_w8a8_int8_gb300.pipeline import HostLinearPipeline, LinearLayer
         pipe = HostLinearPipeline(M, max(L.lin.K for L in layers), max(L.lin.N for L in layers))
         specs = [LinearLayer(L.s, L.Wop, L.sw, L.lin.mode, L.bias, L.residual, L.wl1,
@@ -450,7 +481,9 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
                                             "the Smooth-Static quantiser",
                                  "fused": "FFN-down consumes FFN-up's output: FFN-up's "
                                           "epilogue emits FFN-down's Smooth-Static codes "
-                                          "(sq_linear_i8_requant)"}[args.ffn_chain]},
+                                          "(sq_linear_i8_requant)"}[args.ffn_chain],
+                   "layernorm": ("the QKV and FFN-up inputs pass through LayerNorm fused with "
+                                 "their quantiser (sq_layernorm_quant)" if args.ln else "none")},
         "roofline": {"bound": "tensor", "kernel": "gemm+epilogue",
                      "achieved": round(gemm_tops, 2), "peak": peak_tensor,
                      "unit": "TFLOP/s", "frac": round(gemm_tops / peak_tensor, 4),
@@ -578,6 +611,9 @@ def main():
                     help="chain each layer's FFN-down to its FFN-up (Smooth-Static input): "
                          "through fp32 Y and the quantiser, or through the requantising "
                          "epilogue")
+    ap.add_argument("--ln", action="store_true",
+                    help="the QKV and FFN-up inputs are pre-LayerNorm hidden states: their "
+                         "quantiser is the fused LayerNorm + quantiser")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-step-seconds", type=float, default=2.0)

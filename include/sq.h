@@ -144,6 +144,24 @@ sq_status sq_quantize_act_static(const float *X, const float *s, int64_t M, int6
                                  float scale, int8_t *Xq, float *x_scale, void *Xop,
                                  int32_t *x_row_l1, void *stream);
 
+/* ---- LayerNorm with the next linear's quantiser fused in ------------------ */
+
+/* The encoder's LayerNorm (Table 3 lists it among BERT-large's operators),
+ * emitting the next linear's smoothed int8 codes directly, as SmoothQuant's
+ * folding of the smoothing factor into the normalisation implies:
+ *   y[m][j] = fma((H[m][j] - mean_m) * rstd_m, gamma[j], beta[j]),
+ *   mean_m = fl(sum_j H[m][j] / K), var_m = fl(sum_j (H[m][j] - mean_m)^2 / K)
+ *   (fp32 sums in a tree), rstd_m = RN(1 / sqrt(fl(var_m + eps))),
+ * then the codes of y exactly as sq_quantize_act (static_scale == 0: dynamic
+ * per-token scale) or sq_quantize_act_static (static_scale > 0, finite) would
+ * write them for X = y.  H fp32 [M][K]; gamma, beta fp32 [K] (16-byte
+ * aligned); eps >= 0; Y fp32 [M][K] (nullable): y itself; other outputs as
+ * sq_quantize_act.  K <= 8192 (SQ_ERR_UNSUPPORTED otherwise). */
+sq_status sq_layernorm_quant(const float *H, const float *gamma, const float *beta, float eps,
+                             const float *s, int64_t M, int64_t K, float static_scale, float *Y,
+                             int8_t *Xq, float *x_scale, void *Xop, int32_t *x_row_l1,
+                             void *stream);
+
 /* ---- INT8 GEMM + fused dequantising epilogue ------------------------------ */
 
 /* acc[m][n] = sum_k Xq[m][k] * Wq[n][k], exact in int32, then the epilogue

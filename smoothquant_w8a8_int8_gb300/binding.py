@@ -22,7 +22,8 @@ EPI_NONE, EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESIDUAL, EPI_RAW_I32 = range(5)
 
 EXPORTS = ("sq_status_string", "sq_version", "sq_operand_bytes", "sq_channel_absmax",
            "sq_smooth_factor", "sq_pack_weight", "sq_quantize_act", "sq_act_absmax",
-           "sq_quantize_act_static", "sq_linear_i8", "sq_linear_i8_requant",
+           "sq_quantize_act_static", "sq_layernorm_quant", "sq_linear_i8",
+           "sq_linear_i8_requant",
            "sq_linear_i8_mma_sync",
            "sq_check_division", "sq_device_status")
 
@@ -57,6 +58,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                 "sq_quantize_act": ([vp, vp, i64, i64, vp, vp, vp, vp, vp], i32),
                 "sq_act_absmax": ([vp, vp, i64, i64, vp, vp], i32),
                 "sq_quantize_act_static": ([vp, vp, i64, i64, f32, vp, vp, vp, vp, vp], i32),
+                "sq_layernorm_quant": ([vp, vp, vp, f32, vp, i64, i64, f32, vp, vp, vp, vp, vp,
+                                        vp], i32),
                 "sq_linear_i8": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp],
                                  i32),
                 "sq_linear_i8_requant": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp,
@@ -216,6 +219,31 @@ def quantize_act_static(X: torch.Tensor, s: torch.Tensor, scale: float, want_q: 
     if want_l1 or (out is not None and len(out) > 3):
         return Xq, sx, Xop, l1
     return Xq, sx, Xop
+
+
+def layernorm_quant(H: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float,
+                    s: torch.Tensor, static_scale: float = 0.0, want_y: bool = False,
+                    want_q: bool = True, want_op: bool = True, want_l1: bool = False, out=None,
+                    stream=None):
+    """LayerNorm of H with the next linear's quantiser fused in (dynamic when
+    static_scale is 0); returns (Xq or None, x_scale, Xop or None, Y or None,
+    l1 or None).  `out` may give those five (Xq, Xop, Y, l1 may be None)."""
+    _need(H, torch.float32, "H")
+    M, K = H.shape
+    for t, n in ((gamma, "gamma"), (beta, "beta"), (s, "s")):
+        _need(t, torch.float32, n, (K,))
+    if out is not None:
+        Xq, sx, Xop, Y, l1 = out
+    else:
+        Xq = torch.empty(M, K, dtype=torch.int8, device=H.device) if want_q else None
+        Xop = empty_operand(M, K, H.device) if want_op else None
+        sx = torch.empty(M, dtype=torch.float32, device=H.device)
+        Y = torch.empty(M, K, dtype=torch.float32, device=H.device) if want_y else None
+        l1 = torch.empty(M, dtype=torch.int32, device=H.device) if want_l1 else None
+    _check(load().sq_layernorm_quant(_p(H), _p(gamma), _p(beta), float(eps), _p(s), M, K,
+                                     float(static_scale), _p(Y), _p(Xq), _p(sx), _p(Xop),
+                                     _p(l1), _stream(stream)), "sq_layernorm_quant")
+    return Xq, sx, Xop, Y, l1
 
 
 def _out(Xa, Wa, mode, out):

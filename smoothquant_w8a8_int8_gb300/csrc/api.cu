@@ -172,6 +172,26 @@ sq_status sq_quantize_act_static(const float *X, const float *s, int64_t M, int6
                                 x_row_l1, scale, as_stream(stream));
 }
 
+sq_status sq_layernorm_quant(const float *H, const float *gamma, const float *beta, float eps,
+                             const float *s, int64_t M, int64_t K, float static_scale, float *Y,
+                             int8_t *Xq, float *x_scale, void *Xop, int32_t *x_row_l1,
+                             void *stream) {
+    if (!(eps >= 0.0f) || !(eps <= 3.4028234663852886e38f)) return SQ_ERR_INVALID_ARG;
+    if (!(static_scale >= 0.0f) || !(static_scale <= 3.4028234663852886e38f))
+        return SQ_ERR_INVALID_ARG;
+    sq_status rc = check_quant_args(H, s, M, K, Xq, x_scale, Xop);
+    if (rc != SQ_OK) return rc;
+    if (M == 0) return SQ_OK;
+    if (!gamma || !beta) return SQ_ERR_INVALID_ARG;
+    if (!aligned16(gamma) || !aligned16(beta) || (Y && !aligned16(Y)) ||
+        (x_row_l1 && !aligned4(x_row_l1)))
+        return SQ_ERR_ALIGNMENT;
+    if (K > 8192) return SQ_ERR_UNSUPPORTED;
+    if ((rc = require_sm103()) != SQ_OK) return rc;
+    return launch_layernorm_quant(H, gamma, beta, eps, s, M, K, static_scale, Y, Xq, x_scale,
+                                  static_cast<__nv_bfloat16 *>(Xop), x_row_l1, as_stream(stream));
+}
+
 sq_status sq_linear_i8(const void *Xop, const float *x_scale, const int32_t *x_row_l1,
                        const void *Wop, const float *w_scale, const int32_t *w_row_l1,
                        const float *bias, const float *residual, int64_t M, int64_t N, int64_t K,

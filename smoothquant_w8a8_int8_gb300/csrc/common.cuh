@@ -82,6 +82,10 @@ sq_status launch_quantize_rows(int direction, const float *A, const float *s, in
 sq_status launch_check_division(uint32_t b_first, uint32_t b_count, uint32_t a_first,
                                 uint32_t a_count, int corrected, unsigned long long *out,
                                 cudaStream_t st);
+sq_status launch_layernorm_quant(const float *H, const float *gamma, const float *beta,
+                                 float eps, const float *s, int64_t rows, int64_t K,
+                                 float static_scale, float *Y, int8_t *q, float *scale,
+                                 __nv_bfloat16 *op, int32_t *l1, cudaStream_t st);
 sq_status launch_act_absmax(const float *A, const float *s, int64_t rows, int64_t K,
                             float *amax, cudaStream_t st);
 sq_status launch_gemm_mma_sync(const int8_t *Xq, const float *sx, const int8_t *Wq,

@@ -281,6 +281,95 @@ int resident_blocks(Kern k) {
     return per_sm;
 }
 
+// LayerNorm with the next linear's quantiser fused in (the encoder's
+// normalisation, Table 3, emitting the smoothed int8 codes SmoothQuant's
+// folding implies).  A group of tpr threads owns a row, held in registers:
+//   mean = fl(sum / K), var = fl(sum (h - mean)^2 / K) (fp32 tree sums),
+//   y = fma((h - mean) * rstd, gamma, beta), rstd = RN(1 / sqrt(var + eps)),
+// then the quantiser of KIND on y: v = fl(y / s), per-token scale from the row
+// maximum (dynamic) or the given scale (static), codes as quantize_rows_reg.
+// y is also stored when Y is given.
+template <int KIND, int kVPT>
+__global__ void __launch_bounds__(kThreads) layernorm_quant_kernel(
+    const float *__restrict__ H, const float *__restrict__ gamma, const float *__restrict__ beta,
+    float eps, const float *__restrict__ s, int64_t rows, int K4, int tpr,
+    float *__restrict__ Y, int8_t *__restrict__ q, float *__restrict__ scale,
+    __nv_bfloat16 *__restrict__ op, int32_t *__restrict__ l1, float fixed_scale) {
+    __shared__ float red[kThreads / 32];
+    const int rpb = kThreads / tpr;
+    const int g = threadIdx.x / tpr;
+    const int t = threadIdx.x % tpr;
+    const float4 *s4 = reinterpret_cast<const float4 *>(s);
+    const float4 *g4 = reinterpret_cast<const float4 *>(gamma);
+    const float4 *b4 = reinterpret_cast<const float4 *>(beta);
+    const float Kf = (float)(4 * K4);
+    const int64_t tiles = (rows + rpb - 1) / rpb;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const int64_t row = tile * rpb + g;
+        const bool valid = row < rows;
+        const float4 *h4 = reinterpret_cast<const float4 *>(H) + (valid ? row : 0) * K4;
+        float4 v[kVPT];
+#pragma unroll
+        for (int i = 0; i < kVPT; ++i) {
+            const int j = t + i * tpr;
+            v[i] = (valid && j < K4) ? __ldcs(h4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float sum = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kVPT; ++i) sum += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+        const float mean = __fdiv_rn(group_sum(sum, tpr, red), Kf);
+        float sq = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kVPT; ++i) {
+            const int j = t + i * tpr;
+            if (j < K4) {
+                v[i] = make_float4(v[i].x - mean, v[i].y - mean, v[i].z - mean, v[i].w - mean);
+                sq += (v[i].x * v[i].x + v[i].y * v[i].y) + (v[i].z * v[i].z + v[i].w * v[i].w);
+            }
+        }
+        const float var = __fdiv_rn(group_sum(sq, tpr, red), Kf);
+        const float rstd = __frsqrt_rn(__fadd_rn(var, eps));
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kVPT; ++i) {
+            const int j = t + i * tpr;
+            if (j < K4) {
+                const float4 gv = __ldg(g4 + j), bv = __ldg(b4 + j), sv = __ldg(s4 + j);
+                float4 y;
+                y.x = __fmaf_rn(__fmul_rn(v[i].x, rstd), gv.x, bv.x);
+                y.y = __fmaf_rn(__fmul_rn(v[i].y, rstd), gv.y, bv.y);
+                y.z = __fmaf_rn(__fmul_rn(v[i].z, rstd), gv.z, bv.z);
+                y.w = __fmaf_rn(__fmul_rn(v[i].w, rstd), gv.w, bv.w);
+                if (Y && valid) reinterpret_cast<float4 *>(Y)[row * K4 + j] = y;
+                v[i] = make_float4(__fdiv_rn(y.x, sv.x), __fdiv_rn(y.y, sv.y),
+                                   __fdiv_rn(y.z, sv.z), __fdiv_rn(y.w, sv.w));
+                if (KIND == kActDynamic)
+                    m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)),
+                                       fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+            }
+        }
+        float sc = fixed_scale;
+        if (KIND == kActDynamic) {
+            m = group_max(m, tpr, red);
+            sc = m == 0.0f ? 1.0f : __fdiv_rn(m, 127.0f);
+        }
+        const float rsc = __frcp_rn(sc);
+        float a1 = 0.0f;
+        if (valid) {
+            if (t == 0) scale[row] = sc;
+#pragma unroll
+            for (int i = 0; i < kVPT; ++i) {
+                const int j = t + i * tpr;
+                if (j < K4) a1 += store_codes<KIND>(v[i], sc, rsc, row * K4 + j, q, op);
+            }
+        }
+        if (l1) {
+            a1 = group_sum(a1, tpr, red);
+            if (valid && t == 0) l1[row] = (int32_t)a1;
+        }
+    }
+}
+
 }  // namespace
 
 sq_status launch_quantize_rows(int direction, const float *A, const float *s, int64_t rows,
@@ -320,6 +409,37 @@ sq_status launch_quantize_rows(int direction, const float *A, const float *s, in
         const int64_t grid = std::min<int64_t>(rows, (int64_t)di.sms * 8);
         kern<<<(unsigned)grid, kThreads, 0, st>>>(A, s, rows, K4, q, scale, op, l1, fixed_scale);
     }
+    return cuda_status(cudaGetLastError());
+}
+
+sq_status launch_layernorm_quant(const float *H, const float *gamma, const float *beta,
+                                 float eps, const float *s, int64_t rows, int64_t K,
+                                 float static_scale, float *Y, int8_t *q, float *scale,
+                                 __nv_bfloat16 *op, int32_t *l1, cudaStream_t st) {
+    DeviceInfo di;
+    sq_status rc = device_info(&di);
+    if (rc != SQ_OK) return rc;
+    const int K4 = (int)(K / 4);
+    if (K4 > kThreads * kMaxVPT) return SQ_ERR_UNSUPPORTED;
+    const bool small = K4 <= kThreads * 4;
+    const int vpt = small ? 4 : 8;
+    int tpr = 32;
+    while (tpr * vpt < K4) tpr <<= 1;
+    const int rpb = kThreads / tpr;
+    const int64_t tiles = (rows + rpb - 1) / rpb;
+    using Kern = void (*)(const float *, const float *, const float *, float, const float *,
+                          int64_t, int, int, float *, int8_t *, float *, __nv_bfloat16 *,
+                          int32_t *, float);
+    static const Kern kerns[2][2] = {
+        {layernorm_quant_kernel<kActDynamic, 4>, layernorm_quant_kernel<kActDynamic, 8>},
+        {layernorm_quant_kernel<kActStatic, 4>, layernorm_quant_kernel<kActStatic, 8>}};
+    const Kern kern = kerns[static_scale > 0.0f ? 1 : 0][small ? 0 : 1];
+    static int per_sm[2][2] = {};
+    int &occ = per_sm[static_scale > 0.0f ? 1 : 0][small ? 0 : 1];
+    if (!occ) occ = resident_blocks(kern);
+    const int64_t grid = std::min<int64_t>(tiles, (int64_t)di.sms * occ);
+    kern<<<(unsigned)grid, kThreads, 0, st>>>(H, gamma, beta, eps, s, rows, K4, tpr, Y, q, scale,
+                                              op, l1, static_scale);
     return cuda_status(cudaGetLastError());
 }
 

@@ -143,3 +143,12 @@ def test_argument_checks_fail_before_any_launch(lib):
     assert lib.sq_check_division(0, 1, 0, 1, 1, None, None) == INVALID
     assert lib.sq_check_division(0, 1, 0, 1, 1, _fake(0x10004), None) == ALIGN
     assert lib.sq_check_division(0, 0, 0, 1, 1, None, None) == 0        # empty
+    # fused LayerNorm + quantiser
+    f = lib.sq_layernorm_quant
+    f.argtypes = [vp, vp, vp, ctypes.c_float, vp, i64, i64, ctypes.c_float] + [vp] * 6
+    assert f(a, a, a, -1.0, a, 4, 32, 0.0, None, a, a, None, None, None) == INVALID   # eps
+    assert f(a, a, a, 1e-5, a, 4, 32, -1.0, None, a, a, None, None, None) == INVALID  # scale
+    assert f(a, None, a, 1e-5, a, 4, 32, 0.0, None, a, a, None, None, None) == INVALID  # gamma
+    assert f(a, a, a, 1e-5, a, 4, 24, 0.0, None, a, a, None, None, None) == ALIGN     # K % 16
+    assert f(a, a, a, 1e-5, a, 4, 8208, 0.0, None, a, a, None, None, None) == UNSUP   # K > 8192
+    assert f(None, None, None, 1e-5, None, 0, 32, 0.0, None, None, None, None, None, None) == 0

@@ -618,3 +618,52 @@ def test_requant_feeds_next_linear(sq):
     y2f = sq.linear_i8(Xop2f, sx2f, Wop2, sw2, b2.cuda(), r2.cuda(), wl.EPI_BIAS_RESIDUAL)
     assert torch.equal(Xop2f, Xop2) and torch.equal(sx2f, sx2)
     assert torch.equal(y2f, y2)
+
+
+# ------------------------------------------------ LayerNorm + quantiser
+
+@pytest.mark.parametrize("M,K", [(7, 48), (300, 1024), (64, 4096), (5, 768), (130, 8192)])
+def test_layernorm_quant_parity(sq, M, K):
+    """The fused LayerNorm's fp32 output matches the oracle's LayerNorm within
+    the fp32 tolerance, and its codes, scales and L1 norms equal the oracle's
+    quantisers applied to that output bit for bit (dynamic and static)."""
+    rng = np.random.default_rng(M * 7 + K)
+    H = (rng.standard_normal((M, K)) * 3.0 + 0.5).astype(np.float32)
+    H[:, rng.integers(0, K, max(1, K // 100))] *= np.float32(20.0)  # outlier channels
+    gamma = (1.0 + 0.05 * rng.standard_normal(K)).astype(np.float32)
+    beta = (0.05 * rng.standard_normal(K)).astype(np.float32)
+    s = rng.uniform(0.3, 4.0, K).astype(np.float32)
+    eps = 1e-12
+    y_ref = oracle.layernorm(H, gamma, beta, eps)
+    Xq, sx, Xop, Y, l1 = sq.layernorm_quant(to_dev(H), to_dev(gamma), to_dev(beta), eps,
+                                            to_dev(s), want_y=True, want_l1=True)
+    y = Y.cpu().numpy()
+    assert_close_fp32(y, y_ref, "LayerNorm output")
+    q_ref, sx_ref = oracle.quantize_rows(y, s, "act")
+    assert_codes_equal(Xq.cpu().numpy(), q_ref, "Xq")
+    assert_codes_equal(op_as_int(Xop), q_ref, "Xop")
+    assert_bits_equal(sx.cpu().numpy(), sx_ref, "x_scale")
+    np.testing.assert_array_equal(l1.cpu().numpy(), np.abs(q_ref.astype(np.int64)).sum(axis=1))
+    # without the fp32 output: the same codes
+    _, sx2, Xop2, _, _ = sq.layernorm_quant(to_dev(H), to_dev(gamma), to_dev(beta), eps,
+                                            to_dev(s), want_q=False)
+    assert_codes_equal(op_as_int(Xop2), q_ref, "Xop (no Y)")
+    # static scale (a quarter of the calibrated one saturates)
+    scale = oracle.static_scale(oracle.act_absmax(y, s)) * np.float32(0.25)
+    Xq3, sx3, _, _, _ = sq.layernorm_quant(to_dev(H), to_dev(gamma), to_dev(beta), eps,
+                                           to_dev(s), static_scale=float(scale), want_op=False)
+    assert_codes_equal(Xq3.cpu().numpy(), oracle.quantize_static(y, s, scale), "static Xq")
+    assert np.all(sx3.cpu().numpy() == np.float32(scale))
+
+
+def test_layernorm_quant_constant_rows(sq):
+    """Rows with no spread normalise to beta exactly (zero deviation)."""
+    K = 256
+    H = np.full((3, K), 2.5, np.float32)
+    H[1] = -7.0
+    gamma = np.ones(K, np.float32)
+    beta = np.linspace(-1, 1, K).astype(np.float32)
+    s = np.ones(K, np.float32)
+    _, _, _, Y, _ = sq.layernorm_quant(to_dev(H), to_dev(gamma), to_dev(beta), 1e-5, to_dev(s),
+                                       want_y=True)
+    np.testing.assert_array_equal(Y.cpu().numpy(), np.tile(beta, (3, 1)))
