@@ -158,6 +158,11 @@ class Layer:
 LN_EPS = 1e-12
 
 
+def step_bytes(layers, M):
+    """Bytes one step's kernels touch: activations, packed weights, outputs."""
+    return sum(M * L.lin.K * 4 + L.lin.N * L.lin.K * 2 + 2 * M * L.lin.N * 4 for L in layers)
+
+
 def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
                    quant: str = "dynamic", ffn_chain: str = "off", ln: bool = False):
     from smoothquant_w8a8_int8_gb300 import binding as sq
@@ -273,7 +278,20 @@ def quantise(sq, L, X, sx_buf, Xop):
         sq.quantize_act(X, L.s, out=(None, sx_buf, Xop))
 
 
-def run_layer(sq, gemm, L, bufs, M, X=None, ev=None, ffn_chain="off"):
+def linear(sq, ws, *a, **k):
+    """The tcgen05 linear: split-K schedule on workspace `ws`, or whole tiles."""
+    if ws is None:
+        return sq.linear_i8(*a, **k)
+    return sq.linear_i8_ws(*a, workspace=ws, **k)
+
+
+def linear_requant(sq, ws, *a, **k):
+    if ws is None:
+        return sq.linear_i8_requant(*a, **k)
+    return sq.linear_i8_requant_ws(*a, workspace=ws, **k)
+
+
+def run_layer(sq, gemm, L, bufs, M, X=None, ev=None, ffn_chain="off", ws=None):
     """One linear of the step.  Returns whether an activation quantiser ran."""
     Xq_buf, sx_buf, Xop_buf, l1_buf, Xop_chain, sx_chain = bufs
     K, N = L.lin.K, L.lin.N
@@ -288,8 +306,8 @@ def run_layer(sq, gemm, L, bufs, M, X=None, ev=None, ffn_chain="off"):
                                        out=(None, sx_chain, Xop_chain[: M * K].view(M, K)))
             if ev is not None:
                 ev[1].record()
-            sq.linear_i8(Xop_chain[: M * K].view(M, K), sx_chain, L.Wop, L.sw, L.bias,
-                         L.residual, L.lin.mode, out=L.Y, w_l1=L.wl1)
+            linear(sq, ws, Xop_chain[: M * K].view(M, K), sx_chain, L.Wop, L.sw, L.bias,
+                   L.residual, L.lin.mode, out=L.Y, w_l1=L.wl1)
             if ev is not None:
                 ev[2].record()
             return ffn_chain == "unfused"
@@ -301,13 +319,12 @@ def run_layer(sq, gemm, L, bufs, M, X=None, ev=None, ffn_chain="off"):
             ev[1].record()
         if ffn_chain == "fused":
             nxt = L.feeds
-            sq.linear_i8_requant(Xop, sx_buf, L.Wop, L.sw, L.bias, L.residual, L.lin.mode,
-                                 nxt.s, nxt.static_scale,
-                                 out=(None, Xop_chain[: M * N].view(M, N), sx_chain),
-                                 w_l1=L.wl1)
+            linear_requant(sq, ws, Xop, sx_buf, L.Wop, L.sw, L.bias, L.residual, L.lin.mode,
+                           nxt.s, nxt.static_scale,
+                           out=(None, Xop_chain[: M * N].view(M, N), sx_chain), w_l1=L.wl1)
         else:
-            sq.linear_i8(Xop, sx_buf, L.Wop, L.sw, L.bias, L.residual, L.lin.mode, out=L.Y,
-                         w_l1=L.wl1)
+            linear(sq, ws, Xop, sx_buf, L.Wop, L.sw, L.bias, L.residual, L.lin.mode, out=L.Y,
+                   w_l1=L.wl1)
         if ev is not None:
             ev[2].record()
         return True
@@ -319,8 +336,8 @@ def run_layer(sq, gemm, L, bufs, M, X=None, ev=None, ffn_chain="off"):
         if ev is not None:
             ev[1].record()
         # the packed weights' row L1 norms let the GEMM prove single-pass exactness
-        sq.linear_i8(Xop, sx_buf, L.Wop, L.sw, L.bias, L.residual, L.lin.mode, out=L.Y,
-                     w_l1=L.wl1)
+        linear(sq, ws, Xop, sx_buf, L.Wop, L.sw, L.bias, L.residual, L.lin.mode, out=L.Y,
+               w_l1=L.wl1)
         if ev is not None:
             ev[2].record()
     else:
@@ -351,12 +368,17 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
     M = w.M
     n_gemm = len(layers)
     quantised = [True] * n_gemm  # which linears run an activation quantiser kernel
+    # one split-K workspace, sized for the largest linear, allocated once
+    ws = None
+    if args.gemm == "tc" and args.schedule == "split-k":
+        ws_bytes = max(sq.linear_workspace_bytes(M, lin.N, lin.K) for lin in w.linears)
+        ws = sq.empty_workspace(ws_bytes) if ws_bytes > 0 else None
 
     def step(ev_list=None):
         for i, L in enumerate(layers):
             quantised[i] = run_layer(sq, args.gemm, L, bufs, M,
                                      ev=None if ev_list is None else ev_list[i],
-                                     ffn_chain=args.ffn_chain)
+                                     ffn_chain=args.ffn_chain, ws=ws)
 
     for _ in range(args.warmup):
         step()
@@ -368,6 +390,15 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
     # per-launch events for every kernel in the timed region
     evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_gemm)]
            for _ in range(args.steps)]
+    # a step whose data fits in L2 would run from L2 when repeated: then every
+    # timed step is preceded by a write of a buffer twice the L2 size, outside
+    # its events, and the step times are summed
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = None
+    if step_bytes(layers, M) < 2 * l2:
+        flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device="cuda")
+        step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
     clocks = ClockSampler(torch.cuda.current_device())
     if world > 1:
         torch.distributed.barrier()
@@ -378,7 +409,12 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
     host_t0 = datetime.datetime.now()
     t0.record()
     for k in range(args.steps):
+        if flush is not None:
+            flush.fill_(float(k))
+            step_ev[k][0].record()
         step(evs[k])
+        if flush is not None:
+            step_ev[k][1].record()
     t1.record()
     torch.cuda.synchronize()
     host_t1 = datetime.datetime.now()
@@ -386,6 +422,8 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
         torch.distributed.barrier()
     clock_info = clocks.stop((host_t0, host_t1))
     elapsed_ms = t0.elapsed_time(t1)
+    if flush is not None:
+        elapsed_ms = sum(a.elapsed_time(b) for a, b in step_ev)
     rc = sq.device_status()
     if rc != 0:
         raise RuntimeError(f"device status after timed run: {sq.status_string(rc)}")
@@ -468,8 +506,17 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
         "config": {"workload": w.name, "description": w.description, "M": M,
                    "layers": w.layers, "gemms_per_step": n_gemm,
                    "ops_per_step": ops_per_step, "gemm_kernel": gemm_kernel,
-                   "l2": "inputs larger than L2: every GEMM reads its own activations "
-                         f"({sum(M * L.lin.K * 4 for L in layers) / 1e9:.1f} GB per step)",
+                   "gemm_schedule": ("split K: linears with fewer tiles than SMs and "
+                                     "K >= 2048 cut each tile's K range over up to 4 SMs "
+                                     "(sq_linear_i8_ws workspace)"
+                                     if ws is not None else
+                                     "whole tiles (halves when the last wave is short)"),
+                   "l2": ("inputs larger than L2: every GEMM reads its own activations "
+                          f"({sum(M * L.lin.K * 4 for L in layers) / 1e9:.1f} GB per step)"
+                          if flush is None else
+                          f"L2 flushed before every step (a {2 * l2 / 1e6:.0f} MB buffer "
+                          f"written outside the step's events; the step touches "
+                          f"{step_bytes(layers, M) / 1e6:.0f} MB)"),
                    "weights": "packed once before the timed region",
                    "quantisation": ("Smooth-Static (per-tensor scale calibrated offline on a "
                                     "separate 512-token batch of the same distribution)"
@@ -611,6 +658,9 @@ def main():
                     help="chain each layer's FFN-down to its FFN-up (Smooth-Static input): "
                          "through fp32 Y and the quantiser, or through the requantising "
                          "epilogue")
+    ap.add_argument("--schedule", choices=["split-k", "whole"], default="split-k",
+                    help="tcgen05 GEMM: split K over several SMs where the tiles are fewer "
+                         "than the SMs and K >= 2048 (workspace), or whole tiles only")
     ap.add_argument("--ln", action="store_true",
                     help="the QKV and FFN-up inputs are pre-LayerNorm hidden states: their "
                          "quantiser is the fused LayerNorm + quantiser")

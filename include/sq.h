@@ -204,6 +204,46 @@ sq_status sq_linear_i8_requant(const void *Xop, const float *x_scale, const int3
                                int64_t K, int mode, const float *s_next, float scale, int8_t *Yq,
                                void *Yop, float *x_scale_next, void *stream);
 
+/* ---- Split K over several SMs (caller workspace) ---------------------------- */
+
+/* An output of fewer 128 x 256 tiles than the GPU has SMs keeps most SMs idle
+ * while each busy SM runs the whole K.  With a workspace, sq_linear_i8_ws /
+ * sq_linear_i8_requant_ws cut each tile's K range into min(4, SMs / tiles)
+ * equal pieces when K >= 2048, one per SM: each SM sums its piece exactly
+ * (int32), all but the last SM to finish a tile write their partial sums to
+ * the workspace, and that last SM adds them and runs the epilogue.  Integer
+ * addition is exact and order-free, so the outputs are bit for bit those of
+ * sq_linear_i8 / sq_linear_i8_requant.  Other shapes run the whole-tile
+ * schedule (their workspace size is 0): measured on GB300, the partial sums'
+ * round trip costs more than a split saves there.
+ *
+ * sq_linear_workspace_bytes: *bytes = the workspace an M x N x K launch needs
+ * on the current device (0 when it is not split; at most SMs x (256 KB + 64
+ * bytes), 38 MiB on 152 SMs).  A workspace sized for the largest of several
+ * shapes serves them all.
+ * Workspace rules: device memory, 16-byte aligned, zero-filled once before its
+ * first use (cudaMemset); every launch that completes leaves its counters at
+ * zero again, so it is reused as it is (the partial slots need no clearing).
+ * A workspace serves one launch at a time: launches that share it
+ * must be ordered (one stream, or events), or they race on its counters.  After
+ * sq_device_status has reported SQ_ERR_TIMEOUT, zero-fill it again.  NULL
+ * workspace: the whole-tile schedule of sq_linear_i8.  workspace_bytes below
+ * the requirement: SQ_ERR_INVALID_ARG.  Other arguments, limits and statuses
+ * as sq_linear_i8 / sq_linear_i8_requant. */
+sq_status sq_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes);
+sq_status sq_linear_i8_ws(const void *Xop, const float *x_scale, const int32_t *x_row_l1,
+                          const void *Wop, const float *w_scale, const int32_t *w_row_l1,
+                          const float *bias, const float *residual, int64_t M, int64_t N,
+                          int64_t K, int mode, void *Y, void *workspace, size_t workspace_bytes,
+                          void *stream);
+sq_status sq_linear_i8_requant_ws(const void *Xop, const float *x_scale,
+                                  const int32_t *x_row_l1, const void *Wop, const float *w_scale,
+                                  const int32_t *w_row_l1, const float *bias,
+                                  const float *residual, int64_t M, int64_t N, int64_t K,
+                                  int mode, const float *s_next, float scale, int8_t *Yq,
+                                  void *Yop, float *x_scale_next, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
 /* The same GEMM + epilogue on the legacy warp-level integer MMA path
  * (mma.sync m16n8k32 s8 x s8 -> s32), reading int8 codes directly:
  * Xq int8 [M][K] and Wq int8 [N][K] from sq_quantize_act / sq_pack_weight.

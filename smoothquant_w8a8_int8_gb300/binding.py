@@ -23,8 +23,8 @@ EPI_NONE, EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESIDUAL, EPI_RAW_I32 = range(5)
 EXPORTS = ("sq_status_string", "sq_version", "sq_operand_bytes", "sq_channel_absmax",
            "sq_smooth_factor", "sq_pack_weight", "sq_quantize_act", "sq_act_absmax",
            "sq_quantize_act_static", "sq_layernorm_quant", "sq_linear_i8",
-           "sq_linear_i8_requant",
-           "sq_linear_i8_mma_sync",
+           "sq_linear_i8_requant", "sq_linear_workspace_bytes", "sq_linear_i8_ws",
+           "sq_linear_i8_requant_ws", "sq_linear_i8_mma_sync",
            "sq_check_division", "sq_device_status")
 
 _lock = threading.Lock()
@@ -64,6 +64,11 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                  i32),
                 "sq_linear_i8_requant": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp,
                                           f32, vp, vp, vp, vp], i32),
+                "sq_linear_workspace_bytes": ([i64, i64, i64, vp], i32),
+                "sq_linear_i8_ws": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp,
+                                     ctypes.c_size_t, vp], i32),
+                "sq_linear_i8_requant_ws": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32,
+                                             vp, f32, vp, vp, vp, vp, ctypes.c_size_t, vp], i32),
                 "sq_linear_i8_mma_sync": ([vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp], i32),
                 "sq_check_division": ([ctypes.c_uint32] * 4 + [i32, vp, vp], i32),
                 "sq_device_status": ([vp], i32),
@@ -294,6 +299,66 @@ def linear_i8_requant(Xop, x_scale, Wop, w_scale, bias, residual, mode, s_next, 
                                        _p(w_l1), _p(bias), _p(residual), M, N, K, int(mode),
                                        _p(s_next), float(scale), _p(Yq), _p(Yop), _p(xs),
                                        _stream(stream)), "sq_linear_i8_requant")
+    return Yq, Yop, xs
+
+
+def linear_workspace_bytes(M: int, N: int, K: int) -> int:
+    """Bytes of the split-K workspace of an M x N x K linear (0: none needed)."""
+    n = ctypes.c_size_t(0)
+    _check(load().sq_linear_workspace_bytes(M, N, K, ctypes.byref(n)), "sq_linear_workspace_bytes")
+    return int(n.value)
+
+
+def empty_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A zero-filled split-K workspace (uint8).  Completed launches leave its
+    counters at zero, so it is reused as it is."""
+    return torch.zeros(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+def _workspace(ws):
+    if ws is None:
+        return None, 0
+    _need(ws, torch.uint8, "workspace")
+    return _p(ws), ws.numel()
+
+
+def linear_i8_ws(Xop, x_scale, Wop, w_scale, bias=None, residual=None, mode=EPI_BIAS, out=None,
+                 x_l1=None, w_l1=None, workspace=None, stream=None):
+    """linear_i8 with the split-K schedule on `workspace` (see
+    linear_workspace_bytes / empty_workspace); bit for bit the same output."""
+    _need(Xop, torch.bfloat16, "Xop")
+    _need(Wop, torch.bfloat16, "Wop")
+    M, N, K, out = _out(Xop, Wop, mode, out)
+    wp, wn = _workspace(workspace)
+    _check(load().sq_linear_i8_ws(_p(Xop), _p(x_scale), _p(x_l1), _p(Wop), _p(w_scale), _p(w_l1),
+                                  _p(bias), _p(residual), M, N, K, int(mode), _p(out), wp, wn,
+                                  _stream(stream)), "sq_linear_i8_ws")
+    return out
+
+
+def linear_i8_requant_ws(Xop, x_scale, Wop, w_scale, bias, residual, mode, s_next,
+                         scale: float, want_q: bool = False, want_op: bool = True,
+                         want_x_scale: bool = True, out=None, x_l1=None, w_l1=None,
+                         workspace=None, stream=None):
+    """linear_i8_requant with the split-K schedule on `workspace`."""
+    _need(Xop, torch.bfloat16, "Xop")
+    _need(Wop, torch.bfloat16, "Wop")
+    M, K = Xop.shape
+    N = Wop.shape[0]
+    if Wop.shape[1] != K:
+        raise ValueError("operand K mismatch")
+    _need(s_next, torch.float32, "s_next", (N,))
+    if out is not None:
+        Yq, Yop, xs = out
+    else:
+        Yq = torch.empty(M, N, dtype=torch.int8, device=Xop.device) if want_q else None
+        Yop = empty_operand(M, N, Xop.device) if want_op else None
+        xs = torch.empty(M, dtype=torch.float32, device=Xop.device) if want_x_scale else None
+    wp, wn = _workspace(workspace)
+    _check(load().sq_linear_i8_requant_ws(_p(Xop), _p(x_scale), _p(x_l1), _p(Wop), _p(w_scale),
+                                          _p(w_l1), _p(bias), _p(residual), M, N, K, int(mode),
+                                          _p(s_next), float(scale), _p(Yq), _p(Yop), _p(xs), wp,
+                                          wn, _stream(stream)), "sq_linear_i8_requant_ws")
     return Yq, Yop, xs
 
 

@@ -81,6 +81,57 @@ sq_status check_quant_args(const float *A, const float *s, int64_t rows, int64_t
     return SQ_OK;
 }
 
+sq_status linear_impl(const void *Xop, const float *x_scale, const int32_t *x_row_l1,
+                      const void *Wop, const float *w_scale, const int32_t *w_row_l1,
+                      const float *bias, const float *residual, int64_t M, int64_t N, int64_t K,
+                      int mode, void *Y, void *workspace, size_t workspace_bytes, void *stream) {
+    sq_status rc = check_linear_args(Xop, x_scale, Wop, w_scale, bias, residual, M, N, K, mode, Y);
+    if (rc != SQ_OK) return rc;
+    if (M == 0 || N == 0) return SQ_OK;
+    if ((x_row_l1 && !aligned4(x_row_l1)) || (w_row_l1 && !aligned4(w_row_l1)))
+        return SQ_ERR_ALIGNMENT;
+    if (workspace && !aligned16(workspace)) return SQ_ERR_ALIGNMENT;
+    if ((rc = require_sm103()) != SQ_OK) return rc;
+    return launch_gemm_tc(static_cast<const __nv_bfloat16 *>(Xop), x_scale, x_row_l1,
+                          static_cast<const __nv_bfloat16 *>(Wop), w_scale, w_row_l1, bias,
+                          residual, M, N, K, mode, Y, nullptr, workspace, workspace_bytes,
+                          as_stream(stream));
+}
+
+sq_status requant_impl(const void *Xop, const float *x_scale, const int32_t *x_row_l1,
+                       const void *Wop, const float *w_scale, const int32_t *w_row_l1,
+                       const float *bias, const float *residual, int64_t M, int64_t N, int64_t K,
+                       int mode, const float *s_next, float scale, int8_t *Yq, void *Yop,
+                       float *x_scale_next, void *workspace, size_t workspace_bytes,
+                       void *stream) {
+    if (mode == SQ_EPI_RAW_I32) return SQ_ERR_INVALID_ARG;
+    if (!(scale > 0.0f) || !(scale <= 3.4028234663852886e38f)) return SQ_ERR_INVALID_ARG;
+    const void *out = Yop ? Yop : static_cast<const void *>(Yq);
+    sq_status rc = check_linear_args(Xop, x_scale, Wop, w_scale, bias, residual, M, N, K, mode,
+                                     out);
+    if (rc != SQ_OK) return rc;
+    if (M == 0 || N == 0) return SQ_OK;
+    if (!s_next || (!Yq && !Yop)) return SQ_ERR_INVALID_ARG;
+    if (!aligned4(s_next) || (x_scale_next && !aligned4(x_scale_next)) ||
+        (Yop && (reinterpret_cast<uintptr_t>(Yop) & 1u)))
+        return SQ_ERR_ALIGNMENT;
+    if ((x_row_l1 && !aligned4(x_row_l1)) || (w_row_l1 && !aligned4(w_row_l1)))
+        return SQ_ERR_ALIGNMENT;
+    if (workspace && !aligned16(workspace)) return SQ_ERR_ALIGNMENT;
+    if ((rc = require_sm103()) != SQ_OK) return rc;
+    RequantOut rq;
+    rq.s_next = s_next;
+    rq.scale = scale;
+    rq.rscale = 1.0f / scale;  // IEEE division: the correctly rounded reciprocal
+    rq.Yq = Yq;
+    rq.Yop = static_cast<__nv_bfloat16 *>(Yop);
+    rq.x_scale = x_scale_next;
+    return launch_gemm_tc(static_cast<const __nv_bfloat16 *>(Xop), x_scale, x_row_l1,
+                          static_cast<const __nv_bfloat16 *>(Wop), w_scale, w_row_l1, bias,
+                          residual, M, N, K, mode, nullptr, &rq, workspace, workspace_bytes,
+                          as_stream(stream));
+}
+
 }  // namespace
 
 extern "C" {
@@ -196,15 +247,26 @@ sq_status sq_linear_i8(const void *Xop, const float *x_scale, const int32_t *x_r
                        const void *Wop, const float *w_scale, const int32_t *w_row_l1,
                        const float *bias, const float *residual, int64_t M, int64_t N, int64_t K,
                        int mode, void *Y, void *stream) {
-    sq_status rc = check_linear_args(Xop, x_scale, Wop, w_scale, bias, residual, M, N, K, mode, Y);
-    if (rc != SQ_OK) return rc;
+    return linear_impl(Xop, x_scale, x_row_l1, Wop, w_scale, w_row_l1, bias, residual, M, N, K,
+                       mode, Y, nullptr, 0, stream);
+}
+
+sq_status sq_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes) {
+    if (!bytes) return SQ_ERR_INVALID_ARG;
+    *bytes = 0;
+    if (M < 0 || N < 0 || K <= 0) return SQ_ERR_INVALID_ARG;
+    if (K > kMaxK) return SQ_ERR_UNSUPPORTED;
     if (M == 0 || N == 0) return SQ_OK;
-    if ((x_row_l1 && !aligned4(x_row_l1)) || (w_row_l1 && !aligned4(w_row_l1)))
-        return SQ_ERR_ALIGNMENT;
-    if ((rc = require_sm103()) != SQ_OK) return rc;
-    return launch_gemm_tc(static_cast<const __nv_bfloat16 *>(Xop), x_scale, x_row_l1,
-                          static_cast<const __nv_bfloat16 *>(Wop), w_scale, w_row_l1, bias,
-                          residual, M, N, K, mode, Y, nullptr, as_stream(stream));
+    return gemm_tc_workspace_bytes(M, N, K, bytes);
+}
+
+sq_status sq_linear_i8_ws(const void *Xop, const float *x_scale, const int32_t *x_row_l1,
+                          const void *Wop, const float *w_scale, const int32_t *w_row_l1,
+                          const float *bias, const float *residual, int64_t M, int64_t N,
+                          int64_t K, int mode, void *Y, void *workspace, size_t workspace_bytes,
+                          void *stream) {
+    return linear_impl(Xop, x_scale, x_row_l1, Wop, w_scale, w_row_l1, bias, residual, M, N, K,
+                       mode, Y, workspace, workspace_bytes, stream);
 }
 
 sq_status sq_linear_i8_requant(const void *Xop, const float *x_scale, const int32_t *x_row_l1,
@@ -212,30 +274,20 @@ sq_status sq_linear_i8_requant(const void *Xop, const float *x_scale, const int3
                                const float *bias, const float *residual, int64_t M, int64_t N,
                                int64_t K, int mode, const float *s_next, float scale, int8_t *Yq,
                                void *Yop, float *x_scale_next, void *stream) {
-    if (mode == SQ_EPI_RAW_I32) return SQ_ERR_INVALID_ARG;
-    if (!(scale > 0.0f) || !(scale <= 3.4028234663852886e38f)) return SQ_ERR_INVALID_ARG;
-    const void *out = Yop ? Yop : static_cast<const void *>(Yq);
-    sq_status rc = check_linear_args(Xop, x_scale, Wop, w_scale, bias, residual, M, N, K, mode,
-                                     out);
-    if (rc != SQ_OK) return rc;
-    if (M == 0 || N == 0) return SQ_OK;
-    if (!s_next || (!Yq && !Yop)) return SQ_ERR_INVALID_ARG;
-    if (!aligned4(s_next) || (x_scale_next && !aligned4(x_scale_next)) ||
-        (Yop && (reinterpret_cast<uintptr_t>(Yop) & 1u)))
-        return SQ_ERR_ALIGNMENT;
-    if ((x_row_l1 && !aligned4(x_row_l1)) || (w_row_l1 && !aligned4(w_row_l1)))
-        return SQ_ERR_ALIGNMENT;
-    if ((rc = require_sm103()) != SQ_OK) return rc;
-    RequantOut rq;
-    rq.s_next = s_next;
-    rq.scale = scale;
-    rq.rscale = 1.0f / scale;  // IEEE division: the correctly rounded reciprocal
-    rq.Yq = Yq;
-    rq.Yop = static_cast<__nv_bfloat16 *>(Yop);
-    rq.x_scale = x_scale_next;
-    return launch_gemm_tc(static_cast<const __nv_bfloat16 *>(Xop), x_scale, x_row_l1,
-                          static_cast<const __nv_bfloat16 *>(Wop), w_scale, w_row_l1, bias,
-                          residual, M, N, K, mode, nullptr, &rq, as_stream(stream));
+    return requant_impl(Xop, x_scale, x_row_l1, Wop, w_scale, w_row_l1, bias, residual, M, N, K,
+                        mode, s_next, scale, Yq, Yop, x_scale_next, nullptr, 0, stream);
+}
+
+sq_status sq_linear_i8_requant_ws(const void *Xop, const float *x_scale,
+                                  const int32_t *x_row_l1, const void *Wop, const float *w_scale,
+                                  const int32_t *w_row_l1, const float *bias,
+                                  const float *residual, int64_t M, int64_t N, int64_t K,
+                                  int mode, const float *s_next, float scale, int8_t *Yq,
+                                  void *Yop, float *x_scale_next, void *workspace,
+                                  size_t workspace_bytes, void *stream) {
+    return requant_impl(Xop, x_scale, x_row_l1, Wop, w_scale, w_row_l1, bias, residual, M, N, K,
+                        mode, s_next, scale, Yq, Yop, x_scale_next, workspace, workspace_bytes,
+                        stream);
 }
 
 sq_status sq_linear_i8_mma_sync(const int8_t *Xq, const float *x_scale, const int8_t *Wq,

@@ -97,7 +97,10 @@ sq_status launch_gemm_mma_sync(const int8_t *Xq, const float *sx, const int8_t *
 sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_t *x_l1,
                          const __nv_bfloat16 *Wop, const float *sw, const int32_t *w_l1,
                          const float *bias, const float *residual, int64_t M, int64_t N,
-                         int64_t K, int mode, void *Y, const RequantOut *rq, cudaStream_t st);
+                         int64_t K, int mode, void *Y, const RequantOut *rq, void *workspace,
+                         size_t workspace_bytes, cudaStream_t st);
+// Bytes of the split-K workspace of an M x N x K launch on the current device (0: none used).
+sq_status gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes);
 // Reads and clears the tcgen05 GEMM's device error word (synchronous).
 sq_status gemm_tc_take_error(cudaStream_t st);
 

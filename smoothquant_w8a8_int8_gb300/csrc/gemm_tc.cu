@@ -249,46 +249,153 @@ __device__ __forceinline__ void tmem_wait_st() {
 
 // ------------------------------------------------------------------ kernel
 
-// Work items of a launch.  The BM x BN tiles that fill whole waves of the
-// persistent grid are items as they are; when the last, partial wave holds at
+// Work units of a launch.  Two schedules:
+//
+// Whole tiles (no workspace).  The BM x BN tiles that fill whole waves of the
+// persistent grid are units as they are; when the last, partial wave holds at
 // most half a wave of tiles, each of them is cut into two 128-column halves
 // (MMA N = 128), so that the last round takes half as long.  (Quarters, N = 64,
 // measured slower: the A tile is loaded in full for a quarter of the work.)
+//
+// Split K (a workspace is given).  The K blocks of the last sk_tiles tiles
+// form one range, cut evenly over sk_ctas CTAs (a CTA's share may cover the
+// end of one tile and the start of the next).  A piece of a tile (a K-block
+// range of it) leaves its exact int32 partial sums in the workspace; the CTA
+// whose piece of the tile completes last adds the others' partials to its own
+// and runs the epilogue.  Measured on GB300, the partials' round trip through
+// L2 (about 4 us on the finishing CTA's path) costs more than a split saves
+// unless the tiles are fewer than the SMs and long in K, so the split is used
+// only there: every tile cut into `pieces` <= 4 equal K ranges of at least
+// 1024, one per CTA (small M with a large K: a few tiles would otherwise keep
+// a few SMs busy for the whole K).
+//
 // Tiles are numbered m-fastest, so CTAs working at the same time share B tiles
 // in L2.
+constexpr int kMinSplitKb = 32;  // split K only for K >= 2048 (32 blocks of 64)
+constexpr int kMaxPieces = 4;
+
 struct Schedule {
-    int m_tiles, full_items, sub, items;
+    int m_tiles, nkb;
+    int full_items, sub, items;      // whole-tile schedule (halves in the last wave)
+    int dp_tiles, sk_tiles, sk_ctas;  // split-K part; sk_tiles == 0: not used
+    int sk_cnt_tiles;                 // tiles the counter block has room for (2 x grid)
 };
 
-__host__ __device__ inline Schedule make_schedule(int m_tiles, int n_tiles, int grid) {
+__host__ __device__ inline Schedule make_schedule(int m_tiles, int n_tiles, int nkb, int grid,
+                                                  bool split_k) {
     Schedule sc;
     sc.m_tiles = m_tiles;
+    sc.nkb = nkb;
     const int tiles = m_tiles * n_tiles;
     const int waves = tiles / grid, rem = tiles - waves * grid;
     sc.sub = (waves >= 1 && rem > 0 && 2 * rem <= grid) ? 2 : 1;
     sc.full_items = sc.sub == 1 ? tiles : waves * grid;
     sc.items = sc.full_items + (tiles - sc.full_items) * sc.sub;
+    sc.dp_tiles = tiles;
+    sc.sk_tiles = 0;
+    sc.sk_ctas = 0;
+    sc.sk_cnt_tiles = 0;
+    if (split_k && waves == 0 && nkb >= kMinSplitKb) {
+        // fewer tiles than SMs and a long K: cut every tile into `pieces`
+        // equal K ranges, one per CTA
+        int pieces = grid / tiles;
+        if (pieces > kMaxPieces) pieces = kMaxPieces;
+        if (pieces >= 2) {
+            sc.sub = 1;
+            sc.sk_tiles = tiles;
+            sc.dp_tiles = 0;
+            sc.sk_ctas = tiles * pieces;
+            sc.sk_cnt_tiles = grid;  // >= tiles
+            sc.full_items = sc.items = 0;
+        }
+    }
     return sc;
 }
 
-struct Item {
+// First K-block index (over the split tiles' concatenated K blocks) of CTA c's share.
+__host__ __device__ inline long long sk_start(const Schedule &sc, int c) {
+    return (long long)c * ((long long)sc.sk_tiles * sc.nkb) / sc.sk_ctas;
+}
+
+// The CTA whose share holds K-block index `it`: the largest c with sk_start(c) <= it.
+__host__ __device__ inline int sk_cta_of(const Schedule &sc, long long it) {
+    const long long total = (long long)sc.sk_tiles * sc.nkb;
+    long long c = (it * sc.sk_ctas + sc.sk_ctas - 1) / total;
+    if (c > sc.sk_ctas - 1) c = sc.sk_ctas - 1;
+    if (sk_start(sc, (int)c) > it) --c;
+    return (int)c;
+}
+
+struct Work {
     int m0, n0, bn;
+    int kb0, kb1;  // K blocks [kb0, kb1) of the tile
+    int skt;       // split tile index of a piece, -1 for a whole tile
 };
 
-__device__ __forceinline__ Item item_at(const Schedule &sc, int i) {
-    Item it;
-    if (i < sc.full_items) {
-        it.m0 = (i % sc.m_tiles) * BM;
-        it.n0 = (i / sc.m_tiles) * BN;
-        it.bn = BN;
-    } else {
-        const int j = i - sc.full_items;
-        const int t = sc.full_items + j / sc.sub;
-        it.bn = BN / sc.sub;
-        it.m0 = (t % sc.m_tiles) * BM;
-        it.n0 = (t / sc.m_tiles) * BN + (j % sc.sub) * it.bn;
+// Walks one CTA's units: its whole-tile items, then the pieces of its share
+// (K-block indices fit in 32 bits: at most 2 x grid tiles of 2081 blocks).
+struct Cursor {
+    int i, it, end;
+};
+
+__device__ __forceinline__ void cursor_init(const Schedule &sc, Cursor &cu) {
+    cu.i = blockIdx.x;
+    cu.it = cu.end = 0;
+    if (sc.sk_tiles > 0 && (int)blockIdx.x < sc.sk_ctas) {
+        cu.it = (int)sk_start(sc, blockIdx.x);
+        cu.end = (int)sk_start(sc, blockIdx.x + 1);
     }
-    return it;
+}
+
+__device__ __forceinline__ bool next_work(const Schedule &sc, Cursor &cu, Work &w) {
+    if (cu.i < sc.items) {
+        const int i = cu.i;
+        cu.i += gridDim.x;
+        w.kb0 = 0;
+        w.kb1 = sc.nkb;
+        w.skt = -1;
+        if (i < sc.full_items) {
+            w.m0 = (i % sc.m_tiles) * BM;
+            w.n0 = (i / sc.m_tiles) * BN;
+            w.bn = BN;
+        } else {
+            const int j = i - sc.full_items;
+            const int t = sc.full_items + j / sc.sub;
+            w.bn = BN / sc.sub;
+            w.m0 = (t % sc.m_tiles) * BM;
+            w.n0 = (t / sc.m_tiles) * BN + (j % sc.sub) * w.bn;
+        }
+        return true;
+    }
+    if (cu.it >= cu.end) return false;
+    const int r = cu.it / sc.nkb;
+    const int tb = r * sc.nkb;
+    w.kb0 = cu.it - tb;
+    w.kb1 = min(sc.nkb, cu.end - tb);
+    const int t = sc.dp_tiles + r;
+    w.m0 = (t % sc.m_tiles) * BM;
+    w.n0 = (t / sc.m_tiles) * BN;
+    w.bn = BN;
+    // -1: the whole tile lies in this share
+    w.skt = (w.kb0 == 0 && w.kb1 == sc.nkb) ? -1 : r;
+    cu.it = tb + sc.nkb;
+    return true;
+}
+
+// Workspace of the split-K schedule: two counters per (tile, epilogue warp) --
+// pieces that finished their MMAs, pieces whose partials are written -- then,
+// per CTA, two partial slots (the first and the last piece of its share), each
+// NUM_EPI_WARPS sub-blocks of 32 rows x 128 columns of int32.  The counter
+// block has one size for every shape on a device (room for 2 x grid tiles), so
+// that the counters of one launch never fall on another launch's partial slots
+// in a shared workspace.
+constexpr int kSlotWarpBytes = 32 * 128 * 4;
+__host__ __device__ inline long long sk_counter_bytes(const Schedule &sc) {
+    return ((long long)sc.sk_cnt_tiles * NUM_EPI_WARPS * 2 * 4 + 255) / 256 * 256;
+}
+__host__ __device__ inline long long sk_workspace_bytes(const Schedule &sc) {
+    if (sc.sk_tiles == 0) return 0;
+    return sk_counter_bytes(sc) + (long long)sc.sk_ctas * 2 * NUM_EPI_WARPS * kSlotWarpBytes;
 }
 
 struct Smem {
@@ -312,6 +419,9 @@ struct EpiArgs {
     RequantOut rq;  // the requantising epilogue's outputs (QUANT kernels)
     int rq_vec;     // 1: rows of the code arrays are 16-byte multiples (N % 16 == 0)
     int rq_fast;    // 1: scale >= 2^-70, so the reciprocal division may be used
+    Schedule sched;     // work units (made on the host)
+    int32_t *ws_cnt;    // split-K counters (zero between launches), or null
+    int4 *ws_slots;     // split-K partial slots
 };
 
 // Largest row L1 norm of int8 codes for which 127 * L1 < 2^24: then every
@@ -660,6 +770,114 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int64_t m, int nb,
     }
 }
 
+// Bounded wait until the counter at p reaches `target` (acquire).  The pieces
+// it waits for have already finished their MMAs and only have stores left, so
+// the wait is short; the limit guards against a corrupted workspace.
+__device__ __noinline__ bool wait_count(const int32_t *p, int target, volatile int *abort_flag) {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        int32_t v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+        if (v >= target) return true;
+        if ((it & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kTimeoutNs) {
+                *abort_flag = 1;
+                atomicOr(&g_tc_error, 4u);
+                return false;
+            }
+        }
+    }
+}
+
+// This warp's 32 x 128 sub-block of the partial slot that CTA c uses for its
+// piece of the split tile starting at K-block index tb: slot 0 when the
+// tile is the first of c's share, else slot 1.  Layout (int4 units):
+// [slice s][column quad j][lane], so that each warp access is 512 contiguous bytes.
+__device__ __forceinline__ int4 *sk_slot(const EpiArgs &a, int c, long long tb, int ew) {
+    const int e = sk_start(a.sched, c) >= tb ? 0 : 1;
+    return a.ws_slots + (((long long)c * 2 + e) * NUM_EPI_WARPS + ew) * (kSlotWarpBytes / 16);
+}
+
+// Split-K fixup of one warp's 32 x 128 sub-block of a piece whose exact sums
+// are in tensor memory at T (fp32 when fp32_in, else int32).  Every piece but
+// the last to finish writes its sums to its slot; the last one waits until
+// those writes are visible, adds them to its own, puts the int32 total back at
+// T, resets the tile's counters and returns true (it then runs the epilogue).
+__device__ __forceinline__ bool sk_fixup(uint32_t T, bool fp32_in, const Work &t, int ew,
+                                         int lane, const EpiArgs &a, volatile int *abort_flag) {
+    int32_t *cnt = a.ws_cnt + ((long long)t.skt * NUM_EPI_WARPS + ew) * 2;
+    const long long tb = (long long)t.skt * a.sched.nkb;
+    const int c0 = sk_cta_of(a.sched, tb), c1 = sk_cta_of(a.sched, tb + a.sched.nkb - 1);
+    const int pieces = c1 - c0 + 1;
+    int old = 0;
+    if (lane == 0) old = atomicAdd(cnt, 1);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old < pieces - 1) {
+        int4 *dst = sk_slot(a, blockIdx.x, tb, ew) + lane;
+#pragma unroll 1
+        for (int s = 0; s < SLICES; ++s) {
+            uint32_t v[32];
+            tmem_ld32(T + s * SLICE, v);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                int4 q;
+                q.x = fp32_in ? __float2int_rn(__uint_as_float(v[4 * j])) : (int)v[4 * j];
+                q.y = fp32_in ? __float2int_rn(__uint_as_float(v[4 * j + 1])) : (int)v[4 * j + 1];
+                q.z = fp32_in ? __float2int_rn(__uint_as_float(v[4 * j + 2])) : (int)v[4 * j + 2];
+                q.w = fp32_in ? __float2int_rn(__uint_as_float(v[4 * j + 3])) : (int)v[4 * j + 3];
+                __stcg(dst + (s * 8 + j) * 32, q);
+            }
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(cnt + 1, 1);
+        return false;
+    }
+    int ok = 1;
+    if (lane == 0) ok = wait_count(cnt + 1, pieces - 1, abort_flag);
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+    __threadfence();
+#pragma unroll 1
+    for (int s = 0; s < SLICES; ++s) {
+        uint32_t v[32];
+        tmem_ld32(T + s * SLICE, v);
+        if (fp32_in) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = (uint32_t)__float2int_rn(__uint_as_float(v[j]));
+        }
+        // peers two at a time: 16 loads of 16 bytes in flight per lane
+#pragma unroll 1
+        for (int c = c0; c <= c1; c += 2) {
+            const bool has0 = c != (int)blockIdx.x;
+            const bool has1 = c + 1 <= c1 && c + 1 != (int)blockIdx.x;
+            const int4 *src0 = sk_slot(a, has0 ? c : c1, tb, ew) + lane + s * 256;
+            const int4 *src1 = sk_slot(a, has1 ? c + 1 : c0, tb, ew) + lane + s * 256;
+            int4 q0[8], q1[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                q0[j] = has0 ? __ldcg(src0 + j * 32) : make_int4(0, 0, 0, 0);
+                q1[j] = has1 ? __ldcg(src1 + j * 32) : make_int4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                v[4 * j] = (uint32_t)((int32_t)v[4 * j] + q0[j].x + q1[j].x);
+                v[4 * j + 1] = (uint32_t)((int32_t)v[4 * j + 1] + q0[j].y + q1[j].y);
+                v[4 * j + 2] = (uint32_t)((int32_t)v[4 * j + 2] + q0[j].z + q1[j].z);
+                v[4 * j + 3] = (uint32_t)((int32_t)v[4 * j + 3] + q0[j].w + q1[j].w);
+            }
+        }
+        tmem_st32(T + s * SLICE, v);
+    }
+    tmem_wait_st();
+    __syncwarp();
+    if (lane == 0) {
+        cnt[0] = 0;
+        cnt[1] = 0;
+    }
+    return true;
+}
+
 template <int MODE, bool QUANT>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -700,11 +918,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tmem_base = S.tmem_base;
     volatile int *abort_flag = &S.abort_flag;
 
-    const int m_tiles = (M + BM - 1) / BM;
-    const int n_tiles = (N + BN - 1) / BN;
-    const Schedule sched = make_schedule(m_tiles, n_tiles, gridDim.x);
-    const int num_items = sched.items;
-    const int nkb = (K + BK - 1) / BK;
+    const Schedule &sched = args.sched;
+    const int nkb = sched.nkb;
     // K per exact fp32 pass: 1024, or all of K when the row L1 norms of either
     // operand bound every partial sum below 2^24.  Decided by warps 1..9 (the
     // MMA issuer and the epilogue); the producer does not need it.
@@ -742,10 +957,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued = 0, fill_parity = 0;  // per-stage bits: loads in flight
-            for (int i = blockIdx.x; i < num_items; i += gridDim.x) {
-                const Item t = item_at(sched, i);
+            Cursor cu;
+            cursor_init(sched, cu);
+            Work t;
+            while (next_work(sched, cu, t)) {
                 const bool slice = t.bn < BN;
-                for (int kb = 0; kb < nkb; ++kb) {
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&S.empty[stage]), phase ^ 1, abort_flag)) goto done_p;
                     const uint32_t full = smem_u32(&S.full[stage]);
                     mbar_expect_tx(full, A_BYTES + t.bn * BK * 2);
@@ -771,18 +988,21 @@ __global__ void __launch_bounds__(THREADS, 1)
             int stage = 0;
             uint32_t phase = 0, tph = 0;  // tph: per-buffer use parity bits
             bool issued_any = false;
-            int it = 0;
-            for (int i = blockIdx.x; i < num_items; i += gridDim.x, ++it) {
-                const uint32_t idesc = idesc_for(item_at(sched, i).bn);
-                for (int c = 0; c < nchunks; ++c) {
+            Cursor cu;
+            cursor_init(sched, cu);
+            Work t;
+            for (int it = 0; next_work(sched, cu, t); ++it) {
+                const uint32_t idesc = idesc_for(t.bn);
+                // exact fp32 passes: the unit's K blocks cut at multiples of chunk_kb
+                for (int c = t.kb0 / chunk_kb; c * chunk_kb < t.kb1; ++c) {
                     const uint32_t b = nchunks == 1 ? (uint32_t)(it & 1) : 0u;
                     const uint32_t par = (tph >> b) & 1u;
                     if (!mbar_wait(smem_u32(&S.tempty[b]), par ^ 1, abort_flag)) goto done_m;
                     tph ^= 1u << b;
                     tc_fence_after();
                     const uint32_t d = tmem_base + b * BN;
-                    const int kb0 = c * chunk_kb;
-                    const int kb1 = min(nkb, kb0 + chunk_kb);
+                    const int kb0 = max(t.kb0, c * chunk_kb);
+                    const int kb1 = min(t.kb1, (c + 1) * chunk_kb);
                     for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait(smem_u32(&S.full[stage]), phase, abort_flag)) goto done_m;
                         tc_fence_after();
@@ -821,38 +1041,45 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t fph = 0;                  // accumulator-full parities
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const uint32_t colP = BN;          // int32 partial (multi-chunk shapes)
-        int it = 0;
-        for (int i = blockIdx.x; i < num_items; i += gridDim.x, ++it) {
-            const Item t = item_at(sched, i);
+        Cursor cu;
+        cursor_init(sched, cu);
+        Work t;
+        for (int it = 0; next_work(sched, cu, t); ++it) {
             const int row0 = t.m0 + q * 32;
             const int64_t m = (int64_t)row0 + lane;
             const int nb = t.n0 + half * COLS_PER_WARP;
-            // 32-column slices of this warp's half that the item covers (0..4)
+            // 32-column slices of this warp's half that the unit covers (0..4)
             const int nsl = max(0, min(SLICES, (t.bn - half * COLS_PER_WARP) / SLICE));
-            // operands that do not depend on the accumulators: fetch them now
+            const bool piece = t.skt >= 0;
+            // operands that do not depend on the accumulators: fetched before the
+            // accumulator wait, so that their latency hides (a split-K piece
+            // fetches them only once it is the one that finishes the tile)
             ColParams cp;
-            load_col_params<MODE, QUANT>(cp, args, nb, lane);
-            if (QUANT) stage_next_smoothing(stg, args, nb, lane);
-            if (QUANT && args.rq.x_scale && t.n0 == 0 && half == 0 && m < M)
-                args.rq.x_scale[m] = args.rq.scale;  // the next linear's per-token scales
-            const float xs = (MODE != SQ_EPI_RAW_I32 && m < M) ? __ldg(args.sx + m) : 0.f;
+            float xs = 0.f;
             float4 rnext[8];
-            if (MODE == SQ_EPI_BIAS_RESIDUAL && nsl > 0) load_residual(rnext, args, m, nb);
+            auto fetch = [&]() {
+                load_col_params<MODE, QUANT>(cp, args, nb, lane);
+                if (QUANT) stage_next_smoothing(stg, args, nb, lane);
+                if (QUANT && args.rq.x_scale && t.n0 == 0 && half == 0 && m < M)
+                    args.rq.x_scale[m] = args.rq.scale;  // the next linear's per-token scales
+                xs = (MODE != SQ_EPI_RAW_I32 && m < M) ? __ldg(args.sx + m) : 0.f;
+                if (MODE == SQ_EPI_BIAS_RESIDUAL && nsl > 0) load_residual(rnext, args, m, nb);
+            };
+            if (!piece) fetch();
+            // the unit's exact sums: fp32 in accumulator buffer b (one pass), or
+            // int32 in the partial P (chunk passes)
+            const uint32_t b = (uint32_t)(it & 1);
+            uint32_t T;
             if (nchunks == 1) {
-                const uint32_t b = (uint32_t)(it & 1);
                 if (!mbar_wait(smem_u32(&S.tfull[b]), (fph >> b) & 1u, abort_flag)) goto done_e;
                 fph ^= 1u << b;
                 tc_fence_after();
-                const uint32_t tA = tmem_base + lane_off + b * BN + half * COLS_PER_WARP;
-                epilogue_tile<MODE, false, QUANT>(tA, m, nb, row0, lane, args, xs, cp, rnext, &tmY,
-                                                  stg, nsl);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&S.tempty[b]));
+                T = tmem_base + lane_off + b * BN + half * COLS_PER_WARP;
             } else {
                 const uint32_t tA = tmem_base + lane_off + half * COLS_PER_WARP;
-                const uint32_t tP = tmem_base + lane_off + colP + half * COLS_PER_WARP;
-                for (int c = 0; c < nchunks; ++c) {
+                T = tmem_base + lane_off + colP + half * COLS_PER_WARP;
+                const int cfirst = t.kb0 / chunk_kb;
+                for (int c = cfirst; c * chunk_kb < t.kb1; ++c) {
                     if (!mbar_wait(smem_u32(&S.tfull[0]), fph & 1u, abort_flag)) goto done_e;
                     fph ^= 1u;
                     tc_fence_after();
@@ -863,22 +1090,39 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
                             v[j] = (uint32_t)__float2int_rn(__uint_as_float(v[j]));
-                        if (c > 0) {
+                        if (c > cfirst) {
                             uint32_t p[32];
-                            tmem_ld32(tP + s * SLICE, p);
+                            tmem_ld32(T + s * SLICE, p);
 #pragma unroll
                             for (int j = 0; j < 32; ++j) v[j] = (uint32_t)((int32_t)v[j] + (int32_t)p[j]);
                         }
-                        tmem_st32(tP + s * SLICE, v);
+                        tmem_st32(T + s * SLICE, v);
                     }
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&S.tempty[0]));
                 }
-                // final pass from the int32 partial; overlaps the next tile's MMAs
-                epilogue_tile<MODE, true, QUANT>(tP, m, nb, row0, lane, args, xs, cp, rnext, &tmY, stg,
-                                                 nsl);
+            }
+            // epilogue (the int32 partial's final pass overlaps the next unit's MMAs)
+            if (!piece) {
+                if (nchunks == 1)
+                    epilogue_tile<MODE, false, QUANT>(T, m, nb, row0, lane, args, xs, cp, rnext,
+                                                      &tmY, stg, nsl);
+                else
+                    epilogue_tile<MODE, true, QUANT>(T, m, nb, row0, lane, args, xs, cp, rnext,
+                                                     &tmY, stg, nsl);
+            } else if (sk_fixup(T, nchunks == 1, t, ew, lane, args, abort_flag)) {
+                fetch();
+                epilogue_tile<MODE, true, QUANT>(T, m, nb, row0, lane, args, xs, cp, rnext, &tmY,
+                                                 stg, nsl);
+            } else if (*abort_flag) {
+                goto done_e;
+            }
+            if (nchunks == 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&S.tempty[b]));
             }
         }
     done_e:
@@ -957,11 +1201,46 @@ sq_status launch_mode(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
 
 }  // namespace
 
+// Schedule of an M x N x K launch on `sms` SMs, and the grid it runs on.
+static Schedule plan(int64_t M, int64_t N, int64_t K, int sms, bool split_k, int *grid) {
+    const int m_tiles = (int)((M + BM - 1) / BM), n_tiles = (int)((N + BN - 1) / BN);
+    const int nkb = (int)((K + BK - 1) / BK);
+    const int tiles = m_tiles * n_tiles;
+    if (split_k) {
+        const Schedule sc = make_schedule(m_tiles, n_tiles, nkb, sms, true);
+        if (sc.sk_tiles > 0) {
+            *grid = sc.dp_tiles > 0 ? sms : sc.sk_ctas;
+            return sc;
+        }
+    }
+    *grid = std::min(tiles, sms);
+    return make_schedule(m_tiles, n_tiles, nkb, *grid, false);
+}
+
+static bool shape_ok(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0 || M > 0x7fffffff || N > 0x7fffffff || K > 0x7fffffff)
+        return false;
+    return ((M + BM - 1) / BM) * ((N + BN - 1) / BN) <= 0x7fffffff;
+}
+
+sq_status gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes) {
+    *bytes = 0;
+    if (M == 0 || N == 0) return SQ_OK;
+    if (!shape_ok(M, N, K)) return SQ_ERR_UNSUPPORTED;
+    DeviceInfo di;
+    sq_status rc = device_info(&di);
+    if (rc != SQ_OK) return rc;
+    int grid;
+    *bytes = (size_t)sk_workspace_bytes(plan(M, N, K, di.sms, true, &grid));
+    return SQ_OK;
+}
+
 sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_t *x_l1,
                          const __nv_bfloat16 *Wop, const float *sw, const int32_t *w_l1,
                          const float *bias, const float *residual, int64_t M, int64_t N,
-                         int64_t K, int mode, void *Y, const RequantOut *rq, cudaStream_t st) {
-    if (M > 0x7fffffff || N > 0x7fffffff) return SQ_ERR_UNSUPPORTED;
+                         int64_t K, int mode, void *Y, const RequantOut *rq, void *workspace,
+                         size_t workspace_bytes, cudaStream_t st) {
+    if (!shape_ok(M, N, K)) return SQ_ERR_UNSUPPORTED;
     if (rq && mode == SQ_EPI_RAW_I32) return SQ_ERR_INVALID_ARG;
     sq_status rc = get_encoder();
     if (rc != SQ_OK) return rc;
@@ -992,12 +1271,19 @@ sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_
         return rc;
     if ((rc = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wop, N, K, BN, BK)) != SQ_OK)
         return rc;
-    const int64_t m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN - 1) / BN;
-    const int64_t tiles = m_tiles * n_tiles;
-    if (tiles > 0x7fffffff) return SQ_ERR_UNSUPPORTED;
-    const int grid = (int)std::min<int64_t>(tiles, di.sms);
+    int grid;
+    const Schedule sched = plan(M, N, K, di.sms, workspace != nullptr, &grid);
+    args.sched = sched;
+    args.ws_cnt = nullptr;
+    args.ws_slots = nullptr;
+    if (sched.sk_tiles > 0) {
+        const long long need = sk_workspace_bytes(sched);
+        if ((long long)workspace_bytes < need || !aligned16(workspace)) return SQ_ERR_INVALID_ARG;
+        args.ws_cnt = static_cast<int32_t *>(workspace);
+        args.ws_slots = reinterpret_cast<int4 *>(static_cast<char *>(workspace) +
+                                                 sk_counter_bytes(sched));
+    }
     // B box of the column slices of the last wave's tiles (see make_schedule)
-    const Schedule sched = make_schedule((int)m_tiles, (int)n_tiles, grid);
     tbs = tb;
     if (sched.sub > 1 &&
         (rc = make_map(&tbs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wop, N, K, BN / sched.sub, BK)) !=
