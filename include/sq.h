@@ -244,6 +244,25 @@ sq_status sq_linear_i8_requant_ws(const void *Xop, const float *x_scale,
                                   void *Yop, float *x_scale_next, void *workspace,
                                   size_t workspace_bytes, void *stream);
 
+/* sq_linear_i8_ws on scratch the library holds itself, for callers that
+ * allocate no device memory: a file-scope static device array of
+ * SQ_STATIC_WORKSPACE_BYTES (40 MiB; a GPU of up to 159 SMs), zero-filled at
+ * module load.  Its address is looked up once per device (cudaGetSymbolAddress)
+ * on that device's first call; make that first call outside any stream capture,
+ * after which a call only launches.  Nothing is allocated: a shape whose split
+ * needs more than the array (sq_linear_workspace_bytes) returns
+ * SQ_ERR_UNSUPPORTED.  The scratch is one per device and process: calls whose
+ * launches may overlap (different streams without ordering, several host
+ * threads) race on it and must be serialised by the caller.  Outputs, other
+ * arguments and statuses as sq_linear_i8_ws; after SQ_ERR_TIMEOUT the scratch's
+ * counters may be left non-zero, so the library must be reloaded. */
+#define SQ_STATIC_WORKSPACE_BYTES (40u * 1024u * 1024u)
+sq_status sq_linear_i8_static_ws(const void *Xop, const float *x_scale,
+                                 const int32_t *x_row_l1, const void *Wop, const float *w_scale,
+                                 const int32_t *w_row_l1, const float *bias,
+                                 const float *residual, int64_t M, int64_t N, int64_t K,
+                                 int mode, void *Y, void *stream);
+
 /* The same GEMM + epilogue on the legacy warp-level integer MMA path
  * (mma.sync m16n8k32 s8 x s8 -> s32), reading int8 codes directly:
  * Xq int8 [M][K] and Wq int8 [N][K] from sq_quantize_act / sq_pack_weight.

@@ -24,7 +24,7 @@ EXPORTS = ("sq_status_string", "sq_version", "sq_operand_bytes", "sq_channel_abs
            "sq_smooth_factor", "sq_pack_weight", "sq_quantize_act", "sq_act_absmax",
            "sq_quantize_act_static", "sq_layernorm_quant", "sq_linear_i8",
            "sq_linear_i8_requant", "sq_linear_workspace_bytes", "sq_linear_i8_ws",
-           "sq_linear_i8_requant_ws", "sq_linear_i8_mma_sync",
+           "sq_linear_i8_requant_ws", "sq_linear_i8_static_ws", "sq_linear_i8_mma_sync",
            "sq_check_division", "sq_device_status")
 
 _lock = threading.Lock()
@@ -69,6 +69,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                      ctypes.c_size_t, vp], i32),
                 "sq_linear_i8_requant_ws": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32,
                                              vp, f32, vp, vp, vp, vp, ctypes.c_size_t, vp], i32),
+                "sq_linear_i8_static_ws": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp,
+                                            vp], i32),
                 "sq_linear_i8_mma_sync": ([vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp], i32),
                 "sq_check_division": ([ctypes.c_uint32] * 4 + [i32, vp, vp], i32),
                 "sq_device_status": ([vp], i32),
@@ -333,6 +335,22 @@ def linear_i8_ws(Xop, x_scale, Wop, w_scale, bias=None, residual=None, mode=EPI_
     _check(load().sq_linear_i8_ws(_p(Xop), _p(x_scale), _p(x_l1), _p(Wop), _p(w_scale), _p(w_l1),
                                   _p(bias), _p(residual), M, N, K, int(mode), _p(out), wp, wn,
                                   _stream(stream)), "sq_linear_i8_ws")
+    return out
+
+
+STATIC_WORKSPACE_BYTES = 40 * 1024 * 1024  # SQ_STATIC_WORKSPACE_BYTES of sq.h
+
+
+def linear_i8_static_ws(Xop, x_scale, Wop, w_scale, bias=None, residual=None, mode=EPI_BIAS,
+                        out=None, x_l1=None, w_l1=None, stream=None):
+    """linear_i8_ws on the library's static scratch (no workspace argument, no
+    allocation); calls that may overlap must be serialised by the caller."""
+    _need(Xop, torch.bfloat16, "Xop")
+    _need(Wop, torch.bfloat16, "Wop")
+    M, N, K, out = _out(Xop, Wop, mode, out)
+    _check(load().sq_linear_i8_static_ws(_p(Xop), _p(x_scale), _p(x_l1), _p(Wop), _p(w_scale),
+                                         _p(w_l1), _p(bias), _p(residual), M, N, K, int(mode),
+                                         _p(out), _stream(stream)), "sq_linear_i8_static_ws")
     return out
 
 
