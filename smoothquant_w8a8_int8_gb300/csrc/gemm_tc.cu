@@ -17,7 +17,11 @@
 // memory, converted to int32 (exact) by the epilogue warps and added in
 // int32.  The result equals the int32 dot product for every input.
 //
-// Roles (320 threads, one CTA per SM, persistent over 128 x 256 output tiles):
+// Two kernels share the epilogue code below.  The pair kernel (end of the
+// kernel section) runs every launch with at least 256 rows that is not split
+// over K; the one-CTA kernel runs the rest.
+//
+// One-CTA roles (320 threads, one CTA per SM, persistent over 128 x 256 output tiles):
 //   warp 0, lane 0  TMA producer: A [128 x 64] and B [256 x 64] bf16 tiles,
 //                   128-byte swizzle, into a 4-stage ring (48 KB per stage)
 //   warp 1, lane 0  MMA issuer: tcgen05.mma kind::f16, M=128 N=256 K=16
@@ -245,6 +249,59 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
 }
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---- CTA pairs (cluster of 2, cta_group::2)
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// the shared::cluster address of this CTA's shared-memory offset `saddr` in CTA `rank`
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// arrive on a barrier of either CTA of the pair (after this warp's tensor-memory reads)
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar)
+                 : "memory");
+}
+// TMA load into this CTA's shared memory whose completion is counted on a
+// barrier of either CTA of the pair
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map,
+                                                 uint32_t cbar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(cbar), "r"(x), "r"(y)
+        : "memory");
+}
+// M = 256 (128 rows in each CTA's tensor memory), N = 256, K = 16 over the pair:
+// A is each CTA's own 128 rows, B is each CTA's 128 of the 256 rows, at the
+// same shared-memory offsets in both CTAs
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// arrive once on the barrier at offset `bar` in both CTAs of the pair when
+// this thread's earlier MMAs complete
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+    asm volatile(
+        "{\n .reg .b16 mask;\n mov.b16 mask, 3;\n"
+        " tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], mask;\n}\n" ::"r"(bar)
+        : "memory");
 }
 
 // ------------------------------------------------------------------ kernel
@@ -878,6 +935,38 @@ __device__ __forceinline__ bool sk_fixup(uint32_t T, bool fp32_in, const Work &t
     return true;
 }
 
+// K blocks per exact fp32 pass: 16 (K = 1024), or all of K when the row L1
+// norms of either operand bound every partial sum below 2^24.  Decided by
+// warps 1..9 (the MMA issuer and the epilogue) through named barrier 1; the
+// producer (warp 0) does not need it and returns 16.
+__device__ __forceinline__ int exact_pass_kb(const EpiArgs &args, int nkb, int warp, int lane,
+                                             int32_t (*l1max)[2]) {
+    if (warp == 0 || nkb <= KB_PER_CHUNK || !(args.x_l1 || args.w_l1)) return KB_PER_CHUNK;
+    const int tid = threadIdx.x - 32;
+    int32_t mx = args.x_l1 ? 0 : 0x7fffffff, mw = args.w_l1 ? 0 : 0x7fffffff;
+    if (args.x_l1)
+        for (int i = tid; i < args.M; i += THREADS - 32) mx = max(mx, __ldg(args.x_l1 + i));
+    if (args.w_l1)
+        for (int i = tid; i < args.N; i += THREADS - 32) mw = max(mw, __ldg(args.w_l1 + i));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        mw = max(mw, __shfl_xor_sync(0xffffffffu, mw, o));
+    }
+    if (lane == 0) {
+        l1max[warp - 1][0] = mx;
+        l1max[warp - 1][1] = mw;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(THREADS - 32) : "memory");
+    mx = 0;
+    mw = 0;
+    for (int w = 0; w < 9; ++w) {
+        mx = max(mx, l1max[w][0]);
+        mw = max(mw, l1max[w][1]);
+    }
+    return min(mx, mw) <= kSinglePassL1 ? nkb : KB_PER_CHUNK;
+}
+
 template <int MODE, bool QUANT>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -890,7 +979,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     Smem &S = *reinterpret_cast<Smem *>(staging + NUM_EPI_WARPS * STG_BYTES);
     const uint32_t ring = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int M = args.M, N = args.N;
+    const int M = args.M;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -923,32 +1012,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // K per exact fp32 pass: 1024, or all of K when the row L1 norms of either
     // operand bound every partial sum below 2^24.  Decided by warps 1..9 (the
     // MMA issuer and the epilogue); the producer does not need it.
-    int chunk_kb = KB_PER_CHUNK;
-    if (warp != 0 && nkb > KB_PER_CHUNK && (args.x_l1 || args.w_l1)) {
-        const int tid = threadIdx.x - 32;
-        int32_t mx = args.x_l1 ? 0 : 0x7fffffff, mw = args.w_l1 ? 0 : 0x7fffffff;
-        if (args.x_l1)
-            for (int i = tid; i < M; i += THREADS - 32) mx = max(mx, __ldg(args.x_l1 + i));
-        if (args.w_l1)
-            for (int i = tid; i < N; i += THREADS - 32) mw = max(mw, __ldg(args.w_l1 + i));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            mw = max(mw, __shfl_xor_sync(0xffffffffu, mw, o));
-        }
-        if (lane == 0) {
-            S.l1max[warp - 1][0] = mx;
-            S.l1max[warp - 1][1] = mw;
-        }
-        asm volatile("bar.sync 1, %0;" ::"n"(THREADS - 32) : "memory");
-        mx = 0;
-        mw = 0;
-        for (int w = 0; w < 9; ++w) {
-            mx = max(mx, S.l1max[w][0]);
-            mw = max(mw, S.l1max[w][1]);
-        }
-        if (min(mx, mw) <= kSinglePassL1) chunk_kb = nkb;
-    }
+    const int chunk_kb = exact_pass_kb(args, nkb, warp, lane, S.l1max);
     const int nchunks = (nkb + chunk_kb - 1) / chunk_kb;
 
     if (warp == 0) {
@@ -1140,6 +1204,255 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------- pair kernel
+//
+// The same contraction and epilogue on CTA pairs (clusters of 2) with
+// tcgen05.mma.cta_group::2, M = 256, N = 256: the pair's two SMs share one
+// 256 x 256 output tile, each holding its 128 rows of A and 128 of the 256 rows
+// of B in shared memory and its 128 x 256 accumulators in its own tensor
+// memory.  Per K block an SM then takes in 32 KB instead of 48 KB, and its
+// shared memory serves 32 KB to the tensor cores instead of 48 KB: the
+// one-CTA kernel is bound by that shared-memory traffic (the TMA writing each
+// stage and the MMA reading it), not by the tensor cores.  The 32 KB stage
+// also lets the ring hold 6 stages.
+//   both CTAs, warp 0 lane 0: load their halves into their own ring; the
+//     copies complete on the leader's (rank 0) `full` barrier, which the
+//     leader alone arms, locally, with both halves' bytes;
+//   leader, warp 1 lane 0: the MMAs; their commits arrive on `empty`, `tfull`
+//     and `mma_done` of both CTAs (multicast);
+//   both CTAs, warps 2..9: the epilogue of their own 128 rows, as in the
+//     one-CTA kernel; they release an accumulator on the leader's `tempty`.
+constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_B_ROWS = BN / 2;
+constexpr int PAIR_STAGE_BYTES = A_BYTES + PAIR_B_ROWS * BK * 2;
+constexpr int PAIR_RING_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES;
+constexpr int PAIR_SMEM_BYTES = PAIR_RING_BYTES + NUM_EPI_WARPS * STG_BYTES + BAR_BYTES + 1024;
+constexpr uint32_t IDESC_PAIR = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                                ((uint32_t)((2 * BM) >> 4) << 24);
+
+struct PairSmem {
+    uint64_t full[PAIR_STAGES];
+    uint64_t empty[PAIR_STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
+    int32_t l1max[9][2];
+};
+static_assert(sizeof(PairSmem) <= BAR_BYTES, "barrier block");
+
+template <int MODE, bool QUANT>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmY, const EpiArgs args, int K) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *staging = smem + PAIR_RING_BYTES;
+    PairSmem &S = *reinterpret_cast<PairSmem *>(staging + NUM_EPI_WARPS * STG_BYTES);
+    const uint32_t ring = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int M = args.M, N = args.N;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < PAIR_STAGES; ++s) {
+            mbar_init(smem_u32(&S.full[s]), 1);   // the leader's arming arrive (+ both halves' bytes)
+            mbar_init(smem_u32(&S.empty[s]), 1);  // one multicast commit per phase
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&S.tfull[b]), 1);
+            mbar_init(smem_u32(&S.tempty[b]), 2 * NUM_EPI_WARPS);  // both CTAs' epilogues
+        }
+        mbar_init(smem_u32(&S.mma_done), 1);
+        S.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&S.tmem_base)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // barriers of both CTAs initialised before any remote arrive
+    tc_fence_after();
+    const uint32_t tmem_base = S.tmem_base;
+    volatile int *abort_flag = &S.abort_flag;
+
+    const int m_pairs = (M + 2 * BM - 1) / (2 * BM);  // 256-row pair tiles, numbered m-fastest
+    const int n_tiles = (N + BN - 1) / BN;
+    const int num_tiles = m_pairs * n_tiles;
+    const int nkb = (K + BK - 1) / BK;
+    const int cluster_id = blockIdx.x >> 1;
+    const int num_clusters = gridDim.x >> 1;
+    const int chunk_kb = exact_pass_kb(args, nkb, warp, lane, S.l1max);
+    const int nchunks = (nkb + chunk_kb - 1) / chunk_kb;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer (both CTAs)
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+                const int m0 = (t % m_pairs) * 2 * BM + (int)rank * BM;
+                const int nB = (t / m_pairs) * BN + (int)rank * PAIR_B_ROWS;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(smem_u32(&S.empty[stage]), phase ^ 1, abort_flag)) goto done_p;
+                    const uint32_t full_leader = map_to_rank(smem_u32(&S.full[stage]), 0);
+                    if (leader) mbar_expect_tx(smem_u32(&S.full[stage]), 2 * PAIR_STAGE_BYTES);
+                    const uint32_t sa = ring + stage * PAIR_STAGE_BYTES;
+                    tma_load_2d_pair(sa, &tmA, full_leader, kb * BK, m0);
+                    tma_load_2d_pair(sa + A_BYTES, &tmB, full_leader, kb * BK, nB);
+                    if (++stage == PAIR_STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+        done_p:
+            // every issued copy is consumed by the leader's MMAs, whose commits
+            // complete this CTA's `empty` phases: wait (bounded) for the stages
+            // still in use before the shared memory can go away
+            for (int s = 0; s < PAIR_STAGES; ++s) {
+                mbar_drain(smem_u32(&S.empty[stage]), phase ^ 1);
+                if (++stage == PAIR_STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ------------------------------------------------ MMA issuer (leader)
+            int stage = 0;
+            uint32_t phase = 0, tph = 0;
+            int it = 0;
+            for (int t = cluster_id; t < num_tiles; t += num_clusters, ++it) {
+                for (int c = 0; c < nchunks; ++c) {
+                    const uint32_t b = nchunks == 1 ? (uint32_t)(it & 1) : 0u;
+                    const uint32_t par = (tph >> b) & 1u;
+                    if (!mbar_wait(smem_u32(&S.tempty[b]), par ^ 1, abort_flag)) goto done_m;
+                    tph ^= 1u << b;
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + b * BN;
+                    const int kb0 = c * chunk_kb;
+                    const int kb1 = min(nkb, kb0 + chunk_kb);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait(smem_u32(&S.full[stage]), phase, abort_flag)) goto done_m;
+                        tc_fence_after();
+                        const uint32_t sa = ring + stage * PAIR_STAGE_BYTES;
+                        const uint64_t adesc = sw128_desc(sa);
+                        const uint64_t bdesc = sw128_desc(sa + A_BYTES);
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k)
+                            umma_bf16_pair(d, adesc + 2 * k, bdesc + 2 * k, IDESC_PAIR,
+                                           (kb > kb0 || k > 0) ? 1u : 0u);
+                        umma_commit_pair(smem_u32(&S.empty[stage]));
+                        if (++stage == PAIR_STAGES) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
+                    }
+                    umma_commit_pair(smem_u32(&S.tfull[b]));
+                }
+            }
+        done_m:
+            // arrives on both CTAs once every MMA issued above has completed
+            umma_commit_pair(smem_u32(&S.mma_done));
+        }
+        // no CTA frees its tensor memory while the pair's MMAs may still write it
+        if (lane == 0) mbar_drain(smem_u32(&S.mma_done), 0);
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------- epilogue (both CTAs)
+        const int ew = warp - 2;
+        const int q = warp & 3;
+        const int half = ew >> 2;
+        uint8_t *stg = staging + ew * STG_BYTES;
+        uint32_t fph = 0;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const uint32_t colP = BN;
+        const uint32_t tempty_leader0 = map_to_rank(smem_u32(&S.tempty[0]), 0);
+        const uint32_t tempty_leader1 = map_to_rank(smem_u32(&S.tempty[1]), 0);
+        int it = 0;
+        for (int t = cluster_id; t < num_tiles; t += num_clusters, ++it) {
+            const int m0 = (t % m_pairs) * 2 * BM + (int)rank * BM;
+            const int n0 = (t / m_pairs) * BN;
+            const int row0 = m0 + q * 32;
+            const int64_t m = (int64_t)row0 + lane;
+            const int nb = n0 + half * COLS_PER_WARP;
+            ColParams cp;
+            load_col_params<MODE, QUANT>(cp, args, nb, lane);
+            if (QUANT) stage_next_smoothing(stg, args, nb, lane);
+            if (QUANT && args.rq.x_scale && n0 == 0 && half == 0 && m < M)
+                args.rq.x_scale[m] = args.rq.scale;
+            const float xs = (MODE != SQ_EPI_RAW_I32 && m < M) ? __ldg(args.sx + m) : 0.f;
+            float4 rnext[8];
+            if (MODE == SQ_EPI_BIAS_RESIDUAL) load_residual(rnext, args, m, nb);
+            if (nchunks == 1) {
+                const uint32_t b = (uint32_t)(it & 1);
+                if (!mbar_wait(smem_u32(&S.tfull[b]), (fph >> b) & 1u, abort_flag)) goto done_e;
+                fph ^= 1u << b;
+                tc_fence_after();
+                const uint32_t tA = tmem_base + lane_off + b * BN + half * COLS_PER_WARP;
+                epilogue_tile<MODE, false, QUANT>(tA, m, nb, row0, lane, args, xs, cp, rnext, &tmY,
+                                                  stg, SLICES);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(b ? tempty_leader1 : tempty_leader0);
+            } else {
+                const uint32_t tA = tmem_base + lane_off + half * COLS_PER_WARP;
+                const uint32_t tP = tmem_base + lane_off + colP + half * COLS_PER_WARP;
+                for (int c = 0; c < nchunks; ++c) {
+                    if (!mbar_wait(smem_u32(&S.tfull[0]), fph & 1u, abort_flag)) goto done_e;
+                    fph ^= 1u;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int s = 0; s < SLICES; ++s) {
+                        uint32_t v[32];
+                        tmem_ld32(tA + s * SLICE, v);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            v[j] = (uint32_t)__float2int_rn(__uint_as_float(v[j]));
+                        if (c > 0) {
+                            uint32_t p[32];
+                            tmem_ld32(tP + s * SLICE, p);
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = (uint32_t)((int32_t)v[j] + (int32_t)p[j]);
+                        }
+                        tmem_st32(tP + s * SLICE, v);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(tempty_leader0);
+                }
+                epilogue_tile<MODE, true, QUANT>(tP, m, nb, row0, lane, args, xs, cp, rnext, &tmY,
+                                                 stg, SLICES);
+            }
+        }
+    done_e:
+        if (lane == 0) bulk_wait0();  // stores complete before the CTA exits
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // no remote arrive, copy or MMA touches either CTA after this
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
 // ------------------------------------------------------------------ host
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -1197,6 +1510,59 @@ sq_status launch_mode(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
                       bool quant, cudaStream_t st) {
     return quant ? launch_kernel<MODE, true>(ta, tb, tbs, ty, args, K, grid, device, st)
                  : launch_kernel<MODE, false>(ta, tb, tbs, ty, args, K, grid, device, st);
+}
+
+// The pair kernel on clusters of 2: at most one cluster per pair tile and no
+// more than can be resident at once (it is persistent).
+template <int MODE, bool QUANT>
+sq_status launch_pair_kernel(const CUtensorMap &ta, const CUtensorMap &tbp, const CUtensorMap &ty,
+                             const EpiArgs &args, int K, int pair_tiles, int device,
+                             cudaStream_t st) {
+    static int attr_dev = -1;
+    static int max_clusters = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (attr_dev != device) {
+        if (cudaFuncSetAttribute(gemm_tc_pair_kernel<MODE, QUANT>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PAIR_SMEM_BYTES) != cudaSuccess)
+            return SQ_ERR_CUDA;
+        cfg.gridDim = dim3(2, 1, 1);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_pair_kernel<MODE, QUANT>, &cfg) !=
+                cudaSuccess ||
+            n < 1)
+            return SQ_ERR_CUDA;
+        max_clusters = n;
+        attr_dev = device;
+    }
+    const int clusters = std::min(pair_tiles, max_clusters);
+    cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+    return cuda_status(
+        cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<MODE, QUANT>, ta, tbp, ty, args, K));
+}
+
+template <int MODE>
+sq_status launch_pair_mode(const CUtensorMap &ta, const CUtensorMap &tbp, const CUtensorMap &ty,
+                           const EpiArgs &args, int K, int pair_tiles, int device, bool quant,
+                           cudaStream_t st) {
+    return quant ? launch_pair_kernel<MODE, true>(ta, tbp, ty, args, K, pair_tiles, device, st)
+                 : launch_pair_kernel<MODE, false>(ta, tbp, ty, args, K, pair_tiles, device, st);
+}
+
+// Which kernel runs a launch: CTA pairs for every launch of at least one full
+// 256-row pair tile that is not split over K.
+bool use_pair(int64_t M, const Schedule &sched) {
+    return sched.sk_tiles == 0 && M >= 2 * BM;
 }
 
 }  // namespace
@@ -1297,6 +1663,26 @@ sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_
     }
     const bool q = rq != nullptr;
     const int k = (int)K, dev = di.device;
+    if (use_pair(M, sched)) {
+        // B in 128-row halves, one per CTA of a pair
+        CUtensorMap tbp;
+        if ((rc = make_map(&tbp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wop, N, K, PAIR_B_ROWS, BK)) !=
+            SQ_OK)
+            return rc;
+        const int64_t pt = ((M + 2 * BM - 1) / (2 * BM)) * ((N + BN - 1) / BN);
+        if (pt > 0x7fffffff) return SQ_ERR_UNSUPPORTED;
+        const int p = (int)pt;
+        switch (mode) {
+        case SQ_EPI_NONE: return launch_pair_mode<SQ_EPI_NONE>(ta, tbp, ty, args, k, p, dev, q, st);
+        case SQ_EPI_BIAS: return launch_pair_mode<SQ_EPI_BIAS>(ta, tbp, ty, args, k, p, dev, q, st);
+        case SQ_EPI_BIAS_GELU:
+            return launch_pair_mode<SQ_EPI_BIAS_GELU>(ta, tbp, ty, args, k, p, dev, q, st);
+        case SQ_EPI_BIAS_RESIDUAL:
+            return launch_pair_mode<SQ_EPI_BIAS_RESIDUAL>(ta, tbp, ty, args, k, p, dev, q, st);
+        default:
+            return launch_pair_kernel<SQ_EPI_RAW_I32, false>(ta, tbp, ty, args, k, p, dev, st);
+        }
+    }
     switch (mode) {
     case SQ_EPI_NONE: return launch_mode<SQ_EPI_NONE>(ta, tb, tbs, ty, args, k, grid, dev, q, st);
     case SQ_EPI_BIAS: return launch_mode<SQ_EPI_BIAS>(ta, tb, tbs, ty, args, k, grid, dev, q, st);
