@@ -1227,8 +1227,45 @@ constexpr int PAIR_B_ROWS = BN / 2;
 constexpr int PAIR_STAGE_BYTES = A_BYTES + PAIR_B_ROWS * BK * 2;
 constexpr int PAIR_RING_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES;
 constexpr int PAIR_SMEM_BYTES = PAIR_RING_BYTES + NUM_EPI_WARPS * STG_BYTES + BAR_BYTES + 1024;
-constexpr uint32_t IDESC_PAIR = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                                ((uint32_t)((2 * BM) >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_pair(int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)((2 * BM) >> 4) << 24);
+}
+
+// Work items of the pair kernel: 256 x 256 pair tiles, numbered m-fastest; when
+// the last, partial wave holds at most half the clusters, each of its tiles is
+// cut into two 256 x 128 halves (MMA N = 128, 64 rows of B per CTA).
+struct PairSchedule {
+    int m_pairs, full_items, sub, items;
+};
+
+__host__ __device__ inline PairSchedule make_pair_schedule(int m_pairs, int n_tiles,
+                                                           int clusters) {
+    PairSchedule sc;
+    sc.m_pairs = m_pairs;
+    const int tiles = m_pairs * n_tiles;
+    const int waves = tiles / clusters, rem = tiles - waves * clusters;
+    sc.sub = (waves >= 1 && rem > 0 && 2 * rem <= clusters) ? 2 : 1;
+    sc.full_items = sc.sub == 1 ? tiles : waves * clusters;
+    sc.items = sc.full_items + (tiles - sc.full_items) * sc.sub;
+    return sc;
+}
+
+// item i: pair rows from m0 (256), columns n0.. of width bn (256 or 128)
+__device__ __forceinline__ void pair_item_at(const PairSchedule &sc, int i, int &m0, int &n0,
+                                             int &bn) {
+    if (i < sc.full_items) {
+        m0 = (i % sc.m_pairs) * 2 * BM;
+        n0 = (i / sc.m_pairs) * BN;
+        bn = BN;
+    } else {
+        const int j = i - sc.full_items;
+        const int t = sc.full_items + j / sc.sub;
+        bn = BN / sc.sub;
+        m0 = (t % sc.m_pairs) * 2 * BM;
+        n0 = (t / sc.m_pairs) * BN + (j % sc.sub) * bn;
+    }
+}
 
 struct PairSmem {
     uint64_t full[PAIR_STAGES];
@@ -1246,6 +1283,7 @@ template <int MODE, bool QUANT>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmBq,
                         const __grid_constant__ CUtensorMap tmY, const EpiArgs args, int K) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -1285,12 +1323,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tmem_base = S.tmem_base;
     volatile int *abort_flag = &S.abort_flag;
 
-    const int m_pairs = (M + 2 * BM - 1) / (2 * BM);  // 256-row pair tiles, numbered m-fastest
-    const int n_tiles = (N + BN - 1) / BN;
-    const int num_tiles = m_pairs * n_tiles;
-    const int nkb = (K + BK - 1) / BK;
     const int cluster_id = blockIdx.x >> 1;
     const int num_clusters = gridDim.x >> 1;
+    const PairSchedule sched =
+        make_pair_schedule((M + 2 * BM - 1) / (2 * BM), (N + BN - 1) / BN, num_clusters);
+    const int num_items = sched.items;
+    const int nkb = (K + BK - 1) / BK;
     const int chunk_kb = exact_pass_kb(args, nkb, warp, lane, S.l1max);
     const int nchunks = (nkb + chunk_kb - 1) / chunk_kb;
 
@@ -1299,16 +1337,20 @@ __global__ void __launch_bounds__(THREADS, 1)
             // ------------------------------------------------ TMA producer (both CTAs)
             int stage = 0;
             uint32_t phase = 0;
-            for (int t = cluster_id; t < num_tiles; t += num_clusters) {
-                const int m0 = (t % m_pairs) * 2 * BM + (int)rank * BM;
-                const int nB = (t / m_pairs) * BN + (int)rank * PAIR_B_ROWS;
+            for (int i = cluster_id; i < num_items; i += num_clusters) {
+                int pm0, n0, bn;
+                pair_item_at(sched, i, pm0, n0, bn);
+                const int m0 = pm0 + (int)rank * BM;
+                const int nB = n0 + (int)rank * (bn / 2);  // this CTA's rows of B
+                const CUtensorMap *mapB = bn == BN ? &tmB : &tmBq;
+                const uint32_t bytes = A_BYTES + (bn / 2) * BK * 2;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(smem_u32(&S.empty[stage]), phase ^ 1, abort_flag)) goto done_p;
                     const uint32_t full_leader = map_to_rank(smem_u32(&S.full[stage]), 0);
-                    if (leader) mbar_expect_tx(smem_u32(&S.full[stage]), 2 * PAIR_STAGE_BYTES);
+                    if (leader) mbar_expect_tx(smem_u32(&S.full[stage]), 2 * bytes);
                     const uint32_t sa = ring + stage * PAIR_STAGE_BYTES;
                     tma_load_2d_pair(sa, &tmA, full_leader, kb * BK, m0);
-                    tma_load_2d_pair(sa + A_BYTES, &tmB, full_leader, kb * BK, nB);
+                    tma_load_2d_pair(sa + A_BYTES, mapB, full_leader, kb * BK, nB);
                     if (++stage == PAIR_STAGES) {
                         stage = 0;
                         phase ^= 1;
@@ -1333,7 +1375,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             int stage = 0;
             uint32_t phase = 0, tph = 0;
             int it = 0;
-            for (int t = cluster_id; t < num_tiles; t += num_clusters, ++it) {
+            for (int i = cluster_id; i < num_items; i += num_clusters, ++it) {
+                int pm0, n0, bn;
+                pair_item_at(sched, i, pm0, n0, bn);
+                const uint32_t idesc = idesc_pair(bn);
                 for (int c = 0; c < nchunks; ++c) {
                     const uint32_t b = nchunks == 1 ? (uint32_t)(it & 1) : 0u;
                     const uint32_t par = (tph >> b) & 1u;
@@ -1351,7 +1396,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const uint64_t bdesc = sw128_desc(sa + A_BYTES);
 #pragma unroll
                         for (int k = 0; k < BK / UMMA_K; ++k)
-                            umma_bf16_pair(d, adesc + 2 * k, bdesc + 2 * k, IDESC_PAIR,
+                            umma_bf16_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc,
                                            (kb > kb0 || k > 0) ? 1u : 0u);
                         umma_commit_pair(smem_u32(&S.empty[stage]));
                         if (++stage == PAIR_STAGES) {
@@ -1381,12 +1426,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t tempty_leader0 = map_to_rank(smem_u32(&S.tempty[0]), 0);
         const uint32_t tempty_leader1 = map_to_rank(smem_u32(&S.tempty[1]), 0);
         int it = 0;
-        for (int t = cluster_id; t < num_tiles; t += num_clusters, ++it) {
-            const int m0 = (t % m_pairs) * 2 * BM + (int)rank * BM;
-            const int n0 = (t / m_pairs) * BN;
+        for (int i = cluster_id; i < num_items; i += num_clusters, ++it) {
+            int pm0, n0, bn;
+            pair_item_at(sched, i, pm0, n0, bn);
+            const int m0 = pm0 + (int)rank * BM;
             const int row0 = m0 + q * 32;
             const int64_t m = (int64_t)row0 + lane;
             const int nb = n0 + half * COLS_PER_WARP;
+            // 32-column slices of this warp's half that the item covers (0..4)
+            const int nsl = max(0, min(SLICES, (bn - half * COLS_PER_WARP) / SLICE));
             ColParams cp;
             load_col_params<MODE, QUANT>(cp, args, nb, lane);
             if (QUANT) stage_next_smoothing(stg, args, nb, lane);
@@ -1394,7 +1442,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 args.rq.x_scale[m] = args.rq.scale;
             const float xs = (MODE != SQ_EPI_RAW_I32 && m < M) ? __ldg(args.sx + m) : 0.f;
             float4 rnext[8];
-            if (MODE == SQ_EPI_BIAS_RESIDUAL) load_residual(rnext, args, m, nb);
+            if (MODE == SQ_EPI_BIAS_RESIDUAL && nsl > 0) load_residual(rnext, args, m, nb);
             if (nchunks == 1) {
                 const uint32_t b = (uint32_t)(it & 1);
                 if (!mbar_wait(smem_u32(&S.tfull[b]), (fph >> b) & 1u, abort_flag)) goto done_e;
@@ -1402,7 +1450,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 const uint32_t tA = tmem_base + lane_off + b * BN + half * COLS_PER_WARP;
                 epilogue_tile<MODE, false, QUANT>(tA, m, nb, row0, lane, args, xs, cp, rnext, &tmY,
-                                                  stg, SLICES);
+                                                  stg, nsl);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(b ? tempty_leader1 : tempty_leader0);
@@ -1414,7 +1462,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     fph ^= 1u;
                     tc_fence_after();
 #pragma unroll 1
-                    for (int s = 0; s < SLICES; ++s) {
+                    for (int s = 0; s < nsl; ++s) {
                         uint32_t v[32];
                         tmem_ld32(tA + s * SLICE, v);
 #pragma unroll
@@ -1434,7 +1482,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (lane == 0) mbar_arrive_cluster(tempty_leader0);
                 }
                 epilogue_tile<MODE, true, QUANT>(tP, m, nb, row0, lane, args, xs, cp, rnext, &tmY,
-                                                 stg, SLICES);
+                                                 stg, nsl);
             }
         }
     done_e:
@@ -1515,9 +1563,9 @@ sq_status launch_mode(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
 // The pair kernel on clusters of 2: at most one cluster per pair tile and no
 // more than can be resident at once (it is persistent).
 template <int MODE, bool QUANT>
-sq_status launch_pair_kernel(const CUtensorMap &ta, const CUtensorMap &tbp, const CUtensorMap &ty,
-                             const EpiArgs &args, int K, int pair_tiles, int device,
-                             cudaStream_t st) {
+sq_status launch_pair_kernel(const CUtensorMap &ta, const CUtensorMap &tbp, const CUtensorMap &tbq,
+                             const CUtensorMap &ty, const EpiArgs &args, int K, int pair_tiles,
+                             int device, cudaStream_t st) {
     static int attr_dev = -1;
     static int max_clusters = 0;
     cudaLaunchConfig_t cfg = {};
@@ -1548,15 +1596,16 @@ sq_status launch_pair_kernel(const CUtensorMap &ta, const CUtensorMap &tbp, cons
     const int clusters = std::min(pair_tiles, max_clusters);
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
     return cuda_status(
-        cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<MODE, QUANT>, ta, tbp, ty, args, K));
+        cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<MODE, QUANT>, ta, tbp, tbq, ty, args, K));
 }
 
 template <int MODE>
-sq_status launch_pair_mode(const CUtensorMap &ta, const CUtensorMap &tbp, const CUtensorMap &ty,
-                           const EpiArgs &args, int K, int pair_tiles, int device, bool quant,
-                           cudaStream_t st) {
-    return quant ? launch_pair_kernel<MODE, true>(ta, tbp, ty, args, K, pair_tiles, device, st)
-                 : launch_pair_kernel<MODE, false>(ta, tbp, ty, args, K, pair_tiles, device, st);
+sq_status launch_pair_mode(const CUtensorMap &ta, const CUtensorMap &tbp, const CUtensorMap &tbq,
+                           const CUtensorMap &ty, const EpiArgs &args, int K, int pair_tiles,
+                           int device, bool quant, cudaStream_t st) {
+    return quant ? launch_pair_kernel<MODE, true>(ta, tbp, tbq, ty, args, K, pair_tiles, device, st)
+                 : launch_pair_kernel<MODE, false>(ta, tbp, tbq, ty, args, K, pair_tiles, device,
+                                                   st);
 }
 
 // Which kernel runs a launch: CTA pairs for every launch of at least one full
@@ -1664,23 +1713,28 @@ sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_
     const bool q = rq != nullptr;
     const int k = (int)K, dev = di.device;
     if (use_pair(M, sched)) {
-        // B in 128-row halves, one per CTA of a pair
-        CUtensorMap tbp;
+        // B in 128-row halves, one per CTA of a pair; 64-row quarters for the
+        // halves of a short last wave
+        CUtensorMap tbp, tbq;
         if ((rc = make_map(&tbp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wop, N, K, PAIR_B_ROWS, BK)) !=
-            SQ_OK)
+                SQ_OK ||
+            (rc = make_map(&tbq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wop, N, K, PAIR_B_ROWS / 2,
+                           BK)) != SQ_OK)
             return rc;
         const int64_t pt = ((M + 2 * BM - 1) / (2 * BM)) * ((N + BN - 1) / BN);
         if (pt > 0x7fffffff) return SQ_ERR_UNSUPPORTED;
         const int p = (int)pt;
         switch (mode) {
-        case SQ_EPI_NONE: return launch_pair_mode<SQ_EPI_NONE>(ta, tbp, ty, args, k, p, dev, q, st);
-        case SQ_EPI_BIAS: return launch_pair_mode<SQ_EPI_BIAS>(ta, tbp, ty, args, k, p, dev, q, st);
+        case SQ_EPI_NONE:
+            return launch_pair_mode<SQ_EPI_NONE>(ta, tbp, tbq, ty, args, k, p, dev, q, st);
+        case SQ_EPI_BIAS:
+            return launch_pair_mode<SQ_EPI_BIAS>(ta, tbp, tbq, ty, args, k, p, dev, q, st);
         case SQ_EPI_BIAS_GELU:
-            return launch_pair_mode<SQ_EPI_BIAS_GELU>(ta, tbp, ty, args, k, p, dev, q, st);
+            return launch_pair_mode<SQ_EPI_BIAS_GELU>(ta, tbp, tbq, ty, args, k, p, dev, q, st);
         case SQ_EPI_BIAS_RESIDUAL:
-            return launch_pair_mode<SQ_EPI_BIAS_RESIDUAL>(ta, tbp, ty, args, k, p, dev, q, st);
+            return launch_pair_mode<SQ_EPI_BIAS_RESIDUAL>(ta, tbp, tbq, ty, args, k, p, dev, q, st);
         default:
-            return launch_pair_kernel<SQ_EPI_RAW_I32, false>(ta, tbp, ty, args, k, p, dev, st);
+            return launch_pair_kernel<SQ_EPI_RAW_I32, false>(ta, tbp, tbq, ty, args, k, p, dev, st);
         }
     }
     switch (mode) {
