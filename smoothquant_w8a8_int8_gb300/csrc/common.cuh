@@ -13,6 +13,46 @@ inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3
 
 inline sq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SQ_OK : SQ_ERR_CUDA; }
 
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialisation allowed: once all CTAs of the kernel
+// before it on the stream have started (and called pdl_launch_dependents) or
+// finished, its CTAs may be scheduled, run their set-up (barrier
+// initialisation, tensor-memory allocation) and then block in pdl_wait until
+// the previous kernel has completed and its memory operations are visible.
+// Every global-memory access comes after pdl_wait, so the ordering of the
+// stream is kept for all data; only launch latency and set-up overlap.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch with programmatic stream serialisation (and a cluster of
+// `cluster_x` CTAs along x when cluster_x > 1).
+template <typename... KArgs, typename... Args>
+inline sq_status launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t st, unsigned cluster_x, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cuda_status(cudaLaunchKernelEx(&cfg, kern, args...));
+}
+
 // SM count and compute capability of the current device, cached per device.
 struct DeviceInfo {
     int device = -1;

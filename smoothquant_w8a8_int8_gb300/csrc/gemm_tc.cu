@@ -1004,6 +1004,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_launch_dependents();
+    pdl_wait();  // every global-memory access below follows the previous kernel
     const uint32_t tmem_base = S.tmem_base;
     volatile int *abort_flag = &S.abort_flag;
 
@@ -1320,6 +1322,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     cluster_sync_all();  // barriers of both CTAs initialised before any remote arrive
     tc_fence_after();
+    pdl_launch_dependents();
+    pdl_wait();  // every global-memory access below follows the previous kernel
     const uint32_t tmem_base = S.tmem_base;
     volatile int *abort_flag = &S.abort_flag;
 
@@ -1548,8 +1552,8 @@ sq_status launch_kernel(const CUtensorMap &ta, const CUtensorMap &tb, const CUte
             return SQ_ERR_CUDA;
         attr_dev = device;
     }
-    gemm_tc_kernel<MODE, QUANT><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, tbs, ty, args, K);
-    return cuda_status(cudaGetLastError());
+    return launch_pdl(gemm_tc_kernel<MODE, QUANT>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, 1, ta,
+                      tb, tbs, ty, args, K);
 }
 
 template <int MODE>
@@ -1572,13 +1576,15 @@ sq_status launch_pair_kernel(const CUtensorMap &ta, const CUtensorMap &tbp, cons
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 1;  // the occupancy query: cluster shape only
     if (attr_dev != device) {
         if (cudaFuncSetAttribute(gemm_tc_pair_kernel<MODE, QUANT>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1595,6 +1601,7 @@ sq_status launch_pair_kernel(const CUtensorMap &ta, const CUtensorMap &tbp, cons
     }
     const int clusters = std::min(pair_tiles, max_clusters);
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+    cfg.numAttrs = 2;  // the launch: cluster shape and programmatic serialisation
     return cuda_status(
         cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<MODE, QUANT>, ta, tbp, tbq, ty, args, K));
 }

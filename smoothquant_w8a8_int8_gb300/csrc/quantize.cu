@@ -126,6 +126,8 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_reg(
     const float *__restrict__ A, const float *__restrict__ s, int64_t rows, int K4, int tpr,
     int8_t *__restrict__ q, float *__restrict__ scale, __nv_bfloat16 *__restrict__ op,
     int32_t *__restrict__ l1, float fixed_scale) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ float red[kThreads / 32];
     const int rpb = kThreads / tpr;
     const int g = threadIdx.x / tpr;
@@ -188,6 +190,8 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_loop(
     const float *__restrict__ A, const float *__restrict__ s, int64_t rows, int K4,
     int8_t *__restrict__ q, float *__restrict__ scale, __nv_bfloat16 *__restrict__ op,
     int32_t *__restrict__ l1, float fixed_scale) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ float red[kThreads / 32];
     const float4 *s4 = reinterpret_cast<const float4 *>(s);
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
@@ -235,6 +239,8 @@ __global__ void __launch_bounds__(kThreads) act_absmax_kernel(const float *__res
                                                               const float *__restrict__ s,
                                                               int64_t rows, int K4,
                                                               float *__restrict__ amax) {
+    pdl_launch_dependents();
+    pdl_wait();
     const float4 *a4 = reinterpret_cast<const float4 *>(A);
     const float4 *s4 = reinterpret_cast<const float4 *>(s);
     const int64_t total = rows * (int64_t)K4;
@@ -255,6 +261,8 @@ __global__ void __launch_bounds__(kThreads) act_absmax_kernel(const float *__res
 __global__ void __launch_bounds__(kThreads) channel_absmax_kernel(
     const float *__restrict__ A, int64_t rows, int64_t cols, int64_t rows_per_block,
     float *__restrict__ amax) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t j = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     if (j >= cols) return;
     const int64_t r0 = (int64_t)blockIdx.y * rows_per_block;
@@ -266,6 +274,8 @@ __global__ void __launch_bounds__(kThreads) channel_absmax_kernel(
 
 __global__ void smooth_factor_kernel(const float *__restrict__ ax, const float *__restrict__ aw,
                                      int64_t K, double alpha, float *__restrict__ s) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (j >= K) return;
     double x = (double)ax[j], w = (double)aw[j];
@@ -295,6 +305,8 @@ __global__ void __launch_bounds__(kThreads) layernorm_quant_kernel(
     float eps, const float *__restrict__ s, int64_t rows, int K4, int tpr,
     float *__restrict__ Y, int8_t *__restrict__ q, float *__restrict__ scale,
     __nv_bfloat16 *__restrict__ op, int32_t *__restrict__ l1, float fixed_scale) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ float red[kThreads / 32];
     const int rpb = kThreads / tpr;
     const int g = threadIdx.x / tpr;
@@ -400,16 +412,16 @@ sq_status launch_quantize_rows(int direction, const float *A, const float *s, in
         int &occ = per_sm[direction][small ? 0 : 1];
         if (!occ) occ = resident_blocks(kern);
         const int64_t grid = std::min<int64_t>(tiles, (int64_t)di.sms * occ);
-        kern<<<(unsigned)grid, kThreads, 0, st>>>(A, s, rows, K4, tpr, q, scale, op, l1,
-                                                  fixed_scale);
+        return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), 0, st, 1, A, s, rows, K4,
+                          tpr, q, scale, op, l1, fixed_scale);
     } else {
         auto kern = direction == kActDynamic ? quantize_rows_loop<kActDynamic>
                     : direction == kWeight       ? quantize_rows_loop<kWeight>
                                                  : quantize_rows_loop<kActStatic>;
         const int64_t grid = std::min<int64_t>(rows, (int64_t)di.sms * 8);
-        kern<<<(unsigned)grid, kThreads, 0, st>>>(A, s, rows, K4, q, scale, op, l1, fixed_scale);
+        return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), 0, st, 1, A, s, rows, K4, q,
+                          scale, op, l1, fixed_scale);
     }
-    return cuda_status(cudaGetLastError());
 }
 
 sq_status launch_layernorm_quant(const float *H, const float *gamma, const float *beta,
@@ -438,9 +450,8 @@ sq_status launch_layernorm_quant(const float *H, const float *gamma, const float
     int &occ = per_sm[static_scale > 0.0f ? 1 : 0][small ? 0 : 1];
     if (!occ) occ = resident_blocks(kern);
     const int64_t grid = std::min<int64_t>(tiles, (int64_t)di.sms * occ);
-    kern<<<(unsigned)grid, kThreads, 0, st>>>(H, gamma, beta, eps, s, rows, K4, tpr, Y, q, scale,
-                                              op, l1, static_scale);
-    return cuda_status(cudaGetLastError());
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), 0, st, 1, H, gamma, beta, eps, s,
+                      rows, K4, tpr, Y, q, scale, op, l1, static_scale);
 }
 
 sq_status launch_act_absmax(const float *A, const float *s, int64_t rows, int64_t K,
@@ -451,8 +462,8 @@ sq_status launch_act_absmax(const float *A, const float *s, int64_t rows, int64_
     const int64_t total4 = rows * (K / 4);
     const int64_t grid = std::max<int64_t>(
         1, std::min<int64_t>((total4 + kThreads - 1) / kThreads, (int64_t)di.sms * 8));
-    act_absmax_kernel<<<(unsigned)grid, kThreads, 0, st>>>(A, s, rows, (int)(K / 4), amax);
-    return cuda_status(cudaGetLastError());
+    return launch_pdl(act_absmax_kernel, dim3((unsigned)grid), dim3(kThreads), 0, st, 1, A, s, rows,
+                      (int)(K / 4), amax);
 }
 
 sq_status launch_channel_absmax(const float *A, int64_t rows, int64_t cols, float *amax,
@@ -466,16 +477,15 @@ sq_status launch_channel_absmax(const float *A, int64_t rows, int64_t cols, floa
     const int64_t rpb = (rows + gy - 1) / gy;
     gy = (rows + rpb - 1) / rpb;
     if (gx > 0x7fffffff) return SQ_ERR_UNSUPPORTED;
-    channel_absmax_kernel<<<dim3((unsigned)gx, (unsigned)gy), kThreads, 0, st>>>(A, rows, cols,
-                                                                                 rpb, amax);
-    return cuda_status(cudaGetLastError());
+    return launch_pdl(channel_absmax_kernel, dim3((unsigned)gx, (unsigned)gy), dim3(kThreads), 0, st,
+                      1, A, rows, cols, rpb, amax);
 }
 
 sq_status launch_smooth_factor(const float *ax, const float *aw, int64_t K, float alpha,
                                float *s, cudaStream_t st) {
     const int64_t grid = (K + kThreads - 1) / kThreads;
-    smooth_factor_kernel<<<(unsigned)grid, kThreads, 0, st>>>(ax, aw, K, (double)alpha, s);
-    return cuda_status(cudaGetLastError());
+    return launch_pdl(smooth_factor_kernel, dim3((unsigned)grid), dim3(kThreads), 0, st, 1, ax, aw,
+                      K, (double)alpha, s);
 }
 
 }  // namespace sq
