@@ -18,8 +18,12 @@
 // int32.  The result equals the int32 dot product for every input.
 //
 // Two kernels share the epilogue code below.  The pair kernel (end of the
-// kernel section) runs every launch with at least 256 rows that is not split
-// over K; the one-CTA kernel runs the rest.
+// kernel section: clusters of two CTAs, tcgen05.mma.cta_group::2, 256 x 256
+// tiles) runs every launch with at least 256 rows that is not split over K;
+// the one-CTA kernel runs the rest, including the split-K schedule (fewer
+// tiles than SMs, K >= 2048, a caller workspace).  Both are launched with
+// programmatic dependent launch: set-up overlaps the previous kernel on the
+// stream, every global-memory access follows griddepcontrol.wait.
 //
 // One-CTA roles (320 threads, one CTA per SM, persistent over 128 x 256 output tiles):
 //   warp 0, lane 0  TMA producer: A [128 x 64] and B [256 x 64] bf16 tiles,
