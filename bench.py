@@ -32,6 +32,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+from smoothquant_w8a8_int8_gb300 import replicas  # noqa: E402
 from smoothquant_w8a8_int8_gb300 import roofline as R  # noqa: E402
 from smoothquant_w8a8_int8_gb300 import workloads as wl  # noqa: E402
 
@@ -182,7 +183,7 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
                       torch.empty(w.M, dtype=torch.float32, device=dev))
     for layer, idx in [(l, i) for l in range(w.layers) for i in range(len(w.linears))]:
         lin = w.linears[idx]
-        seed = wl.gemm_seed(w, layer, idx) + 7 * rank
+        seed = replicas.rank_seed(wl.gemm_seed(w, layer, idx), rank)
         up = layers[-1] if (chained and lin.gelu_input and layers) else None
         if up is not None:
             # FFN-down fed by this layer's FFN-up: its smoothing factor and
@@ -192,7 +193,8 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
                              w.outlier_scale, lin.gelu_input, w.alpha, device=dev)
             calib_x = wl.make_activation(512, up.lin.K, seed + 555, w.outlier_frac,
                                          w.outlier_scale, False, device=dev,
-                                         channel_seed=wl.gemm_seed(w, layer, idx - 1) + 7 * rank)
+                                         channel_seed=replicas.rank_seed(
+                                             wl.gemm_seed(w, layer, idx - 1), rank))
             _, sxc, Xopc = sq.quantize_act(calib_x, up.s, want_q=False)
             y_cal = sq.linear_i8(Xopc, sxc, up.Wop, up.sw, up.bias, None, up.lin.mode)
             s = sq.smooth_factor(sq.channel_absmax(y_cal), sq.channel_absmax(c.W), w.alpha)
@@ -400,8 +402,7 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
         step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(args.steps)]
     clocks = ClockSampler(torch.cuda.current_device())
-    if world > 1:
-        torch.distributed.barrier()
+    replicas.barrier()
     torch.cuda.synchronize()
     clocks.start()
     t0 = torch.cuda.Event(enable_timing=True)
@@ -418,8 +419,7 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
     t1.record()
     torch.cuda.synchronize()
     host_t1 = datetime.datetime.now()
-    if world > 1:
-        torch.distributed.barrier()
+    replicas.barrier()
     clock_info = clocks.stop((host_t0, host_t1))
     elapsed_ms = t0.elapsed_time(t1)
     if flush is not None:
@@ -427,10 +427,7 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
     rc = sq.device_status()
     if rc != 0:
         raise RuntimeError(f"device status after timed run: {sq.status_string(rc)}")
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = replicas.max_over_ranks(elapsed_ms, device="cuda")
 
     # kernel pass: the same K steps again, with CUDA events around every launch
     # on the launching stream.  An event between two kernels leaves the GPU idle
@@ -448,7 +445,7 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
 
     ops_per_step = w.ops()
     ms_per_step = elapsed_ms / args.steps
-    tops = ops_per_step * world / (ms_per_step * 1e-3) / 1e12
+    tops = replicas.whole_job_tops(ops_per_step, world, ms_per_step)
 
     # per-kernel durations from the live events
     q_ms = g_ms = 0.0
@@ -482,21 +479,18 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
         d2h = sum(L.Yhost.numel() * 4 for L in layers)
         pipe.run(specs, xh, yh)
         torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
+        replicas.barrier()
         t_a = time.perf_counter()
         for _ in range(args.e2e_steps):
             pipe.run(specs, xh, yh)
         torch.cuda.synchronize()
         e_ms = (time.perf_counter() - t_a) * 1e3 / args.e2e_steps
-        if world > 1:
-            t = torch.tensor([e_ms], device="cuda")
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = replicas.max_over_ranks(e_ms, device="cuda")
         # the outputs that came back match the device-side results
         torch.cuda.synchronize()
         ok = all(torch.equal(L.Yhost[:64].cuda(), L.Y[:64]) for L in layers[-2:])
-        e2e = {"value": round(ops_per_step * world / (e_ms * 1e-3) / 1e12, 3), "unit": "TOPS",
+        e2e = {"value": round(replicas.whole_job_tops(ops_per_step, world, e_ms), 3),
+               "unit": "TOPS",
                "ms_per_step": round(e_ms, 3), "steps": args.e2e_steps,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "outputs_match_device": bool(ok),
@@ -691,8 +685,7 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank, world, local = replicas.rank_world()
     w = wl.WORKLOADS[args.workload]
     if args.layers is not None:
         w = dataclasses.replace(w, layers=max(1, min(args.layers, w.layers)))
@@ -703,7 +696,6 @@ def main():
         return
 
     if world > 1:
-        local = int(os.environ.get("LOCAL_RANK", rank))
         torch.cuda.set_device(local)
         torch.distributed.init_process_group("nccl")
     else:

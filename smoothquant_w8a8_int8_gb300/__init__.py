@@ -11,7 +11,7 @@ import importlib
 
 from . import roofline, workloads  # noqa: F401
 
-_SUBMODULES = ("alpha_sweep", "binding", "build", "pipeline", "roofline", "workloads")
+_SUBMODULES = ("alpha_sweep", "binding", "build", "pipeline", "replicas", "roofline", "workloads")
 
 
 def __getattr__(name):
