@@ -50,6 +50,7 @@
 // records SQ_ERR_TIMEOUT in a device word, lets its issued copies and MMAs
 // drain, frees its tensor memory and returns.
 #include "common.cuh"
+#include "schedule.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -59,11 +60,9 @@
 namespace sq {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64;  // BK in bf16 elements (128 bytes)
+using namespace sched;  // tile shape, chunking and the work schedules (schedule.cuh)
 constexpr int STAGES = 4;
-constexpr int KB_PER_CHUNK = 16;            // 16 * 64 = 1024 K per exact fp32 chunk
 constexpr int UMMA_K = 16;
-constexpr int NUM_EPI_WARPS = 8;
 constexpr int THREADS = 64 + NUM_EPI_WARPS * 32;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
@@ -309,155 +308,6 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
 }
 
 // ------------------------------------------------------------------ kernel
-
-// Work units of a launch.  Two schedules:
-//
-// Whole tiles (no workspace).  The BM x BN tiles that fill whole waves of the
-// persistent grid are units as they are; when the last, partial wave holds at
-// most half a wave of tiles, each of them is cut into two 128-column halves
-// (MMA N = 128), so that the last round takes half as long.  (Quarters, N = 64,
-// measured slower: the A tile is loaded in full for a quarter of the work.)
-//
-// Split K (a workspace is given).  The K blocks of the last sk_tiles tiles
-// form one range, cut evenly over sk_ctas CTAs (a CTA's share may cover the
-// end of one tile and the start of the next).  A piece of a tile (a K-block
-// range of it) leaves its exact int32 partial sums in the workspace; the CTA
-// whose piece of the tile completes last adds the others' partials to its own
-// and runs the epilogue.  Measured on GB300, the partials' round trip through
-// L2 (about 4 us on the finishing CTA's path) costs more than a split saves
-// unless the tiles are fewer than the SMs and long in K, so the split is used
-// only there: every tile cut into `pieces` <= 4 equal K ranges of at least
-// 1024, one per CTA (small M with a large K: a few tiles would otherwise keep
-// a few SMs busy for the whole K).
-//
-// Tiles are numbered m-fastest, so CTAs working at the same time share B tiles
-// in L2.
-constexpr int kMinSplitKb = 32;  // split K only for K >= 2048 (32 blocks of 64)
-constexpr int kMaxPieces = 4;
-
-struct Schedule {
-    int m_tiles, nkb;
-    int full_items, sub, items;      // whole-tile schedule (halves in the last wave)
-    int dp_tiles, sk_tiles, sk_ctas;  // split-K part; sk_tiles == 0: not used
-    int sk_cnt_tiles;                 // tiles the counter block has room for (2 x grid)
-};
-
-__host__ __device__ inline Schedule make_schedule(int m_tiles, int n_tiles, int nkb, int grid,
-                                                  bool split_k) {
-    Schedule sc;
-    sc.m_tiles = m_tiles;
-    sc.nkb = nkb;
-    const int tiles = m_tiles * n_tiles;
-    const int waves = tiles / grid, rem = tiles - waves * grid;
-    sc.sub = (waves >= 1 && rem > 0 && 2 * rem <= grid) ? 2 : 1;
-    sc.full_items = sc.sub == 1 ? tiles : waves * grid;
-    sc.items = sc.full_items + (tiles - sc.full_items) * sc.sub;
-    sc.dp_tiles = tiles;
-    sc.sk_tiles = 0;
-    sc.sk_ctas = 0;
-    sc.sk_cnt_tiles = 0;
-    if (split_k && waves == 0 && nkb >= kMinSplitKb) {
-        // fewer tiles than SMs and a long K: cut every tile into `pieces`
-        // equal K ranges, one per CTA
-        int pieces = grid / tiles;
-        if (pieces > kMaxPieces) pieces = kMaxPieces;
-        if (pieces >= 2) {
-            sc.sub = 1;
-            sc.sk_tiles = tiles;
-            sc.dp_tiles = 0;
-            sc.sk_ctas = tiles * pieces;
-            sc.sk_cnt_tiles = grid;  // >= tiles
-            sc.full_items = sc.items = 0;
-        }
-    }
-    return sc;
-}
-
-// First K-block index (over the split tiles' concatenated K blocks) of CTA c's share.
-__host__ __device__ inline long long sk_start(const Schedule &sc, int c) {
-    return (long long)c * ((long long)sc.sk_tiles * sc.nkb) / sc.sk_ctas;
-}
-
-// The CTA whose share holds K-block index `it`: the largest c with sk_start(c) <= it.
-__host__ __device__ inline int sk_cta_of(const Schedule &sc, long long it) {
-    const long long total = (long long)sc.sk_tiles * sc.nkb;
-    long long c = (it * sc.sk_ctas + sc.sk_ctas - 1) / total;
-    if (c > sc.sk_ctas - 1) c = sc.sk_ctas - 1;
-    if (sk_start(sc, (int)c) > it) --c;
-    return (int)c;
-}
-
-struct Work {
-    int m0, n0, bn;
-    int kb0, kb1;  // K blocks [kb0, kb1) of the tile
-    int skt;       // split tile index of a piece, -1 for a whole tile
-};
-
-// Walks one CTA's units: its whole-tile items, then the pieces of its share
-// (K-block indices fit in 32 bits: at most 2 x grid tiles of 2081 blocks).
-struct Cursor {
-    int i, it, end;
-};
-
-__device__ __forceinline__ void cursor_init(const Schedule &sc, Cursor &cu) {
-    cu.i = blockIdx.x;
-    cu.it = cu.end = 0;
-    if (sc.sk_tiles > 0 && (int)blockIdx.x < sc.sk_ctas) {
-        cu.it = (int)sk_start(sc, blockIdx.x);
-        cu.end = (int)sk_start(sc, blockIdx.x + 1);
-    }
-}
-
-__device__ __forceinline__ bool next_work(const Schedule &sc, Cursor &cu, Work &w) {
-    if (cu.i < sc.items) {
-        const int i = cu.i;
-        cu.i += gridDim.x;
-        w.kb0 = 0;
-        w.kb1 = sc.nkb;
-        w.skt = -1;
-        if (i < sc.full_items) {
-            w.m0 = (i % sc.m_tiles) * BM;
-            w.n0 = (i / sc.m_tiles) * BN;
-            w.bn = BN;
-        } else {
-            const int j = i - sc.full_items;
-            const int t = sc.full_items + j / sc.sub;
-            w.bn = BN / sc.sub;
-            w.m0 = (t % sc.m_tiles) * BM;
-            w.n0 = (t / sc.m_tiles) * BN + (j % sc.sub) * w.bn;
-        }
-        return true;
-    }
-    if (cu.it >= cu.end) return false;
-    const int r = cu.it / sc.nkb;
-    const int tb = r * sc.nkb;
-    w.kb0 = cu.it - tb;
-    w.kb1 = min(sc.nkb, cu.end - tb);
-    const int t = sc.dp_tiles + r;
-    w.m0 = (t % sc.m_tiles) * BM;
-    w.n0 = (t / sc.m_tiles) * BN;
-    w.bn = BN;
-    // -1: the whole tile lies in this share
-    w.skt = (w.kb0 == 0 && w.kb1 == sc.nkb) ? -1 : r;
-    cu.it = tb + sc.nkb;
-    return true;
-}
-
-// Workspace of the split-K schedule: two counters per (tile, epilogue warp) --
-// pieces that finished their MMAs, pieces whose partials are written -- then,
-// per CTA, two partial slots (the first and the last piece of its share), each
-// NUM_EPI_WARPS sub-blocks of 32 rows x 128 columns of int32.  The counter
-// block has one size for every shape on a device (room for 2 x grid tiles), so
-// that the counters of one launch never fall on another launch's partial slots
-// in a shared workspace.
-constexpr int kSlotWarpBytes = 32 * 128 * 4;
-__host__ __device__ inline long long sk_counter_bytes(const Schedule &sc) {
-    return ((long long)sc.sk_cnt_tiles * NUM_EPI_WARPS * 2 * 4 + 255) / 256 * 256;
-}
-__host__ __device__ inline long long sk_workspace_bytes(const Schedule &sc) {
-    if (sc.sk_tiles == 0) return 0;
-    return sk_counter_bytes(sc) + (long long)sc.sk_ctas * 2 * NUM_EPI_WARPS * kSlotWarpBytes;
-}
 
 struct Smem {
     uint64_t full[STAGES];
@@ -1028,9 +878,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t phase = 0;
             uint32_t issued = 0, fill_parity = 0;  // per-stage bits: loads in flight
             Cursor cu;
-            cursor_init(sched, cu);
+            cursor_init(sched, cu, blockIdx.x);
             Work t;
-            while (next_work(sched, cu, t)) {
+            while (next_work(sched, cu, t, gridDim.x)) {
                 const bool slice = t.bn < BN;
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&S.empty[stage]), phase ^ 1, abort_flag)) goto done_p;
@@ -1059,9 +909,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t phase = 0, tph = 0;  // tph: per-buffer use parity bits
             bool issued_any = false;
             Cursor cu;
-            cursor_init(sched, cu);
+            cursor_init(sched, cu, blockIdx.x);
             Work t;
-            for (int it = 0; next_work(sched, cu, t); ++it) {
+            for (int it = 0; next_work(sched, cu, t, gridDim.x); ++it) {
                 const uint32_t idesc = idesc_for(t.bn);
                 // exact fp32 passes: the unit's K blocks cut at multiples of chunk_kb
                 for (int c = t.kb0 / chunk_kb; c * chunk_kb < t.kb1; ++c) {
@@ -1112,9 +962,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const uint32_t colP = BN;          // int32 partial (multi-chunk shapes)
         Cursor cu;
-        cursor_init(sched, cu);
+        cursor_init(sched, cu, blockIdx.x);
         Work t;
-        for (int it = 0; next_work(sched, cu, t); ++it) {
+        for (int it = 0; next_work(sched, cu, t, gridDim.x); ++it) {
             const int row0 = t.m0 + q * 32;
             const int64_t m = (int64_t)row0 + lane;
             const int nb = t.n0 + half * COLS_PER_WARP;
@@ -1236,41 +1086,6 @@ constexpr int PAIR_SMEM_BYTES = PAIR_RING_BYTES + NUM_EPI_WARPS * STG_BYTES + BA
 __host__ __device__ constexpr uint32_t idesc_pair(int n) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
            ((uint32_t)((2 * BM) >> 4) << 24);
-}
-
-// Work items of the pair kernel: 256 x 256 pair tiles, numbered m-fastest; when
-// the last, partial wave holds at most half the clusters, each of its tiles is
-// cut into two 256 x 128 halves (MMA N = 128, 64 rows of B per CTA).
-struct PairSchedule {
-    int m_pairs, full_items, sub, items;
-};
-
-__host__ __device__ inline PairSchedule make_pair_schedule(int m_pairs, int n_tiles,
-                                                           int clusters) {
-    PairSchedule sc;
-    sc.m_pairs = m_pairs;
-    const int tiles = m_pairs * n_tiles;
-    const int waves = tiles / clusters, rem = tiles - waves * clusters;
-    sc.sub = (waves >= 1 && rem > 0 && 2 * rem <= clusters) ? 2 : 1;
-    sc.full_items = sc.sub == 1 ? tiles : waves * clusters;
-    sc.items = sc.full_items + (tiles - sc.full_items) * sc.sub;
-    return sc;
-}
-
-// item i: pair rows from m0 (256), columns n0.. of width bn (256 or 128)
-__device__ __forceinline__ void pair_item_at(const PairSchedule &sc, int i, int &m0, int &n0,
-                                             int &bn) {
-    if (i < sc.full_items) {
-        m0 = (i % sc.m_pairs) * 2 * BM;
-        n0 = (i / sc.m_pairs) * BN;
-        bn = BN;
-    } else {
-        const int j = i - sc.full_items;
-        const int t = sc.full_items + j / sc.sub;
-        bn = BN / sc.sub;
-        m0 = (t % sc.m_pairs) * 2 * BM;
-        n0 = (t / sc.m_pairs) * BN + (j % sc.sub) * bn;
-    }
 }
 
 struct PairSmem {
@@ -1627,22 +1442,6 @@ bool use_pair(int64_t M, const Schedule &sched) {
 
 }  // namespace
 
-// Schedule of an M x N x K launch on `sms` SMs, and the grid it runs on.
-static Schedule plan(int64_t M, int64_t N, int64_t K, int sms, bool split_k, int *grid) {
-    const int m_tiles = (int)((M + BM - 1) / BM), n_tiles = (int)((N + BN - 1) / BN);
-    const int nkb = (int)((K + BK - 1) / BK);
-    const int tiles = m_tiles * n_tiles;
-    if (split_k) {
-        const Schedule sc = make_schedule(m_tiles, n_tiles, nkb, sms, true);
-        if (sc.sk_tiles > 0) {
-            *grid = sc.dp_tiles > 0 ? sms : sc.sk_ctas;
-            return sc;
-        }
-    }
-    *grid = std::min(tiles, sms);
-    return make_schedule(m_tiles, n_tiles, nkb, *grid, false);
-}
-
 static bool shape_ok(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || N <= 0 || K <= 0 || M > 0x7fffffff || N > 0x7fffffff || K > 0x7fffffff)
         return false;
@@ -1657,7 +1456,7 @@ sq_status gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes
     sq_status rc = device_info(&di);
     if (rc != SQ_OK) return rc;
     int grid;
-    *bytes = (size_t)sk_workspace_bytes(plan(M, N, K, di.sms, true, &grid));
+    *bytes = (size_t)sk_workspace_bytes(plan_launch(M, N, K, di.sms, true, &grid));
     return SQ_OK;
 }
 
@@ -1698,7 +1497,7 @@ sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_
     if ((rc = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wop, N, K, BN, BK)) != SQ_OK)
         return rc;
     int grid;
-    const Schedule sched = plan(M, N, K, di.sms, workspace != nullptr, &grid);
+    const Schedule sched = plan_launch(M, N, K, di.sms, workspace != nullptr, &grid);
     args.sched = sched;
     args.ws_cnt = nullptr;
     args.ws_slots = nullptr;
