@@ -45,6 +45,10 @@ extern "C" sq_status sq_linear_i8_static_ws(const void *Xop, const float *x_scal
                                             const float *bias, const float *residual, int64_t M,
                                             int64_t N, int64_t K, int mode, void *Y,
                                             void *stream) {
+    // empty calls: the argument checks of sq_linear_i8_ws, no launch, no device query
+    if (M == 0 || N == 0)
+        return sq_linear_i8_ws(Xop, x_scale, x_row_l1, Wop, w_scale, w_row_l1, bias, residual, M,
+                               N, K, mode, Y, nullptr, 0, stream);
     size_t need = 0;
     sq_status rc = sq_linear_workspace_bytes(M, N, K, &need);
     if (rc != SQ_OK) return rc;

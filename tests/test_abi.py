@@ -152,3 +152,36 @@ def test_argument_checks_fail_before_any_launch(lib):
     assert f(a, a, a, 1e-5, a, 4, 24, 0.0, None, a, a, None, None, None) == ALIGN     # K % 16
     assert f(a, a, a, 1e-5, a, 4, 8208, 0.0, None, a, a, None, None, None) == UNSUP   # K > 8192
     assert f(None, None, None, 1e-5, None, 0, 32, 0.0, None, None, None, None, None, None) == 0
+
+
+def test_workspace_entry_points_check_arguments_first(lib):
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    INVALID, ALIGN, UNSUP = 1, 2, 3
+    a = _fake(0x10000)
+    wb = lib.sq_linear_workspace_bytes
+    wb.argtypes = [i64, i64, i64, vp]
+    n = ctypes.c_size_t(123)
+    assert wb(8, 8, 32, None) == INVALID
+    assert wb(-1, 8, 32, ctypes.byref(n)) == INVALID
+    assert wb(8, 8, 0, ctypes.byref(n)) == INVALID
+    assert wb(8, 8, 133152, ctypes.byref(n)) == UNSUP
+    assert wb(0, 8, 32, ctypes.byref(n)) == 0 and n.value == 0     # empty: no workspace
+    ws = lib.sq_linear_i8_ws
+    ws.argtypes = [vp] * 8 + [i64, i64, i64, i32, vp, vp, sz, vp]
+    assert ws(None, a, None, a, a, None, a, None, 8, 8, 32, 1, a, a, 1 << 20, None) == INVALID
+    assert ws(a, a, None, a, a, None, a, None, 8, 8, 40, 1, a, a, 1 << 20, None) == ALIGN
+    assert ws(a, a, None, a, a, None, a, None, 8, 8, 32, 1, a, _fake(0x10008), 1 << 20,
+              None) == ALIGN                                           # workspace alignment
+    assert ws(a, a, None, a, a, None, a, None, 0, 8, 32, 1, a, None, 0, None) == 0
+    rq = lib.sq_linear_i8_requant_ws
+    rq.argtypes = [vp] * 8 + [i64, i64, i64, i32, vp, ctypes.c_float, vp, vp, vp, vp, sz, vp]
+    assert rq(a, a, None, a, a, None, a, None, 8, 8, 32, 4, a, 1.0, a, a, None, a, 1 << 20,
+              None) == INVALID                                         # raw int32 mode
+    assert rq(a, a, None, a, a, None, a, None, 8, 8, 32, 1, a, 1.0, a, a, None, _fake(0x10004),
+              1 << 20, None) == ALIGN
+    st = lib.sq_linear_i8_static_ws
+    st.argtypes = [vp] * 8 + [i64, i64, i64, i32, vp, vp]
+    assert st(a, a, None, a, a, None, a, None, 8, 8, 133152, 1, a, None) == UNSUP
+    assert st(a, a, None, a, a, None, a, None, -1, 8, 32, 1, a, None) == INVALID
+    assert st(None, None, None, None, None, None, None, None, 0, 8, 32, 1, None, None) == 0
+    assert st(None, None, None, None, None, None, None, None, 0, 8, 24, 1, None, None) == ALIGN
