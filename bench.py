@@ -504,8 +504,9 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
 
     traffic, traffic_src = kernel_traffic() if args.gemm == "tc" else (None, "not captured")
     gemm_kernel = ("tcgen05.mma kind::f16 (int8 codes as exact bf16, fp32 TMEM chunks of "
-                   "K<=1024 summed in int32)" if args.gemm == "tc"
-                   else "mma.sync m16n8k32 s8 (legacy warp MMA)")
+                   "K<=1024 summed in int32); launches of >= 256 rows on CTA pairs "
+                   "(cta_group::2, 256x256 tiles), smaller ones on single CTAs"
+                   if args.gemm == "tc" else "mma.sync m16n8k32 s8 (legacy warp MMA)")
     result = {
         "metric": METRIC, "value": round(tops, 3), "unit": "TOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -519,6 +520,8 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
                                      "(sq_linear_i8_ws workspace)"
                                      if ws is not None else
                                      "whole tiles (halves when the last wave is short)"),
+                   "launch": "programmatic dependent launch (set-up overlaps the previous "
+                             "kernel; all memory access after griddepcontrol.wait)",
                    "l2": ("inputs larger than L2: every GEMM reads its own activations "
                           f"({sum(M * L.lin.K * 4 for L in layers) / 1e9:.1f} GB per step)"
                           if flush is None else
