@@ -13,7 +13,7 @@ library's kernels; this module only orders copies and launches.
 from __future__ import annotations
 
 import dataclasses
-from typing import List, Optional, Sequence
+from typing import Optional, Sequence
 
 import torch
 

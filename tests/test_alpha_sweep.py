@@ -5,7 +5,6 @@ with outlier channels), evaluated with the CPU oracle; and on the GPU, the
 kernels' error curve against the oracle's."""
 import numpy as np
 import pytest
-import torch
 
 import oracle
 from smoothquant_w8a8_int8_gb300 import alpha_sweep
