@@ -15,10 +15,16 @@
  * Conventions for every entry point:
  *  - All array pointers are DEVICE pointers (cudaMalloc'd or equivalent), owned
  *    by the caller, row-major and densely packed, and must be 16-byte aligned
- *    unless stated otherwise.  The library allocates no device memory.
+ *    unless stated otherwise.  No entry point allocates device memory
+ *    (sq_linear_i8_static_ws uses a static array of the library's module).
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
  *    enqueued asynchronously; no entry point synchronises except
- *    sq_device_status().
+ *    sq_device_status().  Kernels are launched with programmatic dependent
+ *    launch: their set-up may overlap the end of the previous kernel on the
+ *    stream, but every memory access waits for that kernel to complete, so the
+ *    stream's ordering holds for all data, as with an ordinary launch.  The
+ *    calls may be captured into CUDA graphs once each has run once eagerly on
+ *    the device (their one-time set-up is not capturable).
  *  - Arguments are checked on the host before anything is enqueued; a non-OK
  *    status means nothing was launched.  A failed launch returns SQ_ERR_CUDA.
  *    No entry point aborts, traps or throws.
