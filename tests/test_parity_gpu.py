@@ -561,7 +561,8 @@ def test_static_linear_block(sq):
 @pytest.mark.parametrize("mode", [wl.EPI_NONE, wl.EPI_BIAS, wl.EPI_BIAS_GELU,
                                   wl.EPI_BIAS_RESIDUAL])
 @pytest.mark.parametrize("M,N,K", [(77, 136, 1024), (256, 1024, 1024), (300, 4096, 1024),
-                                   (2560, 2304, 512), (130, 200, 2064)])
+                                   (2560, 2304, 512), (130, 200, 2064),
+                                   (2560, 2304, 2064)])  # pair kernel: halves + 3 exact passes
 def test_requant_epilogue_matches_static_quantiser(sq, mode, M, N, K):
     """The requantising epilogue's codes equal the oracle's Smooth-Static
     quantiser applied to the fp32 output the plain epilogue stores (the same
