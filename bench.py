@@ -115,37 +115,49 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.fh.close()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        rows = []
         with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 10:
-                    continue
-                try:
-                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
-                    rows.append((ts, float(parts[2]), float(parts[3]),
-                                 [n for n, v in zip(names, parts[6:10]) if v.lower() == "active"]))
-                except ValueError:
-                    continue
+            lines = f.readlines()
         try:
             os.remove(self.path)
         except OSError:
             pass
-        picked = []
-        if window is not None:
-            lo = window[0] - datetime.timedelta(milliseconds=60)
-            hi = window[1] + datetime.timedelta(milliseconds=60)
-            picked = [r for r in rows if lo <= r[0] <= hi]
-        in_region = bool(picked)
-        if not picked:
-            picked = rows
-        if not picked:
-            return None
-        reasons = sorted({n for r in picked for n in r[3]})
-        return {"sm_mhz": statistics.median(r[1] for r in picked),
-                "sm_max_mhz": max(r[2] for r in picked), "samples": len(picked),
-                "in_timed_region": in_region, "reasons": reasons}
+        return clock_summary(lines, window)
+
+
+CLOCK_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+def clock_summary(lines, window=None):
+    """Summary of nvidia-smi samples (lines of the ClockSampler query, CSV with
+    no header and no units): median SM clock, highest maximum clock, and the
+    throttle reasons seen active, over the samples whose timestamps fall in
+    `window` (a pair of host datetimes around the timed region, widened by one
+    sampling period), else over all samples.  Malformed lines are skipped."""
+    rows = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+            rows.append((ts, float(parts[2]), float(parts[3]),
+                         [n for n, v in zip(CLOCK_REASONS, parts[6:10]) if v.lower() == "active"]))
+        except ValueError:
+            continue
+    picked = []
+    if window is not None:
+        lo = window[0] - datetime.timedelta(milliseconds=60)
+        hi = window[1] + datetime.timedelta(milliseconds=60)
+        picked = [r for r in rows if lo <= r[0] <= hi]
+    in_region = bool(picked)
+    if not picked:
+        picked = rows
+    if not picked:
+        return None
+    reasons = sorted({n for r in picked for n in r[3]})
+    return {"sm_mhz": statistics.median(r[1] for r in picked),
+            "sm_max_mhz": max(r[2] for r in picked), "samples": len(picked),
+            "in_timed_region": in_region, "reasons": reasons}
 
 
 # ------------------------------------------------------------------- our arm
