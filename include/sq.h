@@ -82,6 +82,10 @@ int sq_version(void);
  * Returns 0 for negative sizes. */
 size_t sq_operand_bytes(int64_t rows, int64_t K);
 
+/* Bytes of the packed weight operand of an N x K weight (the Wop buffer of
+ * sq_pack_weight): sq_operand_bytes(N, K). */
+size_t sq_packed_weight_bytes(int64_t N, int64_t K);
+
 /* ---- Smoothing factor (SmoothQuant; alpha per model in Table 15) ---------- */
 
 /* Running channel maxima for the smoothing factor:
@@ -307,6 +311,10 @@ sq_status sq_check_division(uint32_t b_first, uint32_t b_count, uint32_t a_first
  * pipeline wait ran out since the last call (that kernel's output is then
  * incomplete), SQ_ERR_CUDA if the stream reported an error, else SQ_OK. */
 sq_status sq_device_status(void *stream);
+
+/* The same as sq_device_status (the name under which the device error word's
+ * report is also known). */
+sq_status sq_get_device_status(void *stream);
 
 #ifdef __cplusplus
 }

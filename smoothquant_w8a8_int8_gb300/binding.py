@@ -20,12 +20,13 @@ LIB_PATH = os.path.join(_HERE, "libsq_gb300.so")
 SQ_OK, SQ_ERR_INVALID_ARG, SQ_ERR_ALIGNMENT, SQ_ERR_UNSUPPORTED, SQ_ERR_CUDA, SQ_ERR_TIMEOUT = range(6)
 EPI_NONE, EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESIDUAL, EPI_RAW_I32 = range(5)
 
-EXPORTS = ("sq_status_string", "sq_version", "sq_operand_bytes", "sq_channel_absmax",
+EXPORTS = ("sq_status_string", "sq_version", "sq_operand_bytes", "sq_packed_weight_bytes",
+           "sq_channel_absmax",
            "sq_smooth_factor", "sq_pack_weight", "sq_quantize_act", "sq_act_absmax",
            "sq_quantize_act_static", "sq_layernorm_quant", "sq_linear_i8",
            "sq_linear_i8_requant", "sq_linear_workspace_bytes", "sq_linear_i8_ws",
            "sq_linear_i8_requant_ws", "sq_linear_i8_static_ws", "sq_linear_i8_mma_sync",
-           "sq_check_division", "sq_device_status")
+           "sq_check_division", "sq_device_status", "sq_get_device_status")
 
 _lock = threading.Lock()
 _lib = None
@@ -52,6 +53,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                 "sq_status_string": ([i32], ctypes.c_char_p),
                 "sq_version": ([], i32),
                 "sq_operand_bytes": ([i64, i64], ctypes.c_size_t),
+                "sq_packed_weight_bytes": ([i64, i64], ctypes.c_size_t),
                 "sq_channel_absmax": ([vp, i64, i64, vp, vp], i32),
                 "sq_smooth_factor": ([vp, vp, i64, f32, vp, vp], i32),
                 "sq_pack_weight": ([vp, vp, i64, i64, vp, vp, vp, vp, vp], i32),
@@ -74,6 +76,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                 "sq_linear_i8_mma_sync": ([vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp], i32),
                 "sq_check_division": ([ctypes.c_uint32] * 4 + [i32, vp, vp], i32),
                 "sq_device_status": ([vp], i32),
+                "sq_get_device_status": ([vp], i32),
             }
             for name, (args, res) in sig.items():
                 f = getattr(lib, name)
@@ -116,6 +119,10 @@ def _need(t: torch.Tensor, dtype, name: str, shape=None):
 
 def operand_bytes(rows: int, K: int) -> int:
     return int(load().sq_operand_bytes(rows, K))
+
+
+def packed_weight_bytes(N: int, K: int) -> int:
+    return int(load().sq_packed_weight_bytes(N, K))
 
 
 def empty_operand(rows: int, K: int, device="cuda") -> torch.Tensor:
@@ -408,3 +415,8 @@ def check_division(b_first: int, b_count: int, a_first: int, a_count: int,
 def device_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status."""
     return int(load().sq_device_status(_stream(stream)))
+
+
+def get_device_status(stream=None) -> int:
+    """The same as device_status."""
+    return int(load().sq_get_device_status(_stream(stream)))

@@ -155,6 +155,8 @@ size_t sq_operand_bytes(int64_t rows, int64_t K) {
     return (size_t)rows * (size_t)K * sizeof(__nv_bfloat16);
 }
 
+size_t sq_packed_weight_bytes(int64_t N, int64_t K) { return sq_operand_bytes(N, K); }
+
 sq_status sq_channel_absmax(const float *A, int64_t rows, int64_t cols, float *amax,
                             void *stream) {
     if (rows < 0 || cols <= 0) return SQ_ERR_INVALID_ARG;
@@ -321,5 +323,7 @@ sq_status sq_device_status(void *stream) {
     if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return SQ_ERR_CUDA;
     return gemm_tc_take_error(as_stream(stream));
 }
+
+sq_status sq_get_device_status(void *stream) { return sq_device_status(stream); }
 
 }  // extern "C"

@@ -52,6 +52,9 @@ def test_status_strings_and_sizes(lib):
     lib.sq_operand_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
     assert lib.sq_operand_bytes(8192, 1024) == 8192 * 1024 * 2
     assert lib.sq_operand_bytes(-1, 16) == 0
+    lib.sq_packed_weight_bytes.restype = ctypes.c_size_t
+    lib.sq_packed_weight_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
+    assert lib.sq_packed_weight_bytes(4096, 1024) == 4096 * 1024 * 2
     assert lib.sq_version() >> 16 == 1
 
 
