@@ -23,6 +23,9 @@ Parity status per function (what pins each one, see ``tests/test_oracle.py``):
   epilogue         textbook normal-CDF values for GELU, zero-input cases
   layernorm        closed forms (constant row -> beta, alternating +-a -> +-1),
                    scale and shift invariance, zero mean / unit variance
+  attention        closed forms (zero queries -> the mean of the values; two
+                   keys -> logistic weights), near-one-hot limit, token
+                   permutation equivariance, head and sequence independence
 """
 from __future__ import annotations
 
@@ -75,12 +78,13 @@ def _load():
             lib.oracle_act_absmax.argtypes = [p, p, i64, i64, p]
             lib.oracle_quantize_static.argtypes = [p, p, i64, i64, ctypes.c_float, p]
             lib.oracle_layernorm.argtypes = [p, p, p, dbl, i64, i64, p]
+            lib.oracle_attention.argtypes = [p, i64, i64, i64, i64, dbl, p]
             for f in (lib.oracle_channel_absmax, lib.oracle_smooth_factor,
                       lib.oracle_smooth, lib.oracle_quantize_rows,
                       lib.oracle_gemm_i32, lib.oracle_epilogue,
                       lib.oracle_linear_block, lib.oracle_num_threads,
                       lib.oracle_act_absmax, lib.oracle_quantize_static,
-                      lib.oracle_layernorm):
+                      lib.oracle_layernorm, lib.oracle_attention):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -190,6 +194,21 @@ def layernorm(H, gamma, beta, eps=1e-12):
     _check(_load().oracle_layernorm(_ptr(H), _ptr(gamma), _ptr(beta), float(eps), rows, K,
                                     _ptr(y)), "layernorm")
     return y
+
+
+def attention(QKV, B, S, H, D, scale=None):
+    """Encoder self-attention (Table 3's attention beside the linear block):
+    QKV [B*S, 3*H*D] (the fused QKV projection's output: Q | K | V blocks,
+    head h at columns h*D of each) -> O [B*S, H*D], softmax(scale Q K^T) V per
+    sequence and head, scale = 1/sqrt(D) by default, no mask, double, rounded
+    once to fp32."""
+    QKV = _c(QKV, np.float32)
+    assert QKV.shape == (B * S, 3 * H * D)
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    O = np.empty((B * S, H * D), np.float32)
+    _check(_load().oracle_attention(_ptr(QKV), B, S, H, D, float(scale), _ptr(O)), "attention")
+    return O
 
 
 def gemm_i32(xq, wq):

@@ -42,6 +42,7 @@
 #include <math.h>
 #include <stdint.h>
 #include <stddef.h>
+#include <stdlib.h>
 #ifdef _OPENMP
 #include <omp.h>
 #endif
@@ -275,6 +276,61 @@ int oracle_layernorm(const float *H, const float *gamma, const float *beta, doub
                                    (double)beta[j]);
     }
     return ORC_OK;
+}
+
+/* Encoder self-attention of one layer, the part of the encoder beside the
+ * linear block in "Efficient INT8 Inference of Small NLP Models on Server
+ * CPUs with PyTorch Native Stack", Table 3: it reads the fused QKV
+ * projection's output and writes the out-projection's input.
+ *   QKV [B*S][3*H*D] row-major, token-major (sequence b, token i in row
+ *   b*S + i); head h's query in columns h*D.., its key in H*D + h*D.., its
+ *   value in 2*H*D + h*D..;  O [B*S][H*D], head h in columns h*D..
+ *   O[b,i,h,:] = sum_j p_ij V[b,j,h,:],  p_ij = exp(z_ij - max_j z_ij) / sum,
+ *   z_ij = scale * <Q[b,i,h,:], K[b,j,h,:]>
+ * Every token attends to every token of its sequence (no mask).  All in
+ * double, rounded once to fp32. */
+int oracle_attention(const float *QKV, int64_t B, int64_t S, int64_t H, int64_t D,
+                     double scale, float *O)
+{
+    if (!QKV || !O || B < 0 || S <= 0 || H <= 0 || D <= 0) return ORC_ERR_ARG;
+    const int64_t ld = 3 * H * D;
+    int err = ORC_OK;
+    #pragma omp parallel
+    {
+        double *z = (double *)malloc((size_t)S * sizeof(double));
+        if (!z) {
+            #pragma omp atomic write
+            err = ORC_ERR_ARG;
+        }
+        #pragma omp for schedule(static)
+        for (int64_t r = 0; r < B * H * S; ++r) {
+            if (!z) continue;
+            const int64_t b = r / (H * S), h = (r / S) % H, i = r % S;
+            const float *q = QKV + (b * S + i) * ld + h * D;
+            double zmax = -INFINITY;
+            for (int64_t j = 0; j < S; ++j) {
+                const float *k = QKV + (b * S + j) * ld + H * D + h * D;
+                double dot = 0.0;
+                for (int64_t d = 0; d < D; ++d) dot += (double)q[d] * (double)k[d];
+                z[j] = scale * dot;
+                if (z[j] > zmax) zmax = z[j];
+            }
+            double sum = 0.0;
+            for (int64_t j = 0; j < S; ++j) {
+                z[j] = exp(z[j] - zmax);
+                sum += z[j];
+            }
+            float *o = O + (b * S + i) * (H * D) + h * D;
+            for (int64_t d = 0; d < D; ++d) {
+                double acc = 0.0;
+                for (int64_t j = 0; j < S; ++j)
+                    acc += z[j] * (double)QKV[(b * S + j) * ld + 2 * H * D + h * D + d];
+                o[d] = (float)(acc / sum);
+            }
+        }
+        free(z);
+    }
+    return err;
 }
 
 /* Number of OpenMP threads a parallel region of this library uses. */

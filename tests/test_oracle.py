@@ -314,3 +314,84 @@ def test_layernorm_invariances():
     np.testing.assert_array_equal(y4, y)
     ys = oracle.layernorm(h + np.float32(0.75), g, b, eps=0.0)
     np.testing.assert_allclose(ys, y, atol=2e-6)
+
+
+# ------------------------------------------------------------- attention
+
+def _qkv(rng, B, S, H, D, scale=1.0):
+    return (rng.standard_normal((B * S, 3 * H * D)) * scale).astype(np.float32)
+
+
+def _blocks(QKV, B, S, H, D):
+    """(Q, K, V) as [B, H, S, D] views of the fused projection's output."""
+    x = QKV.reshape(B, S, 3, H, D).astype(np.float64)
+    return x[:, :, 0].transpose(0, 2, 1, 3), x[:, :, 1].transpose(0, 2, 1, 3), \
+        x[:, :, 2].transpose(0, 2, 1, 3)
+
+
+def test_attention_zero_queries_average_the_values():
+    """All scores equal: the softmax is uniform and every output row is the
+    mean of the sequence's value rows."""
+    B, S, H, D = 2, 5, 3, 4
+    QKV = _qkv(np.random.default_rng(1), B, S, H, D)
+    QKV[:, : H * D] = 0.0
+    O = oracle.attention(QKV, B, S, H, D).reshape(B, S, H, D)
+    _, _, V = _blocks(QKV, B, S, H, D)
+    mean = V.mean(axis=2)                                  # [B, H, D]
+    for i in range(S):
+        np.testing.assert_allclose(O[:, i], mean.astype(np.float32), rtol=0, atol=2e-7)
+
+
+def test_attention_two_keys_logistic_weights():
+    """Two tokens: p_i1 = 1 / (1 + exp(-(z_i1 - z_i2))), the logistic function
+    of the scaled score difference (a wrong scale, sign or normalisation fails)."""
+    B, S, H, D = 1, 2, 1, 4
+    QKV = _qkv(np.random.default_rng(2), B, S, H, D)
+    Q, K, V = _blocks(QKV, B, S, H, D)
+    O = oracle.attention(QKV, B, S, H, D)
+    scale = 1.0 / np.sqrt(D)                               # 0.5
+    for i in range(S):
+        dz = scale * (Q[0, 0, i] @ K[0, 0, 0] - Q[0, 0, i] @ K[0, 0, 1])
+        p1 = 1.0 / (1.0 + np.exp(-dz))
+        ref = p1 * V[0, 0, 0] + (1.0 - p1) * V[0, 0, 1]
+        np.testing.assert_allclose(O[i], ref, rtol=2e-7, atol=1e-7)
+
+
+def test_attention_near_one_hot():
+    """Orthogonal keys and queries aligned with one key each, at a large
+    scale: each query picks its key's value row (to within e^-40)."""
+    B, S, H, D = 1, 4, 1, 4
+    QKV = np.zeros((B * S, 3 * H * D), np.float32)
+    pick = [2, 0, 3, 1]
+    for j in range(S):
+        QKV[j, H * D + j] = 1.0                            # key j = e_j
+    for i in range(S):
+        QKV[i, pick[i]] = 80.0                             # query i = 80 e_pick(i)
+    QKV[:, 2 * H * D:] = np.random.default_rng(3).standard_normal((S, D)).astype(np.float32)
+    O = oracle.attention(QKV, B, S, H, D)                  # scores 40 apart
+    for i in range(S):
+        np.testing.assert_allclose(O[i], QKV[pick[i], 2 * H * D:], rtol=0, atol=1e-12)
+
+
+def test_attention_token_permutation_equivariance():
+    B, S, H, D = 1, 7, 2, 8
+    rng = np.random.default_rng(4)
+    QKV = _qkv(rng, B, S, H, D)
+    perm = rng.permutation(S)
+    O = oracle.attention(QKV, B, S, H, D)
+    Op = oracle.attention(QKV[perm], B, S, H, D)
+    np.testing.assert_allclose(Op, O[perm], rtol=1e-6, atol=1e-7)
+
+
+def test_attention_heads_and_sequences_are_independent():
+    B, S, H, D = 2, 6, 3, 4
+    rng = np.random.default_rng(5)
+    QKV = _qkv(rng, B, S, H, D)
+    O = oracle.attention(QKV, B, S, H, D).reshape(B, S, H, D)
+    other = QKV.reshape(B, S, 3, H, D).copy()
+    other[:, :, :, 1] += 1.0                               # every input of head 1
+    other[1] *= 3.0                                        # every input of sequence 1
+    O2 = oracle.attention(other.reshape(B * S, -1), B, S, H, D).reshape(B, S, H, D)
+    assert np.array_equal(O2[0, :, 0], O[0, :, 0]) and np.array_equal(O2[0, :, 2], O[0, :, 2])
+    assert not np.array_equal(O2[0, :, 1], O[0, :, 1])
+    assert not np.array_equal(O2[1], O[1])
