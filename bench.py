@@ -217,7 +217,7 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
                                               want_op=(gemm == "tc"), want_l1=True)
             L.Wq, L.sw, L.Wop, L.wl1 = Wq, sw, Wop, wl1
             L.bias, L.residual = c.bias, c.residual
-            L.static_scale = sq.static_scale(sq.act_absmax(y_cal, s).item())
+            L.static_scale = sq.static_scale(sq.act_absmax(y_cal, s))
             L.Y = torch.empty(w.M, lin.N, dtype=torch.float32, device=dev)
             L.Xhost = L.Yhost = None
             L.feeds = None
@@ -263,7 +263,7 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
                 ones = torch.ones(lin.K, dtype=torch.float32, device=dev)
                 _, _, _, calib, _ = sq.layernorm_quant(calib, L.ln[0], L.ln[1], LN_EPS, ones,
                                                        want_q=False, want_y=True)
-            L.static_scale = sq.static_scale(sq.act_absmax(calib, s).item())
+            L.static_scale = sq.static_scale(sq.act_absmax(calib, s))
         L.Y = torch.empty(w.M, lin.N, dtype=torch.float32, device=dev)
         L.Xhost = L.Yhost = None
         L.feeds = L.fed_by = None
@@ -366,7 +366,77 @@ def run_layer(sq, gemm, L, bufs, M, X=None, ev=None, ffn_chain="off", ws=None):
     return True
 
 
-def bench_ours(args, w: wl.Workload, rank: int, world: int):
+def copy_ceiling(h2d_pairs, d2h_pairs, reps: int = 2) -> float:
+    """Milliseconds per step of the e2e leg's copies alone: every host-to-
+    device and device-to-host copy of one step, the two directions on two
+    streams at once (the link's duplex rate on this machine, in this run)."""
+    cur = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(cur)
+    s_in.wait_stream(cur)
+    s_out.wait_stream(cur)
+    for _ in range(reps):
+        with torch.cuda.stream(s_in):
+            for dst, src in h2d_pairs:
+                dst.copy_(src, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            for dst, src in d2h_pairs:
+                dst.copy_(src, non_blocking=True)
+    cur.wait_stream(s_in)
+    cur.wait_stream(s_out)
+    e1.record(cur)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def e2e_leg(args, layers, M, ops_per_step, world):
+    """The block end to end through the public host-buffer API
+    (HostLinearPipeline): K steps timed with CUDA events, every output
+    compared with the device path's, and the same bytes copied with no
+    kernels as the link ceiling of this run."""
+    from smoothquant_w8a8_int8_gb300.pipeline import HostLinearPipeline, LinearLayer
+    pipe = HostLinearPipeline(M, max(L.lin.K for L in layers), max(L.lin.N for L in layers))
+    specs = [LinearLayer(L.s, L.Wop, L.sw, L.lin.mode, L.bias, L.residual, L.wl1,
+                         L.static_scale) for L in layers]
+    xh = [L.Xhost for L in layers]
+    yh = [L.Yhost for L in layers]
+    h2d = sum(L.Xhost.numel() * 4 for L in layers)
+    d2h = sum(L.Yhost.numel() * 4 for L in layers)
+    # the copies alone (both directions at once), on the pipeline's own device slots
+    pairs_in = [(pipe.x_slots[i % 2][: x.numel()].view(x.shape), x) for i, x in enumerate(xh)]
+    pairs_out = [(y, pipe.y_slots[i % 2][: y.numel()].view(y.shape)) for i, y in enumerate(yh)]
+    copy_ms = copy_ceiling(pairs_in, pairs_out)
+    pipe.run(specs, xh, yh)
+    torch.cuda.synchronize()
+    replicas.barrier()
+    cur = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    for _ in range(args.e2e_steps):
+        pipe.run(specs, xh, yh)
+    e1.record(cur)
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    e_ms = replicas.max_over_ranks(e_ms, device="cuda")
+    # every output that came back equals the device path's output
+    ok = all(torch.equal(L.Yhost.cuda(non_blocking=True), L.Y) for L in layers)
+    return {"value": round(replicas.whole_job_tops(ops_per_step, world, e_ms), 3),
+            "unit": "TOPS", "ms_per_step": round(e_ms, 3), "steps": args.e2e_steps,
+            "timing": "CUDA events on the calling stream around K pipeline runs",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "link_gbs": round((h2d + d2h) / (e_ms * 1e-3) / 1e9, 1),
+            "copies_only_ms_per_step": round(copy_ms, 3),
+            "copies_only_gbs": round((h2d + d2h) / (copy_ms * 1e-3) / 1e9, 1),
+            "outputs_match_device": bool(ok),
+            "outputs_checked": "every element of every layer's Y",
+            "path": "pinned host X -> device, sq_quantize_act + sq_linear_i8, Y -> pinned "
+                    "host; copies overlapped with kernels on three streams "
+                    "(smoothquant_w8a8_int8_gb300.pipeline.HostLinearPipeline)"}
+
+
+def bench_ours(args, w: wl.Workload, rank: int, world: int, headline: bool = True):
     from smoothquant_w8a8_int8_gb300 import binding as sq
     sq.load()
     peaks, peak_src = load_peaks()
@@ -376,7 +446,8 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
     if args.ln and args.gemm != "tc":
         raise SystemExit("--ln needs the tcgen05 GEMM (--gemm tc)")
     layers, bufs = setup_workload(w, args.gemm, rank,
-                                  want_host=args.e2e_steps > 0 and not chained and not args.ln,
+                                  want_host=(args.e2e_steps > 0 and not chained and not args.ln
+                                             and headline),
                                   quant=args.quant, ffn_chain=args.ffn_chain, ln=args.ln)
     M = w.M
     n_gemm = len(layers)
@@ -412,10 +483,11 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
         flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device="cuda")
         step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(args.steps)]
-    clocks = ClockSampler(torch.cuda.current_device())
+    clocks = ClockSampler(torch.cuda.current_device()) if headline else None
     replicas.barrier()
     torch.cuda.synchronize()
-    clocks.start()
+    if clocks is not None:
+        clocks.start()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     host_t0 = datetime.datetime.now()
@@ -431,7 +503,7 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
     torch.cuda.synchronize()
     host_t1 = datetime.datetime.now()
     replicas.barrier()
-    clock_info = clocks.stop((host_t0, host_t1))
+    clock_info = clocks.stop((host_t0, host_t1)) if clocks is not None else None
     elapsed_ms = t0.elapsed_time(t1)
     if flush is not None:
         elapsed_ms = sum(a.elapsed_time(b) for a, b in step_ev)
@@ -454,6 +526,24 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
     if rc != 0:
         raise RuntimeError(f"device status after kernel pass: {sq.status_string(rc)}")
 
+    # launch-bound shapes: per-call time over many back-to-back steps (no L2
+    # flush between them: the step's data stays in L2)
+    back_to_back = None
+    if w.M <= 256 and args.back_to_back > 0:
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record()
+        for _ in range(args.back_to_back):
+            step()
+        b1.record()
+        torch.cuda.synchronize()
+        rc = sq.device_status()
+        if rc != 0:
+            raise RuntimeError(f"device status after back-to-back run: {sq.status_string(rc)}")
+        back_to_back = {"steps": args.back_to_back,
+                        "us_per_step": round(b0.elapsed_time(b1) * 1e3 / args.back_to_back, 3),
+                        "note": "quantiser + GEMM per step, launched back to back with no L2 "
+                                "flush (warm L2)"}
+
     ops_per_step = w.ops()
     ms_per_step = elapsed_ms / args.steps
     tops = replicas.whole_job_tops(ops_per_step, world, ms_per_step)
@@ -468,7 +558,11 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
     n_launch = args.steps * n_gemm
     gemm_ops = args.steps * ops_per_step
     gemm_tops = gemm_ops / (g_ms * 1e-3) / 1e12
-    peak_tensor = peaks["bf16_tflops_sustained"]
+    # every GEMM launch of the kernel pass is timed on its own (events on both
+    # sides, an idle GPU at each boundary), tens of microseconds long: the
+    # burst figure is the peak that applies (the sustained one is for kernels
+    # timed inside a seconds-long run)
+    peak_tensor = peaks["bf16_tflops"]
     q_bytes = args.steps * sum(R.quantize_bytes(M, L.lin.K)
                                for L, qd in zip(layers, quantised) if qd)
     n_quant = args.steps * sum(quantised)
@@ -477,40 +571,14 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
 
     # e2e through the public API with host buffers: activations in pinned
     # host memory, copied in, the linear block, Y copied out, inside the timed
-    # region (three streams overlap copies with the kernels)
+    # region (three streams overlap copies with the kernels), timed with CUDA
+    # events on the calling stream
     e2e = None
-    if args.e2e_steps > 0 and not chained and not args.ln:
-        from smoothquant_w8a8_int8_gb300.pipeline import HostLinearPipeline, LinearLayer
-        pipe = HostLinearPipeline(M, max(L.lin.K for L in layers), max(L.lin.N for L in layers))
-        specs = [LinearLayer(L.s, L.Wop, L.sw, L.lin.mode, L.bias, L.residual, L.wl1,
-                             L.static_scale) for L in layers]
-        xh = [L.Xhost for L in layers]
-        yh = [L.Yhost for L in layers]
-        h2d = sum(L.Xhost.numel() * 4 for L in layers)
-        d2h = sum(L.Yhost.numel() * 4 for L in layers)
-        pipe.run(specs, xh, yh)
-        torch.cuda.synchronize()
-        replicas.barrier()
-        t_a = time.perf_counter()
-        for _ in range(args.e2e_steps):
-            pipe.run(specs, xh, yh)
-        torch.cuda.synchronize()
-        e_ms = (time.perf_counter() - t_a) * 1e3 / args.e2e_steps
-        e_ms = replicas.max_over_ranks(e_ms, device="cuda")
-        # the outputs that came back match the device-side results
-        torch.cuda.synchronize()
-        ok = all(torch.equal(L.Yhost[:64].cuda(), L.Y[:64]) for L in layers[-2:])
-        e2e = {"value": round(replicas.whole_job_tops(ops_per_step, world, e_ms), 3),
-               "unit": "TOPS",
-               "ms_per_step": round(e_ms, 3), "steps": args.e2e_steps,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "outputs_match_device": bool(ok),
-               "path": "pinned host X -> device, sq_quantize_act + sq_linear_i8, Y -> pinned "
-                       "host; copies overlapped with kernels on three streams "
-                       "(smoothquant_w8a8_int8_gb300.pipeline.HostLinearPipeline)"}
+    if args.e2e_steps > 0 and not chained and not args.ln and headline:
+        e2e = e2e_leg(args, layers, M, ops_per_step, world)
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and headline:
         cpu = cpu_baseline(w, target_s=args.cpu_seconds)
 
     traffic, traffic_src = kernel_traffic() if args.gemm == "tc" else (None, "not captured")
@@ -561,7 +629,10 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
                      "unit": "TFLOP/s", "frac": round(gemm_tops / peak_tensor, 4),
                      "traffic": traffic,
                      "traffic_source": traffic_src,
-                     "peak_source": f"bf16 dense sustained, {peak_src}",
+                     "peak_source": f"bf16 dense burst, {peak_src} (each launch is timed on "
+                                    f"its own; sustained {peaks['bf16_tflops_sustained']} "
+                                    f"gives frac "
+                                    f"{gemm_tops / peaks['bf16_tflops_sustained']:.4f})",
                      "avg_launch_us": round(g_ms * 1e3 / n_launch, 2),
                      "algorithmic_bytes_per_step": g_bytes // args.steps},
         "quantiser_roofline": {"bound": "hbm", "achieved": round(q_gbs, 1),
@@ -573,6 +644,7 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int):
         "kernel_ms_per_step": {"quantize": round(q_ms / args.steps, 4),
                                "gemm": round(g_ms / args.steps, 4)},
         "gpu_launches": n_gemm * args.steps + n_quant,
+        "back_to_back": back_to_back,
         "clocks": clock_info,
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -667,6 +739,27 @@ def bench_reference(args, w: wl.Workload):
                     "d2h_bytes_per_step": 0}}
 
 
+def other_configs(args, headline: wl.Workload, rank: int, world: int):
+    """Every other workload, measured the same way (its own setup, warm-up,
+    timed steps and kernel pass) after the headline one: a compact summary
+    each.  The batch-1 single linears (M = 256) are launch-bound: they also
+    report the per-step time of many back-to-back steps."""
+    out = {}
+    sub = argparse.Namespace(**vars(args))
+    sub.e2e_steps = 0
+    for name in wl.WORKLOAD_ORDER:
+        if name == headline.name:
+            continue
+        r = bench_ours(sub, wl.WORKLOADS[name], rank, world, headline=False)
+        out[name] = {k: r[k] for k in ("value", "unit", "ms_per_step", "roofline",
+                                       "quantiser_roofline", "kernel_ms_per_step",
+                                       "back_to_back")}
+        out[name]["l2"] = r["config"]["l2"]
+        out[name]["gemm_schedule"] = r["config"]["gemm_schedule"]
+        torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -689,10 +782,15 @@ def main():
     ap.add_argument("--ln", action="store_true",
                     help="the QKV and FFN-up inputs are pre-LayerNorm hidden states: their "
                          "quantiser is the fused LayerNorm + quantiser")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-step-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--back-to-back", type=int, default=1000,
+                    help="steps launched back to back for the per-call time of the M = 256 "
+                         "workloads")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="measure only the chosen workload (no sub-results for the others)")
     ap.add_argument("--layers", type=int, default=None,
                     help="run only the first N layers (small cases for profiling)")
     args = ap.parse_args()
@@ -715,6 +813,8 @@ def main():
     else:
         torch.cuda.set_device(0)
     res = bench_ours(args, w, rank, world)
+    if not args.no_configs and args.layers is None:
+        res["configs"] = other_configs(args, w, rank, world)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

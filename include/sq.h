@@ -33,6 +33,9 @@
  *    the pointers (which may be NULL) and without launching.  K must be a
  *    positive multiple of 16.
  *  - Inputs must be finite; results for NaN or Inf inputs are unspecified.
+ *  - Per-device state (function attributes, cluster occupancy, the static
+ *    scratch's address) is set up on a device's first call and kept: a
+ *    cudaDeviceReset while the library is loaded is not supported.
  */
 #ifndef SQ_GB300_H
 #define SQ_GB300_H
@@ -140,10 +143,18 @@ sq_status sq_quantize_act(const float *X, const float *s, int64_t M, int64_t K, 
  *   *amax = max(*amax, max_{m,j} |X[m][j] / s[j]|)     (IEEE fp32 division)
  * X fp32 [M][K], s fp32 [K]; amax one float (4-byte aligned), initialised by
  * the caller (0 for a fresh statistic) and accumulated over calibration
- * batches.  The static scale is then fl32(amax / 127) (1 if amax is 0),
- * computed by the caller in fp32. */
+ * batches.  The static scale then comes from sq_static_scale. */
 sq_status sq_act_absmax(const float *X, const float *s, int64_t M, int64_t K, float *amax,
                         void *stream);
+
+/* Smooth-Static per-tensor scale from the calibration statistic:
+ *   *scale = fl32(*amax / 127)   (IEEE fp32 division; 1 if *amax is 0),
+ * the same rule as the dynamic per-token scale applied to the whole
+ * calibration set.  amax and scale: one float each in device memory, 4-byte
+ * aligned (they may be the same float).  The result is the `scale` argument
+ * of sq_quantize_act_static / sq_linear_i8_requant (read it back once,
+ * offline). */
+sq_status sq_static_scale(const float *amax, float *scale, void *stream);
 
 /* Smooth-Static quantisation with one per-tensor scale `scale` (> 0, finite):
  *   Xq[m][j] = clamp(round_half_even(fl(fl(X[m][j] / s[j]) / scale)), -127, 127)
@@ -259,19 +270,35 @@ sq_status sq_linear_i8_requant_ws(const void *Xop, const float *x_scale,
  * SQ_STATIC_WORKSPACE_BYTES (40 MiB; a GPU of up to 159 SMs), zero-filled at
  * module load.  Its address is looked up once per device (cudaGetSymbolAddress)
  * on that device's first call; make that first call outside any stream capture,
- * after which a call only launches.  Nothing is allocated: a shape whose split
- * needs more than the array (sq_linear_workspace_bytes) returns
- * SQ_ERR_UNSUPPORTED.  The scratch is one per device and process: calls whose
- * launches may overlap (different streams without ordering, several host
- * threads) race on it and must be serialised by the caller.  Outputs, other
- * arguments and statuses as sq_linear_i8_ws; after SQ_ERR_TIMEOUT the scratch's
- * counters may be left non-zero, so the library must be reloaded. */
+ * after which a call only launches.  The address is kept for the life of the
+ * process: a cudaDeviceReset while the library is loaded is not supported by
+ * this entry point.  Nothing is allocated: a shape whose split needs more than
+ * the array (sq_linear_workspace_bytes) returns SQ_ERR_UNSUPPORTED.  The
+ * scratch is one per device and process: calls whose launches may overlap
+ * (different streams without ordering, several host threads) race on it and
+ * must be serialised by the caller.  Arguments are checked first, exactly as
+ * in sq_linear_i8_ws (same statuses); outputs as sq_linear_i8_ws.  A launch
+ * whose bounded wait ran out (SQ_ERR_TIMEOUT) may leave split-K counters in the
+ * scratch: sq_device_status clears them when it reports the timeout, and
+ * sq_static_workspace_reset clears them on demand; a static call made before
+ * either may compute wrong outputs. */
 #define SQ_STATIC_WORKSPACE_BYTES (40u * 1024u * 1024u)
 sq_status sq_linear_i8_static_ws(const void *Xop, const float *x_scale,
                                  const int32_t *x_row_l1, const void *Wop, const float *w_scale,
                                  const int32_t *w_row_l1, const float *bias,
                                  const float *residual, int64_t M, int64_t N, int64_t K,
                                  int mode, void *Y, void *stream);
+
+/* Zero-fills the split-K counters of the static scratch on the current device
+ * (cudaMemsetAsync on `stream`, then a synchronisation; nothing allocated).
+ * SQ_OK without doing anything if the scratch has not been used there. */
+sq_status sq_static_workspace_reset(void *stream);
+
+/* The static scratch of the current device: *ptr = its device address (looked
+ * up as by sq_linear_i8_static_ws), *bytes = SQ_STATIC_WORKSPACE_BYTES.  For
+ * inspection and tests; the library's next static call assumes the counter
+ * block at its start is zero. */
+sq_status sq_static_workspace(void **ptr, size_t *bytes);
 
 /* The same GEMM + epilogue on the legacy warp-level integer MMA path
  * (mma.sync m16n8k32 s8 x s8 -> s32), reading int8 codes directly:

@@ -57,7 +57,7 @@ def gpu_error(X: torch.Tensor, W: torch.Tensor, alpha: float, quant: str = "dyna
     s = sq.smooth_factor(sq.channel_absmax(Xc), sq.channel_absmax(W), alpha)
     _, sw, Wop = sq.pack_weight(W, s, want_q=False)
     if quant == "static":
-        scale = sq.static_scale(sq.act_absmax(Xc, s).item())
+        scale = sq.static_scale(sq.act_absmax(Xc, s))
         _, sx, Xop = sq.quantize_act_static(X, s, scale, want_q=False)
     elif quant == "dynamic":
         _, sx, Xop = sq.quantize_act(X, s, want_q=False)

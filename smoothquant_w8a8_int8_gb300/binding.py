@@ -23,9 +23,10 @@ EPI_NONE, EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESIDUAL, EPI_RAW_I32 = range(5)
 EXPORTS = ("sq_status_string", "sq_version", "sq_operand_bytes", "sq_packed_weight_bytes",
            "sq_channel_absmax",
            "sq_smooth_factor", "sq_pack_weight", "sq_quantize_act", "sq_act_absmax",
-           "sq_quantize_act_static", "sq_layernorm_quant", "sq_linear_i8",
+           "sq_static_scale", "sq_quantize_act_static", "sq_layernorm_quant", "sq_linear_i8",
            "sq_linear_i8_requant", "sq_linear_workspace_bytes", "sq_linear_i8_ws",
-           "sq_linear_i8_requant_ws", "sq_linear_i8_static_ws", "sq_linear_i8_mma_sync",
+           "sq_linear_i8_requant_ws", "sq_linear_i8_static_ws", "sq_static_workspace_reset",
+           "sq_static_workspace", "sq_linear_i8_mma_sync",
            "sq_check_division", "sq_device_status", "sq_get_device_status")
 
 _lock = threading.Lock()
@@ -59,6 +60,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                 "sq_pack_weight": ([vp, vp, i64, i64, vp, vp, vp, vp, vp], i32),
                 "sq_quantize_act": ([vp, vp, i64, i64, vp, vp, vp, vp, vp], i32),
                 "sq_act_absmax": ([vp, vp, i64, i64, vp, vp], i32),
+                "sq_static_scale": ([vp, vp, vp], i32),
                 "sq_quantize_act_static": ([vp, vp, i64, i64, f32, vp, vp, vp, vp, vp], i32),
                 "sq_layernorm_quant": ([vp, vp, vp, f32, vp, i64, i64, f32, vp, vp, vp, vp, vp,
                                         vp], i32),
@@ -73,6 +75,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                              vp, f32, vp, vp, vp, vp, ctypes.c_size_t, vp], i32),
                 "sq_linear_i8_static_ws": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp,
                                             vp], i32),
+                "sq_static_workspace_reset": ([vp], i32),
+                "sq_static_workspace": ([ctypes.POINTER(vp), ctypes.POINTER(ctypes.c_size_t)], i32),
                 "sq_linear_i8_mma_sync": ([vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp], i32),
                 "sq_check_division": ([ctypes.c_uint32] * 4 + [i32, vp, vp], i32),
                 "sq_device_status": ([vp], i32),
@@ -202,11 +206,14 @@ def act_absmax(X: torch.Tensor, s: torch.Tensor, amax: Optional[torch.Tensor] = 
     return amax
 
 
-def static_scale(amax: float) -> float:
-    """The per-tensor static scale fl32(amax / 127) (1 for a zero maximum)."""
-    import numpy as np
-    a = np.float32(amax)
-    return float(np.float32(1.0) if a == 0 else np.float32(a / np.float32(127.0)))
+def static_scale(amax: torch.Tensor, stream=None) -> float:
+    """The per-tensor static scale the library computes from the calibration
+    statistic `amax` (one float on the device, from act_absmax), read back
+    once (offline)."""
+    _need(amax, torch.float32, "amax", (1,))
+    out = torch.empty(1, dtype=torch.float32, device=amax.device)
+    _check(load().sq_static_scale(_p(amax), _p(out), _stream(stream)), "sq_static_scale")
+    return float(out.item())
 
 
 def quantize_act_static(X: torch.Tensor, s: torch.Tensor, scale: float, want_q: bool = True,
@@ -359,6 +366,18 @@ def linear_i8_static_ws(Xop, x_scale, Wop, w_scale, bias=None, residual=None, mo
                                          _p(w_l1), _p(bias), _p(residual), M, N, K, int(mode),
                                          _p(out), _stream(stream)), "sq_linear_i8_static_ws")
     return out
+
+
+def static_workspace_reset(stream=None) -> None:
+    """Zero-fill the static scratch's split-K counters on the current device."""
+    _check(load().sq_static_workspace_reset(_stream(stream)), "sq_static_workspace_reset")
+
+
+def static_workspace():
+    """(device address, bytes) of the static scratch on the current device."""
+    p, n = ctypes.c_void_p(), ctypes.c_size_t()
+    _check(load().sq_static_workspace(ctypes.byref(p), ctypes.byref(n)), "sq_static_workspace")
+    return int(p.value), int(n.value)
 
 
 def linear_i8_requant_ws(Xop, x_scale, Wop, w_scale, bias, residual, mode, s_next,

@@ -81,15 +81,36 @@ sq_status check_quant_args(const float *A, const float *s, int64_t rows, int64_t
     return SQ_OK;
 }
 
-sq_status linear_impl(const void *Xop, const float *x_scale, const int32_t *x_row_l1,
-                      const void *Wop, const float *w_scale, const int32_t *w_row_l1,
-                      const float *bias, const float *residual, int64_t M, int64_t N, int64_t K,
-                      int mode, void *Y, void *workspace, size_t workspace_bytes, void *stream) {
+}  // namespace
+
+namespace sq {
+
+sq_status validate_linear(const void *Xop, const float *x_scale, const int32_t *x_row_l1,
+                          const void *Wop, const float *w_scale, const int32_t *w_row_l1,
+                          const float *bias, const float *residual, int64_t M, int64_t N,
+                          int64_t K, int mode, const void *Y) {
     sq_status rc = check_linear_args(Xop, x_scale, Wop, w_scale, bias, residual, M, N, K, mode, Y);
     if (rc != SQ_OK) return rc;
     if (M == 0 || N == 0) return SQ_OK;
     if ((x_row_l1 && !aligned4(x_row_l1)) || (w_row_l1 && !aligned4(w_row_l1)))
         return SQ_ERR_ALIGNMENT;
+    return SQ_OK;
+}
+
+sq_status require_gb300() { return require_sm103(); }
+
+}  // namespace sq
+
+namespace {
+
+sq_status linear_impl(const void *Xop, const float *x_scale, const int32_t *x_row_l1,
+                      const void *Wop, const float *w_scale, const int32_t *w_row_l1,
+                      const float *bias, const float *residual, int64_t M, int64_t N, int64_t K,
+                      int mode, void *Y, void *workspace, size_t workspace_bytes, void *stream) {
+    sq_status rc = validate_linear(Xop, x_scale, x_row_l1, Wop, w_scale, w_row_l1, bias, residual,
+                                   M, N, K, mode, Y);
+    if (rc != SQ_OK) return rc;
+    if (M == 0 || N == 0) return SQ_OK;
     if (workspace && !aligned16(workspace)) return SQ_ERR_ALIGNMENT;
     if ((rc = require_sm103()) != SQ_OK) return rc;
     return launch_gemm_tc(static_cast<const __nv_bfloat16 *>(Xop), x_scale, x_row_l1,
@@ -212,6 +233,14 @@ sq_status sq_act_absmax(const float *X, const float *s, int64_t M, int64_t K, fl
     return launch_act_absmax(X, s, M, K, amax, as_stream(stream));
 }
 
+sq_status sq_static_scale(const float *amax, float *scale, void *stream) {
+    if (!amax || !scale) return SQ_ERR_INVALID_ARG;
+    if (!aligned4(amax) || !aligned4(scale)) return SQ_ERR_ALIGNMENT;
+    sq_status rc = require_sm103();
+    if (rc != SQ_OK) return rc;
+    return launch_static_scale(amax, scale, as_stream(stream));
+}
+
 sq_status sq_quantize_act_static(const float *X, const float *s, int64_t M, int64_t K,
                                  float scale, int8_t *Xq, float *x_scale, void *Xop,
                                  int32_t *x_row_l1, void *stream) {
@@ -321,7 +350,14 @@ sq_status sq_check_division(uint32_t b_first, uint32_t b_count, uint32_t a_first
 
 sq_status sq_device_status(void *stream) {
     if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return SQ_ERR_CUDA;
-    return gemm_tc_take_error(as_stream(stream));
+    const sq_status rc = gemm_tc_take_error(as_stream(stream));
+    if (rc == SQ_ERR_TIMEOUT) {
+        // a split-K launch that gave up may have left counters in the static
+        // scratch: clear them before the next sq_linear_i8_static_ws call
+        const sq_status r2 = static_ws_reset_counters(as_stream(stream));
+        if (r2 != SQ_OK) return r2;
+    }
+    return rc;
 }
 
 sq_status sq_get_device_status(void *stream) { return sq_device_status(stream); }

@@ -128,6 +128,7 @@ sq_status launch_layernorm_quant(const float *H, const float *gamma, const float
                                  __nv_bfloat16 *op, int32_t *l1, cudaStream_t st);
 sq_status launch_act_absmax(const float *A, const float *s, int64_t rows, int64_t K,
                             float *amax, cudaStream_t st);
+sq_status launch_static_scale(const float *amax, float *scale, cudaStream_t st);
 sq_status launch_gemm_mma_sync(const int8_t *Xq, const float *sx, const int8_t *Wq,
                                const float *sw, const float *bias, const float *residual,
                                int64_t M, int64_t N, int64_t K, int mode, void *Y,
@@ -143,6 +144,18 @@ sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_
 sq_status gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes);
 // Reads and clears the tcgen05 GEMM's device error word (synchronous).
 sq_status gemm_tc_take_error(cudaStream_t st);
+// The host-side argument checks of sq_linear_i8 / sq_linear_i8_ws (everything
+// but the workspace and the device): SQ_OK for a valid call, empty calls
+// included.  require_gb300: SQ_ERR_UNSUPPORTED unless the current device is
+// an sm_103 GPU.
+sq_status validate_linear(const void *Xop, const float *x_scale, const int32_t *x_row_l1,
+                          const void *Wop, const float *w_scale, const int32_t *w_row_l1,
+                          const float *bias, const float *residual, int64_t M, int64_t N,
+                          int64_t K, int mode, const void *Y);
+sq_status require_gb300();
+// Zero-fills the split-K counter block of the static scratch on the current
+// device, if its address has been looked up there (no allocation; synchronous).
+sq_status static_ws_reset_counters(cudaStream_t st);
 
 // fp32 epilogue shared by both GEMM paths: d = acc * sx * sw, then the mode.
 __device__ __forceinline__ float epilogue_value(int32_t acc, float sx, float sw, float b,

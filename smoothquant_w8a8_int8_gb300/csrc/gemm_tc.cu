@@ -1359,18 +1359,45 @@ sq_status make_map(CUtensorMap *map, CUtensorMapDataType dt, int esize, const vo
     return r == CUDA_SUCCESS ? SQ_OK : SQ_ERR_CUDA;
 }
 
+// One-time set-up of a kernel on each device (its dynamic shared-memory
+// attribute and, for the pair kernel, how many clusters fit at once), done
+// under a lock so that host threads launching at once see it complete.
+constexpr int kMaxDevices = 64;  // device_info rejects higher ordinals
+struct KernelSetup {
+    std::mutex mu;
+    bool done[kMaxDevices] = {};
+    int clusters[kMaxDevices] = {};
+};
+
+template <typename Kern>
+sq_status setup_kernel(KernelSetup &ks, Kern kern, int smem_bytes, int device,
+                       const cudaLaunchConfig_t *pair_cfg, int *clusters) {
+    if (device < 0 || device >= kMaxDevices) return SQ_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(ks.mu);
+    if (!ks.done[device]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_bytes) != cudaSuccess)
+            return SQ_ERR_CUDA;
+        if (pair_cfg) {
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, pair_cfg) != cudaSuccess || n < 1)
+                return SQ_ERR_CUDA;
+            ks.clusters[device] = n;
+        }
+        ks.done[device] = true;
+    }
+    if (clusters) *clusters = ks.clusters[device];
+    return SQ_OK;
+}
+
 template <int MODE, bool QUANT>
 sq_status launch_kernel(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tbs,
                         const CUtensorMap &ty, const EpiArgs &args, int K, int grid, int device,
                         cudaStream_t st) {
-    static int attr_dev = -1;
-    if (attr_dev != device) {
-        if (cudaFuncSetAttribute(gemm_tc_kernel<MODE, QUANT>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES) != cudaSuccess)
-            return SQ_ERR_CUDA;
-        attr_dev = device;
-    }
+    static KernelSetup ks;
+    sq_status rc = setup_kernel(ks, gemm_tc_kernel<MODE, QUANT>, SMEM_BYTES, device, nullptr,
+                                nullptr);
+    if (rc != SQ_OK) return rc;
     return launch_pdl(gemm_tc_kernel<MODE, QUANT>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, 1, ta,
                       tb, tbs, ty, args, K);
 }
@@ -1389,8 +1416,7 @@ template <int MODE, bool QUANT>
 sq_status launch_pair_kernel(const CUtensorMap &ta, const CUtensorMap &tbp, const CUtensorMap &tbq,
                              const CUtensorMap &ty, const EpiArgs &args, int K, int pair_tiles,
                              int device, cudaStream_t st) {
-    static int attr_dev = -1;
-    static int max_clusters = 0;
+    static KernelSetup ks;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
@@ -1404,20 +1430,11 @@ sq_status launch_pair_kernel(const CUtensorMap &ta, const CUtensorMap &tbp, cons
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;  // the occupancy query: cluster shape only
-    if (attr_dev != device) {
-        if (cudaFuncSetAttribute(gemm_tc_pair_kernel<MODE, QUANT>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 PAIR_SMEM_BYTES) != cudaSuccess)
-            return SQ_ERR_CUDA;
-        cfg.gridDim = dim3(2, 1, 1);
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_pair_kernel<MODE, QUANT>, &cfg) !=
-                cudaSuccess ||
-            n < 1)
-            return SQ_ERR_CUDA;
-        max_clusters = n;
-        attr_dev = device;
-    }
+    cfg.gridDim = dim3(2, 1, 1);
+    int max_clusters = 0;
+    sq_status rc = setup_kernel(ks, gemm_tc_pair_kernel<MODE, QUANT>, PAIR_SMEM_BYTES, device,
+                                &cfg, &max_clusters);
+    if (rc != SQ_OK) return rc;
     const int clusters = std::min(pair_tiles, max_clusters);
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
     cfg.numAttrs = 2;  // the launch: cluster shape and programmatic serialisation

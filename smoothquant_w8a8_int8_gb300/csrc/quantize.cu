@@ -256,6 +256,15 @@ __global__ void __launch_bounds__(kThreads) act_absmax_kernel(const float *__res
     if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<int *>(amax), __float_as_int(m));
 }
 
+// Smooth-Static per-tensor scale from the calibrated maximum: fl32(amax / 127)
+// (IEEE division), 1 for a zero maximum.
+__global__ void static_scale_kernel(const float *__restrict__ amax, float *__restrict__ scale) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const float a = *amax;
+    *scale = a == 0.0f ? 1.0f : __fdiv_rn(a, 127.0f);
+}
+
 // Column maxima, merged into amax with an integer atomicMax (the bit patterns
 // of non-negative floats order like the floats).
 __global__ void __launch_bounds__(kThreads) channel_absmax_kernel(
@@ -464,6 +473,10 @@ sq_status launch_act_absmax(const float *A, const float *s, int64_t rows, int64_
         1, std::min<int64_t>((total4 + kThreads - 1) / kThreads, (int64_t)di.sms * 8));
     return launch_pdl(act_absmax_kernel, dim3((unsigned)grid), dim3(kThreads), 0, st, 1, A, s, rows,
                       (int)(K / 4), amax);
+}
+
+sq_status launch_static_scale(const float *amax, float *scale, cudaStream_t st) {
+    return launch_pdl(static_scale_kernel, dim3(1), dim3(1), 0, st, 1, amax, scale);
 }
 
 sq_status launch_channel_absmax(const float *A, int64_t rows, int64_t cols, float *amax,

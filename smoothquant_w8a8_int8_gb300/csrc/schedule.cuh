@@ -164,6 +164,15 @@ __host__ __device__ inline long long sk_workspace_bytes(const Schedule &sc) {
     if (sc.sk_tiles == 0) return 0;
     return sk_counter_bytes(sc) + (long long)sc.sk_ctas * 2 * NUM_EPI_WARPS * kSlotWarpBytes;
 }
+// The counter block on a GPU of `sms` SMs (one size for every split shape there).
+__host__ __device__ inline long long sk_counter_bytes_on(int sms) {
+    Schedule sc{};
+    sc.sk_cnt_tiles = sms;
+    return sk_counter_bytes(sc);
+}
+// Whether a launch that needs `need` workspace bytes runs on a fixed scratch
+// of `capacity` bytes (the static scratch of sq_linear_i8_static_ws).
+inline bool fits_scratch(long long need, long long capacity) { return need <= capacity; }
 
 // Work items of the pair kernel: 256 x 256 pair tiles, numbered m-fastest; when
 // the last, partial wave holds at most half the clusters, each of its tiles is

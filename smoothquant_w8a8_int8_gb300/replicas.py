@@ -13,7 +13,11 @@ from typing import Tuple
 
 import torch
 
-SEED_STRIDE = 7  # per-rank offset of every input seed
+# Per-rank offset of every input seed.  A workload's per-GEMM seeds span less
+# than a thousand values and every seed derived from one (weights, bias,
+# residual, calibration and LayerNorm draws) adds at most 1,299,709, so a
+# stride of 2^21 keeps the seed sets of any number of ranks disjoint.
+SEED_STRIDE = 1 << 21
 
 
 def rank_world() -> Tuple[int, int, int]:
@@ -25,7 +29,8 @@ def rank_world() -> Tuple[int, int, int]:
 
 
 def rank_seed(seed: int, rank: int) -> int:
-    """The seed of one input on `rank`: distinct shards, reproducible per rank."""
+    """The seed of one input on `rank`: disjoint from every other rank's seeds
+    (and from the seeds derived from them), reproducible per rank."""
     return seed + SEED_STRIDE * rank
 
 

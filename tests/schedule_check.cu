@@ -116,7 +116,44 @@ static void check_pair(long long M, long long N, int clusters) {
     ++g_checked;
 }
 
+// The static scratch of sq_linear_i8_static_ws (SQ_STATIC_WORKSPACE_BYTES,
+// 40 MiB) holds the split-K workspace of every shape on a GPU of up to 159 SMs;
+// on larger GPUs some shapes need more, and fits_scratch rejects them (the
+// entry point then returns SQ_ERR_UNSUPPORTED without launching).
+static void check_static_scratch() {
+    const long long cap = 40ll * 1024 * 1024;
+    const long long Ms[] = {1, 128, 256, 512, 1000, 2048, 4096};
+    const long long Ns[] = {1, 256, 512, 1024, 4096};
+    const long long Ks[] = {2048, 4096, 8192};
+    for (int sms : {2, 148, 152, 159, 160, 200, 256}) {
+        long long worst = 0;
+        for (long long M : Ms)
+            for (long long N : Ns)
+                for (long long K : Ks) {
+                    int grid = 0;
+                    const long long need = sk_workspace_bytes(plan_launch(M, N, K, sms, true, &grid));
+                    if (need > worst) worst = need;
+                    CHECK(fits_scratch(need, cap) == (need <= cap), "fits_scratch(%lld)", need);
+                }
+        // the largest split uses every SM: sms / 4 tiles of 128 x 256, four pieces each
+        if (sms % 4 == 0) {
+            int grid = 0;
+            const Schedule sc = plan_launch(128ll * (sms / 4), 256, 4096, sms, true, &grid);
+            CHECK(sc.sk_ctas == sms, "sms %d: %d split CTAs", sms, sc.sk_ctas);
+            const long long need = sk_workspace_bytes(sc);
+            if (need > worst) worst = need;
+        }
+        if (sms <= 159) CHECK(fits_scratch(worst, cap), "sms %d: worst split %lld > %lld", sms, worst, cap);
+        if (sms >= 160) CHECK(!fits_scratch(worst, cap), "sms %d: every split fits (%lld)", sms, worst);
+        // the counter block is one size per device, at the workspace's start
+        CHECK(sk_counter_bytes_on(sms) % 256 == 0 && sk_counter_bytes_on(sms) >= sms * 64ll,
+              "counter block on %d SMs", sms);
+        ++g_checked;
+    }
+}
+
 int main() {
+    check_static_scratch();
     const long long Ms[] = {1, 127, 128, 129, 255, 256, 300, 1000, 2560, 8192};
     const long long Ns[] = {1, 255, 256, 257, 1000, 1024, 2304, 3072, 4096};
     const long long Ks[] = {16, 1024, 1040, 2048, 2080, 4096, 8192};

@@ -110,6 +110,10 @@ def test_argument_checks_fail_before_any_launch(lib):
     assert lib.sq_act_absmax(None, a, 4, 32, a, None) == INVALID
     assert lib.sq_act_absmax(a, a, 4, 24, a, None) == ALIGN
     assert lib.sq_act_absmax(None, None, 0, 32, None, None) == 0
+    lib.sq_static_scale.argtypes = [vp, vp, vp]
+    assert lib.sq_static_scale(None, a, None) == INVALID
+    assert lib.sq_static_scale(a, None, None) == INVALID
+    assert lib.sq_static_scale(_fake(0x10002), a, None) == ALIGN
     assert lib.sq_quantize_act_static(a, a, 4, 32, 0.0, a, a, None, None, None) == INVALID
     assert lib.sq_quantize_act_static(a, a, 4, 32, -1.0, a, a, None, None, None) == INVALID
     assert lib.sq_quantize_act_static(a, a, 4, 32, float("inf"), a, a, None, None, None) == INVALID
@@ -188,3 +192,22 @@ def test_workspace_entry_points_check_arguments_first(lib):
     assert st(a, a, None, a, a, None, a, None, -1, 8, 32, 1, a, None) == INVALID
     assert st(None, None, None, None, None, None, None, None, 0, 8, 32, 1, None, None) == 0
     assert st(None, None, None, None, None, None, None, None, 0, 8, 24, 1, None, None) == ALIGN
+    # the static-scratch entry point checks its arguments exactly as the
+    # caller-workspace one does: the same status for every call below
+    f4 = _fake(0x10004)
+    cases = [(None, a, None, a, a, None, a, None, 8, 8, 32, 1, a),       # X missing
+             (a, a, None, a, a, None, None, None, 8, 8, 32, 1, a),       # bias missing
+             (a, a, None, a, a, None, a, None, 8, 8, 32, 3, a),          # residual missing
+             (a, a, None, a, a, None, a, a, 8, 8, 32, 7, a),             # bad mode
+             (a, a, None, a, a, None, a, None, 8, 8, 40, 1, a),          # K % 16
+             (a, a, f4, a, a, None, a, None, 8, 8, 32, 1, a),            # x_l1 alignment ok (4)
+             (a, a, _fake(0x10002), a, a, None, a, None, 8, 8, 32, 1, a),  # x_l1 misaligned
+             (a, a, None, a, a, None, a, None, 8, 8, 133152, 1, a),      # K too large
+             (a, a, None, a, a, None, a, None, 8, 8, 32, 1, _fake(0x10008)),  # Y misaligned
+             (a, a, None, a, a, None, a, None, -3, 8, 32, 1, a)]
+    for c in cases:
+        assert st(*c, None) == ws(*c, None, 0, None), c
+    sw = lib.sq_static_workspace
+    sw.argtypes = [vp, vp]
+    assert sw(None, ctypes.byref(n)) == INVALID
+    assert sw(ctypes.byref(ctypes.c_void_p()), None) == INVALID

@@ -50,6 +50,37 @@ def test_two_gloo_ranks_aggregate(tmp_path):
     assert not set(r[0]["seeds"]) & set(r[1]["seeds"])
 
 
+# Offsets the benchmark and the input recipe add to a GEMM's seed: X, the
+# calibration batch, the LayerNorm parameters, W, bias and residual.
+DERIVED_OFFSETS = (0, 555, 4242, 7919, 104729, 1299709)
+
+
+def _seed_set(rank):
+    from smoothquant_w8a8_int8_gb300 import workloads as wl
+    out = set()
+    for w in wl.WORKLOADS.values():
+        for layer in range(w.layers):
+            for idx in range(len(w.linears)):
+                base = replicas.rank_seed(wl.gemm_seed(w, layer, idx), rank)
+                out.update(base + o for o in DERIVED_OFFSETS)
+    return out
+
+
+def test_rank_seed_sets_disjoint_for_eight_ranks():
+    """Every seed one rank draws from (for every workload, GEMM and derived
+    stream) is drawn by no other rank, for 8 ranks."""
+    sets = [_seed_set(r) for r in range(8)]
+    for a in range(8):
+        for b in range(a + 1, 8):
+            assert not sets[a] & sets[b], (a, b)
+    # the derived offsets themselves are what the recipe uses
+    from smoothquant_w8a8_int8_gb300 import workloads as wl
+    import inspect
+    src = inspect.getsource(wl)
+    for o in (7919, 104729, 1299709):
+        assert f"seed + {o}" in src
+
+
 def test_single_process_aggregation_is_identity():
     assert replicas.max_over_ranks(3.25) == 3.25
     assert replicas.whole_job_tops(2 * 10 ** 12, 1, 1000.0) == pytest.approx(2.0)
