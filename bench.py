@@ -164,7 +164,7 @@ def clock_summary(lines, window=None):
 
 class Layer:
     __slots__ = ("lin", "X", "s", "Wop", "Wq", "sw", "wl1", "bias", "residual", "Y", "Xhost",
-                 "Yhost", "static_scale", "feeds", "fed_by", "ln")
+                 "Yhost", "static_scale", "feeds", "fed_by", "ln", "table", "row_amax")
 
 
 LN_EPS = 1e-12
@@ -191,7 +191,8 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
         # epilogue, or by the static quantiser from FFN-up's fp32 output)
         maxN = max(lin.N for lin in w.linears)
         bufs_chain = (torch.empty(w.M * maxN, dtype=torch.bfloat16, device=dev),
-                      torch.empty(w.M, dtype=torch.float32, device=dev))
+                      torch.empty(w.M, dtype=torch.float32, device=dev),
+                      torch.zeros(w.M, dtype=torch.float32, device=dev))
     for layer, idx in [(l, i) for l in range(w.layers) for i in range(len(w.linears))]:
         lin = w.linears[idx]
         seed = replicas.rank_seed(wl.gemm_seed(w, layer, idx), rank)
@@ -217,7 +218,11 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
                                               want_op=(gemm == "tc"), want_l1=True)
             L.Wq, L.sw, L.Wop, L.wl1 = Wq, sw, Wop, wl1
             L.bias, L.residual = c.bias, c.residual
-            L.static_scale = sq.static_scale(sq.act_absmax(y_cal, s))
+            L.static_scale = (sq.static_scale(sq.act_absmax(y_cal, s))
+                              if ffn_chain in ("unfused", "fused") else None)
+            # the dynamic chain's division table of FFN-down's smoothing factor
+            L.table = sq.division_table(s) if ffn_chain == "dynamic-fused" else None
+            L.row_amax = None
             L.Y = torch.empty(w.M, lin.N, dtype=torch.float32, device=dev)
             L.Xhost = L.Yhost = None
             L.feeds = None
@@ -265,6 +270,7 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
                                                        want_q=False, want_y=True)
             L.static_scale = sq.static_scale(sq.act_absmax(calib, s))
         L.Y = torch.empty(w.M, lin.N, dtype=torch.float32, device=dev)
+        L.table = L.row_amax = None
         L.Xhost = L.Yhost = None
         L.feeds = L.fed_by = None
         if want_host:
@@ -275,7 +281,7 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
         layers.append(L)
     torch.cuda.synchronize()
     bufs = (Xq_buf, sx_buf, Xop_buf, l1_buf)
-    return layers, bufs + (bufs_chain if chained else (None, None))
+    return layers, bufs + (bufs_chain if chained else (None, None, None))
 
 
 def quantise(sq, L, X, sx_buf, Xop):
@@ -306,7 +312,7 @@ def linear_requant(sq, ws, *a, **k):
 
 def run_layer(sq, gemm, L, bufs, M, X=None, ev=None, ffn_chain="off", ws=None):
     """One linear of the step.  Returns whether an activation quantiser ran."""
-    Xq_buf, sx_buf, Xop_buf, l1_buf, Xop_chain, sx_chain = bufs
+    Xq_buf, sx_buf, Xop_buf, l1_buf, Xop_chain, sx_chain, amax_chain = bufs
     K, N = L.lin.K, L.lin.N
     X = L.X if X is None else X
     if ffn_chain != "off" and (L.feeds is not None or L.fed_by is not None):
@@ -314,16 +320,21 @@ def run_layer(sq, gemm, L, bufs, M, X=None, ev=None, ffn_chain="off", ws=None):
         if L.fed_by is not None:
             if ev is not None:
                 ev[0].record()
+            chain_op = Xop_chain[: M * K].view(M, K)
             if ffn_chain == "unfused":
                 sq.quantize_act_static(L.fed_by.Y, L.s, L.static_scale,
-                                       out=(None, sx_chain, Xop_chain[: M * K].view(M, K)))
+                                       out=(None, sx_chain, chain_op))
+            elif ffn_chain == "dynamic-unfused":
+                sq.quantize_act(L.fed_by.Y, L.s, out=(None, sx_chain, chain_op))
+            elif ffn_chain == "dynamic-fused":
+                sq.quantize_act_rowmax(L.fed_by.Y, L.s, amax_chain, out=(None, sx_chain, chain_op))
             if ev is not None:
                 ev[1].record()
             linear(sq, ws, Xop_chain[: M * K].view(M, K), sx_chain, L.Wop, L.sw, L.bias,
                    L.residual, L.lin.mode, out=L.Y, w_l1=L.wl1)
             if ev is not None:
                 ev[2].record()
-            return ffn_chain == "unfused"
+            return ffn_chain != "fused"
         Xop = Xop_buf[: M * K].view(M, K)
         if ev is not None:
             ev[0].record()
@@ -335,6 +346,11 @@ def run_layer(sq, gemm, L, bufs, M, X=None, ev=None, ffn_chain="off", ws=None):
             linear_requant(sq, ws, Xop, sx_buf, L.Wop, L.sw, L.bias, L.residual, L.lin.mode,
                            nxt.s, nxt.static_scale,
                            out=(None, Xop_chain[: M * N].view(M, N), sx_chain), w_l1=L.wl1)
+        elif ffn_chain == "dynamic-fused":
+            # the epilogue also merges FFN-down's per-token statistic
+            amax_chain.zero_()
+            sq.linear_i8_rowmax(Xop, sx_buf, L.Wop, L.sw, L.bias, L.residual, L.lin.mode,
+                                L.feeds.table, row_amax=amax_chain, out=L.Y, w_l1=L.wl1)
         else:
             linear(sq, ws, Xop, sx_buf, L.Wop, L.sw, L.bias, L.residual, L.lin.mode, out=L.Y,
                    w_l1=L.wl1)
@@ -404,10 +420,6 @@ def e2e_leg(args, layers, M, ops_per_step, world):
     yh = [L.Yhost for L in layers]
     h2d = sum(L.Xhost.numel() * 4 for L in layers)
     d2h = sum(L.Yhost.numel() * 4 for L in layers)
-    # the copies alone (both directions at once), on the pipeline's own device slots
-    pairs_in = [(pipe.x_slots[i % 2][: x.numel()].view(x.shape), x) for i, x in enumerate(xh)]
-    pairs_out = [(y, pipe.y_slots[i % 2][: y.numel()].view(y.shape)) for i, y in enumerate(yh)]
-    copy_ms = copy_ceiling(pairs_in, pairs_out)
     pipe.run(specs, xh, yh)
     torch.cuda.synchronize()
     replicas.barrier()
@@ -422,6 +434,12 @@ def e2e_leg(args, layers, M, ops_per_step, world):
     e_ms = replicas.max_over_ranks(e_ms, device="cuda")
     # every output that came back equals the device path's output
     ok = all(torch.equal(L.Yhost.cuda(non_blocking=True), L.Y) for L in layers)
+    # the same copies alone (both directions at once, on the pipeline's own
+    # device slots, after the buffers' first use): the link's rate in this run
+    pairs_in = [(pipe.x_slots[i % 2][: x.numel()].view(x.shape), x) for i, x in enumerate(xh)]
+    pairs_out = [(y, pipe.y_slots[i % 2][: y.numel()].view(y.shape)) for i, y in enumerate(yh)]
+    copy_ceiling(pairs_in, pairs_out, reps=1)
+    copy_ms = copy_ceiling(pairs_in, pairs_out, reps=3)
     return {"value": round(replicas.whole_job_tops(ops_per_step, world, e_ms), 3),
             "unit": "TOPS", "ms_per_step": round(e_ms, 3), "steps": args.e2e_steps,
             "timing": "CUDA events on the calling stream around K pipeline runs",
@@ -526,23 +544,35 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int, headline: bool = Tru
     if rc != 0:
         raise RuntimeError(f"device status after kernel pass: {sq.status_string(rc)}")
 
-    # launch-bound shapes: per-call time over many back-to-back steps (no L2
-    # flush between them: the step's data stays in L2)
+    # launch-bound shapes: per-step time over many back-to-back steps, replayed
+    # from a CUDA graph (no host launch cost, no L2 flush: the step's data
+    # stays in L2)
     back_to_back = None
     if w.M <= 256 and args.back_to_back > 0:
+        per_graph = 50
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(per_graph):
+                step()
+        graph.replay()
+        torch.cuda.synchronize()
+        reps = max(1, args.back_to_back // per_graph)
         b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         b0.record()
-        for _ in range(args.back_to_back):
-            step()
+        for _ in range(reps):
+            graph.replay()
         b1.record()
         torch.cuda.synchronize()
         rc = sq.device_status()
         if rc != 0:
             raise RuntimeError(f"device status after back-to-back run: {sq.status_string(rc)}")
-        back_to_back = {"steps": args.back_to_back,
-                        "us_per_step": round(b0.elapsed_time(b1) * 1e3 / args.back_to_back, 3),
-                        "note": "quantiser + GEMM per step, launched back to back with no L2 "
-                                "flush (warm L2)"}
+        n_b2b = reps * per_graph
+        us_b2b = b0.elapsed_time(b1) * 1e3 / n_b2b
+        back_to_back = {"steps": n_b2b, "us_per_step": round(us_b2b, 3),
+                        "tops": round(w.ops() / (us_b2b * 1e-6) / 1e12, 3),
+                        "note": "quantiser + GEMM per step: CUDA-graph replays of 50 captured "
+                                "steps, back to back, no L2 flush (warm L2)"}
+        del graph
 
     ops_per_step = w.ops()
     ms_per_step = elapsed_ms / args.steps
@@ -621,7 +651,15 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int, headline: bool = Tru
                                             "the Smooth-Static quantiser",
                                  "fused": "FFN-down consumes FFN-up's output: FFN-up's "
                                           "epilogue emits FFN-down's Smooth-Static codes "
-                                          "(sq_linear_i8_requant)"}[args.ffn_chain],
+                                          "(sq_linear_i8_requant)",
+                                 "dynamic-unfused": "FFN-down consumes FFN-up's output: fp32 Y, "
+                                                    "then the Smooth-Dynamic quantiser "
+                                                    "(sq_quantize_act)",
+                                 "dynamic-fused": "FFN-down consumes FFN-up's output: FFN-up's "
+                                                  "epilogue also merges FFN-down's per-token "
+                                                  "maxima (sq_linear_i8_rowmax), then the "
+                                                  "given-maximum quantiser "
+                                                  "(sq_quantize_act_rowmax)"}[args.ffn_chain],
                    "layernorm": ("the QKV and FFN-up inputs pass through LayerNorm fused with "
                                  "their quantiser (sq_layernorm_quant)" if args.ln else "none")},
         "roofline": {"bound": "tensor", "kernel": "gemm+epilogue",
@@ -772,10 +810,14 @@ def main():
     ap.add_argument("--quant", choices=["dynamic", "static"], default="dynamic",
                     help="activation quantisation: per-token dynamic (Smooth-Dynamic, the "
                          "default) or per-tensor static (Smooth-Static)")
-    ap.add_argument("--ffn-chain", choices=["off", "unfused", "fused"], default="off",
-                    help="chain each layer's FFN-down to its FFN-up (Smooth-Static input): "
-                         "through fp32 Y and the quantiser, or through the requantising "
-                         "epilogue")
+    ap.add_argument("--ffn-chain",
+                    choices=["off", "unfused", "fused", "dynamic-unfused", "dynamic-fused"],
+                    default="off",
+                    help="chain each layer's FFN-down to its FFN-up: Smooth-Static input "
+                         "through fp32 Y and the static quantiser (unfused) or the requantising "
+                         "epilogue (fused); Smooth-Dynamic input through fp32 Y and the dynamic "
+                         "quantiser (dynamic-unfused) or the row-maximum epilogue and the "
+                         "given-maximum quantiser (dynamic-fused)")
     ap.add_argument("--schedule", choices=["split-k", "whole"], default="split-k",
                     help="tcgen05 GEMM: split K over several SMs where the tiles are fewer "
                          "than the SMs and K >= 2048 (workspace), or whole tiles only")

@@ -225,6 +225,61 @@ sq_status sq_linear_i8_requant(const void *Xop, const float *x_scale, const int3
                                int64_t K, int mode, const float *s_next, float scale, int8_t *Yq,
                                void *Yop, float *x_scale_next, void *stream);
 
+/* ---- Producer-fused Smooth-Dynamic quantisation ----------------------------- */
+
+/* Division table of a smoothing factor, for sq_linear_i8_rowmax (offline, once
+ * per layer, like the packed weights):
+ *   table[2j] = -s[j],  table[2j+1] = RN(1/s[j])  (NaN when |s[j]| is outside
+ *   [2^-20, 2^20]; such columns then take IEEE divisions).
+ * s fp32 [K] (4-byte aligned); table fp32 [K][2] (16-byte aligned). */
+sq_status sq_division_table(const float *s, int64_t K, float *table, void *stream);
+
+/* sq_linear_i8 whose epilogue also produces the NEXT linear's Smooth-Dynamic
+ * statistic (Table 10; the pages' INT8 subgraph fusion, with the per-token
+ * maximum across the output's column tiles):
+ *   Y as sq_linear_i8 writes it (bit for bit), and
+ *   row_amax[m] = max(row_amax[m], max_n |fl(Y[m][n] / s_next[n])|)
+ * (IEEE fp32 quotients), merged across tiles with integer atomics on the bit
+ * patterns.  next_table: sq_division_table of s_next [N].  row_amax fp32 [M]
+ * (4-byte aligned), zero-filled by the caller before the call (or holding a
+ * running maximum).  sq_quantize_act_rowmax(Y, s_next, row_amax, ...) then
+ * writes the next linear's codes without its own row reduction.  Modes 0-3
+ * (not SQ_EPI_RAW_I32); other arguments, limits and statuses as sq_linear_i8. */
+sq_status sq_linear_i8_rowmax(const void *Xop, const float *x_scale, const int32_t *x_row_l1,
+                              const void *Wop, const float *w_scale, const int32_t *w_row_l1,
+                              const float *bias, const float *residual, int64_t M, int64_t N,
+                              int64_t K, int mode, void *Y, const float *next_table,
+                              float *row_amax, void *stream);
+
+/* sq_quantize_act with the per-token maxima given: row_amax[m] must be
+ *   max_j |fl(X[m][j] / s[j])|
+ * (as sq_linear_i8_rowmax leaves it); then x_scale, Xq, Xop and x_row_l1 are
+ * bit for bit those of sq_quantize_act(X, s, ...), and no row reduction runs.
+ * A maximum below the true one only saturates codes at +-127 (results are then
+ * unspecified, but stay in range).  row_amax fp32 [M] (4-byte aligned); other
+ * arguments as sq_quantize_act. */
+sq_status sq_quantize_act_rowmax(const float *X, const float *s, const float *row_amax,
+                                 int64_t M, int64_t K, int8_t *Xq, float *x_scale, void *Xop,
+                                 int32_t *x_row_l1, void *stream);
+
+/* ---- Encoder self-attention (Table 3, beside the linear block) -------------- */
+
+/* Scaled dot-product attention per sequence b and head h on the fused QKV
+ * projection's output:
+ *   O[b*S + i][h*D + d] = sum_j P[i][j] V[b*S + j][h*D + d],
+ *   P[i][j] = exp(scale q_i.k_j - m_i) / sum_j' exp(scale q_i.k_j' - m_i),
+ * m_i the row maximum, every token attending to every token of its sequence
+ * (no mask).  QKV fp32 [B*S][3*H*D]: the Q, K and V blocks of H*D columns
+ * each, head h at columns h*D of a block (sq_linear_i8's output with
+ * N = 3*H*D); O fp32 [B*S][H*D]; both 16-byte aligned, not overlapping.
+ * scale finite (1/sqrt(D) for BERT).  D = 64; S a multiple of 64, at most 448
+ * (SQ_ERR_UNSUPPORTED otherwise).  The contractions run on the tensor cores in
+ * split tf32 (each operand as an exact pair of tf32 numbers, products within
+ * about 2^-21 relative), the softmax in fp32: O agrees with the exact
+ * definition to about 1e-6 of max |O|. */
+sq_status sq_attention(const float *QKV, int64_t B, int64_t S, int64_t H, int64_t D,
+                       float scale, float *O, void *stream);
+
 /* ---- Split K over several SMs (caller workspace) ---------------------------- */
 
 /* An output of fewer 128 x 256 tiles than the GPU has SMs keeps most SMs idle

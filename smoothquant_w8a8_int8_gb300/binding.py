@@ -24,7 +24,8 @@ EXPORTS = ("sq_status_string", "sq_version", "sq_operand_bytes", "sq_packed_weig
            "sq_channel_absmax",
            "sq_smooth_factor", "sq_pack_weight", "sq_quantize_act", "sq_act_absmax",
            "sq_static_scale", "sq_quantize_act_static", "sq_layernorm_quant", "sq_linear_i8",
-           "sq_linear_i8_requant", "sq_linear_workspace_bytes", "sq_linear_i8_ws",
+           "sq_linear_i8_requant", "sq_division_table", "sq_linear_i8_rowmax",
+           "sq_quantize_act_rowmax", "sq_attention", "sq_linear_workspace_bytes", "sq_linear_i8_ws",
            "sq_linear_i8_requant_ws", "sq_linear_i8_static_ws", "sq_static_workspace_reset",
            "sq_static_workspace", "sq_linear_i8_mma_sync",
            "sq_check_division", "sq_device_status", "sq_get_device_status")
@@ -68,6 +69,11 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                  i32),
                 "sq_linear_i8_requant": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp,
                                           f32, vp, vp, vp, vp], i32),
+                "sq_division_table": ([vp, i64, vp, vp], i32),
+                "sq_linear_i8_rowmax": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp,
+                                         vp, vp, vp], i32),
+                "sq_quantize_act_rowmax": ([vp, vp, vp, i64, i64, vp, vp, vp, vp, vp], i32),
+                "sq_attention": ([vp, i64, i64, i64, i64, f32, vp, vp], i32),
                 "sq_linear_workspace_bytes": ([i64, i64, i64, vp], i32),
                 "sq_linear_i8_ws": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp,
                                      ctypes.c_size_t, vp], i32),
@@ -316,6 +322,72 @@ def linear_i8_requant(Xop, x_scale, Wop, w_scale, bias, residual, mode, s_next, 
                                        _p(s_next), float(scale), _p(Yq), _p(Yop), _p(xs),
                                        _stream(stream)), "sq_linear_i8_requant")
     return Yq, Yop, xs
+
+
+def division_table(s: torch.Tensor, stream=None) -> torch.Tensor:
+    """(-s, RN(1/s)) per column ([K, 2] fp32) for linear_i8_rowmax."""
+    _need(s, torch.float32, "s")
+    K = s.numel()
+    table = torch.empty(K, 2, dtype=torch.float32, device=s.device)
+    _check(load().sq_division_table(_p(s), K, _p(table), _stream(stream)), "sq_division_table")
+    return table
+
+
+def linear_i8_rowmax(Xop, x_scale, Wop, w_scale, bias, residual, mode, next_table,
+                     row_amax=None, out=None, x_l1=None, w_l1=None, stream=None):
+    """linear_i8 whose epilogue also merges each row's max |Y / s_next| into
+    row_amax (zero-filled here when None).  Returns (Y, row_amax)."""
+    _need(Xop, torch.bfloat16, "Xop")
+    _need(Wop, torch.bfloat16, "Wop")
+    M, N, K, out = _out(Xop, Wop, mode, out)
+    _need(next_table, torch.float32, "next_table", (N, 2))
+    if row_amax is None:
+        row_amax = torch.zeros(M, dtype=torch.float32, device=Xop.device)
+    _need(row_amax, torch.float32, "row_amax", (M,))
+    _check(load().sq_linear_i8_rowmax(_p(Xop), _p(x_scale), _p(x_l1), _p(Wop), _p(w_scale),
+                                      _p(w_l1), _p(bias), _p(residual), M, N, K, int(mode),
+                                      _p(out), _p(next_table), _p(row_amax), _stream(stream)),
+           "sq_linear_i8_rowmax")
+    return out, row_amax
+
+
+def quantize_act_rowmax(X, s, row_amax, want_q: bool = True, want_op: bool = True,
+                        want_l1: bool = False, out=None, stream=None):
+    """quantize_act with the per-token maxima given (from linear_i8_rowmax);
+    returns (Xq or None, x_scale, Xop or None) (+ l1 when want_l1 or a 4-tuple out)."""
+    _need(X, torch.float32, "X")
+    M, K = X.shape
+    _need(s, torch.float32, "s", (K,))
+    _need(row_amax, torch.float32, "row_amax", (M,))
+    l1 = None
+    if out is not None:
+        Xq, sx, Xop = out[:3]
+        l1 = out[3] if len(out) > 3 else None
+    else:
+        Xq = torch.empty(M, K, dtype=torch.int8, device=X.device) if want_q else None
+        Xop = empty_operand(M, K, X.device) if want_op else None
+        sx = torch.empty(M, dtype=torch.float32, device=X.device)
+        l1 = torch.empty(M, dtype=torch.int32, device=X.device) if want_l1 else None
+    _check(load().sq_quantize_act_rowmax(_p(X), _p(s), _p(row_amax), M, K, _p(Xq), _p(sx),
+                                         _p(Xop), _p(l1), _stream(stream)),
+           "sq_quantize_act_rowmax")
+    if want_l1 or (out is not None and len(out) > 3):
+        return Xq, sx, Xop, l1
+    return Xq, sx, Xop
+
+
+def attention(QKV: torch.Tensor, B: int, S: int, H: int, D: int = 64, scale=None, out=None,
+              stream=None) -> torch.Tensor:
+    """Encoder self-attention on the fused QKV output [B*S, 3*H*D] -> O [B*S, H*D]."""
+    _need(QKV, torch.float32, "QKV", (B * S, 3 * H * D))
+    if scale is None:
+        scale = 1.0 / float(D) ** 0.5
+    if out is None:
+        out = torch.empty(B * S, H * D, dtype=torch.float32, device=QKV.device)
+    _need(out, torch.float32, "O", (B * S, H * D))
+    _check(load().sq_attention(_p(QKV), B, S, H, D, float(scale), _p(out), _stream(stream)),
+           "sq_attention")
+    return out
 
 
 def linear_workspace_bytes(M: int, N: int, K: int) -> int:

@@ -2,6 +2,7 @@
 // stream.  Declarations and the contract of every entry point are in sq.h.
 #include "common.cuh"
 
+#include <cmath>
 #include <mutex>
 
 namespace sq {
@@ -233,6 +234,63 @@ sq_status sq_act_absmax(const float *X, const float *s, int64_t M, int64_t K, fl
     return launch_act_absmax(X, s, M, K, amax, as_stream(stream));
 }
 
+sq_status sq_division_table(const float *s, int64_t K, float *table, void *stream) {
+    if (K < 0) return SQ_ERR_INVALID_ARG;
+    if (K == 0) return SQ_OK;
+    if (!s || !table) return SQ_ERR_INVALID_ARG;
+    if (!aligned4(s) || !aligned16(table)) return SQ_ERR_ALIGNMENT;
+    sq_status rc = require_sm103();
+    if (rc != SQ_OK) return rc;
+    return launch_division_table(s, K, table, as_stream(stream));
+}
+
+sq_status sq_linear_i8_rowmax(const void *Xop, const float *x_scale, const int32_t *x_row_l1,
+                              const void *Wop, const float *w_scale, const int32_t *w_row_l1,
+                              const float *bias, const float *residual, int64_t M, int64_t N,
+                              int64_t K, int mode, void *Y, const float *next_table,
+                              float *row_amax, void *stream) {
+    if (mode == SQ_EPI_RAW_I32) return SQ_ERR_INVALID_ARG;
+    sq_status rc = validate_linear(Xop, x_scale, x_row_l1, Wop, w_scale, w_row_l1, bias, residual,
+                                   M, N, K, mode, Y);
+    if (rc != SQ_OK) return rc;
+    if (M == 0 || N == 0) return SQ_OK;
+    if (!next_table || !row_amax) return SQ_ERR_INVALID_ARG;
+    if (!aligned16(next_table) || !aligned4(row_amax)) return SQ_ERR_ALIGNMENT;
+    if ((rc = require_sm103()) != SQ_OK) return rc;
+    return launch_gemm_tc(static_cast<const __nv_bfloat16 *>(Xop), x_scale, x_row_l1,
+                          static_cast<const __nv_bfloat16 *>(Wop), w_scale, w_row_l1, bias,
+                          residual, M, N, K, mode, Y, nullptr, nullptr, 0, as_stream(stream),
+                          next_table, row_amax);
+}
+
+sq_status sq_quantize_act_rowmax(const float *X, const float *s, const float *row_amax,
+                                 int64_t M, int64_t K, int8_t *Xq, float *x_scale, void *Xop,
+                                 int32_t *x_row_l1, void *stream) {
+    sq_status rc = check_quant_args(X, s, M, K, Xq, x_scale, Xop);
+    if (rc != SQ_OK) return rc;
+    if (M == 0) return SQ_OK;
+    if (!row_amax) return SQ_ERR_INVALID_ARG;
+    if (!aligned4(row_amax) || (x_row_l1 && !aligned4(x_row_l1))) return SQ_ERR_ALIGNMENT;
+    if ((rc = require_sm103()) != SQ_OK) return rc;
+    return launch_quantize_act_given_max(X, s, row_amax, M, K, Xq, x_scale,
+                                         static_cast<__nv_bfloat16 *>(Xop), x_row_l1,
+                                         as_stream(stream));
+}
+
+sq_status sq_attention(const float *QKV, int64_t B, int64_t S, int64_t H, int64_t D,
+                       float scale, float *O, void *stream) {
+    if (B < 0 || S < 0 || H < 0 || D <= 0) return SQ_ERR_INVALID_ARG;
+    if (!(scale == scale) || !(fabsf(scale) <= 3.4028234663852886e38f)) return SQ_ERR_INVALID_ARG;
+    if (D != 64 || S % 64 != 0 || S > 448) return SQ_ERR_UNSUPPORTED;
+    if (B == 0 || S == 0 || H == 0) return SQ_OK;
+    if (B * S > ((int64_t)1 << 31) || H > 65536) return SQ_ERR_UNSUPPORTED;
+    if (!QKV || !O) return SQ_ERR_INVALID_ARG;
+    if (!aligned16(QKV) || !aligned16(O)) return SQ_ERR_ALIGNMENT;
+    sq_status rc = require_sm103();
+    if (rc != SQ_OK) return rc;
+    return launch_attention(QKV, B, S, H, scale, O, as_stream(stream));
+}
+
 sq_status sq_static_scale(const float *amax, float *scale, void *stream) {
     if (!amax || !scale) return SQ_ERR_INVALID_ARG;
     if (!aligned4(amax) || !aligned4(scale)) return SQ_ERR_ALIGNMENT;
@@ -350,7 +408,13 @@ sq_status sq_check_division(uint32_t b_first, uint32_t b_count, uint32_t a_first
 
 sq_status sq_device_status(void *stream) {
     if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return SQ_ERR_CUDA;
-    const sq_status rc = gemm_tc_take_error(as_stream(stream));
+    const sq_status rq = quant_take_error(as_stream(stream));
+    if (rq == SQ_ERR_CUDA) return rq;
+    const sq_status ra = attention_take_error(as_stream(stream));
+    if (ra == SQ_ERR_CUDA) return ra;
+    sq_status rc = gemm_tc_take_error(as_stream(stream));
+    if (rc == SQ_OK) rc = rq;
+    if (rc == SQ_OK) rc = ra;
     if (rc == SQ_ERR_TIMEOUT) {
         // a split-K launch that gave up may have left counters in the static
         // scratch: clear them before the next sq_linear_i8_static_ws call

@@ -53,6 +53,38 @@ inline sq_status launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_
     return cuda_status(cudaLaunchKernelEx(&cfg, kern, args...));
 }
 
+// ---- packed fp32 pairs (f32x2: two lanes of arithmetic per instruction) ----
+
+__device__ __forceinline__ unsigned long long pk(float a, float b) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void upk(unsigned long long r, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long sub2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // SM count and compute capability of the current device, cached per device.
 struct DeviceInfo {
     int device = -1;
@@ -129,21 +161,35 @@ sq_status launch_layernorm_quant(const float *H, const float *gamma, const float
 sq_status launch_act_absmax(const float *A, const float *s, int64_t rows, int64_t K,
                             float *amax, cudaStream_t st);
 sq_status launch_static_scale(const float *amax, float *scale, cudaStream_t st);
+sq_status launch_division_table(const float *s, int64_t K, float *table, cudaStream_t st);
+sq_status launch_quantize_act_given_max(const float *A, const float *s, const float *row_amax,
+                                        int64_t rows, int64_t K, int8_t *q, float *scale,
+                                        __nv_bfloat16 *op, int32_t *l1, cudaStream_t st);
 sq_status launch_gemm_mma_sync(const int8_t *Xq, const float *sx, const int8_t *Wq,
                                const float *sw, const float *bias, const float *residual,
                                int64_t M, int64_t N, int64_t K, int mode, void *Y,
                                cudaStream_t st);
 // rq == NULL: Y gets the epilogue's fp32 (or int32) values; otherwise the
 // epilogue's values are requantised into rq's code arrays and Y is unused.
+// rm_pairs / row_amax (both non-NULL, rq NULL): Y as usual, and each row's
+// maximum of |fl(Y / s_next)| merged into row_amax (pairs: the division table
+// of s_next, see sq_division_table).
 sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_t *x_l1,
                          const __nv_bfloat16 *Wop, const float *sw, const int32_t *w_l1,
                          const float *bias, const float *residual, int64_t M, int64_t N,
                          int64_t K, int mode, void *Y, const RequantOut *rq, void *workspace,
-                         size_t workspace_bytes, cudaStream_t st);
+                         size_t workspace_bytes, cudaStream_t st,
+                         const float *rm_pairs = nullptr, float *row_amax = nullptr);
 // Bytes of the split-K workspace of an M x N x K launch on the current device (0: none used).
 sq_status gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes);
-// Reads and clears the tcgen05 GEMM's device error word (synchronous).
+// Read and clear the device error words of the tcgen05 GEMM and of the
+// activation quantiser (synchronous).
 sq_status gemm_tc_take_error(cudaStream_t st);
+sq_status quant_take_error(cudaStream_t st);
+sq_status attention_take_error(cudaStream_t st);
+// Encoder self-attention (head dimension 64): QKV [B*S][3*H*64] -> O [B*S][H*64].
+sq_status launch_attention(const float *QKV, int64_t B, int64_t S, int64_t H, float scale,
+                           float *O, cudaStream_t st);
 // The host-side argument checks of sq_linear_i8 / sq_linear_i8_ws (everything
 // but the workspace and the device): SQ_OK for a valid call, empty calls
 // included.  require_gb300: SQ_ERR_UNSUPPORTED unless the current device is

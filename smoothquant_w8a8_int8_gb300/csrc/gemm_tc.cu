@@ -327,7 +327,11 @@ struct EpiArgs {
     void *Y;
     int M, N;
     int tma_io;  // 1: TMA staging for Y (and the residual); 0: plain per-element I/O
-    RequantOut rq;  // the requantising epilogue's outputs (QUANT kernels)
+    RequantOut rq;  // the requantising epilogue's outputs (kOutRequant kernels)
+    // kOutRowMax kernels: per column n, (-s_next[n], RN(1/s_next[n]) or NaN),
+    // two columns per float4; and the [M] running maxima they merge into
+    const float4 *rm_pairs;
+    float *row_amax;
     int rq_vec;     // 1: rows of the code arrays are 16-byte multiples (N % 16 == 0)
     int rq_fast;    // 1: scale >= 2^-70, so the reciprocal division may be used
     Schedule sched;     // work units (made on the host)
@@ -335,37 +339,17 @@ struct EpiArgs {
     int4 *ws_slots;     // split-K partial slots
 };
 
+// What the epilogue hands out: fp32 (or int32) Y; the next linear's
+// Smooth-Static codes instead of Y; or Y plus each row's maximum of
+// |fl(Y / s_next)| (the next linear's dynamic statistic, merged across the
+// row's tiles by an integer atomicMax on the bit pattern).
+constexpr int kOutPlain = 0, kOutRequant = 1, kOutRowMax = 2;
+
 // Largest row L1 norm of int8 codes for which 127 * L1 < 2^24: then every
 // partial sum of that row's products with any codes stays below 2^24 in
 // magnitude and the whole K accumulates exactly in one fp32 pass.
 constexpr int32_t kSinglePassL1 = 132104;
 
-// ---- packed fp32 pairs (f32x2: two lanes of arithmetic per instruction) ----
-
-__device__ __forceinline__ unsigned long long pk(float a, float b) {
-    unsigned long long r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ void upk(unsigned long long r, float &a, float &b) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
-}
-__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
-                                                   unsigned long long c) {
-    unsigned long long d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
-    unsigned long long d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
-    unsigned long long d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
 __device__ __forceinline__ float rcp_approx(float x) {
     float r;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
@@ -414,7 +398,7 @@ struct ColParams {
     float b[SLICES];
 };
 
-template <int MODE, bool QUANT>
+template <int MODE, int OUT>
 __device__ __forceinline__ void load_col_params(ColParams &cp, const EpiArgs &a, int nb,
                                                 int lane) {
 #pragma unroll
@@ -555,6 +539,57 @@ __device__ __forceinline__ void requant_slice(const uint32_t (&v)[32], int64_t m
     }
 }
 
+// max over this thread's slice (row m, columns n..n+31 that are < N) of
+// |fl(y / s_next[col])|, exactly: the corrected reciprocal division
+// (div_smooth on f32x2 pairs) with the column pairs read as warp-uniform
+// broadcasts.  It is the IEEE quotient wherever |s| is in [2^-20, 2^20] (else
+// the table holds NaN), |y| >= 2^-100 and the quotient's first product is at
+// most 2^100; a slice whose maximum is below 2^-70 may hold inexact tiny
+// quotients, so it, a NaN or a product above 2^100 sends the slice to IEEE
+// divisions (rare).  Partial slices take IEEE divisions too.
+__device__ __forceinline__ float max3_nan_f(float a, float b, float c) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __noinline__ float slice_rowmax_exact(const float *y, const float4 *pairs, int64_t n,
+                                                 int N) {
+    float mx = 0.0f;
+    for (int j = 0; j < 32 && n + j < N; ++j) {
+        const float4 c = pairs[(n + j) >> 1];
+        const float ns = ((n + j) & 1) ? c.z : c.x;
+        mx = fmaxf(mx, fabsf(__fdiv_rn(y[j], -ns)));
+    }
+    return mx;
+}
+
+__device__ __forceinline__ float slice_rowmax(const uint32_t (&v)[32], int64_t n,
+                                              const EpiArgs &a) {
+    if (n + 31 < a.N) {
+        const float4 *tab = a.rm_pairs + (n >> 1);
+        float mx = 0.0f, qm = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+            const float4 c = __ldg(tab + (j >> 1));
+            const unsigned long long y2 = pk(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+            const unsigned long long yn2 = pk(c.y, c.w);
+            const unsigned long long q0 = mul2(y2, yn2);
+            float a0, a1, b0, b1;
+            upk(fma2(fma2(q0, pk(c.x, c.z), y2), yn2, q0), a0, a1);
+            upk(q0, b0, b1);
+            mx = max3_nan_f(mx, fabsf(a0), fabsf(a1));
+            qm = max3_nan_f(qm, fabsf(b0), fabsf(b1));
+        }
+        if (qm <= 0x1p100f && mx >= 0x1p-70f) return mx;  // NaN fails both
+    }
+    // rare: the slice's values through memory (a stack copy), IEEE divisions
+    float y[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(v[j]);
+    return slice_rowmax_exact(y, a.rm_pairs, n, a.N);
+}
+
 // residual row segment of one slice: 32 floats of this thread's row
 __device__ __forceinline__ void load_residual(float4 (&r)[8], const EpiArgs &a, int64_t m,
                                               int64_t n) {
@@ -583,12 +618,12 @@ __device__ __forceinline__ void load_residual(float4 (&r)[8], const EpiArgs &a, 
 // so the store's latency hides behind it.  Staging tile row `lane` holds this
 // thread's 32 values, 16-byte chunk c at c ^ (lane & 7) (the TMA 128-byte
 // swizzle: conflict-free for the warp).
-template <int MODE, bool INT_IN, bool QUANT>
+template <int MODE, bool INT_IN, int OUT>
 __device__ __forceinline__ void epilogue_slice(uint32_t (&v)[32], int64_t m, int64_t n,
                                                int row0, int lane, const EpiArgs &a, float xs,
                                                float wl, float bl, int slice_index,
                                                const float4 (&r4)[8], const CUtensorMap *tmY,
-                                               uint8_t *stg) {
+                                               uint8_t *stg, float &rmax) {
     if (n >= a.N || row0 >= a.M) return;  // slice wholly outside Y
     if (MODE == SQ_EPI_RAW_I32) {
         if (!INT_IN) {
@@ -629,7 +664,8 @@ __device__ __forceinline__ void epilogue_slice(uint32_t (&v)[32], int64_t m, int
             v[j + 1] = __float_as_uint(o1);
         }
     }
-    if (QUANT) {
+    if (OUT == kOutRowMax) rmax = fmaxf(rmax, slice_rowmax(v, n, a));
+    if (OUT == kOutRequant) {
         // this slice's columns in the warp's staging area (written per tile)
         requant_slice(v, m, n, a, reinterpret_cast<const float4 *>(stg) + 16 * slice_index);
         return;
@@ -659,11 +695,12 @@ __device__ __forceinline__ void epilogue_slice(uint32_t (&v)[32], int64_t m, int
 // The first `nsl` slices of this warp's part of a tile (all four for a full
 // tile, fewer for a column slice of one), reading tensor memory at `taddr`
 // (fp32 sums, or int32 with INT_IN).
-template <int MODE, bool INT_IN, bool QUANT>
+template <int MODE, bool INT_IN, int OUT>
 __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int64_t m, int nb, int row0,
                                               int lane, const EpiArgs &a, float xs,
                                               const ColParams &cp, float4 (&rnext)[8],
                                               const CUtensorMap *tmY, uint8_t *stg, int nsl) {
+    float rmax = 0.0f;  // kOutRowMax: this row's maximum over the tile's columns
 #pragma unroll 1
     for (int s = 0; s < nsl; ++s) {
         float4 rcur[8];
@@ -676,9 +713,12 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int64_t m, int nb,
         const float bl = s == 0 ? cp.b[0] : s == 1 ? cp.b[1] : s == 2 ? cp.b[2] : cp.b[3];
         uint32_t v[32];
         tmem_ld32(taddr + s * SLICE, v);
-        epilogue_slice<MODE, INT_IN, QUANT>(v, m, nb + s * SLICE, row0, lane, a, xs, wl, bl, s,
-                                            rcur, tmY, stg);
+        epilogue_slice<MODE, INT_IN, OUT>(v, m, nb + s * SLICE, row0, lane, a, xs, wl, bl, s,
+                                          rcur, tmY, stg, rmax);
     }
+    // non-negative floats order like their bit patterns
+    if (OUT == kOutRowMax && m < a.M && rmax > 0.0f)
+        atomicMax(reinterpret_cast<int *>(a.row_amax) + m, __float_as_int(rmax));
 }
 
 // Bounded wait until the counter at p reaches `target` (acquire).  The pieces
@@ -821,7 +861,7 @@ __device__ __forceinline__ int exact_pass_kb(const EpiArgs &args, int nkb, int w
     return min(mx, mw) <= kSinglePassL1 ? nkb : KB_PER_CHUNK;
 }
 
-template <int MODE, bool QUANT>
+template <int MODE, int OUT>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmBs, const __grid_constant__ CUtensorMap tmY,
@@ -978,9 +1018,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             float xs = 0.f;
             float4 rnext[8];
             auto fetch = [&]() {
-                load_col_params<MODE, QUANT>(cp, args, nb, lane);
-                if (QUANT) stage_next_smoothing(stg, args, nb, lane);
-                if (QUANT && args.rq.x_scale && t.n0 == 0 && half == 0 && m < M)
+                load_col_params<MODE, OUT>(cp, args, nb, lane);
+                if (OUT == kOutRequant) stage_next_smoothing(stg, args, nb, lane);
+                if (OUT == kOutRequant && args.rq.x_scale && t.n0 == 0 && half == 0 && m < M)
                     args.rq.x_scale[m] = args.rq.scale;  // the next linear's per-token scales
                 xs = (MODE != SQ_EPI_RAW_I32 && m < M) ? __ldg(args.sx + m) : 0.f;
                 if (MODE == SQ_EPI_BIAS_RESIDUAL && nsl > 0) load_residual(rnext, args, m, nb);
@@ -1027,14 +1067,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             // epilogue (the int32 partial's final pass overlaps the next unit's MMAs)
             if (!piece) {
                 if (nchunks == 1)
-                    epilogue_tile<MODE, false, QUANT>(T, m, nb, row0, lane, args, xs, cp, rnext,
+                    epilogue_tile<MODE, false, OUT>(T, m, nb, row0, lane, args, xs, cp, rnext,
                                                       &tmY, stg, nsl);
                 else
-                    epilogue_tile<MODE, true, QUANT>(T, m, nb, row0, lane, args, xs, cp, rnext,
+                    epilogue_tile<MODE, true, OUT>(T, m, nb, row0, lane, args, xs, cp, rnext,
                                                      &tmY, stg, nsl);
             } else if (sk_fixup(T, nchunks == 1, t, ew, lane, args, abort_flag)) {
                 fetch();
-                epilogue_tile<MODE, true, QUANT>(T, m, nb, row0, lane, args, xs, cp, rnext, &tmY,
+                epilogue_tile<MODE, true, OUT>(T, m, nb, row0, lane, args, xs, cp, rnext, &tmY,
                                                  stg, nsl);
             } else if (*abort_flag) {
                 goto done_e;
@@ -1100,7 +1140,7 @@ struct PairSmem {
 };
 static_assert(sizeof(PairSmem) <= BAR_BYTES, "barrier block");
 
-template <int MODE, bool QUANT>
+template <int MODE, int OUT>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
@@ -1259,9 +1299,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             // 32-column slices of this warp's half that the item covers (0..4)
             const int nsl = max(0, min(SLICES, (bn - half * COLS_PER_WARP) / SLICE));
             ColParams cp;
-            load_col_params<MODE, QUANT>(cp, args, nb, lane);
-            if (QUANT) stage_next_smoothing(stg, args, nb, lane);
-            if (QUANT && args.rq.x_scale && n0 == 0 && half == 0 && m < M)
+            load_col_params<MODE, OUT>(cp, args, nb, lane);
+            if (OUT == kOutRequant) stage_next_smoothing(stg, args, nb, lane);
+            if (OUT == kOutRequant && args.rq.x_scale && n0 == 0 && half == 0 && m < M)
                 args.rq.x_scale[m] = args.rq.scale;
             const float xs = (MODE != SQ_EPI_RAW_I32 && m < M) ? __ldg(args.sx + m) : 0.f;
             float4 rnext[8];
@@ -1272,7 +1312,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 fph ^= 1u << b;
                 tc_fence_after();
                 const uint32_t tA = tmem_base + lane_off + b * BN + half * COLS_PER_WARP;
-                epilogue_tile<MODE, false, QUANT>(tA, m, nb, row0, lane, args, xs, cp, rnext, &tmY,
+                epilogue_tile<MODE, false, OUT>(tA, m, nb, row0, lane, args, xs, cp, rnext, &tmY,
                                                   stg, nsl);
                 tc_fence_before();
                 __syncwarp();
@@ -1304,7 +1344,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(tempty_leader0);
                 }
-                epilogue_tile<MODE, true, QUANT>(tP, m, nb, row0, lane, args, xs, cp, rnext, &tmY,
+                epilogue_tile<MODE, true, OUT>(tP, m, nb, row0, lane, args, xs, cp, rnext, &tmY,
                                                  stg, nsl);
             }
         }
@@ -1390,29 +1430,32 @@ sq_status setup_kernel(KernelSetup &ks, Kern kern, int smem_bytes, int device,
     return SQ_OK;
 }
 
-template <int MODE, bool QUANT>
+template <int MODE, int OUT>
 sq_status launch_kernel(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tbs,
                         const CUtensorMap &ty, const EpiArgs &args, int K, int grid, int device,
                         cudaStream_t st) {
     static KernelSetup ks;
-    sq_status rc = setup_kernel(ks, gemm_tc_kernel<MODE, QUANT>, SMEM_BYTES, device, nullptr,
+    sq_status rc = setup_kernel(ks, gemm_tc_kernel<MODE, OUT>, SMEM_BYTES, device, nullptr,
                                 nullptr);
     if (rc != SQ_OK) return rc;
-    return launch_pdl(gemm_tc_kernel<MODE, QUANT>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, 1, ta,
+    return launch_pdl(gemm_tc_kernel<MODE, OUT>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, 1, ta,
                       tb, tbs, ty, args, K);
 }
 
 template <int MODE>
 sq_status launch_mode(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tbs,
                       const CUtensorMap &ty, const EpiArgs &args, int K, int grid, int device,
-                      bool quant, cudaStream_t st) {
-    return quant ? launch_kernel<MODE, true>(ta, tb, tbs, ty, args, K, grid, device, st)
-                 : launch_kernel<MODE, false>(ta, tb, tbs, ty, args, K, grid, device, st);
+                      int out, cudaStream_t st) {
+    if (out == kOutRequant)
+        return launch_kernel<MODE, kOutRequant>(ta, tb, tbs, ty, args, K, grid, device, st);
+    if (out == kOutRowMax)
+        return launch_kernel<MODE, kOutRowMax>(ta, tb, tbs, ty, args, K, grid, device, st);
+    return launch_kernel<MODE, kOutPlain>(ta, tb, tbs, ty, args, K, grid, device, st);
 }
 
 // The pair kernel on clusters of 2: at most one cluster per pair tile and no
 // more than can be resident at once (it is persistent).
-template <int MODE, bool QUANT>
+template <int MODE, int OUT>
 sq_status launch_pair_kernel(const CUtensorMap &ta, const CUtensorMap &tbp, const CUtensorMap &tbq,
                              const CUtensorMap &ty, const EpiArgs &args, int K, int pair_tiles,
                              int device, cudaStream_t st) {
@@ -1432,23 +1475,28 @@ sq_status launch_pair_kernel(const CUtensorMap &ta, const CUtensorMap &tbp, cons
     cfg.numAttrs = 1;  // the occupancy query: cluster shape only
     cfg.gridDim = dim3(2, 1, 1);
     int max_clusters = 0;
-    sq_status rc = setup_kernel(ks, gemm_tc_pair_kernel<MODE, QUANT>, PAIR_SMEM_BYTES, device,
+    sq_status rc = setup_kernel(ks, gemm_tc_pair_kernel<MODE, OUT>, PAIR_SMEM_BYTES, device,
                                 &cfg, &max_clusters);
     if (rc != SQ_OK) return rc;
     const int clusters = std::min(pair_tiles, max_clusters);
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
     cfg.numAttrs = 2;  // the launch: cluster shape and programmatic serialisation
     return cuda_status(
-        cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<MODE, QUANT>, ta, tbp, tbq, ty, args, K));
+        cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<MODE, OUT>, ta, tbp, tbq, ty, args, K));
 }
 
 template <int MODE>
 sq_status launch_pair_mode(const CUtensorMap &ta, const CUtensorMap &tbp, const CUtensorMap &tbq,
                            const CUtensorMap &ty, const EpiArgs &args, int K, int pair_tiles,
-                           int device, bool quant, cudaStream_t st) {
-    return quant ? launch_pair_kernel<MODE, true>(ta, tbp, tbq, ty, args, K, pair_tiles, device, st)
-                 : launch_pair_kernel<MODE, false>(ta, tbp, tbq, ty, args, K, pair_tiles, device,
-                                                   st);
+                           int device, int out, cudaStream_t st) {
+    if (out == kOutRequant)
+        return launch_pair_kernel<MODE, kOutRequant>(ta, tbp, tbq, ty, args, K, pair_tiles,
+                                                     device, st);
+    if (out == kOutRowMax)
+        return launch_pair_kernel<MODE, kOutRowMax>(ta, tbp, tbq, ty, args, K, pair_tiles,
+                                                    device, st);
+    return launch_pair_kernel<MODE, kOutPlain>(ta, tbp, tbq, ty, args, K, pair_tiles, device,
+                                               st);
 }
 
 // Which kernel runs a launch: CTA pairs for every launch of at least one full
@@ -1481,9 +1529,11 @@ sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_
                          const __nv_bfloat16 *Wop, const float *sw, const int32_t *w_l1,
                          const float *bias, const float *residual, int64_t M, int64_t N,
                          int64_t K, int mode, void *Y, const RequantOut *rq, void *workspace,
-                         size_t workspace_bytes, cudaStream_t st) {
+                         size_t workspace_bytes, cudaStream_t st, const float *rm_pairs,
+                         float *row_amax) {
     if (!shape_ok(M, N, K)) return SQ_ERR_UNSUPPORTED;
-    if (rq && mode == SQ_EPI_RAW_I32) return SQ_ERR_INVALID_ARG;
+    if ((rq || row_amax) && mode == SQ_EPI_RAW_I32) return SQ_ERR_INVALID_ARG;
+    if (rq && row_amax) return SQ_ERR_INVALID_ARG;
     sq_status rc = get_encoder();
     if (rc != SQ_OK) return rc;
     DeviceInfo di;
@@ -1508,6 +1558,8 @@ sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_
     args.rq_vec = rq && N % 16 == 0 && (!rq->Yq || aligned16(rq->Yq)) &&
                   (!rq->Yop || aligned16(rq->Yop));
     args.rq_fast = rq && rq->scale >= 0x1p-70f;
+    args.rm_pairs = reinterpret_cast<const float4 *>(rm_pairs);
+    args.row_amax = row_amax;
     CUtensorMap ta, tb, tbs, ty;
     if ((rc = make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Xop, M, K, BM, BK)) != SQ_OK)
         return rc;
@@ -1537,7 +1589,7 @@ sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_
                                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
         if ((rc = make_map(&ty, yt, 4, Y, M, N, SLICE, SLICE)) != SQ_OK) return rc;
     }
-    const bool q = rq != nullptr;
+    const int q = rq ? kOutRequant : row_amax ? kOutRowMax : kOutPlain;
     const int k = (int)K, dev = di.device;
     if (use_pair(M, sched)) {
         // B in 128-row halves, one per CTA of a pair; 64-row quarters for the
@@ -1561,7 +1613,8 @@ sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_
         case SQ_EPI_BIAS_RESIDUAL:
             return launch_pair_mode<SQ_EPI_BIAS_RESIDUAL>(ta, tbp, tbq, ty, args, k, p, dev, q, st);
         default:
-            return launch_pair_kernel<SQ_EPI_RAW_I32, false>(ta, tbp, tbq, ty, args, k, p, dev, st);
+            return launch_pair_kernel<SQ_EPI_RAW_I32, kOutPlain>(ta, tbp, tbq, ty, args, k, p, dev,
+                                                                 st);
         }
     }
     switch (mode) {
@@ -1572,7 +1625,7 @@ sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_
     case SQ_EPI_BIAS_RESIDUAL:
         return launch_mode<SQ_EPI_BIAS_RESIDUAL>(ta, tb, tbs, ty, args, k, grid, dev, q, st);
     default:
-        return launch_kernel<SQ_EPI_RAW_I32, false>(ta, tb, tbs, ty, args, k, grid, dev, st);
+        return launch_kernel<SQ_EPI_RAW_I32, kOutPlain>(ta, tb, tbs, ty, args, k, grid, dev, st);
     }
 }
 

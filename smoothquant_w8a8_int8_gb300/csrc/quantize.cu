@@ -18,6 +18,7 @@
 #include "common.cuh"
 
 #include <algorithm>
+#include <mutex>
 
 namespace sq {
 namespace {
@@ -391,7 +392,509 @@ __global__ void __launch_bounds__(kThreads) layernorm_quant_kernel(
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// Smooth-Dynamic activation quantiser (Table 10's run-time step).
+//
+// One persistent block per SM streams its rows through a ring of shared-memory
+// stages: a producer thread copies `groups` consecutive rows per stage with one
+// bulk copy (cp.async.bulk, completion counted on the stage's mbarrier), and
+// each group of `wpr` consumer warps codes one row of the stage from shared
+// memory, then frees the stage.  The copies of the next stages stay in flight
+// while rows are coded, so the row maximum's dependency (every code waits for
+// it) no longer empties the memory pipeline.  Lane l of warp w of a group
+// holds the float4 f = (32 w + l) + 32 wpr i, i < VPT4, of its row.
+//  * row maximum: max |fl(x / s)| by the corrected reciprocal division
+//    q0 = RN(x y), q = RN(q0 + RN(x - s q0) y), y = RN(1/s) (div_smooth: the
+//    IEEE quotient where |s| is in [2^-20, 2^20], |x| >= 2^-100 and |q0| <=
+//    2^100), with s and y per column from tables in shared memory (y NaN where
+//    |s| is outside that range).  Rows whose maximum is NaN or outside
+//    [2^-60, 2^100] take the exact path, so the maximum, and the scale
+//    fl(max / 127), are bit-exact.
+//  * codes: p = RN(RN(x y) RN(1/scale)) is within 5u of fl(x / s) / scale,
+//    |fl(x / s) / scale| <= 127.0001, and so within 4.2e-5 of
+//    fl(fl(x / s) / scale); where p is farther than 2^-14 from every
+//    half-integer, rint(p) is the round-half-even code (rint by the addition
+//    and subtraction of 1.5 * 2^23, on f32x2 pairs).  A float4 holding a value
+//    within 2^-14 of a half-integer recomputes those elements with IEEE
+//    divisions.  Elements with subnormal products are below 2^-126 while the
+//    scale is above 2^-67: their code is 0 either way.
+// Every wait (stages, group reductions) is bounded; on expiry the block
+// records an error for sq_device_status, lets its copies land and exits.
+constexpr int kRingWarps = 16;  // consumer warps of a block at most
+constexpr float kRoundMagic = 12582912.0f;      // 1.5 * 2^23
+constexpr float kTieLimit = 0.49993896484375f;  // 0.5 - 2^-14
+constexpr unsigned long long kRingTimeoutNs = 2000000000ull;
+
+__device__ unsigned int g_quant_error;
+
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float max2_nan(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t saddr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ bool mb_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t gtimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Bounded wait for the phase of parity `parity`; false (and the block's abort
+// flag and the error word set) when it runs out or the block has aborted.
+__device__ __noinline__ bool mb_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort) {
+    const uint64_t t0 = gtimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mb_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*abort) return false;
+            if (gtimer() - t0 > kRingTimeoutNs) {
+                *abort = 1;
+                atomicOr(&g_quant_error, 1u);
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ bool mb_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+    if (mb_try_wait(bar, parity)) return true;
+    return mb_wait_slow(bar, parity, abort);
+}
+// wait used while letting issued copies land (ignores the abort flag)
+__device__ __noinline__ void mb_drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = gtimer();
+    while (!mb_try_wait(bar, parity))
+        if (gtimer() - t0 > kRingTimeoutNs) {
+            atomicOr(&g_quant_error, 2u);
+            return;
+        }
+}
+
+// The warps of one row group and their reduction state: partials in red
+// (two phases used in turn), an mbarrier of count wpr per group.
+struct RingGroup {
+    int wpr, g, wg, lane;
+    uint32_t bar, bph;
+    float *red;  // [2][8]
+    int rp;
+    volatile int *abort;
+};
+
+// Group-wide NaN-keeping maximum (sum when SUM); false if the block aborted.
+// A phase of red is written again only after the next reduction's barrier,
+// which every warp reaches after reading it.
+template <bool SUM>
+__device__ __forceinline__ bool group_reduce(float &v, RingGroup &G) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = SUM ? v + w : max2_nan(v, w);
+    }
+    if (G.wpr == 1) return true;
+    if (G.lane == 0) {
+        G.red[8 * G.rp + G.wg] = v;
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(G.bar) : "memory");
+    }
+    int ok = 1;
+    if (G.lane == 0) ok = mb_wait(G.bar, G.bph, G.abort);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();  // lane 0's acquire orders the other warps' partials for every lane
+    G.bph ^= 1u;
+    if (!ok) return false;
+    v = G.red[8 * G.rp];
+    for (int w = 1; w < G.wpr; ++w) v = SUM ? v + G.red[8 * G.rp + w] : max2_nan(v, G.red[8 * G.rp + w]);
+    G.rp ^= 1;
+    return true;
+}
+
+// Four codes (integer-valued floats) to the outputs at element offset off
+// (a multiple of 4): bf16 operand (8 bytes) and/or int8 (4 bytes).
+__device__ __forceinline__ void store4_codes(float t0, float t1, float t2, float t3, int64_t off,
+                                             int8_t *q, __nv_bfloat16 *op) {
+    if (op) {
+        // integers |t| <= 127: the high half of the fp32 pattern is the exact bf16
+        const uint2 w = make_uint2(__byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x7632),
+                                   __byte_perm(__float_as_uint(t2), __float_as_uint(t3), 0x7632));
+        *reinterpret_cast<uint2 *>(op + off) = w;
+    }
+    if (q) {
+        // t + 1.5 * 2^23 holds the code in its low byte (two's complement)
+        float f0, f1, f2, f3;
+        upk(add2(pk(t0, t1), pk(kRoundMagic, kRoundMagic)), f0, f1);
+        upk(add2(pk(t2, t3), pk(kRoundMagic, kRoundMagic)), f2, f3);
+        *reinterpret_cast<uint32_t *>(q + off) =
+            __byte_perm(__byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x0040),
+                        __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x0040), 0x5410);
+    }
+}
+
+// The code of x as the definition states it: round_half_even(fl(fl(x / s) /
+// scale)), clamped (IEEE divisions; the rare near-tie elements).  By value and
+// not inlined, so that the caller's register arrays stay in registers.
+__device__ __noinline__ float exact_code(float x, float s, float scale) {
+    return fminf(127.0f, fmaxf(-127.0f, rintf(__fdiv_rn(__fdiv_rn(x, s), scale))));
+}
+
+// The exact path for one row (rare): IEEE divisions throughout, the codes as
+// the definition states them.  Every warp of the group runs it together.
+__device__ __noinline__ bool dynamic_row_exact(const float *__restrict__ xr,
+                                               const float *__restrict__ s, int F4, int f0,
+                                               int stride4, int vpt4, RingGroup &G, int64_t row,
+                                               int64_t K, int8_t *q, float *scale,
+                                               __nv_bfloat16 *op, int32_t *l1) {
+    float m = 0.0f;
+    for (int i = 0; i < vpt4; ++i) {
+        const int f = f0 + i * stride4;
+        if (f >= F4) break;
+        for (int e = 0; e < 4; ++e)
+            m = fmaxf(m, fabsf(__fdiv_rn(xr[4 * f + e], __ldg(s + 4 * f + e))));
+    }
+    if (!group_reduce<false>(m, G)) return false;
+    const float sc = m == 0.0f ? 1.0f : __fdiv_rn(m, 127.0f);
+    if (G.wg == 0 && G.lane == 0) scale[row] = sc;
+    float a1 = 0.0f;
+    for (int i = 0; i < vpt4; ++i) {
+        const int f = f0 + i * stride4;
+        if (f >= F4) break;
+        float t[4];
+        for (int e = 0; e < 4; ++e) {
+            const float v = __fdiv_rn(xr[4 * f + e], __ldg(s + 4 * f + e));
+            t[e] = fminf(127.0f, fmaxf(-127.0f, rintf(__fdiv_rn(v, sc))));
+            a1 += fabsf(t[e]);
+        }
+        store4_codes(t[0], t[1], t[2], t[3], row * K + 4 * f, q, op);
+    }
+    if (l1) {
+        if (!group_reduce<true>(a1, G)) return false;
+        if (G.wg == 0 && G.lane == 0) l1[row] = (int32_t)a1;
+    }
+    return true;
+}
+
+// GIVEN: the row maxima come from row_amax (max_j |fl(x / s)|, as the GEMM's
+// row-maximum epilogue merges them), so no reduction runs before the codes; a
+// wrong maximum only makes the codes saturate at +-127.
+template <int VPT4, bool GIVEN>
+__global__ void __launch_bounds__(32 * (kRingWarps + 1), 1) quantize_act_ring(
+    const float *__restrict__ X, const float *__restrict__ s, int64_t rows, int K, int wpr,
+    int groups, int stages, int8_t *__restrict__ q, float *__restrict__ scale,
+    __nv_bfloat16 *__restrict__ op, int32_t *__restrict__ l1,
+    const float *__restrict__ row_amax) {
+    extern __shared__ __align__(128) unsigned char ring_smem[];
+    const int64_t stage_floats = (int64_t)groups * K;
+    float *ring = reinterpret_cast<float *>(ring_smem);
+    float *ytab = ring + stages * stage_floats;  // K reciprocals of s
+    float *nstab = ytab + K;                     // K negated smoothing factors
+    uint64_t *full = reinterpret_cast<uint64_t *>(nstab + K);
+    uint64_t *empty = full + stages;
+    uint64_t *gbar = empty + stages;                        // [kRingWarps]
+    float *red = reinterpret_cast<float *>(gbar + kRingWarps);  // [kRingWarps][2][8]
+    int *abort_flag = reinterpret_cast<int *>(red + kRingWarps * 16);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nconsumer = groups * wpr;  // warps 0 .. nconsumer-1; the producer is the last
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < stages; ++i) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&full[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(&empty[i])),
+                         "r"(nconsumer));
+        }
+        for (int g = 0; g < groups; ++g)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(&gbar[g])), "r"(wpr));
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    pdl_launch_dependents();
+    pdl_wait();  // every global-memory access below follows the previous kernel
+    for (int j = threadIdx.x; j < K; j += blockDim.x) {
+        const float sj = __ldg(s + j);
+        const float a = fabsf(sj);
+        ytab[j] = (a >= 0x1p-20f && a <= 0x1p20f) ? __frcp_rn(sj) : __int_as_float(0x7fffffff);
+        nstab[j] = -sj;
+    }
+    __syncthreads();
+    volatile int *abort = abort_flag;
+    const int64_t nst = (rows + groups - 1) / groups;  // stages of `groups` rows
+    if (warp == nconsumer) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int slot = 0;
+            uint32_t ph = 0, issued = 0, fill_par = 0;  // per slot: a copy issued, its phase
+            for (int64_t t = blockIdx.x; t < nst; t += gridDim.x) {
+                if (!mb_wait(saddr(&empty[slot]), ph ^ 1u, abort)) break;
+                const int64_t r0 = t * groups;
+                const int64_t nr = rows - r0 < groups ? rows - r0 : groups;
+                const uint32_t bytes = (uint32_t)(nr * K * 4);
+                const uint32_t fb = saddr(&full[slot]);
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
+                             "r"(bytes)
+                             : "memory");
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], "
+                    "%2, [%3];" ::"r"(saddr(ring + slot * stage_floats)),
+                    "l"(X + r0 * K), "r"(bytes), "r"(fb)
+                    : "memory");
+                issued |= 1u << slot;
+                fill_par = (fill_par & ~(1u << slot)) | (ph << slot);
+                if (++slot == stages) {
+                    slot = 0;
+                    ph ^= 1u;
+                }
+            }
+            // every issued copy lands before the block's shared memory goes away
+            for (int i = 0; i < stages; ++i)
+                if (issued & (1u << i)) mb_drain(saddr(&full[i]), (fill_par >> i) & 1u);
+        }
+        return;
+    }
+    // ---------------------------------------------------------------- consumers
+    RingGroup G;
+    G.wpr = wpr;
+    G.g = warp / wpr;
+    G.wg = warp - G.g * wpr;
+    G.lane = lane;
+    G.bar = saddr(&gbar[G.g]);
+    G.bph = 0;
+    G.red = red + 16 * G.g;
+    G.rp = 0;
+    G.abort = abort;
+    const int F4 = K >> 2;
+    const int stride4 = 32 * wpr;
+    const int f0 = 32 * G.wg + lane;
+    const float4 *y4 = reinterpret_cast<const float4 *>(ytab);
+    const unsigned long long magic2 = pk(kRoundMagic, kRoundMagic);
+    int slot = 0;
+    uint32_t ph = 0;
+    for (int64_t t = blockIdx.x; t < nst; t += gridDim.x) {
+        int ok = 1;
+        if (lane == 0) ok = mb_wait(saddr(&full[slot]), ph, abort);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        const int64_t row = t * groups + G.g;
+        bool alive = true;
+        if (row < rows) {
+            const float4 *xs = reinterpret_cast<const float4 *>(ring + slot * stage_floats +
+                                                                (int64_t)G.g * K);
+            float x[VPT4][4];
+#pragma unroll
+            for (int i = 0; i < VPT4; ++i) {
+                const int f = f0 + i * stride4;
+                const float4 v = f < F4 ? xs[f] : make_float4(0.f, 0.f, 0.f, 0.f);
+                x[i][0] = v.x;
+                x[i][1] = v.y;
+                x[i][2] = v.z;
+                x[i][3] = v.w;
+            }
+            float m;
+            if (GIVEN) {
+                m = __ldg(row_amax + row);
+            } else {
+                // the row maximum of |fl(x / s)|: the corrected reciprocal division
+                // (div_smooth) on f32x2 pairs, the IEEE quotient for |s| in
+                // [2^-20, 2^20], |x| >= 2^-100 and a first product of at most
+                // 2^100.  Tinier x give tinier quotients, which decide nothing
+                // unless the whole row is below 2^-60 (the exact path then).
+                float lm = 0.0f;
+                const float4 *ns4 = reinterpret_cast<const float4 *>(nstab);
+#pragma unroll
+                for (int i = 0; i < VPT4; ++i) {
+                    const int f = f0 + i * stride4;
+                    if (f < F4) {
+                        const float4 y = y4[f], ns = ns4[f];
+                        const unsigned long long x01 = pk(x[i][0], x[i][1]);
+                        const unsigned long long x23 = pk(x[i][2], x[i][3]);
+                        const unsigned long long y01 = pk(y.x, y.y), y23 = pk(y.z, y.w);
+                        const unsigned long long q01 = mul2(x01, y01), q23 = mul2(x23, y23);
+                        float v0, v1, v2, v3;
+                        upk(fma2(fma2(q01, pk(ns.x, ns.y), x01), y01, q01), v0, v1);
+                        upk(fma2(fma2(q23, pk(ns.z, ns.w), x23), y23, q23), v2, v3);
+                        lm = max3_nan(lm, fabsf(v0), fabsf(v1));
+                        lm = max3_nan(lm, fabsf(v2), fabsf(v3));
+                    }
+                }
+                alive = group_reduce<false>(lm, G);
+                m = lm;
+            }
+            if (alive && !(m >= 0x1p-60f && m <= 0x1p100f)) {
+                alive = dynamic_row_exact(X + row * K, s, F4, f0, stride4, VPT4, G, row, K, q,
+                                          scale, op, l1);
+            } else if (alive) {
+                const float sc = __fdiv_rn(m, 127.0f);
+                const float rsc = __frcp_rn(sc);
+                if (G.wg == 0 && lane == 0) scale[row] = sc;
+                const unsigned long long r2 = pk(rsc, rsc);
+                float a1 = 0.0f;
+#pragma unroll
+                for (int i = 0; i < VPT4; ++i) {
+                    const int f = f0 + i * stride4;
+                    if (f >= F4) continue;
+                    const float4 y = y4[f];
+                    const unsigned long long p01 = mul2(mul2(pk(x[i][0], x[i][1]), pk(y.x, y.y)), r2);
+                    const unsigned long long p23 = mul2(mul2(pk(x[i][2], x[i][3]), pk(y.z, y.w)), r2);
+                    const unsigned long long t01 = sub2(add2(p01, magic2), magic2);
+                    const unsigned long long t23 = sub2(add2(p23, magic2), magic2);
+                    float t[4], d[4];
+                    upk(t01, t[0], t[1]);
+                    upk(t23, t[2], t[3]);
+                    upk(sub2(p01, t01), d[0], d[1]);
+                    upk(sub2(p23, t23), d[2], d[3]);
+                    const float dm = max3(fabsf(d[0]), fabsf(d[1]), fmaxf(fabsf(d[2]), fabsf(d[3])));
+                    if (!(dm <= kTieLimit)) {
+                        // rare: a value within 2^-14 of a half-integer
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (!(fabsf(d[e]) <= kTieLimit))
+                                t[e] = exact_code(x[i][e], -nstab[4 * f + e], sc);
+                    }
+                    if (GIVEN) {
+                        // a maximum below the row's true one: saturate
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) t[e] = fminf(127.0f, fmaxf(-127.0f, t[e]));
+                    }
+                    store4_codes(t[0], t[1], t[2], t[3], row * K + 4 * f, q, op);
+                    if (l1) a1 += (fabsf(t[0]) + fabsf(t[1])) + (fabsf(t[2]) + fabsf(t[3]));
+                }
+                if (l1) {
+                    alive = group_reduce<true>(a1, G);  // exact: at most 127 * 8192 < 2^24
+                    if (alive && G.wg == 0 && lane == 0) l1[row] = (int32_t)a1;
+                }
+            }
+        }
+        // this warp is done with the stage (its group's reads are its own)
+        __syncwarp();
+        if (lane == 0)
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(&empty[slot]))
+                         : "memory");
+        if (!alive) break;
+        if (++slot == stages) {
+            slot = 0;
+            ph ^= 1u;
+        }
+    }
+}
+
 }  // namespace
+
+// Smooth-Dynamic activations of up to 8192 elements per row: the ring kernel
+// above.  wpr warps per row (a warp covers 1024 elements), VPT4 float4 per lane,
+// `groups` rows per stage (16 / wpr, fewer when the rows would not give every
+// SM a stage), as many stages of up to 64 KB as the shared memory holds.
+sq_status launch_quantize_act_dynamic(const float *A, const float *s, int64_t rows, int64_t K,
+                                      int8_t *q, float *scale, __nv_bfloat16 *op, int32_t *l1,
+                                      const DeviceInfo &di, cudaStream_t st,
+                                      const float *row_amax) {
+    const int wpr = (int)((K + 1023) / 1024);
+    const int F4 = (int)(K / 4);
+    const int need4 = (F4 + 32 * wpr - 1) / (32 * wpr);  // float4 per lane, 1..8
+    const int vpt4 = need4 <= 1 ? 1 : need4 <= 2 ? 2 : need4 <= 4 ? 4 : need4 <= 6 ? 6 : 8;
+    int groups = kRingWarps / wpr;
+    const int64_t per_sm = (rows + di.sms - 1) / di.sms;
+    if (per_sm < groups) groups = (int)std::max<int64_t>(1, per_sm);
+    const size_t stage_bytes = (size_t)groups * K * 4;
+    const size_t fixed = (size_t)K * 8 + (size_t)kRingWarps * 8 + kRingWarps * 16 * 4 + 16 + 256;
+    const size_t budget = di.smem_optin > 0 ? di.smem_optin : 227 * 1024;
+    int stages = (int)std::min<size_t>(6, (budget - fixed - 2 * 6 * 8) / stage_bytes);
+    if (stages < 2) return SQ_ERR_UNSUPPORTED;
+    const size_t smem = stages * stage_bytes + (size_t)K * 8 + 2 * stages * 8 +
+                        (size_t)kRingWarps * 8 + kRingWarps * 16 * 4 + 16;
+    using Kern = void (*)(const float *, const float *, int64_t, int, int, int, int, int8_t *,
+                          float *, __nv_bfloat16 *, int32_t *, const float *);
+    static const Kern kerns[2][5] = {
+        {quantize_act_ring<1, false>, quantize_act_ring<2, false>, quantize_act_ring<4, false>,
+         quantize_act_ring<6, false>, quantize_act_ring<8, false>},
+        {quantize_act_ring<1, true>, quantize_act_ring<2, true>, quantize_act_ring<4, true>,
+         quantize_act_ring<6, true>, quantize_act_ring<8, true>}};
+    const int vi = vpt4 == 1 ? 0 : vpt4 == 2 ? 1 : vpt4 == 4 ? 2 : vpt4 == 6 ? 3 : 4;
+    const int given = row_amax ? 1 : 0;
+    const Kern kern = kerns[given][vi];
+    // the shared-memory opt-in, once per (device, kernel)
+    static std::mutex mu;
+    static bool attr_set[64][2][5] = {};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        bool &done = attr_set[di.device & 63][given][vi];
+        if (!done) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)budget) != cudaSuccess)
+                return SQ_ERR_CUDA;
+            done = true;
+        }
+    }
+    const int64_t nst = (rows + groups - 1) / groups;
+    const int64_t grid = std::min<int64_t>(nst, (int64_t)di.sms);
+    const int threads = 32 * (groups * wpr + 1);
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(threads), smem, st, 1, A, s, rows, (int)K,
+                      wpr, groups, stages, q, scale, op, l1, row_amax);
+}
+
+sq_status quant_take_error(cudaStream_t st) {
+    unsigned int word = 0;
+    if (cudaMemcpyFromSymbolAsync(&word, g_quant_error, sizeof(word), 0, cudaMemcpyDeviceToHost,
+                                  st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return SQ_ERR_CUDA;
+    if (word != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbolAsync(g_quant_error, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice,
+                                    st) != cudaSuccess ||
+            cudaStreamSynchronize(st) != cudaSuccess)
+            return SQ_ERR_CUDA;
+        return SQ_ERR_TIMEOUT;
+    }
+    return SQ_OK;
+}
+
+// Division table of a smoothing factor: (-s[j], RN(1/s[j])) per column, NaN for
+// the reciprocal where |s[j]| is outside [2^-20, 2^20].
+__global__ void division_table_kernel(const float *__restrict__ s, int64_t K,
+                                      float2 *__restrict__ table) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= K) return;
+    const float sj = s[j];
+    const float a = fabsf(sj);
+    table[j] = make_float2(-sj, (a >= 0x1p-20f && a <= 0x1p20f) ? __frcp_rn(sj)
+                                                                 : __int_as_float(0x7fffffff));
+}
+
+sq_status launch_division_table(const float *s, int64_t K, float *table, cudaStream_t st) {
+    const int64_t grid = (K + kThreads - 1) / kThreads;
+    return launch_pdl(division_table_kernel, dim3((unsigned)grid), dim3(kThreads), 0, st, 1, s, K,
+                      reinterpret_cast<float2 *>(table));
+}
+
+sq_status launch_quantize_act_given_max(const float *A, const float *s, const float *row_amax,
+                                        int64_t rows, int64_t K, int8_t *q, float *scale,
+                                        __nv_bfloat16 *op, int32_t *l1, cudaStream_t st) {
+    DeviceInfo di;
+    sq_status rc = device_info(&di);
+    if (rc != SQ_OK) return rc;
+    if (K <= 8192)
+        return launch_quantize_act_dynamic(A, s, rows, K, q, scale, op, l1, di, st, row_amax);
+    // other rows: the full quantiser (it finds the same maxima itself)
+    return launch_quantize_rows(kActDynamic, A, s, rows, K, q, scale, op, l1, 0.0f, st);
+}
 
 sq_status launch_quantize_rows(int direction, const float *A, const float *s, int64_t rows,
                                int64_t K, int8_t *q, float *scale, __nv_bfloat16 *op,
@@ -399,6 +902,14 @@ sq_status launch_quantize_rows(int direction, const float *A, const float *s, in
     DeviceInfo di;
     sq_status rc = device_info(&di);
     if (rc != SQ_OK) return rc;
+    // Smooth-Dynamic activations: rows of 1024 * 2^k elements fill the register
+    // kernel's thread groups exactly, and there it is the faster one (measured
+    // on GB300: 21 us against 25 us at 8192 x 1024, 54 against 74 us at
+    // 8192 x 4096); other rows up to 8192 elements take the ring kernel
+    // (44 against 58 us at 32768 x 768, 185 against 212 us at 32768 x 3072)
+    const bool pow2_rows = K >= 1024 && K <= 8192 && (K & (K - 1)) == 0;
+    if (direction == kActDynamic && K <= 8192 && !pow2_rows)
+        return launch_quantize_act_dynamic(A, s, rows, K, q, scale, op, l1, di, st, nullptr);
     const int K4 = (int)(K / 4);
     if (K4 <= kThreads * kMaxVPT) {
         // 4 float4 per thread when that covers the row with one block (more

@@ -207,6 +207,39 @@ def test_workspace_entry_points_check_arguments_first(lib):
              (a, a, None, a, a, None, a, None, -3, 8, 32, 1, a)]
     for c in cases:
         assert st(*c, None) == ws(*c, None, 0, None), c
+    # producer-fused dynamic quantisation
+    dt = lib.sq_division_table
+    dt.argtypes = [vp, i64, vp, vp]
+    assert dt(None, 8, a, None) == INVALID
+    assert dt(a, -1, a, None) == INVALID
+    assert dt(a, 8, _fake(0x10008), None) == ALIGN
+    assert dt(None, 0, None, None) == 0
+    rm = lib.sq_linear_i8_rowmax
+    rm.argtypes = [vp] * 8 + [i64, i64, i64, i32, vp, vp, vp, vp]
+    assert rm(a, a, None, a, a, None, a, None, 8, 8, 32, 4, a, a, a, None) == INVALID  # raw
+    assert rm(a, a, None, a, a, None, a, None, 8, 8, 32, 1, a, None, a, None) == INVALID
+    assert rm(a, a, None, a, a, None, a, None, 8, 8, 32, 1, a, a, None, None) == INVALID
+    assert rm(a, a, None, a, a, None, a, None, 8, 8, 32, 1, a, _fake(0x10008), a,
+              None) == ALIGN
+    assert rm(a, a, None, a, a, None, a, None, 8, 8, 40, 1, a, a, a, None) == ALIGN
+    assert rm(None, None, None, None, None, None, None, None, 0, 8, 32, 1, None, None, None,
+              None) == 0
+    qr = lib.sq_quantize_act_rowmax
+    qr.argtypes = [vp, vp, vp, i64, i64, vp, vp, vp, vp, vp]
+    assert qr(a, a, None, 4, 32, a, a, None, None, None) == INVALID     # no maxima
+    assert qr(a, a, a, 4, 32, None, a, None, None, None) == INVALID     # no output
+    assert qr(a, a, _fake(0x10002), 4, 32, a, a, None, None, None) == ALIGN
+    assert qr(None, None, None, 0, 32, None, None, None, None, None) == 0
+    at = lib.sq_attention
+    at.argtypes = [vp, i64, i64, i64, i64, ctypes.c_float, vp, vp]
+    assert at(a, 2, 128, 4, 64, 0.125, None, None) == INVALID
+    assert at(a, -1, 128, 4, 64, 0.125, a, None) == INVALID
+    assert at(a, 2, 128, 4, 64, float("nan"), a, None) == INVALID
+    assert at(a, 2, 128, 4, 32, 0.125, a, None) == UNSUP          # head dimension
+    assert at(a, 2, 100, 4, 64, 0.125, a, None) == UNSUP          # S % 64
+    assert at(a, 2, 512, 4, 64, 0.125, a, None) == UNSUP          # S > 448
+    assert at(_fake(0x10008), 2, 128, 4, 64, 0.125, a, None) == ALIGN
+    assert at(None, 0, 128, 4, 64, 0.125, None, None) == 0
     sw = lib.sq_static_workspace
     sw.argtypes = [vp, vp]
     assert sw(None, ctypes.byref(n)) == INVALID
