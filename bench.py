@@ -777,6 +777,54 @@ def bench_reference(args, w: wl.Workload):
                     "d2h_bytes_per_step": 0}}
 
 
+def bench_attention(args, B=32, S=256, H=16, D=64, reps=20):
+    """The encoder's self-attention at the BERT-large layer shape on the fused
+    QKV output (sq_attention): per-call time with L2 flushed before each call
+    (the 101 MB input fits in L2), and its rooflines."""
+    from smoothquant_w8a8_int8_gb300 import binding as sq
+    peaks, peak_src = load_peaks()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1240)
+    QKV = (torch.randn(B * S, 3 * H * D, generator=g, device="cuda") * 0.6).contiguous()
+    O = torch.empty(B * S, H * D, dtype=torch.float32, device="cuda")
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        sq.attention(QKV, B, S, H, D, out=O)
+    torch.cuda.synchronize()
+    times = []
+    for r in range(reps):
+        flush.fill_(float(r))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        sq.attention(QKV, B, S, H, D, out=O)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    rc = sq.device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status after attention: {sq.status_string(rc)}")
+    ms = statistics.median(times)
+    flops = 4 * B * H * S * S * D                 # Q K^T and P V, 2 flops per multiply-add
+    issued = 3 * flops                            # three tf32 products per split contraction
+    nbytes = B * S * 3 * H * D * 4 + B * S * H * D * 4
+    tf32_peak = peaks["bf16_tflops"] * (1.1 / 2.25)
+    del flush
+    return {"shape": {"batch": B, "seq": S, "heads": H, "head_dim": D},
+            "us_per_call": round(ms * 1e3, 2), "calls": reps,
+            "l2": "flushed before every call (a 2x L2 buffer written outside the events)",
+            "tflops_exact_math": round(flops / (ms * 1e-3) / 1e12, 2),
+            "roofline": {"bound": "tensor", "achieved": round(issued / (ms * 1e-3) / 1e12, 2),
+                         "peak": round(tf32_peak, 1), "unit": "TFLOP/s (tf32 issued)",
+                         "frac": round(issued / (ms * 1e-3) / 1e12 / tf32_peak, 4),
+                         "peak_source": f"bf16 dense burst ({peak_src}) x 1.1/2.25, the "
+                                        "nominal tf32/bf16 ratio"},
+            "hbm": {"achieved_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                    "peak_gbs": peaks["hbm_gbs"],
+                    "frac": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                    "bytes": nbytes}}
+
+
 def other_configs(args, headline: wl.Workload, rank: int, world: int):
     """Every other workload, measured the same way (its own setup, warm-up,
     timed steps and kernel pass) after the headline one: a compact summary
@@ -857,6 +905,7 @@ def main():
     res = bench_ours(args, w, rank, world)
     if not args.no_configs and args.layers is None:
         res["configs"] = other_configs(args, w, rank, world)
+        res["attention"] = bench_attention(args)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

@@ -890,9 +890,9 @@ sq_status launch_quantize_act_given_max(const float *A, const float *s, const fl
     DeviceInfo di;
     sq_status rc = device_info(&di);
     if (rc != SQ_OK) return rc;
-    if (K <= 8192)
+    if (K <= 8192 && rows >= 16 * (int64_t)di.sms)
         return launch_quantize_act_dynamic(A, s, rows, K, q, scale, op, l1, di, st, row_amax);
-    // other rows: the full quantiser (it finds the same maxima itself)
+    // other launches: the full quantiser (it finds the same maxima itself)
     return launch_quantize_rows(kActDynamic, A, s, rows, K, q, scale, op, l1, 0.0f, st);
 }
 
@@ -907,8 +907,10 @@ sq_status launch_quantize_rows(int direction, const float *A, const float *s, in
     // on GB300: 21 us against 25 us at 8192 x 1024, 54 against 74 us at
     // 8192 x 4096); other rows up to 8192 elements take the ring kernel
     // (44 against 58 us at 32768 x 768, 185 against 212 us at 32768 x 3072)
+    // (and only with at least 16 rows per SM: below that the ring's stages
+    // stay short and its set-up dominates, 17 against 9 us at 256 x 1024)
     const bool pow2_rows = K >= 1024 && K <= 8192 && (K & (K - 1)) == 0;
-    if (direction == kActDynamic && K <= 8192 && !pow2_rows)
+    if (direction == kActDynamic && K <= 8192 && !pow2_rows && rows >= 16 * (int64_t)di.sms)
         return launch_quantize_act_dynamic(A, s, rows, K, q, scale, op, l1, di, st, nullptr);
     const int K4 = (int)(K / 4);
     if (K4 <= kThreads * kMaxVPT) {

@@ -174,17 +174,20 @@ __host__ __device__ inline long long sk_counter_bytes_on(int sms) {
 // of `capacity` bytes (the static scratch of sq_linear_i8_static_ws).
 inline bool fits_scratch(long long need, long long capacity) { return need <= capacity; }
 
-// Work items of the pair kernel: 256 x 256 pair tiles, numbered m-fastest; when
-// the last, partial wave holds at most half the clusters, each of its tiles is
-// cut into two 256 x 128 halves (MMA N = 128, 64 rows of B per CTA).
+// Work items of the pair kernel: 256 x 256 pair tiles, numbered n-fastest, so
+// that the clusters of a wave work on all column tiles of a few row blocks and
+// every row block of A is read from DRAM once (the weights, a few MB, stay in
+// L2); when the last, partial wave holds at most half the clusters, each of its
+// tiles is cut into two 256 x 128 halves (MMA N = 128, 64 rows of B per CTA).
 struct PairSchedule {
-    int m_pairs, full_items, sub, items;
+    int m_pairs, n_tiles, full_items, sub, items;
 };
 
 __host__ __device__ inline PairSchedule make_pair_schedule(int m_pairs, int n_tiles,
                                                            int clusters) {
     PairSchedule sc;
     sc.m_pairs = m_pairs;
+    sc.n_tiles = n_tiles;
     const int tiles = m_pairs * n_tiles;
     const int waves = tiles / clusters, rem = tiles - waves * clusters;
     sc.sub = (waves >= 1 && rem > 0 && 2 * rem <= clusters) ? 2 : 1;
@@ -197,15 +200,15 @@ __host__ __device__ inline PairSchedule make_pair_schedule(int m_pairs, int n_ti
 __host__ __device__ __forceinline__ void pair_item_at(const PairSchedule &sc, int i, int &m0, int &n0,
                                              int &bn) {
     if (i < sc.full_items) {
-        m0 = (i % sc.m_pairs) * 2 * BM;
-        n0 = (i / sc.m_pairs) * BN;
+        n0 = (i % sc.n_tiles) * BN;
+        m0 = (i / sc.n_tiles) * 2 * BM;
         bn = BN;
     } else {
         const int j = i - sc.full_items;
         const int t = sc.full_items + j / sc.sub;
         bn = BN / sc.sub;
-        m0 = (t % sc.m_pairs) * 2 * BM;
-        n0 = (t / sc.m_pairs) * BN + (j % sc.sub) * bn;
+        n0 = (t % sc.n_tiles) * BN + (j % sc.sub) * bn;
+        m0 = (t / sc.n_tiles) * 2 * BM;
     }
 }
 
