@@ -789,7 +789,7 @@ def bench_attention(args, B=32, S=256, H=16, D=64, reps=20):
     O = torch.empty(B * S, H * D, dtype=torch.float32, device="cuda")
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device="cuda")
-    for _ in range(3):
+    for _ in range(max(3, getattr(args, "warmup", 3))):
         sq.attention(QKV, B, S, H, D, out=O)
     torch.cuda.synchronize()
     times = []
@@ -879,6 +879,8 @@ def main():
     ap.add_argument("--back-to-back", type=int, default=1000,
                     help="steps launched back to back for the per-call time of the M = 256 "
                          "workloads")
+    ap.add_argument("--only-attention", action="store_true",
+                    help="measure only sq_attention at the BERT-large layer shape")
     ap.add_argument("--no-configs", action="store_true",
                     help="measure only the chosen workload (no sub-results for the others)")
     ap.add_argument("--layers", type=int, default=None,
@@ -902,6 +904,12 @@ def main():
         torch.distributed.init_process_group("nccl")
     else:
         torch.cuda.set_device(0)
+    if args.only_attention:
+        from smoothquant_w8a8_int8_gb300 import binding as sq
+        sq.load()
+        if rank == 0:
+            print(json.dumps({"attention": bench_attention(args, reps=args.steps)}), flush=True)
+        return
     res = bench_ours(args, w, rank, world)
     if not args.no_configs and args.layers is None:
         res["configs"] = other_configs(args, w, rank, world)

@@ -590,9 +590,26 @@ __device__ __forceinline__ float slice_rowmax(const uint32_t (&v)[32], int64_t n
     return slice_rowmax_exact(y, a.rm_pairs, n, a.N);
 }
 
-// residual row segment of one slice: 32 floats of this thread's row
+// The residual of one slice (the warp's 32 rows from m - lane, 32 columns
+// from n).  A whole slice on the TMA output path (COAL) is read coalesced:
+// r[c] = row 4 c + lane / 8, columns n + 4 (lane % 8) .. +3, four 128-byte
+// lines per instruction (epilogue_slice transposes it through the staging
+// tile); otherwise r holds this thread's own row segment.
+template <bool COAL>
 __device__ __forceinline__ void load_residual(float4 (&r)[8], const EpiArgs &a, int64_t m,
                                               int64_t n) {
+    if (COAL && a.tma_io && n + 31 < a.N) {
+        const int lane = threadIdx.x & 31;
+        const int64_t r0 = m - lane + (lane >> 3);
+        const float *base = a.residual + n + 4 * (lane & 7);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int64_t rr = r0 + 4 * c;
+            r[c] = rr < a.M ? *reinterpret_cast<const float4 *>(base + rr * (int64_t)a.N)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        return;
+    }
     const bool row_ok = m < a.M;
     const float *rrow = a.residual + (row_ok ? m : 0) * (int64_t)a.N;
     const bool vec = a.tma_io && n + 31 < a.N;
@@ -607,6 +624,21 @@ __device__ __forceinline__ void load_residual(float4 (&r)[8], const EpiArgs &a, 
             r[c].z = (row_ok && n4 + 2 < a.N) ? rrow[n4 + 2] : 0.f;
             r[c].w = (row_ok && n4 + 3 < a.N) ? rrow[n4 + 3] : 0.f;
         }
+    }
+}
+
+// L2 prefetch of this thread's residual row segment for the item's `nsl`
+// slices (128-byte lines), issued before the accumulator wait: the per-slice
+// loads then find it in L2 instead of waiting on DRAM one slice at a time
+__device__ __forceinline__ void prefetch_residual(const EpiArgs &a, int64_t m, int64_t n,
+                                                  int nsl) {
+    if (m >= a.M) return;
+    const float *rrow = a.residual + m * (int64_t)a.N;
+    for (int s = 0; s < nsl; ++s) {
+        if (n + s * SLICE >= a.N) break;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(rrow + n + s * SLICE));
+        if (n + s * SLICE + SLICE - 1 < a.N)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(rrow + n + s * SLICE + SLICE - 1));
     }
 }
 
@@ -625,6 +657,30 @@ __device__ __forceinline__ void epilogue_slice(uint32_t (&v)[32], int64_t m, int
                                                const float4 (&r4)[8], const CUtensorMap *tmY,
                                                uint8_t *stg, float &rmax) {
     if (n >= a.N || row0 >= a.M) return;  // slice wholly outside Y
+    float4 rrow[8];  // this thread's row of the residual slice
+    if (MODE == SQ_EPI_BIAS_RESIDUAL) {
+        if (OUT != kOutRequant && a.tma_io && n + 31 < a.N) {
+            // r4 is in the coalesced layout (load_residual<true>): through the
+            // staging tile (free once the previous store has read it), written
+            // row 4 c + lane / 8, read back as row `lane`, both conflict-free
+            // under the 128-byte swizzle
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int r = 4 * c + (lane >> 3), k = lane & 7;
+                *reinterpret_cast<float4 *>(stg + r * 128 + ((k ^ (r & 7)) << 4)) = r4[c];
+            }
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                rrow[c] = *reinterpret_cast<const float4 *>(stg + lane * 128 +
+                                                            ((c ^ (lane & 7)) << 4));
+        } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) rrow[c] = r4[c];
+        }
+    }
     if (MODE == SQ_EPI_RAW_I32) {
         if (!INT_IN) {
 #pragma unroll
@@ -654,7 +710,7 @@ __device__ __forceinline__ void epilogue_slice(uint32_t (&v)[32], int64_t m, int
                 } else if (MODE == SQ_EPI_BIAS_GELU) {
                     o2 = gelu2(t2);
                 } else {
-                    const float4 rq = r4[j >> 2];
+                    const float4 rq = rrow[j >> 2];
                     o2 = add2(t2, (j & 2) ? pk(rq.z, rq.w) : pk(rq.x, rq.y));
                 }
             }
@@ -707,7 +763,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int64_t m, int nb,
         if (MODE == SQ_EPI_BIAS_RESIDUAL) {
 #pragma unroll
             for (int c = 0; c < 8; ++c) rcur[c] = rnext[c];
-            if (s + 1 < nsl) load_residual(rnext, a, m, nb + (s + 1) * SLICE);
+            if (s + 1 < nsl) load_residual<OUT != kOutRequant>(rnext, a, m, nb + (s + 1) * SLICE);
         }
         const float wl = s == 0 ? cp.w[0] : s == 1 ? cp.w[1] : s == 2 ? cp.w[2] : cp.w[3];
         const float bl = s == 0 ? cp.b[0] : s == 1 ? cp.b[1] : s == 2 ? cp.b[2] : cp.b[3];
@@ -1023,7 +1079,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (OUT == kOutRequant && args.rq.x_scale && t.n0 == 0 && half == 0 && m < M)
                     args.rq.x_scale[m] = args.rq.scale;  // the next linear's per-token scales
                 xs = (MODE != SQ_EPI_RAW_I32 && m < M) ? __ldg(args.sx + m) : 0.f;
-                if (MODE == SQ_EPI_BIAS_RESIDUAL && nsl > 0) load_residual(rnext, args, m, nb);
+                if (MODE == SQ_EPI_BIAS_RESIDUAL && nsl > 0) {
+                    prefetch_residual(args, m, nb, nsl);
+                    load_residual<OUT != kOutRequant>(rnext, args, m, nb);
+                }
             };
             if (!piece) fetch();
             // the unit's exact sums: fp32 in accumulator buffer b (one pass), or
@@ -1295,9 +1354,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int m0 = pm0 + (int)rank * BM;
             const int row0 = m0 + q * 32;
             const int64_t m = (int64_t)row0 + lane;
-            const int nb = n0 + half * COLS_PER_WARP;
-            // 32-column slices of this warp's half that the item covers (0..4)
-            const int nsl = max(0, min(SLICES, (bn - half * COLS_PER_WARP) / SLICE));
+            // the two warps of a lane quarter split the item's columns: 128 each
+            // of a whole tile, 64 each of a half (all eight warps busy either way)
+            const int wcols = bn / 2;
+            const int nb = n0 + half * wcols;
+            const int nsl = wcols / SLICE;  // 32-column slices of this warp (4 or 2)
             ColParams cp;
             load_col_params<MODE, OUT>(cp, args, nb, lane);
             if (OUT == kOutRequant) stage_next_smoothing(stg, args, nb, lane);
@@ -1305,20 +1366,26 @@ __global__ void __launch_bounds__(THREADS, 1)
                 args.rq.x_scale[m] = args.rq.scale;
             const float xs = (MODE != SQ_EPI_RAW_I32 && m < M) ? __ldg(args.sx + m) : 0.f;
             float4 rnext[8];
-            if (MODE == SQ_EPI_BIAS_RESIDUAL && nsl > 0) load_residual(rnext, args, m, nb);
+            if (MODE == SQ_EPI_BIAS_RESIDUAL && nsl > 0) {
+                prefetch_residual(args, m, nb, nsl);
+                load_residual<OUT != kOutRequant>(rnext, args, m, nb);
+            }
             if (nchunks == 1) {
                 const uint32_t b = (uint32_t)(it & 1);
                 if (!mbar_wait(smem_u32(&S.tfull[b]), (fph >> b) & 1u, abort_flag)) goto done_e;
                 fph ^= 1u << b;
                 tc_fence_after();
-                const uint32_t tA = tmem_base + lane_off + b * BN + half * COLS_PER_WARP;
+                const uint32_t tA = tmem_base + lane_off + b * BN + half * wcols;
                 epilogue_tile<MODE, false, OUT>(tA, m, nb, row0, lane, args, xs, cp, rnext, &tmY,
                                                   stg, nsl);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(b ? tempty_leader1 : tempty_leader0);
             } else {
-                const uint32_t tA = tmem_base + lane_off + half * COLS_PER_WARP;
+                const uint32_t tA = tmem_base + lane_off + half * wcols;
+                // the int32 partial stays in this warp's own 128 columns whatever
+                // the item's width: the quarter's other warp may still be reading
+                // its partial of the previous item when this one starts the next
                 const uint32_t tP = tmem_base + lane_off + colP + half * COLS_PER_WARP;
                 for (int c = 0; c < nchunks; ++c) {
                     if (!mbar_wait(smem_u32(&S.tfull[0]), fph & 1u, abort_flag)) goto done_e;

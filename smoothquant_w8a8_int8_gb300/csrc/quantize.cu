@@ -557,6 +557,162 @@ __device__ __noinline__ float exact_code(float x, float s, float scale) {
     return fminf(127.0f, fmaxf(-127.0f, rintf(__fdiv_rn(__fdiv_rn(x, s), scale))));
 }
 
+// |fl(x / s)| (IEEE division), out of line for the rare exact path
+__device__ __noinline__ float abs_quotient(float x, float s) { return fabsf(__fdiv_rn(x, s)); }
+
+// Row maximum across the TPR threads of a row group, NaN kept (max.NaN).
+__device__ __forceinline__ float group_max_nan(float m, int tpr, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max2_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (tpr > 32) {
+        const int warp = threadIdx.x >> 5;
+        const int wpg = tpr >> 5;
+        const int g = warp / wpg;
+        if ((threadIdx.x & 31) == 0) red[warp] = m;
+        __syncthreads();
+        m = 0.0f;
+        for (int w = 0; w < wpg; ++w) m = max2_nan(m, red[g * wpg + w]);
+        __syncthreads();
+    }
+    return m;
+}
+
+// Smooth-Dynamic activations, the row in registers (K4 <= tpr * kVPT): the
+// arithmetic of the ring kernel below on the register kernel's layout (tpr
+// threads per row, float4 f = t + i tpr of it in thread t), with the
+// smoothing factors, negated, and their reciprocals in shared-memory tables
+// (2 x K floats) built once per block.
+//  * row maximum of |fl(x / s)| by the corrected reciprocal division with
+//    y = RN(1/s) (NaN for |s| outside [2^-20, 2^20]), on f32x2 pairs;
+//  * codes: rint of p = RN(RN(x y) RN(1/scale)), the IEEE divisions for a
+//    value within 2^-14 of a half-integer.
+// A row whose maximum is NaN or outside [2^-60, 2^100] takes IEEE divisions
+// throughout; the choice is made per block (the group reductions hold block
+// barriers), so a block with one such row codes all its rows that way, which
+// is exact too.
+template <int kVPT>
+__global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
+    const float *__restrict__ A, const float *__restrict__ s, int64_t rows, int K4, int tpr,
+    int8_t *__restrict__ q, float *__restrict__ scale, __nv_bfloat16 *__restrict__ op,
+    int32_t *__restrict__ l1, float /* unused: the register kernels' common signature */) {
+    extern __shared__ float4 qtab[];
+    float4 *nstab = qtab;       // -s
+    float4 *ytab = qtab + K4;   // RN(1/s) or NaN
+    pdl_launch_dependents();
+    pdl_wait();
+    __shared__ float red[kThreads / 32];
+    auto recip = [](float x) {
+        const float a = fabsf(x);
+        return (a >= 0x1p-20f && a <= 0x1p20f) ? __frcp_rn(x) : __int_as_float(0x7fffffff);
+    };
+    const float4 *s4 = reinterpret_cast<const float4 *>(s);
+    for (int j = threadIdx.x; j < K4; j += kThreads) {
+        const float4 v = __ldg(s4 + j);
+        nstab[j] = make_float4(-v.x, -v.y, -v.z, -v.w);
+        ytab[j] = make_float4(recip(v.x), recip(v.y), recip(v.z), recip(v.w));
+    }
+    __syncthreads();
+    const int rpb = kThreads / tpr;
+    const int g = threadIdx.x / tpr;
+    const int t = threadIdx.x % tpr;
+    const unsigned long long magic2 = pk(kRoundMagic, kRoundMagic);
+    const int64_t tiles = (rows + rpb - 1) / rpb;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const int64_t row = tile * rpb + g;
+        const bool valid = row < rows;
+        const float4 *a4 = reinterpret_cast<const float4 *>(A) + (valid ? row : 0) * K4;
+        float4 v[kVPT];
+#pragma unroll
+        for (int i = 0; i < kVPT; ++i) {
+            int j = t + i * tpr;
+            v[i] = (valid && j < K4) ? __ldcs(a4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // row maximum, div_smooth on f32x2 pairs
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kVPT; ++i) {
+            const int j = t + i * tpr;
+            if (j >= K4) continue;
+            const float4 y = ytab[j], ns = nstab[j];
+            const unsigned long long x01 = pk(v[i].x, v[i].y), x23 = pk(v[i].z, v[i].w);
+            const unsigned long long y01 = pk(y.x, y.y), y23 = pk(y.z, y.w);
+            const unsigned long long q01 = mul2(x01, y01), q23 = mul2(x23, y23);
+            float d0, d1, d2, d3;
+            upk(fma2(fma2(q01, pk(ns.x, ns.y), x01), y01, q01), d0, d1);
+            upk(fma2(fma2(q23, pk(ns.z, ns.w), x23), y23, q23), d2, d3);
+            m = max3_nan(m, fabsf(d0), fabsf(d1));
+            m = max3_nan(m, fabsf(d2), fabsf(d3));
+        }
+        m = group_max_nan(m, tpr, red);
+        const bool exact = __syncthreads_or(valid && !(m >= 0x1p-60f && m <= 0x1p100f));
+        float a1 = 0.0f;
+        if (exact) {
+            // IEEE divisions throughout (the definition as stated)
+            float me = 0.0f;
+            for (int i = 0; i < kVPT; ++i) {
+                const int j = t + i * tpr;
+                if (j >= K4) continue;
+                const float4 ns = nstab[j];
+                me = fmaxf(me, fmaxf(abs_quotient(v[i].x, -ns.x), abs_quotient(v[i].y, -ns.y)));
+                me = fmaxf(me, fmaxf(abs_quotient(v[i].z, -ns.z), abs_quotient(v[i].w, -ns.w)));
+            }
+            me = group_max(me, tpr, red);
+            const float sc = me == 0.0f ? 1.0f : abs_quotient(me, 127.0f);
+            if (valid) {
+                if (t == 0) scale[row] = sc;
+                for (int i = 0; i < kVPT; ++i) {
+                    const int j = t + i * tpr;
+                    if (j >= K4) continue;
+                    const float4 ns = nstab[j];
+                    const float c0 = exact_code(v[i].x, -ns.x, sc);
+                    const float c1 = exact_code(v[i].y, -ns.y, sc);
+                    const float c2 = exact_code(v[i].z, -ns.z, sc);
+                    const float c3 = exact_code(v[i].w, -ns.w, sc);
+                    store4_codes(c0, c1, c2, c3, ((int64_t)row * K4 + j) * 4, q, op);
+                    a1 += (fabsf(c0) + fabsf(c1)) + (fabsf(c2) + fabsf(c3));
+                }
+            }
+        } else {
+            const float sc = __fdiv_rn(m, 127.0f);
+            const float rsc = __frcp_rn(sc);
+            const unsigned long long r2 = pk(rsc, rsc);
+            if (valid) {
+                if (t == 0) scale[row] = sc;
+#pragma unroll
+                for (int i = 0; i < kVPT; ++i) {
+                    const int j = t + i * tpr;
+                    if (j >= K4) continue;
+                    const float4 y = ytab[j];
+                    const unsigned long long p01 = mul2(mul2(pk(v[i].x, v[i].y), pk(y.x, y.y)), r2);
+                    const unsigned long long p23 = mul2(mul2(pk(v[i].z, v[i].w), pk(y.z, y.w)), r2);
+                    const unsigned long long t01 = sub2(add2(p01, magic2), magic2);
+                    const unsigned long long t23 = sub2(add2(p23, magic2), magic2);
+                    float c[4], d[4];
+                    upk(t01, c[0], c[1]);
+                    upk(t23, c[2], c[3]);
+                    upk(sub2(p01, t01), d[0], d[1]);
+                    upk(sub2(p23, t23), d[2], d[3]);
+                    const float dm = max3(fabsf(d[0]), fabsf(d[1]), fmaxf(fabsf(d[2]), fabsf(d[3])));
+                    if (!(dm <= kTieLimit)) {
+                        // rare: a value within 2^-14 of a half-integer
+                        const float4 ns = nstab[j];
+                        if (!(fabsf(d[0]) <= kTieLimit)) c[0] = exact_code(v[i].x, -ns.x, sc);
+                        if (!(fabsf(d[1]) <= kTieLimit)) c[1] = exact_code(v[i].y, -ns.y, sc);
+                        if (!(fabsf(d[2]) <= kTieLimit)) c[2] = exact_code(v[i].z, -ns.z, sc);
+                        if (!(fabsf(d[3]) <= kTieLimit)) c[3] = exact_code(v[i].w, -ns.w, sc);
+                    }
+                    store4_codes(c[0], c[1], c[2], c[3], ((int64_t)row * K4 + j) * 4, q, op);
+                    a1 += (fabsf(c[0]) + fabsf(c[1])) + (fabsf(c[2]) + fabsf(c[3]));
+                }
+            }
+        }
+        if (l1) {
+            a1 = group_sum(a1, tpr, red);  // exact: at most 127 * 8192 < 2^24
+            if (valid && t == 0) l1[row] = (int32_t)a1;
+        }
+    }
+}
+
 // The exact path for one row (rare): IEEE divisions throughout, the codes as
 // the definition states them.  Every warp of the group runs it together.
 __device__ __noinline__ bool dynamic_row_exact(const float *__restrict__ xr,
@@ -902,15 +1058,15 @@ sq_status launch_quantize_rows(int direction, const float *A, const float *s, in
     DeviceInfo di;
     sq_status rc = device_info(&di);
     if (rc != SQ_OK) return rc;
-    // Smooth-Dynamic activations: rows of 1024 * 2^k elements fill the register
-    // kernel's thread groups exactly, and there it is the faster one (measured
-    // on GB300: 21 us against 25 us at 8192 x 1024, 54 against 74 us at
-    // 8192 x 4096); other rows up to 8192 elements take the ring kernel
-    // (44 against 58 us at 32768 x 768, 185 against 212 us at 32768 x 3072)
-    // (and only with at least 16 rows per SM: below that the ring's stages
-    // stay short and its set-up dominates, 17 against 9 us at 256 x 1024)
+    // Smooth-Dynamic activations: the register kernel (quantize_act_reg) for
+    // rows of 1024 * 2^k elements, which fill its thread groups exactly, and
+    // for rows above 2048 elements (measured on GB300, L2 flushed: 19 us at
+    // 8192 x 1024, 56 us at 8192 x 4096, 160 us against the ring's 183 us at
+    // 32768 x 3072); the ring kernel for the other rows up to 2048 elements
+    // (44 against 46 us at 32768 x 768), and only with at least 16 rows per SM:
+    // below that the ring's stages stay short and its set-up dominates
     const bool pow2_rows = K >= 1024 && K <= 8192 && (K & (K - 1)) == 0;
-    if (direction == kActDynamic && K <= 8192 && !pow2_rows && rows >= 16 * (int64_t)di.sms)
+    if (direction == kActDynamic && K <= 2048 && !pow2_rows && rows >= 16 * (int64_t)di.sms)
         return launch_quantize_act_dynamic(A, s, rows, K, q, scale, op, l1, di, st, nullptr);
     const int K4 = (int)(K / 4);
     if (K4 <= kThreads * kMaxVPT) {
@@ -924,9 +1080,39 @@ sq_status launch_quantize_rows(int direction, const float *A, const float *s, in
         const int64_t tiles = (rows + rpb - 1) / rpb;
         void (*kern)(const float *, const float *, int64_t, int, int, int8_t *, float *,
                      __nv_bfloat16 *, int32_t *, float);
-        if (direction == kActDynamic)
-            kern = small ? quantize_rows_reg<kActDynamic, 4> : quantize_rows_reg<kActDynamic, 8>;
-        else if (direction == kWeight)
+        if (direction == kActDynamic) {
+            // tables of -s and 1/s in shared memory: 8 bytes per column
+            kern = small ? quantize_act_reg<4> : quantize_act_reg<8>;
+            const int smem = K4 * 32;
+            constexpr int kMaxTab = kThreads * kMaxVPT * 32;  // 64 KB at K = 8192
+            static std::mutex mu;
+            static bool opted[64][2] = {};
+            static int occ_dyn[64][2][8] = {};  // per device, vpt, 256-float4 bucket of K4
+            int occ = 0;
+            {
+                std::lock_guard<std::mutex> lock(mu);
+                const int dv = di.device & 63, vi = small ? 0 : 1;
+                if (!opted[dv][vi]) {
+                    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kMaxTab) != cudaSuccess)
+                        return SQ_ERR_CUDA;
+                    opted[dv][vi] = true;
+                }
+                // residency at the bucket's largest table (never above the true one)
+                const int bucket = (K4 - 1) / 256;
+                int &o = occ_dyn[dv][vi][bucket];
+                if (!o &&
+                    (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, kThreads,
+                                                                   (bucket + 1) * 256 * 32) !=
+                         cudaSuccess ||
+                     o < 1))
+                    return SQ_ERR_CUDA;
+                occ = o;
+            }
+            const int64_t grid = std::min<int64_t>(tiles, (int64_t)di.sms * occ);
+            return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, 1, A, s, rows,
+                              K4, tpr, q, scale, op, l1, fixed_scale);
+        } else if (direction == kWeight)
             kern = small ? quantize_rows_reg<kWeight, 4> : quantize_rows_reg<kWeight, 8>;
         else
             kern = small ? quantize_rows_reg<kActStatic, 4> : quantize_rows_reg<kActStatic, 8>;

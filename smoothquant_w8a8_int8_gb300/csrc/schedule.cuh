@@ -178,7 +178,11 @@ inline bool fits_scratch(long long need, long long capacity) { return need <= ca
 // that the clusters of a wave work on all column tiles of a few row blocks and
 // every row block of A is read from DRAM once (the weights, a few MB, stay in
 // L2); when the last, partial wave holds at most half the clusters, each of its
-// tiles is cut into two 256 x 128 halves (MMA N = 128, 64 rows of B per CTA).
+// tiles is cut into two 256 x 128 halves (MMA N = 128, 64 rows of B per CTA):
+// one round of halves then replaces the round of whole tiles.  (With more
+// than half the clusters busy, halves would need two rounds, and a half
+// tile, which reads as much of A as a whole one for half the products, takes
+// well over half a tile's time: measured slower on GB300.)
 struct PairSchedule {
     int m_pairs, n_tiles, full_items, sub, items;
 };

@@ -267,6 +267,30 @@ def test_gemm_tail_wave_slices(sq, M, N, K, mode):
         assert_close_fp32(y.cpu().numpy(), ref, f"mode {mode}")
 
 
+# CTA-pair shapes (M >= 256) with a partial last wave of 256 x 256 tiles.  On
+# 152 SMs (76 clusters):
+#   (2048, 2560): 80 tiles, 4 in the last wave -> 256 x 128 halves, whose 128
+#     columns the two epilogue warps of a lane quarter split 64 / 64
+#   (2304, 3584): 126 tiles, 50 in the last wave -> whole tiles (control)
+# K = 1088 without row L1 norms takes two exact passes (the chunked epilogue,
+# whose int32 partial each warp keeps in its own columns from item to item).
+PAIR_TAIL_SHAPES = [(2048, 2560, 256, wl.EPI_BIAS), (2304, 3584, 256, wl.EPI_BIAS_RESIDUAL),
+                    (2304, 3584, 1088, wl.EPI_BIAS_GELU), (2048, 2560, 1088, wl.EPI_BIAS_RESIDUAL)]
+
+
+@pytest.mark.parametrize("M,N,K,mode", PAIR_TAIL_SHAPES)
+def test_pair_tail_halves(sq, M, N, K, mode):
+    c, xq, sx, wq, sw, d = _quantised_case(sq, M, K, N, wl.EPI_BIAS_RESIDUAL, seed=M + 3 * N + K)
+    acc_ref = oracle.gemm_i32(xq, wq)
+    acc = sq.linear_i8(d["Xop"], None, d["Wop"], None, None, None, sq.EPI_RAW_I32)
+    assert_codes_equal(acc.cpu().numpy(), acc_ref, "acc")
+    b, r = c.bias.numpy(), c.residual.numpy()
+    ref = oracle.epilogue(acc_ref, sx, sw, b, r, mode)
+    y = sq.linear_i8(d["Xop"], d["sx"], d["Wop"], d["sw"], to_dev(b),
+                     to_dev(r) if mode == wl.EPI_BIAS_RESIDUAL else None, mode)
+    assert_close_fp32(y.cpu().numpy(), ref, f"mode {mode}")
+
+
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("K", [1024, 1040, 2048, 4096, 8192])
 def test_gemm_adversarial_exactness(sq, path, K):
