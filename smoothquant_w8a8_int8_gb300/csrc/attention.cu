@@ -18,19 +18,37 @@
 //
 // One CTA per (sequence, head, tile of 128 queries); S a multiple of 64, at
 // most 448 (the logits of a query tile live in tensor memory: S columns, plus
-// 64 for O).  Roles (288 threads):
-//   warps 0-3  softmax and epilogue: thread r owns query row r of the tile and
-//              tensor-memory lane r; reads all S logits for the exact row
-//              maximum, then writes exp2((s - max) * scale * log2 e) chunk by
-//              chunk as the split A operand of P V, and finally O / sum;
-//   warps 4-7  loaders: the Q tile, then the K chunks and the V chunks (64
-//              keys each; V transposed so that keys run along K), split into
-//              hi / lo tf32 parts in shared memory (128-byte swizzle, K-major);
+// 64 for O).  Roles (448 threads):
+//   warps 0-3, 10-13  softmax and epilogue, two warps per tensor-memory lane
+//              quarter (query rows), each taking 32 of every chunk's 64 keys:
+//              the exact row maximum over all S logits (the two halves'
+//              maxima combined through shared memory), then exp2((s - max) *
+//              scale * log2 e) chunk by chunk as the split A operand of P V,
+//              and finally O / sum (the two halves' sums added), each warp
+//              storing half of O's columns;
+//   warp 9     lane 0 copies the raw fp32 operands with TMA (64-row x 32-column
+//              boxes, 128-byte swizzle): the Q tile and each K chunk (64 keys)
+//              straight into the layout of their tf32 "hi" parts, each V chunk
+//              into the "lo" half of its slot;
+//   warps 4-7  split them into hi / lo tf32 parts in shared memory (K-major,
+//              128-byte swizzle): Q and K in place (hi over the raw value, lo
+//              beside it), V transposed so that keys run along K (every warp
+//              reads its share of the raw chunk before any writes);
+// K chunks cycle through four 32 KB slots (hi + lo): two of their own and the
+// two halves of the first P buffer (unused until the logits are complete), so
+// that up to four are in flight; V chunks go through the first two.  P is
+// double-buffered, the second buffer over the Q tile (dead once the logits are
+// complete), so that the softmax writes chunk c + 1 while the MMAs read c.
 //   warp 8     tensor memory, and lane 0 issues the MMAs:
 //              S[:, 64c..] = Q K_c^T, then O += P_c V_c.
+// A query tile that runs past its sequence (S % 128 == 64) copies the next
+// rows of the input (or zeros past its end) into its unused query rows; their
+// outputs are not stored and no other row reads them.
 // Every wait is bounded (about 4 s); on expiry the CTA records an error for
 // sq_device_status, lets its MMAs drain, frees tensor memory and exits.
 #include "common.cuh"
+
+#include <cuda.h>
 
 #include <mutex>
 
@@ -41,7 +59,8 @@ constexpr int AD = 64;    // head dimension
 constexpr int ABQ = 128;  // queries per CTA (the MMA's M)
 constexpr int ACH = 64;   // keys per chunk (the first MMA's N, the second's K)
 constexpr int AMAXS = 448;
-constexpr int A_THREADS = 288;
+constexpr int A_THREADS = 448;
+constexpr int A_TMA_WARP = 9;
 constexpr int Q_PART = ABQ * AD * 4;   // 32 KB: one tf32 part of the Q tile
 constexpr int KV_PART = ACH * AD * 4;  // 16 KB: one part of a K or V^T chunk
 constexpr int P_PART = ABQ * ACH * 4;  // 32 KB: one part of a P chunk
@@ -49,7 +68,10 @@ constexpr int OFF_QH = 0, OFF_QL = Q_PART;
 constexpr int OFF_RING = 2 * Q_PART;  // 2 stages x (hi, lo)
 constexpr int OFF_PH = OFF_RING + 4 * KV_PART, OFF_PL = OFF_PH + P_PART;
 constexpr int OFF_BAR = OFF_PL + P_PART;
-constexpr int A_SMEM = OFF_BAR + 256 + 1024;  // barriers; 1024-byte alignment slack
+constexpr int OFF_XCH = OFF_BAR + 256;  // [2][128] row maxima, then [2][128] row sums
+constexpr int SLOT_BYTES = 2 * KV_PART;  // hi + lo parts of one 64-row chunk
+static_assert(OFF_QL == OFF_QH + SLOT_BYTES && OFF_PL == OFF_PH + SLOT_BYTES, "slot layout");
+constexpr int A_SMEM = OFF_XCH + 2 * 2 * ABQ * 4 + 1024;  // + 1024-byte alignment slack
 constexpr int TMEM_COLS = 512;                // S (<= 448) + O (64)
 constexpr unsigned long long kAttnTimeoutNs = 4000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -61,7 +83,10 @@ constexpr uint32_t IDESC_TF32 =
 __device__ unsigned int g_attn_error;
 
 struct AttnBars {
-    uint64_t q_full, ring_full[2], ring_empty[2], s_full, p_full, p_empty, o_full, mma_done;
+    uint64_t q_full, s_full, p_full[2], p_empty[2], o_full, mma_done, q_tma;
+    uint64_t slot_tma[4], slot_full[4], slot_empty[4];  // copy landed / split / MMAs done
+    uint64_t v_read;  // the splitters have read a V chunk's raw values
+    uint64_t row_x;   // both softmax halves have posted their row maxima / sums
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -177,13 +202,36 @@ __device__ __forceinline__ uint32_t sw_off(int row, int k, int rows) {
                       ((k & 3) << 2));
 }
 
+// Shared-memory offset of slot s: 0, 1 of their own, 2, 3 the first P buffer;
+// chunk n (K chunks first, then V) and the slot it uses; P buffer c % 2.
+__device__ __forceinline__ int slot_off(int s) {
+    return s < 2 ? OFF_RING + s * SLOT_BYTES : OFF_PH + (s - 2) * SLOT_BYTES;
+}
+__device__ __forceinline__ int chunk_slot(int n, int nch) {
+    return n < nch ? (n & 3) : ((n - nch) & 1);
+}
+__device__ __forceinline__ int p_off(int c) { return (c & 1) ? OFF_QH : OFF_PH; }
+
+__device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x,
+                                        int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void arrive_expect(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
 // exact split of x into a tf32 part and the fp32 remainder
 __device__ __forceinline__ float hi_part(float x) {
     return __uint_as_float(__float_as_uint(x) & 0xffffe000u);
 }
 
 __global__ void __launch_bounds__(A_THREADS, 1)
-    attention_kernel(const float *__restrict__ QKV, int S, int H, float scale,
+    attention_kernel(const __grid_constant__ CUtensorMap tmQKV, int S, int H, float scale,
                      float *__restrict__ O) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -196,20 +244,25 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     const int b = blockIdx.x / (qtiles * H);
     const int q0 = qt * ABQ;
     const int nch = S / ACH;
-    const int64_t ld = 3LL * H * AD;  // QKV row stride (floats)
-    const float *qkv_b = QKV + (int64_t)b * S * ld;
+    const int row_b = b * S;  // the sequence's first row of QKV
 
     if (threadIdx.x == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(su32(&B.q_full)));
-        for (int i = 0; i < 2; ++i) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(su32(&B.ring_full[i])));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&B.ring_empty[i])));
+        for (int i = 0; i < 4; ++i) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&B.slot_tma[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(su32(&B.slot_full[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&B.slot_empty[i])));
         }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(su32(&B.v_read)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(su32(&B.row_x)));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&B.s_full)));
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(su32(&B.p_full)));
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&B.p_empty)));
+        for (int i = 0; i < 2; ++i) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(su32(&B.p_full[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&B.p_empty[i])));
+        }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&B.o_full)));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&B.mma_done)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&B.q_tma)));
         B.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -229,85 +282,144 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     volatile int *abort = &B.abort_flag;
     const uint32_t sbase = su32(smem);
 
-    if (warp >= 4 && warp < 8) {
-        // -------------------------------------------------------------- loaders
+    if (warp == A_TMA_WARP) {
+        // ------------------------------------------------------------ TMA copies
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmQKV))
+                         : "memory");
+            const int xq = h * AD, xk = H * AD + h * AD, xv = 2 * H * AD + h * AD;
+            // the Q tile: four boxes (two 32-column K blocks x two 64-row halves)
+            arrive_expect(su32(&B.q_tma), Q_PART);
+            for (int kb = 0; kb < 2; ++kb)
+                for (int rh = 0; rh < 2; ++rh)
+                    tma_box(sbase + OFF_QH + kb * (ABQ * 128) + rh * (64 * 128), &tmQKV,
+                            su32(&B.q_tma), xq + 32 * kb, row_b + q0 + 64 * rh);
+            // the V chunks (and any K chunks past the first four) into L2 now,
+            // so that their copies, issued as slots free up, find them there
+            for (int n = 4; n < 2 * nch; ++n) {
+                const bool kc = n < nch;
+                const int x = kc ? xk : xv, y = row_b + (kc ? n : n - nch) * ACH;
+                for (int kb = 0; kb < 2; ++kb)
+                    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                                 ::"l"(reinterpret_cast<uint64_t>(&tmQKV)), "r"(x + 32 * kb), "r"(y)
+                                 : "memory");
+            }
+            int uses[4] = {0, 0, 0, 0};
+            for (int n = 0; n < 2 * nch; ++n) {
+                const int sl = chunk_slot(n, nch);
+                const int use = uses[sl];
+                // the slot's previous chunk is done with
+                if (use > 0 &&
+                    !wait_bar(su32(&B.slot_empty[sl]), (uint32_t)(use - 1) & 1u, abort))
+                    break;
+                ++uses[sl];
+                // K chunk n raw into the slot's hi part, V chunk n - nch into its lo part
+                const bool kc = n < nch;
+                const uint32_t dst = sbase + slot_off(sl) + (kc ? 0 : KV_PART);
+                const int x = kc ? xk : xv, y = row_b + (kc ? n : n - nch) * ACH;
+                arrive_expect(su32(&B.slot_tma[sl]), KV_PART);
+                for (int kb = 0; kb < 2; ++kb)
+                    tma_box(dst + kb * (ACH * 128), &tmQKV, su32(&B.slot_tma[sl]), x + 32 * kb, y);
+            }
+            // every copy issued has landed before the shared memory can go away
+            drain_bar(su32(&B.q_tma), 0);
+            for (int sl = 0; sl < 4; ++sl)
+                if (uses[sl] > 0) drain_bar(su32(&B.slot_tma[sl]), (uint32_t)(uses[sl] - 1) & 1u);
+        }
+        __syncwarp();
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ splitters
         const int t = threadIdx.x - 128;
+        int uses[4] = {0, 0, 0, 0};  // chunks taken per slot
         {
-            // the Q tile: thread t owns query row t (rows past S load zeros)
-            const bool ok = q0 + t < S;
-            const float4 *src =
-                reinterpret_cast<const float4 *>(qkv_b + (int64_t)(ok ? q0 + t : 0) * ld + h * AD);
+            // the Q tile, in place: hi over the copied value, lo beside it
+            if (!warp_wait(su32(&B.q_tma), 0, abort)) goto done_l;
+            float4 *qh = reinterpret_cast<float4 *>(smem + OFF_QH);
+            float4 *ql = reinterpret_cast<float4 *>(smem + OFF_QL);
 #pragma unroll 4
-            for (int i = 0; i < AD / 4; ++i) {
-                const float4 v = ok ? __ldg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int i = 0; i < Q_PART / 16 / 128; ++i) {
+                const int f = i * 128 + t;
+                const float4 v = qh[f];
                 const float4 vh = make_float4(hi_part(v.x), hi_part(v.y), hi_part(v.z),
                                               hi_part(v.w));
-                const float4 vl = make_float4(v.x - vh.x, v.y - vh.y, v.z - vh.z, v.w - vh.w);
-                const uint32_t off = sw_off(t, 4 * i, ABQ);
-                *reinterpret_cast<float4 *>(smem + OFF_QH + off) = vh;
-                *reinterpret_cast<float4 *>(smem + OFF_QL + off) = vl;
+                qh[f] = vh;
+                ql[f] = make_float4(v.x - vh.x, v.y - vh.y, v.z - vh.z, v.w - vh.w);
             }
             fence_async_smem();
             __syncwarp();
             if (lane == 0) bar_arrive(su32(&B.q_full));
         }
         for (int n = 0; n < 2 * nch; ++n) {
-            const int slot = n & 1;
-            const uint32_t ph = (uint32_t)(n >> 1) & 1u;
-            if (!warp_wait(su32(&B.ring_empty[slot]), ph ^ 1u, abort)) break;
-            uint8_t *hi = smem + OFF_RING + slot * 2 * KV_PART;
+            const int sl = chunk_slot(n, nch);
+            const uint32_t ph = (uint32_t)uses[sl]++ & 1u;
+            uint8_t *hi = smem + slot_off(sl);
             uint8_t *lo = hi + KV_PART;
+            if (!warp_wait(su32(&B.slot_tma[sl]), ph, abort)) break;
             if (n < nch) {
-                // K chunk n: thread t takes key t / 2, dimensions 32 (t % 2) ..
-                const int key = t >> 1, half = t & 1;
-                const float4 *src = reinterpret_cast<const float4 *>(
-                    qkv_b + (int64_t)(n * ACH + key) * ld + (int64_t)H * AD + h * AD + 32 * half);
+                // K chunk n, in place: hi over the copied value, lo beside it
+                float4 *kh = reinterpret_cast<float4 *>(hi);
+                float4 *kl = reinterpret_cast<float4 *>(lo);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 v = __ldg(src + i);
+                for (int i = 0; i < KV_PART / 16 / 128; ++i) {
+                    const int f = i * 128 + t;
+                    const float4 v = kh[f];
                     const float4 vh = make_float4(hi_part(v.x), hi_part(v.y), hi_part(v.z),
                                                   hi_part(v.w));
-                    const float4 vl = make_float4(v.x - vh.x, v.y - vh.y, v.z - vh.z, v.w - vh.w);
-                    const uint32_t off = sw_off(key, 32 * half + 4 * i, ACH);
-                    *reinterpret_cast<float4 *>(hi + off) = vh;
-                    *reinterpret_cast<float4 *>(lo + off) = vl;
+                    kh[f] = vh;
+                    kl[f] = make_float4(v.x - vh.x, v.y - vh.y, v.z - vh.z, v.w - vh.w);
                 }
             } else {
-                // V chunk n - nch, transposed (rows: dimensions, K: keys): thread t
-                // takes key t % 64, dimensions 32 (t / 64) ..; a warp writes 32
-                // consecutive keys of one row per store
-                const int key = t & 63, dh = t >> 6;
-                const float4 *src = reinterpret_cast<const float4 *>(
-                    qkv_b + (int64_t)((n - nch) * ACH + key) * ld + 2LL * H * AD + h * AD +
-                    32 * dh);
+                // V chunk j (copied into the lo part as [key][dimension]), transposed
+                // into the hi / lo parts (rows: dimensions, K: keys): lane l takes
+                // key 32 kb + l and four dimensions per pass; the raw reads (a float4
+                // of one key row) and the part writes (32 consecutive keys of one
+                // dimension row) are conflict-free under the swizzle.  All four warps
+                // read their share before any warp overwrites the lo part.
+                const int j = n - nch;
+                const int w = warp - 4;
+                float4 v[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 v = __ldg(src + i);
-                    const float e[4] = {v.x, v.y, v.z, v.w};
+                for (int it = 0; it < 8; ++it) {
+                    const int c = w * 8 + it;  // 32 (key block, dimension group) pairs
+                    const int key = 32 * (c >> 4) + lane, d = 4 * (c & 15);
+                    v[it] = *reinterpret_cast<const float4 *>(
+                        lo + (d >> 5) * (ACH * 128) + key * 128 +
+                        ((((d & 31) >> 2) ^ (key & 7)) << 4));
+                }
+                __syncwarp();
+                if (lane == 0) bar_arrive(su32(&B.v_read));
+                if (!warp_wait(su32(&B.v_read), (uint32_t)j & 1u, abort)) break;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float eh = hi_part(e[j]);
-                        const uint32_t off = sw_off(32 * dh + 4 * i + j, key, AD);
+                for (int it = 0; it < 8; ++it) {
+                    const int c = w * 8 + it;
+                    const int key = 32 * (c >> 4) + lane, d = 4 * (c & 15);
+                    const float e[4] = {v[it].x, v[it].y, v[it].z, v[it].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float eh = hi_part(e[q]);
+                        const uint32_t off = sw_off(d + q, key, AD);
                         *reinterpret_cast<float *>(hi + off) = eh;
-                        *reinterpret_cast<float *>(lo + off) = e[j] - eh;
+                        *reinterpret_cast<float *>(lo + off) = e[q] - eh;
                     }
                 }
             }
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) bar_arrive(su32(&B.ring_full[slot]));
+            if (lane == 0) bar_arrive(su32(&B.slot_full[sl]));
         }
+    done_l:;
     } else if (warp == 8) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
+            int uses[4] = {0, 0, 0, 0};  // chunks taken per slot
             if (!wait_bar(su32(&B.q_full), 0, abort)) goto done_m;
             tc_after();
             for (int c = 0; c < nch; ++c) {
-                const int slot = c & 1;
-                if (!wait_bar(su32(&B.ring_full[slot]), (uint32_t)(c >> 1) & 1u, abort))
+                const int sl = chunk_slot(c, nch);
+                if (!wait_bar(su32(&B.slot_full[sl]), (uint32_t)uses[sl]++ & 1u, abort))
                     goto done_m;
                 tc_after();
-                const uint32_t kh = sbase + OFF_RING + slot * 2 * KV_PART, kl = kh + KV_PART;
+                const uint32_t kh = sbase + slot_off(sl), kl = kh + KV_PART;
                 const uint32_t d = tmem + (uint32_t)(c * ACH);
 #pragma unroll
                 for (int p = 0; p < 3; ++p) {
@@ -322,20 +434,21 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                             mma_tf32(d, ad + 2 * k, bd + 2 * k, (p | kb | k) ? 1u : 0u);
                     }
                 }
-                mma_commit(su32(&B.ring_empty[slot]));
+                mma_commit(su32(&B.slot_empty[sl]));
             }
             mma_commit(su32(&B.s_full));
             for (int c = 0; c < nch; ++c) {
-                const int n = nch + c, slot = n & 1;
-                if (!wait_bar(su32(&B.ring_full[slot]), (uint32_t)(n >> 1) & 1u, abort))
+                const int sl = chunk_slot(nch + c, nch);
+                if (!wait_bar(su32(&B.slot_full[sl]), (uint32_t)uses[sl]++ & 1u, abort))
                     goto done_m;
-                if (!wait_bar(su32(&B.p_full), (uint32_t)c & 1u, abort)) goto done_m;
+                if (!wait_bar(su32(&B.p_full[c & 1]), (uint32_t)(c >> 1) & 1u, abort)) goto done_m;
                 tc_after();
-                const uint32_t vh = sbase + OFF_RING + slot * 2 * KV_PART, vl = vh + KV_PART;
+                const uint32_t vh = sbase + slot_off(sl), vl = vh + KV_PART;
+                const uint32_t pa = sbase + p_off(c);
                 const uint32_t d = tmem + (uint32_t)AMAXS;  // O after the logits' columns
 #pragma unroll
                 for (int p = 0; p < 3; ++p) {
-                    const uint32_t a = p == 2 ? sbase + OFF_PL : sbase + OFF_PH;
+                    const uint32_t a = p == 2 ? pa + P_PART : pa;
                     const uint32_t bb = p == 1 ? vl : vh;
 #pragma unroll
                     for (int kb = 0; kb < 2; ++kb) {
@@ -346,8 +459,8 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                             mma_tf32(d, ad + 2 * k, bd + 2 * k, (c | p | kb | k) ? 1u : 0u);
                     }
                 }
-                mma_commit(su32(&B.ring_empty[slot]));
-                mma_commit(su32(&B.p_empty));
+                mma_commit(su32(&B.slot_empty[sl]));
+                mma_commit(su32(&B.p_empty[c & 1]));
             }
             mma_commit(su32(&B.o_full));
         done_m:
@@ -358,62 +471,77 @@ __global__ void __launch_bounds__(A_THREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------ softmax and epilogue
-        const int r = threadIdx.x;  // query row of the tile, tensor-memory lane
-        const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+        const int qw = warp & 3;                // lane quarter: query rows 32 qw ..
+        const int half = warp >= 8 ? 1 : 0;     // keys 32 half .. of every chunk
+        const int r = 32 * qw + lane;           // query row of the tile, tensor-memory lane
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * qw) << 16);
         const float cl2e = scale * kLog2e;
+        float *xm = reinterpret_cast<float *>(smem + OFF_XCH);  // [half][row] maxima
+        float *xs = xm + 2 * ABQ;                               // [half][row] sums
         if (!warp_wait(su32(&B.s_full), 0, abort)) goto done_s;
         tc_after();
         {
-            // the row maximum over all S logits
+            // the row maximum over all S logits: this half's columns, then the
+            // other half's maximum from shared memory
             float m = -INFINITY;
-            for (int sl = 0; sl < S / 32; ++sl) {
+            for (int c = 0; c < nch; ++c) {
                 float v[32];
-                tmem_ld32(lane_addr + 32 * sl, v);
+                tmem_ld32(lane_addr + c * ACH + 32 * half, v);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) m = fmaxf(m, v[j]);
             }
+            xm[half * ABQ + r] = m;
+            __syncwarp();
+            if (lane == 0) bar_arrive(su32(&B.row_x));
+            if (!warp_wait(su32(&B.row_x), 0, abort)) goto done_s;
+            __syncwarp();
+            m = fmaxf(xm[r], xm[ABQ + r]);
             const float mc = m * cl2e;
             float sum = 0.0f;
             for (int c = 0; c < nch; ++c) {
-                // the P buffer is free once the previous chunk's MMAs are done
-                if (!warp_wait(su32(&B.p_empty), ((uint32_t)c & 1u) ^ 1u, abort)) goto done_s;
+                // P buffer c % 2 is free once chunk c - 2's MMAs are done
+                if (!warp_wait(su32(&B.p_empty[c & 1]), ((uint32_t)(c >> 1) & 1u) ^ 1u, abort))
+                    goto done_s;
+                uint8_t *pbuf = smem + p_off(c);
+                float v[32];
+                tmem_ld32(lane_addr + c * ACH + 32 * half, v);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float v[32];
-                    tmem_ld32(lane_addr + c * ACH + 32 * half, v);
+                for (int j = 0; j < 32; j += 4) {
+                    float pp[4], ph[4], pl[4];
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        float pp[4], ph[4], pl[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            pp[e] = exp2f(__fmaf_rn(v[j + e], cl2e, -mc));
-                            sum += pp[e];
-                            ph[e] = hi_part(pp[e]);
-                            pl[e] = pp[e] - ph[e];
-                        }
-                        const uint32_t off = sw_off(r, 32 * half + j, ABQ);
-                        *reinterpret_cast<float4 *>(smem + OFF_PH + off) =
-                            make_float4(ph[0], ph[1], ph[2], ph[3]);
-                        *reinterpret_cast<float4 *>(smem + OFF_PL + off) =
-                            make_float4(pl[0], pl[1], pl[2], pl[3]);
+                    for (int e = 0; e < 4; ++e) {
+                        pp[e] = exp2f(__fmaf_rn(v[j + e], cl2e, -mc));
+                        sum += pp[e];
+                        ph[e] = hi_part(pp[e]);
+                        pl[e] = pp[e] - ph[e];
                     }
+                    const uint32_t off = sw_off(r, 32 * half + j, ABQ);
+                    *reinterpret_cast<float4 *>(pbuf + off) = make_float4(ph[0], ph[1], ph[2], ph[3]);
+                    *reinterpret_cast<float4 *>(pbuf + P_PART + off) =
+                        make_float4(pl[0], pl[1], pl[2], pl[3]);
                 }
                 fence_async_smem();
                 tc_before();
                 __syncwarp();
-                if (lane == 0) bar_arrive(su32(&B.p_full));
+                if (lane == 0) bar_arrive(su32(&B.p_full[c & 1]));
             }
+            // the row sum: half 0's plus half 1's
+            xs[half * ABQ + r] = sum;
+            __syncwarp();
+            if (lane == 0) bar_arrive(su32(&B.row_x));
+            if (!warp_wait(su32(&B.row_x), 1, abort)) goto done_s;
+            __syncwarp();
+            sum = xs[r] + xs[ABQ + r];
             if (!warp_wait(su32(&B.o_full), 0, abort)) goto done_s;
             tc_after();
             const float inv = __frcp_rn(sum);
-            float o[64];
-            tmem_ld32(lane_addr + AMAXS, *reinterpret_cast<float(*)[32]>(o));
-            tmem_ld32(lane_addr + AMAXS + 32, *reinterpret_cast<float(*)[32]>(o + 32));
+            float o[32];
+            tmem_ld32(lane_addr + AMAXS + 32 * half, o);
             if (q0 + r < S) {
                 float4 *dst = reinterpret_cast<float4 *>(O + ((int64_t)b * S + q0 + r) * H * AD +
-                                                         h * AD);
+                                                         h * AD + 32 * half);
 #pragma unroll
-                for (int i = 0; i < AD / 4; ++i)
+                for (int i = 0; i < 8; ++i)
                     dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
                                          o[4 * i + 3] * inv);
             }
@@ -449,8 +577,11 @@ sq_status launch_attention(const float *QKV, int64_t B, int64_t S, int64_t H, fl
         }
     }
     const int64_t grid = B * H * ((S + ABQ - 1) / ABQ);
-    if (grid > 0x7fffffff) return SQ_ERR_UNSUPPORTED;
-    return launch_pdl(attention_kernel, dim3((unsigned)grid), dim3(A_THREADS), A_SMEM, st, 1, QKV,
+    if (grid > 0x7fffffff || B * S > 0x7fffffff) return SQ_ERR_UNSUPPORTED;
+    // QKV as B*S rows of 3*H*64 floats, copied in boxes of 64 rows x 32 columns
+    CUtensorMap map;
+    if ((rc = make_map_f32(&map, QKV, B * S, 3 * H * AD, 64, 32)) != SQ_OK) return rc;
+    return launch_pdl(attention_kernel, dim3((unsigned)grid), dim3(A_THREADS), A_SMEM, st, 1, map,
                       (int)S, (int)H, scale, O);
 }
 

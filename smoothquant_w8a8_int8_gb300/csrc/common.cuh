@@ -187,6 +187,10 @@ sq_status gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes
 sq_status gemm_tc_take_error(cudaStream_t st);
 sq_status quant_take_error(cudaStream_t st);
 sq_status attention_take_error(cudaStream_t st);
+// A 2-D TMA tensor map (a CUtensorMap, 128 bytes) over a row-major fp32 matrix
+// of rows x cols, boxes of box_rows x box_cols, 128-byte swizzle.
+sq_status make_map_f32(void *map, const float *base, int64_t rows, int64_t cols, int box_rows,
+                       int box_cols);
 // Encoder self-attention (head dimension 64): QKV [B*S][3*H*64] -> O [B*S][H*64].
 sq_status launch_attention(const float *QKV, int64_t B, int64_t S, int64_t H, float scale,
                            float *O, cudaStream_t st);

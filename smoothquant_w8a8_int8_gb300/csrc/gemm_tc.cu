@@ -1592,6 +1592,14 @@ sq_status gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes
     return SQ_OK;
 }
 
+sq_status make_map_f32(void *map, const float *base, int64_t rows, int64_t cols, int box_rows,
+                       int box_cols) {
+    sq_status rc = get_encoder();
+    if (rc != SQ_OK) return rc;
+    return make_map(static_cast<CUtensorMap *>(map), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base,
+                    rows, cols, box_rows, box_cols);
+}
+
 sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_t *x_l1,
                          const __nv_bfloat16 *Wop, const float *sw, const int32_t *w_l1,
                          const float *bias, const float *residual, int64_t M, int64_t N,
