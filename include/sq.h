@@ -272,8 +272,8 @@ sq_status sq_quantize_act_rowmax(const float *X, const float *s, const float *ro
  * (no mask).  QKV fp32 [B*S][3*H*D]: the Q, K and V blocks of H*D columns
  * each, head h at columns h*D of a block (sq_linear_i8's output with
  * N = 3*H*D); O fp32 [B*S][H*D]; both 16-byte aligned, not overlapping.
- * scale finite (1/sqrt(D) for BERT).  D = 64; S a multiple of 64, at most 448
- * (SQ_ERR_UNSUPPORTED otherwise).  The contractions run on the tensor cores in
+ * scale finite (1/sqrt(D) for BERT).  D = 64; S a multiple of 64, at most 448;
+ * B*S below 2^31 and H at most 65536 (SQ_ERR_UNSUPPORTED otherwise).  The contractions run on the tensor cores in
  * split tf32 (each operand as an exact pair of tf32 numbers, products within
  * about 2^-21 relative), the softmax in fp32: O agrees with the exact
  * definition to about 1e-6 of max |O|. */

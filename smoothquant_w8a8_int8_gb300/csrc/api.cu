@@ -283,7 +283,7 @@ sq_status sq_attention(const float *QKV, int64_t B, int64_t S, int64_t H, int64_
     if (!(scale == scale) || !(fabsf(scale) <= 3.4028234663852886e38f)) return SQ_ERR_INVALID_ARG;
     if (D != 64 || S % 64 != 0 || S > 448) return SQ_ERR_UNSUPPORTED;
     if (B == 0 || S == 0 || H == 0) return SQ_OK;
-    if (B * S > ((int64_t)1 << 31) || H > 65536) return SQ_ERR_UNSUPPORTED;
+    if (B * S >= ((int64_t)1 << 31) || H > 65536) return SQ_ERR_UNSUPPORTED;
     if (!QKV || !O) return SQ_ERR_INVALID_ARG;
     if (!aligned16(QKV) || !aligned16(O)) return SQ_ERR_ALIGNMENT;
     sq_status rc = require_sm103();

@@ -238,6 +238,8 @@ def test_workspace_entry_points_check_arguments_first(lib):
     assert at(a, 2, 128, 4, 32, 0.125, a, None) == UNSUP          # head dimension
     assert at(a, 2, 100, 4, 64, 0.125, a, None) == UNSUP          # S % 64
     assert at(a, 2, 512, 4, 64, 0.125, a, None) == UNSUP          # S > 448
+    assert at(a, 1 << 25, 64, 4, 64, 0.125, a, None) == UNSUP     # B*S = 2^31
+    assert at(a, 2, 128, 65537, 64, 0.125, a, None) == UNSUP      # H
     assert at(_fake(0x10008), 2, 128, 4, 64, 0.125, a, None) == ALIGN
     assert at(None, 0, 128, 4, 64, 0.125, None, None) == 0
     sw = lib.sq_static_workspace
