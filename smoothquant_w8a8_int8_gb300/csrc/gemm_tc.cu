@@ -335,6 +335,7 @@ struct EpiArgs {
     int rq_vec;     // 1: rows of the code arrays are 16-byte multiples (N % 16 == 0)
     int rq_fast;    // 1: scale >= 2^-70, so the reciprocal division may be used
     Schedule sched;     // work units (made on the host)
+    int pair_plan;      // pair kernel: the cluster count its schedule is planned for
     int32_t *ws_cnt;    // split-K counters (zero between launches), or null
     int4 *ws_slots;     // split-K partial slots
 };
@@ -1248,7 +1249,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int cluster_id = blockIdx.x >> 1;
     const int num_clusters = gridDim.x >> 1;
     const PairSchedule sched =
-        make_pair_schedule((M + 2 * BM - 1) / (2 * BM), (N + BN - 1) / BN, num_clusters);
+        make_pair_schedule((M + 2 * BM - 1) / (2 * BM), (N + BN - 1) / BN, args.pair_plan);
     const int num_items = sched.items;
     const int nkb = (K + BK - 1) / BK;
     const int chunk_kb = exact_pass_kb(args, nkb, warp, lane, S.l1max);
@@ -1545,11 +1546,18 @@ sq_status launch_pair_kernel(const CUtensorMap &ta, const CUtensorMap &tbp, cons
     sq_status rc = setup_kernel(ks, gemm_tc_pair_kernel<MODE, OUT>, PAIR_SMEM_BYTES, device,
                                 &cfg, &max_clusters);
     if (rc != SQ_OK) return rc;
-    const int clusters = std::min(pair_tiles, max_clusters);
+    // the schedule is planned for every cluster that fits; the grid holds no
+    // more clusters than it has items (the kernel strides by the grid's count)
+    (void)pair_tiles;
+    EpiArgs a = args;
+    a.pair_plan = max_clusters;
+    const PairSchedule ps = make_pair_schedule((args.M + 2 * BM - 1) / (2 * BM),
+                                               (args.N + BN - 1) / BN, max_clusters);
+    const int clusters = std::min(ps.items, max_clusters);
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
     cfg.numAttrs = 2;  // the launch: cluster shape and programmatic serialisation
     return cuda_status(
-        cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<MODE, OUT>, ta, tbp, tbq, ty, args, K));
+        cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<MODE, OUT>, ta, tbp, tbq, ty, a, K));
 }
 
 template <int MODE>

@@ -182,7 +182,9 @@ inline bool fits_scratch(long long need, long long capacity) { return need <= ca
 // one round of halves then replaces the round of whole tiles.  (With more
 // than half the clusters busy, halves would need two rounds, and a half
 // tile, which reads as much of A as a whole one for half the products, takes
-// well over half a tile's time: measured slower on GB300.)
+// well over half a tile's time: measured slower on GB300.)  A launch with at
+// most half as many tiles as clusters runs all its tiles as halves, on twice
+// the clusters.
 struct PairSchedule {
     int m_pairs, n_tiles, full_items, sub, items;
 };
@@ -194,7 +196,7 @@ __host__ __device__ inline PairSchedule make_pair_schedule(int m_pairs, int n_ti
     sc.n_tiles = n_tiles;
     const int tiles = m_pairs * n_tiles;
     const int waves = tiles / clusters, rem = tiles - waves * clusters;
-    sc.sub = (waves >= 1 && rem > 0 && 2 * rem <= clusters) ? 2 : 1;
+    sc.sub = (rem > 0 && 2 * rem <= clusters) ? 2 : 1;  // waves = 0: 2 tiles <= clusters
     sc.full_items = sc.sub == 1 ? tiles : waves * clusters;
     sc.items = sc.full_items + (tiles - sc.full_items) * sc.sub;
     return sc;

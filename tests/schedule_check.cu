@@ -93,9 +93,9 @@ static void check_one_cta(long long M, long long N, long long K, int sms, bool s
 
 static void check_pair(long long M, long long N, int clusters) {
     const int m_pairs = (int)((M + 2 * BM - 1) / (2 * BM)), n_tiles = (int)((N + BN - 1) / BN);
-    const int tiles = m_pairs * n_tiles;
-    const int used = tiles < clusters ? tiles : clusters;
-    const PairSchedule sc = make_pair_schedule(m_pairs, n_tiles, used);
+    // planned for every cluster that fits, run on no more clusters than items
+    const PairSchedule sc = make_pair_schedule(m_pairs, n_tiles, clusters);
+    const int used = sc.items < clusters ? sc.items : clusters;
     std::vector<unsigned char> cover((size_t)m_pairs * n_tiles * 2, 0);
     for (int cl = 0; cl < used; ++cl) {
         for (int i = cl; i < sc.items; i += used) {
