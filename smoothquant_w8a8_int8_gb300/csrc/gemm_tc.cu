@@ -1525,8 +1525,8 @@ sq_status launch_mode(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
 // more than can be resident at once (it is persistent).
 template <int MODE, int OUT>
 sq_status launch_pair_kernel(const CUtensorMap &ta, const CUtensorMap &tbp, const CUtensorMap &tbq,
-                             const CUtensorMap &ty, const EpiArgs &args, int K, int pair_tiles,
-                             int device, cudaStream_t st) {
+                             const CUtensorMap &ty, const EpiArgs &args, int K, int device,
+                             cudaStream_t st) {
     static KernelSetup ks;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(THREADS, 1, 1);
@@ -1548,7 +1548,6 @@ sq_status launch_pair_kernel(const CUtensorMap &ta, const CUtensorMap &tbp, cons
     if (rc != SQ_OK) return rc;
     // the schedule is planned for every cluster that fits; the grid holds no
     // more clusters than it has items (the kernel strides by the grid's count)
-    (void)pair_tiles;
     EpiArgs a = args;
     a.pair_plan = max_clusters;
     const PairSchedule ps = make_pair_schedule((args.M + 2 * BM - 1) / (2 * BM),
@@ -1562,16 +1561,15 @@ sq_status launch_pair_kernel(const CUtensorMap &ta, const CUtensorMap &tbp, cons
 
 template <int MODE>
 sq_status launch_pair_mode(const CUtensorMap &ta, const CUtensorMap &tbp, const CUtensorMap &tbq,
-                           const CUtensorMap &ty, const EpiArgs &args, int K, int pair_tiles,
-                           int device, int out, cudaStream_t st) {
+                           const CUtensorMap &ty, const EpiArgs &args, int K, int device,
+                           int out, cudaStream_t st) {
     if (out == kOutRequant)
-        return launch_pair_kernel<MODE, kOutRequant>(ta, tbp, tbq, ty, args, K, pair_tiles,
-                                                     device, st);
+        return launch_pair_kernel<MODE, kOutRequant>(ta, tbp, tbq, ty, args, K, device,
+                                                     st);
     if (out == kOutRowMax)
-        return launch_pair_kernel<MODE, kOutRowMax>(ta, tbp, tbq, ty, args, K, pair_tiles,
-                                                    device, st);
-    return launch_pair_kernel<MODE, kOutPlain>(ta, tbp, tbq, ty, args, K, pair_tiles, device,
-                                               st);
+        return launch_pair_kernel<MODE, kOutRowMax>(ta, tbp, tbq, ty, args, K, device,
+                                                    st);
+    return launch_pair_kernel<MODE, kOutPlain>(ta, tbp, tbq, ty, args, K, device, st);
 }
 
 // Which kernel runs a launch: CTA pairs for every launch of at least one full
@@ -1683,20 +1681,20 @@ sq_status launch_gemm_tc(const __nv_bfloat16 *Xop, const float *sx, const int32_
             (rc = make_map(&tbq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Wop, N, K, PAIR_B_ROWS / 2,
                            BK)) != SQ_OK)
             return rc;
-        const int64_t pt = ((M + 2 * BM - 1) / (2 * BM)) * ((N + BN - 1) / BN);
-        if (pt > 0x7fffffff) return SQ_ERR_UNSUPPORTED;
-        const int p = (int)pt;
+        // the pair schedule counts its tiles (and twice that in halves) in int
+        if (((M + 2 * BM - 1) / (2 * BM)) * ((N + BN - 1) / BN) > 0x3fffffff)
+            return SQ_ERR_UNSUPPORTED;
         switch (mode) {
         case SQ_EPI_NONE:
-            return launch_pair_mode<SQ_EPI_NONE>(ta, tbp, tbq, ty, args, k, p, dev, q, st);
+            return launch_pair_mode<SQ_EPI_NONE>(ta, tbp, tbq, ty, args, k, dev, q, st);
         case SQ_EPI_BIAS:
-            return launch_pair_mode<SQ_EPI_BIAS>(ta, tbp, tbq, ty, args, k, p, dev, q, st);
+            return launch_pair_mode<SQ_EPI_BIAS>(ta, tbp, tbq, ty, args, k, dev, q, st);
         case SQ_EPI_BIAS_GELU:
-            return launch_pair_mode<SQ_EPI_BIAS_GELU>(ta, tbp, tbq, ty, args, k, p, dev, q, st);
+            return launch_pair_mode<SQ_EPI_BIAS_GELU>(ta, tbp, tbq, ty, args, k, dev, q, st);
         case SQ_EPI_BIAS_RESIDUAL:
-            return launch_pair_mode<SQ_EPI_BIAS_RESIDUAL>(ta, tbp, tbq, ty, args, k, p, dev, q, st);
+            return launch_pair_mode<SQ_EPI_BIAS_RESIDUAL>(ta, tbp, tbq, ty, args, k, dev, q, st);
         default:
-            return launch_pair_kernel<SQ_EPI_RAW_I32, kOutPlain>(ta, tbp, tbq, ty, args, k, p, dev,
+            return launch_pair_kernel<SQ_EPI_RAW_I32, kOutPlain>(ta, tbp, tbq, ty, args, k, dev,
                                                                  st);
         }
     }
