@@ -137,7 +137,10 @@ def test_quantize_row_max_near_ties(sq):
     assert_codes_equal(op_as_int(Xop), q_ref, "Xop")
 
 
-@pytest.mark.parametrize("K", [1024, 4096])
+# 1024 and 4096: the register kernel on rows of 1024 * 2^k; 3072: the register
+# kernel on rows it fills unevenly; 768: the ring kernel (the rows repeated to
+# 2520, at least 16 per SM of a GB300, where the dispatch takes the ring)
+@pytest.mark.parametrize("K", [768, 1024, 3072, 4096])
 def test_quantize_extreme_magnitudes(sq, K):
     """Rows whose largest |x/s| sits at extreme magnitudes (2^-61 .. 2^101,
     each a hair below, at and above a power of two), smoothing factors far
@@ -152,6 +155,8 @@ def test_quantize_extreme_magnitudes(sq, K):
         for f in (np.float32(1 - 2.0 ** -20), np.float32(1), np.float32(1 + 2.0 ** -20)):
             rows.append((base * np.float32(m) * f * s).astype(np.float32))
     X = np.stack(rows).astype(np.float32)
+    if K == 768:
+        X = np.tile(X, (140, 1))
     for s_case in (s, np.where(np.arange(K) == 5, np.float32(1e-7), s).astype(np.float32),
                    np.where(np.arange(K) == 9, np.float32(3e7), s).astype(np.float32)):
         q_ref, sx_ref = oracle.quantize_rows(X, s_case, "act")
