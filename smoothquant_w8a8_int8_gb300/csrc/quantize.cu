@@ -608,6 +608,18 @@ __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
         const float a = fabsf(x);
         return (a >= 0x1p-20f && a <= 0x1p20f) ? __frcp_rn(x) : __int_as_float(0x7fffffff);
     };
+    const int rpb = kThreads / tpr;
+    const int g = threadIdx.x / tpr;
+    const int t = threadIdx.x % tpr;
+    {
+        // the group's first row on its way into L2 while the tables are built
+        const int64_t row0 = (int64_t)blockIdx.x * rpb + g;
+        if (t == 0 && row0 < rows)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                             reinterpret_cast<const float4 *>(A) + row0 * K4),
+                         "r"((uint32_t)K4 * 16u)
+                         : "memory");
+    }
     const float4 *s4 = reinterpret_cast<const float4 *>(s);
     for (int j = threadIdx.x; j < K4; j += kThreads) {
         const float4 v = __ldg(s4 + j);
@@ -615,9 +627,6 @@ __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
         ytab[j] = make_float4(recip(v.x), recip(v.y), recip(v.z), recip(v.w));
     }
     __syncthreads();
-    const int rpb = kThreads / tpr;
-    const int g = threadIdx.x / tpr;
-    const int t = threadIdx.x % tpr;
     const unsigned long long magic2 = pk(kRoundMagic, kRoundMagic);
     const int64_t tiles = (rows + rpb - 1) / rpb;
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
