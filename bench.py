@@ -407,6 +407,44 @@ def copy_ceiling(h2d_pairs, d2h_pairs, reps: int = 2) -> float:
     return e0.elapsed_time(e1) / reps
 
 
+def codes_operand_leg(args, layers, bufs, M, ops_per_step, world):
+    """The same step with the activation codes in their int8 format: the
+    quantiser writes Xq (1 B per element) and sq_linear_i8_codes widens them
+    into the bf16 operand before the GEMM (the default step has the quantiser
+    write the bf16 operand itself).  Timed like `value`: K steps, no events
+    between kernels, warm-up first."""
+    from smoothquant_w8a8_int8_gb300 import binding as sq
+    Xq_buf, sx_buf, Xop_buf = bufs[0], bufs[1], bufs[2]
+    ws = Xop_buf.view(torch.uint8)  # the widened operand, where the default step keeps it
+
+    def step():
+        for L in layers:
+            K = L.lin.K
+            Xq = Xq_buf[: M * K].view(M, K)
+            sq.quantize_act(L.X, L.s, out=(Xq, sx_buf, None))
+            sq.linear_i8_codes(Xq, sx_buf, L.Wop, L.sw, L.bias, L.residual, L.lin.mode,
+                               out=L.Y, w_l1=L.wl1, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    replicas.barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    rc = sq.device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status after the int8-operand run: {sq.status_string(rc)}")
+    ms = replicas.max_over_ranks(t0.elapsed_time(t1), device="cuda") / args.steps
+    return {"value": round(replicas.whole_job_tops(ops_per_step, world, ms), 3), "unit": "TOPS",
+            "ms_per_step": round(ms, 4),
+            "path": "sq_quantize_act writing int8 codes, then sq_linear_i8_codes (an exact "
+                    "widening pass into the bf16 operand, then the same tcgen05 GEMM)"}
+
+
 def e2e_leg(args, layers, M, ops_per_step, world):
     """The block end to end through the public host-buffer API
     (HostLinearPipeline): K steps timed with CUDA events, every output
@@ -606,6 +644,9 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int, headline: bool = Tru
     e2e = None
     if args.e2e_steps > 0 and not chained and not args.ln and headline:
         e2e = e2e_leg(args, layers, M, ops_per_step, world)
+    codes = None
+    if headline and args.gemm == "tc" and args.quant == "dynamic" and not chained and not args.ln:
+        codes = codes_operand_leg(args, layers, bufs, M, ops_per_step, world)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and headline:
@@ -683,6 +724,7 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int, headline: bool = Tru
                                "gemm": round(g_ms / args.steps, 4)},
         "gpu_launches": n_gemm * args.steps + n_quant,
         "back_to_back": back_to_back,
+        "int8_operand": codes,
         "clocks": clock_info,
         "e2e": e2e,
         "cpu_baseline": cpu,

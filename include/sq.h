@@ -204,6 +204,27 @@ sq_status sq_linear_i8(const void *Xop, const float *x_scale, const int32_t *x_r
                        const float *bias, const float *residual, int64_t M, int64_t N, int64_t K,
                        int mode, void *Y, void *stream);
 
+/* sq_linear_i8 on the int8 activation codes Xq [M][K] (as sq_quantize_act
+ * writes them) instead of the GEMM-operand buffer: the per-token x per-channel
+ * INT8 recipe's own input format.  sm_103a's tensor cores take no int8
+ * operands, so the codes are first widened, exactly, into the bf16 operand in
+ * `workspace` (one streaming pass: M*K bytes read, 2*M*K written), and the
+ * tcgen05 GEMM then runs as sq_linear_i8 on it: results bit for bit those of
+ * sq_linear_i8 on sq_quantize_act's Xop.  (The pair kernel cannot widen inside
+ * its operand path without a per-stage handshake between its two CTAs; the
+ * quantiser writes the bf16 operand in the time it writes the codes, so
+ * sq_quantize_act + sq_linear_i8 stays the faster pair.)
+ * sq_linear_codes_workspace_bytes: *bytes = the workspace an M x K call needs
+ * (2*M*K rounded up to 256).  Xq and workspace 16-byte aligned, the workspace
+ * overlapping no other argument; workspace_bytes below the requirement:
+ * SQ_ERR_INVALID_ARG.  Other arguments, limits and statuses as sq_linear_i8. */
+sq_status sq_linear_codes_workspace_bytes(int64_t M, int64_t K, size_t *bytes);
+sq_status sq_linear_i8_codes(const int8_t *Xq, const float *x_scale, const int32_t *x_row_l1,
+                             const void *Wop, const float *w_scale, const int32_t *w_row_l1,
+                             const float *bias, const float *residual, int64_t M, int64_t N,
+                             int64_t K, int mode, void *Y, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
 /* ---- Producer-fused Smooth-Static quantisation ------------------------------ */
 
 /* sq_linear_i8 whose epilogue hands its results straight to the NEXT linear

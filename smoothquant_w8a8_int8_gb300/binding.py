@@ -24,6 +24,7 @@ EXPORTS = ("sq_status_string", "sq_version", "sq_operand_bytes", "sq_packed_weig
            "sq_channel_absmax",
            "sq_smooth_factor", "sq_pack_weight", "sq_quantize_act", "sq_act_absmax",
            "sq_static_scale", "sq_quantize_act_static", "sq_layernorm_quant", "sq_linear_i8",
+           "sq_linear_codes_workspace_bytes", "sq_linear_i8_codes",
            "sq_linear_i8_requant", "sq_division_table", "sq_linear_i8_rowmax",
            "sq_quantize_act_rowmax", "sq_attention", "sq_linear_workspace_bytes", "sq_linear_i8_ws",
            "sq_linear_i8_requant_ws", "sq_linear_i8_static_ws", "sq_static_workspace_reset",
@@ -75,6 +76,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                 "sq_quantize_act_rowmax": ([vp, vp, vp, i64, i64, vp, vp, vp, vp, vp], i32),
                 "sq_attention": ([vp, i64, i64, i64, i64, f32, vp, vp], i32),
                 "sq_linear_workspace_bytes": ([i64, i64, i64, vp], i32),
+                "sq_linear_codes_workspace_bytes": ([i64, i64, vp], i32),
+                "sq_linear_i8_codes": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp,
+                                        vp, ctypes.c_size_t, vp], i32),
                 "sq_linear_i8_ws": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp,
                                      ctypes.c_size_t, vp], i32),
                 "sq_linear_i8_requant_ws": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32,
@@ -294,6 +298,33 @@ def linear_i8(Xop, x_scale, Wop, w_scale, bias=None, residual=None, mode=EPI_BIA
     _check(load().sq_linear_i8(_p(Xop), _p(x_scale), _p(x_l1), _p(Wop), _p(w_scale), _p(w_l1),
                                _p(bias), _p(residual), M, N, K, int(mode), _p(out),
                                _stream(stream)), "sq_linear_i8")
+    return out
+
+
+def codes_workspace_bytes(M: int, K: int) -> int:
+    """Bytes of the workspace linear_i8_codes widens an M x K code matrix into."""
+    n = ctypes.c_size_t(0)
+    _check(load().sq_linear_codes_workspace_bytes(M, K, ctypes.byref(n)),
+           "sq_linear_codes_workspace_bytes")
+    return int(n.value)
+
+
+def linear_i8_codes(Xq, x_scale, Wop, w_scale, bias=None, residual=None, mode=EPI_BIAS,
+                    out=None, x_l1=None, w_l1=None, workspace=None, stream=None):
+    """linear_i8 on int8 activation codes Xq [M, K]: the codes are widened
+    exactly into the bf16 operand in `workspace` (uint8, at least
+    codes_workspace_bytes(M, K); allocated here if None), then the tcgen05
+    GEMM runs on it."""
+    _need(Xq, torch.int8, "Xq")
+    _need(Wop, torch.bfloat16, "Wop")
+    M, N, K, out = _out(Xq, Wop, mode, out)
+    if workspace is None:
+        workspace = torch.empty(max(codes_workspace_bytes(M, K), 16), dtype=torch.uint8,
+                                device=Xq.device)
+    wp, wn = _workspace(workspace)
+    _check(load().sq_linear_i8_codes(_p(Xq), _p(x_scale), _p(x_l1), _p(Wop), _p(w_scale),
+                                     _p(w_l1), _p(bias), _p(residual), M, N, K, int(mode),
+                                     _p(out), wp, wn, _stream(stream)), "sq_linear_i8_codes")
     return out
 
 

@@ -358,6 +358,41 @@ sq_status sq_linear_i8_ws(const void *Xop, const float *x_scale, const int32_t *
                        mode, Y, workspace, workspace_bytes, stream);
 }
 
+sq_status sq_linear_codes_workspace_bytes(int64_t M, int64_t K, size_t *bytes) {
+    if (!bytes) return SQ_ERR_INVALID_ARG;
+    *bytes = 0;
+    if (M < 0 || K <= 0) return SQ_ERR_INVALID_ARG;
+    if (K % 16 != 0) return SQ_ERR_ALIGNMENT;
+    if (K > kMaxK || M > ((int64_t)1 << 40) / K) return SQ_ERR_UNSUPPORTED;
+    *bytes = (size_t)((M * K * 2 + 255) / 256 * 256);
+    return SQ_OK;
+}
+
+sq_status sq_linear_i8_codes(const int8_t *Xq, const float *x_scale, const int32_t *x_row_l1,
+                             const void *Wop, const float *w_scale, const int32_t *w_row_l1,
+                             const float *bias, const float *residual, int64_t M, int64_t N,
+                             int64_t K, int mode, void *Y, void *workspace, size_t workspace_bytes,
+                             void *stream) {
+    size_t need = 0;
+    sq_status rc = sq_linear_codes_workspace_bytes(M, K, &need);
+    if (rc != SQ_OK) return rc;
+    if (M > 0 && N > 0) {
+        if (!Xq || !workspace) return SQ_ERR_INVALID_ARG;
+        if (!aligned16(Xq) || !aligned16(workspace)) return SQ_ERR_ALIGNMENT;
+        if (workspace_bytes < need) return SQ_ERR_INVALID_ARG;
+    }
+    // the operand the codes widen into is the workspace: the checks of sq_linear_i8 on it
+    if ((rc = validate_linear(workspace, x_scale, x_row_l1, Wop, w_scale, w_row_l1, bias,
+                              residual, M, N, K, mode, Y)) != SQ_OK ||
+        M == 0 || N == 0)
+        return rc;
+    if ((rc = require_gb300()) != SQ_OK) return rc;
+    __nv_bfloat16 *op = static_cast<__nv_bfloat16 *>(workspace);
+    if ((rc = launch_widen_codes(Xq, op, M * K, as_stream(stream))) != SQ_OK) return rc;
+    return linear_impl(op, x_scale, x_row_l1, Wop, w_scale, w_row_l1, bias, residual, M, N, K,
+                       mode, Y, nullptr, 0, stream);
+}
+
 sq_status sq_linear_i8_requant(const void *Xop, const float *x_scale, const int32_t *x_row_l1,
                                const void *Wop, const float *w_scale, const int32_t *w_row_l1,
                                const float *bias, const float *residual, int64_t M, int64_t N,

@@ -186,6 +186,9 @@ sq_status gemm_tc_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes
 // activation quantiser (synchronous).
 sq_status gemm_tc_take_error(cudaStream_t st);
 sq_status quant_take_error(cudaStream_t st);
+// int8 codes [count] -> the bf16 GEMM operand (exact); count % 16 == 0, both
+// pointers 16-byte aligned.
+sq_status launch_widen_codes(const int8_t *q, __nv_bfloat16 *op, int64_t count, cudaStream_t st);
 sq_status attention_take_error(cudaStream_t st);
 // A 2-D TMA tensor map (a CUtensorMap, 128 bytes) over a row-major fp32 matrix
 // of rows x cols, boxes of box_rows x box_cols, 128-byte swizzle.

@@ -1024,6 +1024,52 @@ sq_status launch_quantize_act_dynamic(const float *A, const float *s, int64_t ro
                       wpr, groups, stages, q, scale, op, l1, row_amax);
 }
 
+// int8 codes -> the bf16 GEMM operand, 16 codes per thread per pass (one
+// 16-byte load, two 16-byte stores); every |q| <= 127 is exact in bf16, whose
+// bit pattern is the high half of the fp32 value.
+__global__ void __launch_bounds__(kThreads) widen_codes_kernel(const uint4 *__restrict__ q,
+                                                             uint4 *__restrict__ op, int64_t n16) {
+    pdl_launch_dependents();
+    pdl_wait();
+    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < n16;
+         i += (int64_t)gridDim.x * kThreads) {
+        const uint4 c = __ldcs(q + i);
+        const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t b0 = __float_as_uint((float)(int8_t)(w[k] & 0xff));
+            const uint32_t b1 = __float_as_uint((float)(int8_t)((w[k] >> 8) & 0xff));
+            const uint32_t b2 = __float_as_uint((float)(int8_t)((w[k] >> 16) & 0xff));
+            const uint32_t b3 = __float_as_uint((float)(int8_t)(w[k] >> 24));
+            o[2 * k] = __byte_perm(b0, b1, 0x7632);
+            o[2 * k + 1] = __byte_perm(b2, b3, 0x7632);
+        }
+        op[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
+        op[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+sq_status launch_widen_codes(const int8_t *q, __nv_bfloat16 *op, int64_t count, cudaStream_t st) {
+    DeviceInfo di;
+    sq_status rc = device_info(&di);
+    if (rc != SQ_OK) return rc;
+    const int64_t n16 = count / 16;
+    if (n16 == 0) return SQ_OK;
+    static std::mutex mu;
+    static int occ[64] = {};
+    int o = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        int &r = occ[di.device & 63];
+        if (!r) r = resident_blocks(widen_codes_kernel);
+        o = r;
+    }
+    const int64_t grid = std::min<int64_t>((n16 + kThreads - 1) / kThreads, (int64_t)di.sms * o);
+    return launch_pdl(widen_codes_kernel, dim3((unsigned)grid), dim3(kThreads), 0, st, 1,
+                      reinterpret_cast<const uint4 *>(q), reinterpret_cast<uint4 *>(op), n16);
+}
+
 sq_status quant_take_error(cudaStream_t st) {
     unsigned int word = 0;
     if (cudaMemcpyFromSymbolAsync(&word, g_quant_error, sizeof(word), 0, cudaMemcpyDeviceToHost,

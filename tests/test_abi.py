@@ -186,6 +186,28 @@ def test_workspace_entry_points_check_arguments_first(lib):
               None) == INVALID                                         # raw int32 mode
     assert rq(a, a, None, a, a, None, a, None, 8, 8, 32, 1, a, 1.0, a, a, None, _fake(0x10004),
               1 << 20, None) == ALIGN
+    cb = lib.sq_linear_codes_workspace_bytes
+    cb.argtypes = [i64, i64, vp]
+    assert cb(8, 32, None) == INVALID
+    assert cb(-1, 32, ctypes.byref(n)) == INVALID
+    assert cb(8, 40, ctypes.byref(n)) == ALIGN
+    assert cb(8, 133152, ctypes.byref(n)) == UNSUP
+    assert cb(3, 32, ctypes.byref(n)) == 0 and n.value == 256       # 2*3*32 rounded up
+    assert cb(1024, 1024, ctypes.byref(n)) == 0 and n.value == 2 << 20
+    cd = lib.sq_linear_i8_codes
+    cd.argtypes = [vp] * 8 + [i64, i64, i64, i32, vp, vp, sz, vp]
+    assert cd(None, a, None, a, a, None, a, None, 8, 8, 32, 1, a, a, 1 << 20, None) == INVALID
+    assert cd(a, a, None, a, a, None, a, None, 8, 8, 32, 1, a, None, 1 << 20, None) == INVALID
+    assert cd(a, a, None, a, a, None, a, None, 8, 8, 32, 1, a, a, 256, None) == INVALID  # small
+    assert cd(_fake(0x10004), a, None, a, a, None, a, None, 8, 8, 32, 1, a, a, 1 << 20,
+              None) == ALIGN
+    assert cd(a, a, None, a, a, None, a, None, 8, 8, 32, 1, a, _fake(0x10008), 1 << 20,
+              None) == ALIGN
+    assert cd(a, a, None, a, a, None, None, None, 8, 8, 32, 1, a, a, 1 << 20,
+              None) == INVALID                                         # bias mode, no bias
+    assert cd(a, a, None, a, a, None, a, None, 8, 8, 40, 1, a, a, 1 << 20, None) == ALIGN
+    assert cd(None, None, None, None, None, None, None, None, 0, 8, 32, 1, None, None, 0,
+              None) == 0
     st = lib.sq_linear_i8_static_ws
     st.argtypes = [vp] * 8 + [i64, i64, i64, i32, vp, vp]
     assert st(a, a, None, a, a, None, a, None, 8, 8, 133152, 1, a, None) == UNSUP
