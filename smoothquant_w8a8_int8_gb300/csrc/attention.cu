@@ -304,6 +304,32 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                                  ::"l"(reinterpret_cast<uint64_t>(&tmQKV)), "r"(x + 32 * kb), "r"(y)
                                  : "memory");
             }
+            {
+                // the operands of the block one wave on (likely to start on an SM
+                // as this wave's blocks finish) into L2, so that its first copies
+                // come from L2 rather than DRAM
+                const int fb = blockIdx.x + 152;
+                if (fb < (int)gridDim.x) {
+                    const int fqt = fb % qtiles, fh = (fb / qtiles) % H, fbb = fb / (qtiles * H);
+                    const int frow = fbb * S;
+                    for (int kb = 0; kb < 2; ++kb) {
+                        for (int rh = 0; rh < 2; ++rh)
+                            if (fqt * ABQ + 64 * rh < S)  // its query rows inside its sequence
+                                asm volatile(
+                                    "cp.async.bulk.prefetch.tensor.2d.L2.global.tile"
+                                    " [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(&tmQKV)),
+                                    "r"(fh * AD + 32 * kb), "r"(frow + fqt * ABQ + 64 * rh)
+                                    : "memory");
+                        for (int n = 0; n < nch; ++n)
+                            for (int part = 1; part < 3; ++part)
+                                asm volatile(
+                                    "cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                                    ::"l"(reinterpret_cast<uint64_t>(&tmQKV)),
+                                    "r"(part * H * AD + fh * AD + 32 * kb), "r"(frow + n * ACH)
+                                    : "memory");
+                    }
+                }
+            }
             int uses[4] = {0, 0, 0, 0};
             for (int n = 0; n < 2 * nch; ++n) {
                 const int sl = chunk_slot(n, nch);
