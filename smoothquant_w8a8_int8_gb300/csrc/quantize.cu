@@ -1176,7 +1176,13 @@ sq_status launch_quantize_rows(int direction, const float *A, const float *s, in
                     return SQ_ERR_CUDA;
                 occ = o;
             }
-            const int64_t grid = std::min<int64_t>(tiles, (int64_t)di.sms * occ);
+            // twice the blocks that fit at once: measured on GB300 in the
+            // BERT-large step (each quantiser between two GEMMs, launched
+            // with programmatic dependent launch) 756 -> 782-788 TOPS against
+            // one resident wave, while three, four times or one tile per
+            // block ran slower (763, 754, 698 TOPS); a launch timed on its own
+            // runs a little slower (2.63 against 2.55 ms per step)
+            const int64_t grid = std::min<int64_t>(tiles, 2 * (int64_t)di.sms * occ);
             return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, 1, A, s, rows,
                               K4, tpr, q, scale, op, l1, fixed_scale);
         } else if (direction == kWeight)
