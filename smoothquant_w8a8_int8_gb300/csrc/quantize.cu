@@ -589,15 +589,19 @@ __device__ __forceinline__ float group_max_nan(float m, int tpr, float *red) {
 // A row whose maximum is NaN or outside [2^-60, 2^100] takes IEEE divisions
 // throughout; the choice is made per block (the group reductions hold block
 // barriers), so a block with one such row codes all its rows that way, which
-// is exact too.  While a tile is coded, one thread per row group asks for the
+// is exact too.  GIVEN: the row maxima come from row_amax (as the row-maximum
+// GEMM epilogue leaves them) instead of the reduction, and the codes saturate
+// at +-127 (a maximum below the true one cannot wrap them); an out-of-range
+// maximum still sends the block to the IEEE path, which finds its own.
+// While a tile is coded, one thread per row group asks for the
 // group's next row to be brought into L2 (a bulk prefetch, no registers held),
 // so that DRAM stays busy through the reductions and stores (measured 7% on
 // 8192 x 4096; a second row ahead measured slower).
-template <int kVPT>
+template <int kVPT, bool GIVEN>
 __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
     const float *__restrict__ A, const float *__restrict__ s, int64_t rows, int K4, int tpr,
     int8_t *__restrict__ q, float *__restrict__ scale, __nv_bfloat16 *__restrict__ op,
-    int32_t *__restrict__ l1, float /* unused: the register kernels' common signature */) {
+    int32_t *__restrict__ l1, const float *__restrict__ row_amax) {
     extern __shared__ float4 qtab[];
     float4 *nstab = qtab;       // -s
     float4 *ytab = qtab + K4;   // RN(1/s) or NaN
@@ -648,12 +652,13 @@ __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
             int j = t + i * tpr;
             v[i] = (valid && j < K4) ? __ldcs(a4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        // row maximum, div_smooth on f32x2 pairs
+        // row maximum, div_smooth on f32x2 pairs (GIVEN: read)
         float m = 0.0f;
+        if (GIVEN) m = valid ? __ldg(row_amax + row) : 0.0f;
 #pragma unroll
         for (int i = 0; i < kVPT; ++i) {
             const int j = t + i * tpr;
-            if (j >= K4) continue;
+            if (GIVEN || j >= K4) continue;
             const float4 y = ytab[j], ns = nstab[j];
             const unsigned long long x01 = pk(v[i].x, v[i].y), x23 = pk(v[i].z, v[i].w);
             const unsigned long long y01 = pk(y.x, y.y), y23 = pk(y.z, y.w);
@@ -664,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
             m = max3_nan(m, fabsf(d0), fabsf(d1));
             m = max3_nan(m, fabsf(d2), fabsf(d3));
         }
-        m = group_max_nan(m, tpr, red);
+        if (!GIVEN) m = group_max_nan(m, tpr, red);
         const bool exact = __syncthreads_or(valid && !(m >= 0x1p-60f && m <= 0x1p100f));
         float a1 = 0.0f;
         if (exact) {
@@ -721,6 +726,10 @@ __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
                         if (!(fabsf(d[1]) <= kTieLimit)) c[1] = exact_code(v[i].y, -ns.y, sc);
                         if (!(fabsf(d[2]) <= kTieLimit)) c[2] = exact_code(v[i].z, -ns.z, sc);
                         if (!(fabsf(d[3]) <= kTieLimit)) c[3] = exact_code(v[i].w, -ns.w, sc);
+                    }
+                    if (GIVEN) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) c[e] = fminf(127.0f, fmaxf(-127.0f, c[e]));
                     }
                     store4_codes(c[0], c[1], c[2], c[3], ((int64_t)row * K4 + j) * 4, q, op);
                     a1 += (fabsf(c[0]) + fabsf(c[1])) + (fabsf(c[2]) + fabsf(c[3]));
@@ -1107,12 +1116,71 @@ sq_status launch_division_table(const float *s, int64_t K, float *table, cudaStr
                       reinterpret_cast<float2 *>(table));
 }
 
+// The register Smooth-Dynamic kernel (K <= 8192): its tables of -s and 1/s in
+// shared memory (8 bytes per column), its residency at that size, and the grid.
+sq_status launch_act_reg(const float *A, const float *s, int64_t rows, int64_t K, int8_t *q,
+                         float *scale, __nv_bfloat16 *op, int32_t *l1, const float *row_amax,
+                         const DeviceInfo &di, cudaStream_t st) {
+    const int K4 = (int)(K / 4);
+    const bool small = K4 <= kThreads * 4;
+    const int vpt = small ? 4 : 8;
+    int tpr = 32;
+    while (tpr * vpt < K4) tpr <<= 1;
+    const int rpb = kThreads / tpr;
+    const int64_t tiles = (rows + rpb - 1) / rpb;
+    using Kern = void (*)(const float *, const float *, int64_t, int, int, int8_t *, float *,
+                          __nv_bfloat16 *, int32_t *, const float *);
+    static const Kern kerns[2][2] = {{quantize_act_reg<4, false>, quantize_act_reg<8, false>},
+                                     {quantize_act_reg<4, true>, quantize_act_reg<8, true>}};
+    const int gi = row_amax ? 1 : 0, vi = small ? 0 : 1;
+    const Kern kern = kerns[gi][vi];
+    const int smem = K4 * 32;
+    constexpr int kMaxTab = kThreads * kMaxVPT * 32;  // 64 KB at K = 8192
+    static std::mutex mu;
+    static bool opted[64][2][2] = {};
+    static int occ_dyn[64][2][2][8] = {};  // per device, mode, vpt, 256-float4 bucket of K4
+    int occ = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        const int dv = di.device & 63;
+        if (!opted[dv][gi][vi]) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kMaxTab) != cudaSuccess)
+                return SQ_ERR_CUDA;
+            opted[dv][gi][vi] = true;
+        }
+        // residency at the bucket's largest table (never above the true one)
+        const int bucket = (K4 - 1) / 256;
+        int &o = occ_dyn[dv][gi][vi][bucket];
+        if (!o && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, kThreads,
+                                                                 (bucket + 1) * 256 * 32) !=
+                       cudaSuccess ||
+                   o < 1))
+            return SQ_ERR_CUDA;
+        occ = o;
+    }
+    // twice the blocks that fit at once: measured on GB300 in the BERT-large
+    // step (each quantiser between two GEMMs, launched with programmatic
+    // dependent launch) 756 -> 782-788 TOPS against one resident wave, while
+    // 1.5, 2.5, 3, 4 times or one tile per block ran slower (761, 765, 763,
+    // 754, 698 TOPS); a launch timed on its own runs a little slower
+    const int64_t grid = std::min<int64_t>(tiles, 2 * (int64_t)di.sms * occ);
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, 1, A, s, rows, K4,
+                      tpr, q, scale, op, l1, row_amax);
+}
+
 sq_status launch_quantize_act_given_max(const float *A, const float *s, const float *row_amax,
                                         int64_t rows, int64_t K, int8_t *q, float *scale,
                                         __nv_bfloat16 *op, int32_t *l1, cudaStream_t st) {
     DeviceInfo di;
     sq_status rc = device_info(&di);
     if (rc != SQ_OK) return rc;
+    // the register kernel on the given maxima (measured on GB300 at 8192 x 4096:
+    // faster than the ring kernel's given-maximum mode, which the shorter rows
+    // that are not 1024 * 2^k keep, as in the dynamic dispatch)
+    const bool pow2_rows = K >= 1024 && K <= 8192 && (K & (K - 1)) == 0;
+    if (K <= 8192 && (pow2_rows || K > 2048))
+        return launch_act_reg(A, s, rows, K, q, scale, op, l1, row_amax, di, st);
     if (K <= 8192 && rows >= 16 * (int64_t)di.sms)
         return launch_quantize_act_dynamic(A, s, rows, K, q, scale, op, l1, di, st, row_amax);
     // other launches: the full quantiser (it finds the same maxima itself)
@@ -1147,45 +1215,9 @@ sq_status launch_quantize_rows(int direction, const float *A, const float *s, in
         const int64_t tiles = (rows + rpb - 1) / rpb;
         void (*kern)(const float *, const float *, int64_t, int, int, int8_t *, float *,
                      __nv_bfloat16 *, int32_t *, float);
-        if (direction == kActDynamic) {
-            // tables of -s and 1/s in shared memory: 8 bytes per column
-            kern = small ? quantize_act_reg<4> : quantize_act_reg<8>;
-            const int smem = K4 * 32;
-            constexpr int kMaxTab = kThreads * kMaxVPT * 32;  // 64 KB at K = 8192
-            static std::mutex mu;
-            static bool opted[64][2] = {};
-            static int occ_dyn[64][2][8] = {};  // per device, vpt, 256-float4 bucket of K4
-            int occ = 0;
-            {
-                std::lock_guard<std::mutex> lock(mu);
-                const int dv = di.device & 63, vi = small ? 0 : 1;
-                if (!opted[dv][vi]) {
-                    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kMaxTab) != cudaSuccess)
-                        return SQ_ERR_CUDA;
-                    opted[dv][vi] = true;
-                }
-                // residency at the bucket's largest table (never above the true one)
-                const int bucket = (K4 - 1) / 256;
-                int &o = occ_dyn[dv][vi][bucket];
-                if (!o &&
-                    (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, kThreads,
-                                                                   (bucket + 1) * 256 * 32) !=
-                         cudaSuccess ||
-                     o < 1))
-                    return SQ_ERR_CUDA;
-                occ = o;
-            }
-            // twice the blocks that fit at once: measured on GB300 in the
-            // BERT-large step (each quantiser between two GEMMs, launched
-            // with programmatic dependent launch) 756 -> 782-788 TOPS against
-            // one resident wave, while three, four times or one tile per
-            // block ran slower (763, 754, 698 TOPS); a launch timed on its own
-            // runs a little slower (2.63 against 2.55 ms per step)
-            const int64_t grid = std::min<int64_t>(tiles, 2 * (int64_t)di.sms * occ);
-            return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, 1, A, s, rows,
-                              K4, tpr, q, scale, op, l1, fixed_scale);
-        } else if (direction == kWeight)
+        if (direction == kActDynamic)
+            return launch_act_reg(A, s, rows, K, q, scale, op, l1, nullptr, di, st);
+        if (direction == kWeight)
             kern = small ? quantize_rows_reg<kWeight, 4> : quantize_rows_reg<kWeight, 8>;
         else
             kern = small ? quantize_rows_reg<kActStatic, 4> : quantize_rows_reg<kActStatic, 8>;
