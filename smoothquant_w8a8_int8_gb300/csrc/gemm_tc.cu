@@ -397,6 +397,7 @@ __device__ __forceinline__ unsigned long long gelu2(unsigned long long t2) {
 struct ColParams {
     float w[SLICES];
     float b[SLICES];
+    float rs[SLICES], ry[SLICES];  // kOutRowMax: -s_next and RN(1/s_next) (or NaN)
 };
 
 template <int MODE, int OUT>
@@ -408,6 +409,13 @@ __device__ __forceinline__ void load_col_params(ColParams &cp, const EpiArgs &a,
         const bool ok = n < a.N;
         cp.w[s] = (MODE != SQ_EPI_RAW_I32 && ok) ? __ldg(a.sw + n) : 0.f;
         cp.b[s] = (MODE != SQ_EPI_RAW_I32 && MODE != SQ_EPI_NONE && ok) ? __ldg(a.bias + n) : 0.f;
+        if (OUT == kOutRowMax) {
+            // column n's pair alone (a float2: the table holds exactly N of them)
+            const float2 c = ok ? __ldg(reinterpret_cast<const float2 *>(a.rm_pairs) + n)
+                                : make_float2(-1.f, 1.f);
+            cp.rs[s] = c.x;
+            cp.ry[s] = c.y;
+        }
     }
 }
 
@@ -565,19 +573,25 @@ __device__ __noinline__ float slice_rowmax_exact(const float *y, const float4 *p
     return mx;
 }
 
+// rml: this lane's column (n + lane) pair (-s_next, RN(1/s_next)), shuffled out
+// to every lane column by column (warp-uniform global loads here measured
+// ~13 us slower per FFN up-projection: the L1 left beside the shared memory is
+// small, so they wait on L2)
 __device__ __forceinline__ float slice_rowmax(const uint32_t (&v)[32], int64_t n,
-                                              const EpiArgs &a) {
+                                              const EpiArgs &a, float2 rml) {
     if (n + 31 < a.N) {
-        const float4 *tab = a.rm_pairs + (n >> 1);
         float mx = 0.0f, qm = 0.0f;
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
-            const float4 c = __ldg(tab + (j >> 1));
+            const float ns0 = __shfl_sync(0xffffffffu, rml.x, j);
+            const float ns1 = __shfl_sync(0xffffffffu, rml.x, j + 1);
+            const float yy0 = __shfl_sync(0xffffffffu, rml.y, j);
+            const float yy1 = __shfl_sync(0xffffffffu, rml.y, j + 1);
             const unsigned long long y2 = pk(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
-            const unsigned long long yn2 = pk(c.y, c.w);
+            const unsigned long long yn2 = pk(yy0, yy1);
             const unsigned long long q0 = mul2(y2, yn2);
             float a0, a1, b0, b1;
-            upk(fma2(fma2(q0, pk(c.x, c.z), y2), yn2, q0), a0, a1);
+            upk(fma2(fma2(q0, pk(ns0, ns1), y2), yn2, q0), a0, a1);
             upk(q0, b0, b1);
             mx = max3_nan_f(mx, fabsf(a0), fabsf(a1));
             qm = max3_nan_f(qm, fabsf(b0), fabsf(b1));
@@ -654,7 +668,7 @@ __device__ __forceinline__ void prefetch_residual(const EpiArgs &a, int64_t m, i
 template <int MODE, bool INT_IN, int OUT>
 __device__ __forceinline__ void epilogue_slice(uint32_t (&v)[32], int64_t m, int64_t n,
                                                int row0, int lane, const EpiArgs &a, float xs,
-                                               float wl, float bl, int slice_index,
+                                               float wl, float bl, float2 rml, int slice_index,
                                                const float4 (&r4)[8], const CUtensorMap *tmY,
                                                uint8_t *stg, float &rmax) {
     if (n >= a.N || row0 >= a.M) return;  // slice wholly outside Y
@@ -721,7 +735,7 @@ __device__ __forceinline__ void epilogue_slice(uint32_t (&v)[32], int64_t m, int
             v[j + 1] = __float_as_uint(o1);
         }
     }
-    if (OUT == kOutRowMax) rmax = fmaxf(rmax, slice_rowmax(v, n, a));
+    if (OUT == kOutRowMax) rmax = fmaxf(rmax, slice_rowmax(v, n, a, rml));
     if (OUT == kOutRequant) {
         // this slice's columns in the warp's staging area (written per tile)
         requant_slice(v, m, n, a, reinterpret_cast<const float4 *>(stg) + 16 * slice_index);
@@ -768,9 +782,15 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int64_t m, int nb,
         }
         const float wl = s == 0 ? cp.w[0] : s == 1 ? cp.w[1] : s == 2 ? cp.w[2] : cp.w[3];
         const float bl = s == 0 ? cp.b[0] : s == 1 ? cp.b[1] : s == 2 ? cp.b[2] : cp.b[3];
+        const float2 rml =
+            OUT != kOutRowMax ? make_float2(0.f, 0.f)
+            : s == 0          ? make_float2(cp.rs[0], cp.ry[0])
+            : s == 1          ? make_float2(cp.rs[1], cp.ry[1])
+            : s == 2          ? make_float2(cp.rs[2], cp.ry[2])
+                              : make_float2(cp.rs[3], cp.ry[3]);
         uint32_t v[32];
         tmem_ld32(taddr + s * SLICE, v);
-        epilogue_slice<MODE, INT_IN, OUT>(v, m, nb + s * SLICE, row0, lane, a, xs, wl, bl, s,
+        epilogue_slice<MODE, INT_IN, OUT>(v, m, nb + s * SLICE, row0, lane, a, xs, wl, bl, rml, s,
                                           rcur, tmY, stg, rmax);
     }
     // non-negative floats order like their bit patterns
