@@ -577,6 +577,33 @@ __device__ __forceinline__ float group_max_nan(float m, int tpr, float *red) {
     return m;
 }
 
+// Reductions across the tpr threads of row group g for the register kernel
+// below, synchronised on the group's own named barrier (1 + g, tpr threads)
+// instead of the block's, so that the groups of a block run their tiles
+// independently.  The caller alternates two slot arrays between consecutive
+// reductions: a slot is rewritten only after the group has passed the next
+// reduction's barrier, hence after every thread read it, so one barrier per
+// reduction is enough.
+__device__ __forceinline__ void row_group_sync(int g, int tpr) {
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(tpr) : "memory");
+}
+template <int OP>  // 0: max (NaN kept), 1: max, 2: sum
+__device__ __forceinline__ float row_group_reduce(float v, int tpr, int g, float *red) {
+    auto op = [](float a, float b) {
+        return OP == 0 ? max2_nan(a, b) : OP == 1 ? fmaxf(a, b) : a + b;
+    };
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (tpr > 32) {
+        const int wpg = tpr >> 5;
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+        row_group_sync(g, tpr);
+        v = red[g * wpg];
+        for (int w = 1; w < wpg; ++w) v = op(v, red[g * wpg + w]);
+    }
+    return v;
+}
+
 // Smooth-Dynamic activations, the row in registers (K4 <= tpr * kVPT): the
 // arithmetic of the ring kernel below on the register kernel's layout (tpr
 // threads per row, float4 f = t + i tpr of it in thread t), with the
@@ -587,9 +614,8 @@ __device__ __forceinline__ float group_max_nan(float m, int tpr, float *red) {
 //  * codes: rint of p = RN(RN(x y) RN(1/scale)), the IEEE divisions for a
 //    value within 2^-14 of a half-integer.
 // A row whose maximum is NaN or outside [2^-60, 2^100] takes IEEE divisions
-// throughout; the choice is made per block (the group reductions hold block
-// barriers), so a block with one such row codes all its rows that way, which
-// is exact too.  GIVEN: the row maxima come from row_amax (as the row-maximum
+// throughout (the maximum is uniform across the row group, and so is the
+// choice; the group's reductions sync on its own barrier).  GIVEN: the row maxima come from row_amax (as the row-maximum
 // GEMM epilogue leaves them) instead of the reduction, and the codes saturate
 // at +-127 (a maximum below the true one cannot wrap them); an out-of-range
 // maximum still sends the block to the IEEE path, which finds its own.
@@ -607,7 +633,8 @@ __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
     float4 *ytab = qtab + K4;   // RN(1/s) or NaN
     pdl_launch_dependents();
     pdl_wait();
-    __shared__ float red[kThreads / 32];
+    __shared__ float red2[2][kThreads / 32];
+    int rb = 0;  // the slot array of the group's next reduction
     auto recip = [](float x) {
         const float a = fabsf(x);
         return (a >= 0x1p-20f && a <= 0x1p20f) ? __frcp_rn(x) : __int_as_float(0x7fffffff);
@@ -669,8 +696,11 @@ __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
             m = max3_nan(m, fabsf(d0), fabsf(d1));
             m = max3_nan(m, fabsf(d2), fabsf(d3));
         }
-        if (!GIVEN) m = group_max_nan(m, tpr, red);
-        const bool exact = __syncthreads_or(valid && !(m >= 0x1p-60f && m <= 0x1p100f));
+        if (!GIVEN) {
+            m = row_group_reduce<0>(m, tpr, g, red2[rb]);
+            rb ^= 1;
+        }
+        const bool exact = valid && !(m >= 0x1p-60f && m <= 0x1p100f);
         float a1 = 0.0f;
         if (exact) {
             // IEEE divisions throughout (the definition as stated)
@@ -682,7 +712,8 @@ __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
                 me = fmaxf(me, fmaxf(abs_quotient(v[i].x, -ns.x), abs_quotient(v[i].y, -ns.y)));
                 me = fmaxf(me, fmaxf(abs_quotient(v[i].z, -ns.z), abs_quotient(v[i].w, -ns.w)));
             }
-            me = group_max(me, tpr, red);
+            me = row_group_reduce<1>(me, tpr, g, red2[rb]);
+            rb ^= 1;
             const float sc = me == 0.0f ? 1.0f : abs_quotient(me, 127.0f);
             if (valid) {
                 if (t == 0) scale[row] = sc;
@@ -737,7 +768,8 @@ __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
             }
         }
         if (l1) {
-            a1 = group_sum(a1, tpr, red);  // exact: at most 127 * 8192 < 2^24
+            a1 = row_group_reduce<2>(a1, tpr, g, red2[rb]);  // exact: <= 127 * 8192 < 2^24
+            rb ^= 1;
             if (valid && t == 0) l1[row] = (int32_t)a1;
         }
     }
