@@ -174,6 +174,38 @@ def test_quantize_extreme_magnitudes(sq, K):
             assert_codes_equal(op_as_int(Xop), q_ref, f"static Xop, scale {scale}")
 
 
+# The register kernel builds its tables of s while the kernel before it on the
+# stream may still run, then checks s after the wait: here that kernel is the
+# library's smoothing-factor kernel rewriting the same buffer each time.
+@pytest.mark.parametrize("M,K", [(2400, 1024), (700, 4096)])
+def test_quantize_after_smoothing_factor_rewrite(sq, M, K):
+    rng = np.random.default_rng(M + K)
+    X = (rng.standard_normal((M, K)) * 2).astype(np.float32)
+    X[:, 7] *= 40.0
+    ax = np.abs(X).max(axis=0).astype(np.float32)
+    aw = np.abs(rng.standard_normal(K) * 0.05).astype(np.float32) + np.float32(1e-3)
+    lib, st = sq.load(), torch.cuda.current_stream().cuda_stream
+    X_d, ax_d, aw_d = to_dev(X), to_dev(ax), to_dev(aw)
+    s_buf = to_dev(np.ones(K, np.float32))
+    Xq = torch.empty(M, K, dtype=torch.int8, device="cuda")
+    sx = torch.empty(M, dtype=torch.float32, device="cuda")
+    Xop = sq.empty_operand(M, K)
+    torch.cuda.synchronize()
+    outs = []
+    for alpha in (0.5, 0.8, 0.25, 0.5, 0.65, 0.9):
+        rc = lib.sq_smooth_factor(ax_d.data_ptr(), aw_d.data_ptr(), K, alpha, s_buf.data_ptr(),
+                                  st)
+        assert rc == 0
+        sq.quantize_act(X_d, s_buf, out=(Xq, sx, Xop))
+        outs.append((s_buf.clone(), Xq.clone(), sx.clone(), Xop.clone()))
+    torch.cuda.synchronize()
+    for s_used, q, scale, op in outs:
+        q_ref, sx_ref = oracle.quantize_rows(X, s_used.cpu().numpy(), "act")
+        assert_bits_equal(scale.cpu().numpy(), sx_ref, "x_scale")
+        assert_codes_equal(q.cpu().numpy(), q_ref, "Xq")
+        assert_codes_equal(op_as_int(op), q_ref, "Xop")
+
+
 @pytest.mark.parametrize("N,K", [(1, 16), (5, 48), (1024, 1024), (3072, 1024), (768, 3072),
                                  (9, 8208)])
 def test_pack_weight_parity(sq, N, K):
