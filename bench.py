@@ -164,7 +164,8 @@ def clock_summary(lines, window=None):
 
 class Layer:
     __slots__ = ("lin", "X", "s", "Wop", "Wq", "sw", "wl1", "bias", "residual", "Y", "Xhost",
-                 "Yhost", "static_scale", "feeds", "fed_by", "ln", "table", "row_amax")
+                 "Yhost", "static_scale", "feeds", "fed_by", "ln", "table", "row_amax",
+                 "qtab")
 
 
 LN_EPS = 1e-12
@@ -176,7 +177,8 @@ def step_bytes(layers, M):
 
 
 def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
-                   quant: str = "dynamic", ffn_chain: str = "off", ln: bool = False):
+                   quant: str = "dynamic", ffn_chain: str = "off", ln: bool = False,
+                   division_table: bool = True):
     from smoothquant_w8a8_int8_gb300 import binding as sq
     dev = torch.device("cuda")
     layers = []
@@ -222,6 +224,10 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
                               if ffn_chain in ("unfused", "fused") else None)
             # the dynamic chain's division table of FFN-down's smoothing factor
             L.table = sq.division_table(s) if ffn_chain == "dynamic-fused" else None
+            # the Smooth-Dynamic quantiser's own copy of it (offline, like Wop)
+            L.qtab = (sq.division_table(s)
+                      if division_table and ffn_chain in ("dynamic-unfused", "dynamic-fused")
+                      else None)
             L.row_amax = None
             L.Y = torch.empty(w.M, lin.N, dtype=torch.float32, device=dev)
             L.Xhost = L.Yhost = None
@@ -271,6 +277,9 @@ def setup_workload(w: wl.Workload, gemm: str, rank: int, want_host: bool,
             L.static_scale = sq.static_scale(sq.act_absmax(calib, s))
         L.Y = torch.empty(w.M, lin.N, dtype=torch.float32, device=dev)
         L.table = L.row_amax = None
+        # the Smooth-Dynamic quantiser's division table of s (offline, like Wop)
+        L.qtab = (sq.division_table(s) if division_table and quant == "dynamic" and L.ln is None
+                  else None)
         L.Xhost = L.Yhost = None
         L.feeds = L.fed_by = None
         if want_host:
@@ -293,6 +302,8 @@ def quantise(sq, L, X, sx_buf, Xop):
                            out=(None, sx_buf, Xop, None, None))
     elif L.static_scale is not None:
         sq.quantize_act_static(X, L.s, L.static_scale, out=(None, sx_buf, Xop))
+    elif L.qtab is not None:
+        sq.quantize_act_table(X, L.s, L.qtab, out=(None, sx_buf, Xop))
     else:
         sq.quantize_act(X, L.s, out=(None, sx_buf, Xop))
 
@@ -324,8 +335,13 @@ def run_layer(sq, gemm, L, bufs, M, X=None, ev=None, ffn_chain="off", ws=None):
             if ffn_chain == "unfused":
                 sq.quantize_act_static(L.fed_by.Y, L.s, L.static_scale,
                                        out=(None, sx_chain, chain_op))
+            elif ffn_chain == "dynamic-unfused" and L.qtab is not None:
+                sq.quantize_act_table(L.fed_by.Y, L.s, L.qtab, out=(None, sx_chain, chain_op))
             elif ffn_chain == "dynamic-unfused":
                 sq.quantize_act(L.fed_by.Y, L.s, out=(None, sx_chain, chain_op))
+            elif ffn_chain == "dynamic-fused" and L.qtab is not None:
+                sq.quantize_act_table(L.fed_by.Y, L.s, L.qtab, row_amax=amax_chain,
+                                      out=(None, sx_chain, chain_op))
             elif ffn_chain == "dynamic-fused":
                 sq.quantize_act_rowmax(L.fed_by.Y, L.s, amax_chain, out=(None, sx_chain, chain_op))
             if ev is not None:
@@ -421,7 +437,10 @@ def codes_operand_leg(args, layers, bufs, M, ops_per_step, world):
         for L in layers:
             K = L.lin.K
             Xq = Xq_buf[: M * K].view(M, K)
-            sq.quantize_act(L.X, L.s, out=(Xq, sx_buf, None))
+            if L.qtab is not None:
+                sq.quantize_act_table(L.X, L.s, L.qtab, out=(Xq, sx_buf, None))
+            else:
+                sq.quantize_act(L.X, L.s, out=(Xq, sx_buf, None))
             sq.linear_i8_codes(Xq, sx_buf, L.Wop, L.sw, L.bias, L.residual, L.lin.mode,
                                out=L.Y, w_l1=L.wl1, workspace=ws)
 
@@ -441,7 +460,7 @@ def codes_operand_leg(args, layers, bufs, M, ops_per_step, world):
     ms = replicas.max_over_ranks(t0.elapsed_time(t1), device="cuda") / args.steps
     return {"value": round(replicas.whole_job_tops(ops_per_step, world, ms), 3), "unit": "TOPS",
             "ms_per_step": round(ms, 4),
-            "path": "sq_quantize_act writing int8 codes, then sq_linear_i8_codes (an exact "
+            "path": "sq_quantize_act(_table) writing int8 codes, then sq_linear_i8_codes (an exact "
                     "widening pass into the bf16 operand, then the same tcgen05 GEMM)"}
 
 
@@ -453,7 +472,7 @@ def e2e_leg(args, layers, M, ops_per_step, world):
     from smoothquant_w8a8_int8_gb300.pipeline import HostLinearPipeline, LinearLayer
     pipe = HostLinearPipeline(M, max(L.lin.K for L in layers), max(L.lin.N for L in layers))
     specs = [LinearLayer(L.s, L.Wop, L.sw, L.lin.mode, L.bias, L.residual, L.wl1,
-                         L.static_scale) for L in layers]
+                         L.static_scale, L.qtab) for L in layers]
     xh = [L.Xhost for L in layers]
     yh = [L.Yhost for L in layers]
     h2d = sum(L.Xhost.numel() * 4 for L in layers)
@@ -487,7 +506,7 @@ def e2e_leg(args, layers, M, ops_per_step, world):
             "copies_only_gbs": round((h2d + d2h) / (copy_ms * 1e-3) / 1e9, 1),
             "outputs_match_device": bool(ok),
             "outputs_checked": "every element of every layer's Y",
-            "path": "pinned host X -> device, sq_quantize_act + sq_linear_i8, Y -> pinned "
+            "path": "pinned host X -> device, sq_quantize_act(_table) + sq_linear_i8, Y -> pinned "
                     "host; copies overlapped with kernels on three streams "
                     "(smoothquant_w8a8_int8_gb300.pipeline.HostLinearPipeline)"}
 
@@ -504,7 +523,8 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int, headline: bool = Tru
     layers, bufs = setup_workload(w, args.gemm, rank,
                                   want_host=(args.e2e_steps > 0 and not chained and not args.ln
                                              and headline),
-                                  quant=args.quant, ffn_chain=args.ffn_chain, ln=args.ln)
+                                  quant=args.quant, ffn_chain=args.ffn_chain, ln=args.ln,
+                                  division_table=args.division_table == "on")
     M = w.M
     n_gemm = len(layers)
     quantised = [True] * n_gemm  # which linears run an activation quantiser kernel
@@ -685,7 +705,10 @@ def bench_ours(args, w: wl.Workload, rank: int, world: int, headline: bool = Tru
                    "quantisation": ("Smooth-Static (per-tensor scale calibrated offline on a "
                                     "separate 512-token batch of the same distribution)"
                                     if args.quant == "static"
-                                    else "Smooth-Dynamic (per-token scales at run time)"),
+                                    else "Smooth-Dynamic (per-token scales at run time"
+                                    + ("; s's division table made offline with the packed "
+                                       "weights, sq_quantize_act_table)"
+                                       if args.division_table == "on" else ")")),
                    "parallelism": f"replicas x{world} (rows shard, no collective)",
                    "ffn_chain": {"off": "not chained: every linear has its own input",
                                  "unfused": "FFN-down consumes FFN-up's output: fp32 Y, then "
@@ -911,6 +934,10 @@ def main():
     ap.add_argument("--schedule", choices=["split-k", "whole"], default="split-k",
                     help="tcgen05 GEMM: split K over several SMs where the tiles are fewer "
                          "than the SMs and K >= 2048 (workspace), or whole tiles only")
+    ap.add_argument("--division-table", choices=["on", "off"], default="on",
+                    help="Smooth-Dynamic quantisers read s's division table, made offline "
+                         "with the packed weights (sq_quantize_act_table), or form the "
+                         "reciprocals of s in every block (sq_quantize_act)")
     ap.add_argument("--ln", action="store_true",
                     help="the QKV and FFN-up inputs are pre-LayerNorm hidden states: their "
                          "quantiser is the fused LayerNorm + quantiser")

@@ -283,6 +283,18 @@ sq_status sq_quantize_act_rowmax(const float *X, const float *s, const float *ro
                                  int64_t M, int64_t K, int8_t *Xq, float *x_scale, void *Xop,
                                  int32_t *x_row_l1, void *stream);
 
+/* sq_quantize_act (row_amax NULL) or sq_quantize_act_rowmax (row_amax given)
+ * with s's division table beside s: s_table = sq_division_table(s), computed
+ * offline with the packed weights.  Outputs bit for bit those of the call
+ * without the table; where the rows are held in registers the kernel reads -s
+ * and RN(1/s) from the table instead of forming the reciprocals in every
+ * block.  A table that is not sq_division_table(s) gives unspecified codes
+ * (in range).  s_table fp32 [K][2] (16-byte aligned); other arguments as
+ * sq_quantize_act / sq_quantize_act_rowmax. */
+sq_status sq_quantize_act_table(const float *X, const float *s, const float *s_table,
+                                const float *row_amax, int64_t M, int64_t K, int8_t *Xq,
+                                float *x_scale, void *Xop, int32_t *x_row_l1, void *stream);
+
 /* ---- Encoder self-attention (Table 3, beside the linear block) -------------- */
 
 /* Scaled dot-product attention per sequence b and head h on the fused QKV

@@ -26,8 +26,8 @@ EXPORTS = ("sq_status_string", "sq_version", "sq_operand_bytes", "sq_packed_weig
            "sq_static_scale", "sq_quantize_act_static", "sq_layernorm_quant", "sq_linear_i8",
            "sq_linear_codes_workspace_bytes", "sq_linear_i8_codes",
            "sq_linear_i8_requant", "sq_division_table", "sq_linear_i8_rowmax",
-           "sq_quantize_act_rowmax", "sq_attention", "sq_linear_workspace_bytes", "sq_linear_i8_ws",
-           "sq_linear_i8_requant_ws", "sq_linear_i8_static_ws", "sq_static_workspace_reset",
+           "sq_quantize_act_rowmax", "sq_quantize_act_table", "sq_attention",
+           "sq_linear_workspace_bytes", "sq_linear_i8_ws", "sq_linear_i8_requant_ws", "sq_linear_i8_static_ws", "sq_static_workspace_reset",
            "sq_static_workspace", "sq_linear_i8_mma_sync",
            "sq_check_division", "sq_device_status", "sq_get_device_status")
 
@@ -74,6 +74,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                 "sq_linear_i8_rowmax": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp,
                                          vp, vp, vp], i32),
                 "sq_quantize_act_rowmax": ([vp, vp, vp, i64, i64, vp, vp, vp, vp, vp], i32),
+                "sq_quantize_act_table": ([vp, vp, vp, vp, i64, i64, vp, vp, vp, vp, vp], i32),
                 "sq_attention": ([vp, i64, i64, i64, i64, f32, vp, vp], i32),
                 "sq_linear_workspace_bytes": ([i64, i64, i64, vp], i32),
                 "sq_linear_codes_workspace_bytes": ([i64, i64, vp], i32),
@@ -402,6 +403,33 @@ def quantize_act_rowmax(X, s, row_amax, want_q: bool = True, want_op: bool = Tru
     _check(load().sq_quantize_act_rowmax(_p(X), _p(s), _p(row_amax), M, K, _p(Xq), _p(sx),
                                          _p(Xop), _p(l1), _stream(stream)),
            "sq_quantize_act_rowmax")
+    if want_l1 or (out is not None and len(out) > 3):
+        return Xq, sx, Xop, l1
+    return Xq, sx, Xop
+
+
+def quantize_act_table(X, s, table, row_amax=None, want_q: bool = True, want_op: bool = True,
+                       want_l1: bool = False, out=None, stream=None):
+    """quantize_act (row_amax None) or quantize_act_rowmax (row_amax given)
+    with s's division table (division_table(s)); same returns."""
+    _need(X, torch.float32, "X")
+    M, K = X.shape
+    _need(s, torch.float32, "s", (K,))
+    _need(table, torch.float32, "table", (K, 2))
+    if row_amax is not None:
+        _need(row_amax, torch.float32, "row_amax", (M,))
+    l1 = None
+    if out is not None:
+        Xq, sx, Xop = out[:3]
+        l1 = out[3] if len(out) > 3 else None
+    else:
+        Xq = torch.empty(M, K, dtype=torch.int8, device=X.device) if want_q else None
+        Xop = empty_operand(M, K, X.device) if want_op else None
+        sx = torch.empty(M, dtype=torch.float32, device=X.device)
+        l1 = torch.empty(M, dtype=torch.int32, device=X.device) if want_l1 else None
+    _check(load().sq_quantize_act_table(_p(X), _p(s), _p(table), _p(row_amax), M, K, _p(Xq),
+                                        _p(sx), _p(Xop), _p(l1), _stream(stream)),
+           "sq_quantize_act_table")
     if want_l1 or (out is not None and len(out) > 3):
         return Xq, sx, Xop, l1
     return Xq, sx, Xop

@@ -277,6 +277,22 @@ sq_status sq_quantize_act_rowmax(const float *X, const float *s, const float *ro
                                          as_stream(stream));
 }
 
+sq_status sq_quantize_act_table(const float *X, const float *s, const float *s_table,
+                                const float *row_amax, int64_t M, int64_t K, int8_t *Xq,
+                                float *x_scale, void *Xop, int32_t *x_row_l1, void *stream) {
+    sq_status rc = check_quant_args(X, s, M, K, Xq, x_scale, Xop);
+    if (rc != SQ_OK) return rc;
+    if (M == 0) return SQ_OK;
+    if (!s_table) return SQ_ERR_INVALID_ARG;
+    if (!aligned16(s_table) || (row_amax && !aligned4(row_amax)) ||
+        (x_row_l1 && !aligned4(x_row_l1)))
+        return SQ_ERR_ALIGNMENT;
+    if ((rc = require_sm103()) != SQ_OK) return rc;
+    return launch_quantize_act_table(X, s, s_table, row_amax, M, K, Xq, x_scale,
+                                     static_cast<__nv_bfloat16 *>(Xop), x_row_l1,
+                                     as_stream(stream));
+}
+
 sq_status sq_attention(const float *QKV, int64_t B, int64_t S, int64_t H, int64_t D,
                        float scale, float *O, void *stream) {
     if (B < 0 || S < 0 || H < 0 || D <= 0) return SQ_ERR_INVALID_ARG;

@@ -165,6 +165,12 @@ sq_status launch_division_table(const float *s, int64_t K, float *table, cudaStr
 sq_status launch_quantize_act_given_max(const float *A, const float *s, const float *row_amax,
                                         int64_t rows, int64_t K, int8_t *q, float *scale,
                                         __nv_bfloat16 *op, int32_t *l1, cudaStream_t st);
+// the Smooth-Dynamic quantiser (row_amax NULL) or its given-maximum form with
+// s's division table (launch_division_table) beside s
+sq_status launch_quantize_act_table(const float *A, const float *s, const float *table,
+                                    const float *row_amax, int64_t rows, int64_t K, int8_t *q,
+                                    float *scale, __nv_bfloat16 *op, int32_t *l1,
+                                    cudaStream_t st);
 sq_status launch_gemm_mma_sync(const int8_t *Xq, const float *sx, const int8_t *Wq,
                                const float *sw, const float *bias, const float *residual,
                                int64_t M, int64_t N, int64_t K, int mode, void *Y,

@@ -560,23 +560,6 @@ __device__ __noinline__ float exact_code(float x, float s, float scale) {
 // |fl(x / s)| (IEEE division), out of line for the rare exact path
 __device__ __noinline__ float abs_quotient(float x, float s) { return fabsf(__fdiv_rn(x, s)); }
 
-// Row maximum across the TPR threads of a row group, NaN kept (max.NaN).
-__device__ __forceinline__ float group_max_nan(float m, int tpr, float *red) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = max2_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (tpr > 32) {
-        const int warp = threadIdx.x >> 5;
-        const int wpg = tpr >> 5;
-        const int g = warp / wpg;
-        if ((threadIdx.x & 31) == 0) red[warp] = m;
-        __syncthreads();
-        m = 0.0f;
-        for (int w = 0; w < wpg; ++w) m = max2_nan(m, red[g * wpg + w]);
-        __syncthreads();
-    }
-    return m;
-}
-
 // Reductions across the tpr threads of row group g for the register kernel
 // below, synchronised on the group's own named barrier (1 + g, tpr threads)
 // instead of the block's, so that the groups of a block run their tiles
@@ -622,12 +605,17 @@ __device__ __forceinline__ float row_group_reduce(float v, int tpr, int g, float
 // While a tile is coded, one thread per row group asks for the
 // group's next row to be brought into L2 (a bulk prefetch, no registers held),
 // so that DRAM stays busy through the reductions and stores (measured 7% on
-// 8192 x 4096; a second row ahead measured slower).
-template <int kVPT, bool GIVEN>
+// 8192 x 4096; a second row ahead measured slower).  TAB: the tables are
+// copied from the caller's division table of s instead of formed in every
+// block (the block's reciprocals cost 3% of the quantiser's time in the
+// BERT-large step, 2.51 -> 2.43 ms; reading the table through L1 inside the
+// tile loop, with no shared-memory copy, measured 8% slower than forming it).
+template <int kVPT, bool GIVEN, bool TAB>
 __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
-    const float *__restrict__ A, const float *__restrict__ s, int64_t rows, int K4, int tpr,
-    int8_t *__restrict__ q, float *__restrict__ scale, __nv_bfloat16 *__restrict__ op,
-    int32_t *__restrict__ l1, const float *__restrict__ row_amax) {
+    const float *__restrict__ A, const float *__restrict__ s, const float4 *__restrict__ tab,
+    int64_t rows, int K4, int tpr, int8_t *__restrict__ q, float *__restrict__ scale,
+    __nv_bfloat16 *__restrict__ op, int32_t *__restrict__ l1,
+    const float *__restrict__ row_amax) {
     extern __shared__ float4 qtab[];
     float4 *nstab = qtab;       // -s
     float4 *ytab = qtab + K4;   // RN(1/s) or NaN
@@ -651,11 +639,21 @@ __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
                          "r"((uint32_t)K4 * 16u)
                          : "memory");
     }
-    const float4 *s4 = reinterpret_cast<const float4 *>(s);
-    for (int j = threadIdx.x; j < K4; j += kThreads) {
-        const float4 v = __ldg(s4 + j);
-        nstab[j] = make_float4(-v.x, -v.y, -v.z, -v.w);
-        ytab[j] = make_float4(recip(v.x), recip(v.y), recip(v.z), recip(v.w));
+    if (TAB) {
+        // the caller's division table: float4 2j and 2j + 1 hold the pairs
+        // (-s, RN(1/s)) of columns 4j .. 4j + 3
+        for (int j = threadIdx.x; j < K4; j += kThreads) {
+            const float4 a = __ldg(tab + 2 * j), b = __ldg(tab + 2 * j + 1);
+            nstab[j] = make_float4(a.x, a.z, b.x, b.z);
+            ytab[j] = make_float4(a.y, a.w, b.y, b.w);
+        }
+    } else {
+        const float4 *s4 = reinterpret_cast<const float4 *>(s);
+        for (int j = threadIdx.x; j < K4; j += kThreads) {
+            const float4 v = __ldg(s4 + j);
+            nstab[j] = make_float4(-v.x, -v.y, -v.z, -v.w);
+            ytab[j] = make_float4(recip(v.x), recip(v.y), recip(v.z), recip(v.w));
+        }
     }
     __syncthreads();
     const unsigned long long magic2 = pk(kRoundMagic, kRoundMagic);
@@ -1149,10 +1147,11 @@ sq_status launch_division_table(const float *s, int64_t K, float *table, cudaStr
 }
 
 // The register Smooth-Dynamic kernel (K <= 8192): its tables of -s and 1/s in
-// shared memory (8 bytes per column), its residency at that size, and the grid.
-sq_status launch_act_reg(const float *A, const float *s, int64_t rows, int64_t K, int8_t *q,
-                         float *scale, __nv_bfloat16 *op, int32_t *l1, const float *row_amax,
-                         const DeviceInfo &di, cudaStream_t st) {
+// shared memory (8 bytes per column; formed from s, or copied from s's
+// division table when one is given), its residency at that size, and the grid.
+sq_status launch_act_reg(const float *A, const float *s, const float *tab, int64_t rows,
+                         int64_t K, int8_t *q, float *scale, __nv_bfloat16 *op, int32_t *l1,
+                         const float *row_amax, const DeviceInfo &di, cudaStream_t st) {
     const int K4 = (int)(K / 4);
     const bool small = K4 <= kThreads * 4;
     const int vpt = small ? 4 : 8;
@@ -1160,33 +1159,35 @@ sq_status launch_act_reg(const float *A, const float *s, int64_t rows, int64_t K
     while (tpr * vpt < K4) tpr <<= 1;
     const int rpb = kThreads / tpr;
     const int64_t tiles = (rows + rpb - 1) / rpb;
-    using Kern = void (*)(const float *, const float *, int64_t, int, int, int8_t *, float *,
-                          __nv_bfloat16 *, int32_t *, const float *);
-    static const Kern kerns[2][2] = {{quantize_act_reg<4, false>, quantize_act_reg<8, false>},
-                                     {quantize_act_reg<4, true>, quantize_act_reg<8, true>}};
-    const int gi = row_amax ? 1 : 0, vi = small ? 0 : 1;
-    const Kern kern = kerns[gi][vi];
+    using Kern = void (*)(const float *, const float *, const float4 *, int64_t, int, int,
+                          int8_t *, float *, __nv_bfloat16 *, int32_t *, const float *);
+    static const Kern kerns[2][2][2] = {
+        {{quantize_act_reg<4, false, false>, quantize_act_reg<8, false, false>},
+         {quantize_act_reg<4, true, false>, quantize_act_reg<8, true, false>}},
+        {{quantize_act_reg<4, false, true>, quantize_act_reg<8, false, true>},
+         {quantize_act_reg<4, true, true>, quantize_act_reg<8, true, true>}}};
+    const int ti = tab ? 1 : 0, gi = row_amax ? 1 : 0, vi = small ? 0 : 1;
+    const Kern kern = kerns[ti][gi][vi];
     const int smem = K4 * 32;
     constexpr int kMaxTab = kThreads * kMaxVPT * 32;  // 64 KB at K = 8192
     static std::mutex mu;
-    static bool opted[64][2][2] = {};
-    static int occ_dyn[64][2][2][8] = {};  // per device, mode, vpt, 256-float4 bucket of K4
+    static bool opted[64][2][2][2] = {};
+    static int occ_dyn[64][2][2][2][8] = {};  // per device, table, mode, vpt, 256-float4 bucket
     int occ = 0;
     {
         std::lock_guard<std::mutex> lock(mu);
         const int dv = di.device & 63;
-        if (!opted[dv][gi][vi]) {
+        if (!opted[dv][ti][gi][vi]) {
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kMaxTab) != cudaSuccess)
                 return SQ_ERR_CUDA;
-            opted[dv][gi][vi] = true;
+            opted[dv][ti][gi][vi] = true;
         }
         // residency at the bucket's largest table (never above the true one)
         const int bucket = (K4 - 1) / 256;
-        int &o = occ_dyn[dv][gi][vi][bucket];
-        if (!o && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, kThreads,
-                                                                 (bucket + 1) * 256 * 32) !=
-                       cudaSuccess ||
+        int &o = occ_dyn[dv][ti][gi][vi][bucket];
+        if (!o && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                       &o, kern, kThreads, (bucket + 1) * 256 * 32) != cudaSuccess ||
                    o < 1))
             return SQ_ERR_CUDA;
         occ = o;
@@ -1197,8 +1198,9 @@ sq_status launch_act_reg(const float *A, const float *s, int64_t rows, int64_t K
     // 1.5, 2.5, 3, 4 times or one tile per block ran slower (761, 765, 763,
     // 754, 698 TOPS); a launch timed on its own runs a little slower
     const int64_t grid = std::min<int64_t>(tiles, 2 * (int64_t)di.sms * occ);
-    return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, 1, A, s, rows, K4,
-                      tpr, q, scale, op, l1, row_amax);
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, 1, A, s,
+                      reinterpret_cast<const float4 *>(tab), rows, K4, tpr, q, scale, op, l1,
+                      row_amax);
 }
 
 sq_status launch_quantize_act_given_max(const float *A, const float *s, const float *row_amax,
@@ -1212,10 +1214,29 @@ sq_status launch_quantize_act_given_max(const float *A, const float *s, const fl
     // that are not 1024 * 2^k keep, as in the dynamic dispatch)
     const bool pow2_rows = K >= 1024 && K <= 8192 && (K & (K - 1)) == 0;
     if (K <= 8192 && (pow2_rows || K > 2048))
-        return launch_act_reg(A, s, rows, K, q, scale, op, l1, row_amax, di, st);
+        return launch_act_reg(A, s, nullptr, rows, K, q, scale, op, l1, row_amax, di, st);
     if (K <= 8192 && rows >= 16 * (int64_t)di.sms)
         return launch_quantize_act_dynamic(A, s, rows, K, q, scale, op, l1, di, st, row_amax);
     // other launches: the full quantiser (it finds the same maxima itself)
+    return launch_quantize_rows(kActDynamic, A, s, rows, K, q, scale, op, l1, 0.0f, st);
+}
+
+sq_status launch_quantize_act_table(const float *A, const float *s, const float *table,
+                                    const float *row_amax, int64_t rows, int64_t K, int8_t *q,
+                                    float *scale, __nv_bfloat16 *op, int32_t *l1,
+                                    cudaStream_t st) {
+    DeviceInfo di;
+    sq_status rc = device_info(&di);
+    if (rc != SQ_OK) return rc;
+    // the register kernel reads the table wherever the dispatch below (and in
+    // the given-maximum quantiser) would take it; the other kernels take s
+    const bool pow2_rows = K >= 1024 && K <= 8192 && (K & (K - 1)) == 0;
+    const bool reg = K <= 8192 && (row_amax ? (pow2_rows || K > 2048)
+                                            : !(K <= 2048 && !pow2_rows &&
+                                                rows >= 16 * (int64_t)di.sms));
+    if (reg) return launch_act_reg(A, s, table, rows, K, q, scale, op, l1, row_amax, di, st);
+    if (row_amax)
+        return launch_quantize_act_given_max(A, s, row_amax, rows, K, q, scale, op, l1, st);
     return launch_quantize_rows(kActDynamic, A, s, rows, K, q, scale, op, l1, 0.0f, st);
 }
 
@@ -1248,7 +1269,7 @@ sq_status launch_quantize_rows(int direction, const float *A, const float *s, in
         void (*kern)(const float *, const float *, int64_t, int, int, int8_t *, float *,
                      __nv_bfloat16 *, int32_t *, float);
         if (direction == kActDynamic)
-            return launch_act_reg(A, s, rows, K, q, scale, op, l1, nullptr, di, st);
+            return launch_act_reg(A, s, nullptr, rows, K, q, scale, op, l1, nullptr, di, st);
         if (direction == kWeight)
             kern = small ? quantize_rows_reg<kWeight, 4> : quantize_rows_reg<kWeight, 8>;
         else

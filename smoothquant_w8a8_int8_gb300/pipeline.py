@@ -2,7 +2,8 @@
 host memory.
 
 `HostLinearPipeline` streams each layer's activations X (fp32, pinned host
-memory) to the GPU, runs the linear block there (sq_quantize_act, then
+memory) to the GPU, runs the linear block there (sq_quantize_act, or
+sq_quantize_act_table when the layer carries s's division table, then
 sq_linear_i8 with its fused epilogue) and streams Y back, with the three kinds
 of work on three CUDA streams and two device slots for X and for Y, so that
 the host-to-device copy of layer i+1 and the device-to-host copy of layer i-1
@@ -31,6 +32,7 @@ class LinearLayer:
     residual: Optional[torch.Tensor] = None   # [M, N] fp32, device
     w_l1: Optional[torch.Tensor] = None       # [N] int32 row L1 norms of the codes
     static_scale: Optional[float] = None      # Smooth-Static per-tensor scale, else dynamic
+    s_table: Optional[torch.Tensor] = None    # [K, 2] division table of s (dynamic only)
 
 
 class HostLinearPipeline:
@@ -82,6 +84,9 @@ class HostLinearPipeline:
                 if L.static_scale is not None:
                     sq.quantize_act_static(dX, L.s, L.static_scale, out=(None, self.sx, xop),
                                            stream=self.comp)
+                elif L.s_table is not None:
+                    sq.quantize_act_table(dX, L.s, L.s_table, out=(None, self.sx, xop),
+                                          stream=self.comp)
                 else:
                     sq.quantize_act(dX, L.s, out=(None, self.sx, xop), stream=self.comp)
                 ev = torch.cuda.Event()

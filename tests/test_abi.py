@@ -252,6 +252,15 @@ def test_workspace_entry_points_check_arguments_first(lib):
     assert qr(a, a, a, 4, 32, None, a, None, None, None) == INVALID     # no output
     assert qr(a, a, _fake(0x10002), 4, 32, a, a, None, None, None) == ALIGN
     assert qr(None, None, None, 0, 32, None, None, None, None, None) == 0
+    qt = lib.sq_quantize_act_table
+    qt.argtypes = [vp, vp, vp, vp, i64, i64, vp, vp, vp, vp, vp]
+    assert qt(a, a, None, None, 4, 32, a, a, None, None, None) == INVALID   # no table
+    assert qt(a, None, a, None, 4, 32, a, a, None, None, None) == INVALID   # no s
+    assert qt(a, a, a, None, 4, 32, None, a, None, None, None) == INVALID   # no output
+    assert qt(a, a, _fake(0x10008), None, 4, 32, a, a, None, None, None) == ALIGN
+    assert qt(a, a, a, _fake(0x10002), 4, 32, a, a, None, None, None) == ALIGN  # maxima
+    assert qt(a, a, a, None, 4, 40, a, a, None, None, None) == ALIGN        # K % 16
+    assert qt(None, None, None, None, 0, 32, None, None, None, None, None) == 0
     at = lib.sq_attention
     at.argtypes = [vp, i64, i64, i64, i64, ctypes.c_float, vp, vp]
     assert at(a, 2, 128, 4, 64, 0.125, None, None) == INVALID

@@ -538,7 +538,9 @@ def test_host_pipeline_matches_direct_calls(sq):
         r = c.residual.cuda() if c.residual is not None else None
         _, sx, Xop = sq.quantize_act(X, s, want_q=False)
         ref.append(sq.linear_i8(Xop, sx, Wop, sw, b, r, mode, w_l1=wl1).cpu())
-        layers.append(LinearLayer(s, Wop, sw, mode, b, r, wl1))
+        # odd layers carry s's division table (sq_quantize_act_table)
+        layers.append(LinearLayer(s, Wop, sw, mode, b, r, wl1,
+                                  s_table=sq.division_table(s) if i % 2 else None))
         xh.append(c.X.pin_memory())
         yh.append(torch.empty(M, N, dtype=torch.float32).pin_memory())
     pipe = HostLinearPipeline(M, max(k for k, _, _ in shapes), max(n for _, n, _ in shapes))
