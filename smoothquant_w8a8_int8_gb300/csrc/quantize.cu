@@ -438,11 +438,6 @@ __device__ __forceinline__ float max2_nan(float a, float b) {
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
     return d;
 }
-__device__ __forceinline__ float max3(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
 
 __device__ __forceinline__ uint32_t saddr(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -747,9 +742,12 @@ __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
                     upk(t23, c[2], c[3]);
                     upk(sub2(p01, t01), d[0], d[1]);
                     upk(sub2(p23, t23), d[2], d[3]);
-                    const float dm = max3(fabsf(d[0]), fabsf(d[1]), fmaxf(fabsf(d[2]), fabsf(d[3])));
+                    // NaN kept: with the maxima given, a column whose s has no
+                    // reciprocal (NaN in the table) reaches this point
+                    const float dm = max3_nan(fabsf(d[0]), fabsf(d[1]),
+                                              max2_nan(fabsf(d[2]), fabsf(d[3])));
                     if (!(dm <= kTieLimit)) {
-                        // rare: a value within 2^-14 of a half-integer
+                        // rare: a value within 2^-14 of a half-integer (or NaN)
                         const float4 ns = nstab[j];
                         if (!(fabsf(d[0]) <= kTieLimit)) c[0] = exact_code(v[i].x, -ns.x, sc);
                         if (!(fabsf(d[1]) <= kTieLimit)) c[1] = exact_code(v[i].y, -ns.y, sc);
@@ -974,9 +972,12 @@ __global__ void __launch_bounds__(32 * (kRingWarps + 1), 1) quantize_act_ring(
                     upk(t23, t[2], t[3]);
                     upk(sub2(p01, t01), d[0], d[1]);
                     upk(sub2(p23, t23), d[2], d[3]);
-                    const float dm = max3(fabsf(d[0]), fabsf(d[1]), fmaxf(fabsf(d[2]), fabsf(d[3])));
+                    // NaN kept: with the maxima given, a column whose s has no
+                    // reciprocal (NaN in the table) reaches this point
+                    const float dm = max3_nan(fabsf(d[0]), fabsf(d[1]),
+                                              max2_nan(fabsf(d[2]), fabsf(d[3])));
                     if (!(dm <= kTieLimit)) {
-                        // rare: a value within 2^-14 of a half-integer
+                        // rare: a value within 2^-14 of a half-integer (or NaN)
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             if (!(fabsf(d[e]) <= kTieLimit))

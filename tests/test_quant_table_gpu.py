@@ -82,3 +82,29 @@ def test_quantize_act_table_extremes(sq, K):
     for s_case in (s, np.where(np.arange(K) == 5, np.float32(1e-7), s).astype(np.float32),
                    np.where(np.arange(K) == 9, np.float32(3e7), s).astype(np.float32)):
         _check(sq, X, s_case)
+
+
+# (rows, K): the register kernel (1024, 3072) and the staged-ring kernel (768
+# with 2520 rows) in their given-maximum form
+@pytest.mark.parametrize("M,K", [(40, 1024), (40, 3072), (2520, 768)])
+def test_given_maxima_with_extreme_smoothing_factors(sq, M, K):
+    """Columns whose smoothing factor lies outside [2^-20, 2^20] have no
+    reciprocal in the division table (NaN): their codes come from IEEE
+    divisions also when the row maxima are given and in range."""
+    rng = np.random.default_rng(M * K)
+    s = rng.uniform(0.5, 2.0, K).astype(np.float32)
+    s[[3, 11]] = np.float32(1e-7), np.float32(3e7)
+    X = rng.standard_normal((M, K)).astype(np.float32)
+    X[:, 3] *= np.float32(1e-7)          # |x / s| of order 1 in the tiny-s column
+    X[:, 11] *= np.float32(3e7)          # and in the huge-s column
+    X[::7, 11] = 0.0
+    amax = np.abs(oracle.smooth(X, s, "act")).max(axis=1).astype(np.float32)
+    q_ref, sx_ref = oracle.quantize_rows(X, s, "act")
+    s_d, a_d = to_dev(s), to_dev(amax)
+    for label, (Xq, sx, Xop) in (
+            ("rowmax", sq.quantize_act_rowmax(to_dev(X), s_d, a_d)),
+            ("table", sq.quantize_act_table(to_dev(X), s_d, sq.division_table(s_d),
+                                            row_amax=a_d))):
+        assert_bits_equal(sx.cpu().numpy(), sx_ref, f"x_scale ({label})")
+        assert_codes_equal(Xq.cpu().numpy(), q_ref, f"Xq ({label})")
+        assert_codes_equal(op_as_int(Xop), q_ref, f"Xop ({label})")
