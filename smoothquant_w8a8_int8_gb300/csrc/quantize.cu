@@ -422,6 +422,8 @@ __global__ void __launch_bounds__(kThreads) layernorm_quant_kernel(
 // Every wait (stages, group reductions) is bounded; on expiry the block
 // records an error for sq_device_status, lets its copies land and exits.
 constexpr int kRingWarps = 16;  // consumer warps of a block at most
+// modes of the register kernel: the row maximum found, given, or none (static)
+constexpr int kRegDynamic = 0, kRegGiven = 1, kRegStatic = 2;
 constexpr float kRoundMagic = 12582912.0f;      // 1.5 * 2^23
 constexpr float kTieLimit = 0.49993896484375f;  // 0.5 - 2^-14
 constexpr unsigned long long kRingTimeoutNs = 2000000000ull;
@@ -593,11 +595,15 @@ __device__ __forceinline__ float row_group_reduce(float v, int tpr, int g, float
 //    value within 2^-14 of a half-integer.
 // A row whose maximum is NaN or outside [2^-60, 2^100] takes IEEE divisions
 // throughout (the maximum is uniform across the row group, and so is the
-// choice; the group's reductions sync on its own barrier).  GIVEN: the row maxima come from row_amax (as the row-maximum
-// GEMM epilogue leaves them) instead of the reduction, and the codes saturate
+// choice; the group's reductions sync on its own barrier).  GIVEN: the row
+// maxima come from row_amax (as the row-maximum GEMM epilogue leaves them) instead of the reduction, and the codes saturate
 // at +-127 (a maximum below the true one cannot wrap them); an out-of-range
 // maximum still sends the block to the IEEE path, which finds its own.
-// While a tile is coded, one thread per row group asks for the
+// STATIC (Smooth-Static): no maximum; the given per-tensor scale, codes
+// saturating at +-127 (the launcher takes this kernel only for scales in
+// [2^-60, 2^60]: a subnormal or overflowing product then decides no code, and
+// a product at or beyond 2^22 fails the near-tie check and takes the IEEE
+// division).  While a tile is coded, one thread per row group asks for the
 // group's next row to be brought into L2 (a bulk prefetch, no registers held),
 // so that DRAM stays busy through the reductions and stores (measured 7% on
 // 8192 x 4096; a second row ahead measured slower).  TAB: the tables are
@@ -605,12 +611,13 @@ __device__ __forceinline__ float row_group_reduce(float v, int tpr, int g, float
 // block (the block's reciprocals cost 3% of the quantiser's time in the
 // BERT-large step, 2.51 -> 2.43 ms; reading the table through L1 inside the
 // tile loop, with no shared-memory copy, measured 8% slower than forming it).
-template <int kVPT, bool GIVEN, bool TAB>
+template <int kVPT, int MODE, bool TAB>
 __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
     const float *__restrict__ A, const float *__restrict__ s, const float4 *__restrict__ tab,
     int64_t rows, int K4, int tpr, int8_t *__restrict__ q, float *__restrict__ scale,
     __nv_bfloat16 *__restrict__ op, int32_t *__restrict__ l1,
-    const float *__restrict__ row_amax) {
+    const float *__restrict__ row_amax, float fixed_scale) {
+    constexpr bool GIVEN = MODE == kRegGiven, STATIC = MODE == kRegStatic;
     extern __shared__ float4 qtab[];
     float4 *nstab = qtab;       // -s
     float4 *ytab = qtab + K4;   // RN(1/s) or NaN
@@ -672,13 +679,13 @@ __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
             int j = t + i * tpr;
             v[i] = (valid && j < K4) ? __ldcs(a4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        // row maximum, div_smooth on f32x2 pairs (GIVEN: read)
+        // row maximum, div_smooth on f32x2 pairs (GIVEN: read; STATIC: none)
         float m = 0.0f;
         if (GIVEN) m = valid ? __ldg(row_amax + row) : 0.0f;
 #pragma unroll
         for (int i = 0; i < kVPT; ++i) {
             const int j = t + i * tpr;
-            if (GIVEN || j >= K4) continue;
+            if (MODE != kRegDynamic || j >= K4) continue;
             const float4 y = ytab[j], ns = nstab[j];
             const unsigned long long x01 = pk(v[i].x, v[i].y), x23 = pk(v[i].z, v[i].w);
             const unsigned long long y01 = pk(y.x, y.y), y23 = pk(y.z, y.w);
@@ -689,11 +696,11 @@ __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
             m = max3_nan(m, fabsf(d0), fabsf(d1));
             m = max3_nan(m, fabsf(d2), fabsf(d3));
         }
-        if (!GIVEN) {
+        if (MODE == kRegDynamic) {
             m = row_group_reduce<0>(m, tpr, g, red2[rb]);
             rb ^= 1;
         }
-        const bool exact = valid && !(m >= 0x1p-60f && m <= 0x1p100f);
+        const bool exact = !STATIC && valid && !(m >= 0x1p-60f && m <= 0x1p100f);
         float a1 = 0.0f;
         if (exact) {
             // IEEE divisions throughout (the definition as stated)
@@ -723,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
                 }
             }
         } else {
-            const float sc = __fdiv_rn(m, 127.0f);
+            const float sc = STATIC ? fixed_scale : __fdiv_rn(m, 127.0f);
             const float rsc = __frcp_rn(sc);
             const unsigned long long r2 = pk(rsc, rsc);
             if (valid) {
@@ -754,7 +761,7 @@ __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
                         if (!(fabsf(d[2]) <= kTieLimit)) c[2] = exact_code(v[i].z, -ns.z, sc);
                         if (!(fabsf(d[3]) <= kTieLimit)) c[3] = exact_code(v[i].w, -ns.w, sc);
                     }
-                    if (GIVEN) {
+                    if (MODE != kRegDynamic) {
 #pragma unroll
                         for (int e = 0; e < 4; ++e) c[e] = fminf(127.0f, fmaxf(-127.0f, c[e]));
                     }
@@ -1150,9 +1157,11 @@ sq_status launch_division_table(const float *s, int64_t K, float *table, cudaStr
 // The register Smooth-Dynamic kernel (K <= 8192): its tables of -s and 1/s in
 // shared memory (8 bytes per column; formed from s, or copied from s's
 // division table when one is given), its residency at that size, and the grid.
-sq_status launch_act_reg(const float *A, const float *s, const float *tab, int64_t rows,
-                         int64_t K, int8_t *q, float *scale, __nv_bfloat16 *op, int32_t *l1,
-                         const float *row_amax, const DeviceInfo &di, cudaStream_t st) {
+// mode: kRegDynamic, kRegGiven (row_amax) or kRegStatic (fixed_scale).
+sq_status launch_act_reg(int mode, const float *A, const float *s, const float *tab,
+                         int64_t rows, int64_t K, int8_t *q, float *scale, __nv_bfloat16 *op,
+                         int32_t *l1, const float *row_amax, float fixed_scale,
+                         const DeviceInfo &di, cudaStream_t st) {
     const int K4 = (int)(K / 4);
     const bool small = K4 <= kThreads * 4;
     const int vpt = small ? 4 : 8;
@@ -1161,19 +1170,21 @@ sq_status launch_act_reg(const float *A, const float *s, const float *tab, int64
     const int rpb = kThreads / tpr;
     const int64_t tiles = (rows + rpb - 1) / rpb;
     using Kern = void (*)(const float *, const float *, const float4 *, int64_t, int, int,
-                          int8_t *, float *, __nv_bfloat16 *, int32_t *, const float *);
-    static const Kern kerns[2][2][2] = {
-        {{quantize_act_reg<4, false, false>, quantize_act_reg<8, false, false>},
-         {quantize_act_reg<4, true, false>, quantize_act_reg<8, true, false>}},
-        {{quantize_act_reg<4, false, true>, quantize_act_reg<8, false, true>},
-         {quantize_act_reg<4, true, true>, quantize_act_reg<8, true, true>}}};
-    const int ti = tab ? 1 : 0, gi = row_amax ? 1 : 0, vi = small ? 0 : 1;
+                          int8_t *, float *, __nv_bfloat16 *, int32_t *, const float *, float);
+    static const Kern kerns[2][3][2] = {
+        {{quantize_act_reg<4, kRegDynamic, false>, quantize_act_reg<8, kRegDynamic, false>},
+         {quantize_act_reg<4, kRegGiven, false>, quantize_act_reg<8, kRegGiven, false>},
+         {quantize_act_reg<4, kRegStatic, false>, quantize_act_reg<8, kRegStatic, false>}},
+        {{quantize_act_reg<4, kRegDynamic, true>, quantize_act_reg<8, kRegDynamic, true>},
+         {quantize_act_reg<4, kRegGiven, true>, quantize_act_reg<8, kRegGiven, true>},
+         {quantize_act_reg<4, kRegStatic, true>, quantize_act_reg<8, kRegStatic, true>}}};
+    const int ti = tab ? 1 : 0, gi = mode, vi = small ? 0 : 1;
     const Kern kern = kerns[ti][gi][vi];
     const int smem = K4 * 32;
     constexpr int kMaxTab = kThreads * kMaxVPT * 32;  // 64 KB at K = 8192
     static std::mutex mu;
-    static bool opted[64][2][2][2] = {};
-    static int occ_dyn[64][2][2][2][8] = {};  // per device, table, mode, vpt, 256-float4 bucket
+    static bool opted[64][2][3][2] = {};
+    static int occ_dyn[64][2][3][2][8] = {};  // per device, table, mode, vpt, 256-float4 bucket
     int occ = 0;
     {
         std::lock_guard<std::mutex> lock(mu);
@@ -1201,7 +1212,7 @@ sq_status launch_act_reg(const float *A, const float *s, const float *tab, int64
     const int64_t grid = std::min<int64_t>(tiles, 2 * (int64_t)di.sms * occ);
     return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, 1, A, s,
                       reinterpret_cast<const float4 *>(tab), rows, K4, tpr, q, scale, op, l1,
-                      row_amax);
+                      row_amax, fixed_scale);
 }
 
 sq_status launch_quantize_act_given_max(const float *A, const float *s, const float *row_amax,
@@ -1215,7 +1226,8 @@ sq_status launch_quantize_act_given_max(const float *A, const float *s, const fl
     // that are not 1024 * 2^k keep, as in the dynamic dispatch)
     const bool pow2_rows = K >= 1024 && K <= 8192 && (K & (K - 1)) == 0;
     if (K <= 8192 && (pow2_rows || K > 2048))
-        return launch_act_reg(A, s, nullptr, rows, K, q, scale, op, l1, row_amax, di, st);
+        return launch_act_reg(kRegGiven, A, s, nullptr, rows, K, q, scale, op, l1, row_amax,
+                              0.0f, di, st);
     if (K <= 8192 && rows >= 16 * (int64_t)di.sms)
         return launch_quantize_act_dynamic(A, s, rows, K, q, scale, op, l1, di, st, row_amax);
     // other launches: the full quantiser (it finds the same maxima itself)
@@ -1235,7 +1247,9 @@ sq_status launch_quantize_act_table(const float *A, const float *s, const float 
     const bool reg = K <= 8192 && (row_amax ? (pow2_rows || K > 2048)
                                             : !(K <= 2048 && !pow2_rows &&
                                                 rows >= 16 * (int64_t)di.sms));
-    if (reg) return launch_act_reg(A, s, table, rows, K, q, scale, op, l1, row_amax, di, st);
+    if (reg)
+        return launch_act_reg(row_amax ? kRegGiven : kRegDynamic, A, s, table, rows, K, q, scale,
+                              op, l1, row_amax, 0.0f, di, st);
     if (row_amax)
         return launch_quantize_act_given_max(A, s, row_amax, rows, K, q, scale, op, l1, st);
     return launch_quantize_rows(kActDynamic, A, s, rows, K, q, scale, op, l1, 0.0f, st);
@@ -1270,7 +1284,13 @@ sq_status launch_quantize_rows(int direction, const float *A, const float *s, in
         void (*kern)(const float *, const float *, int64_t, int, int, int8_t *, float *,
                      __nv_bfloat16 *, int32_t *, float);
         if (direction == kActDynamic)
-            return launch_act_reg(A, s, nullptr, rows, K, q, scale, op, l1, nullptr, di, st);
+            return launch_act_reg(kRegDynamic, A, s, nullptr, rows, K, q, scale, op, l1, nullptr,
+                                  0.0f, di, st);
+        // Smooth-Static: the register kernel's static mode (f32x2 codes from the
+        // division tables) for scales where its shortcut is proven
+        if (direction == kActStatic && fixed_scale >= 0x1p-60f && fixed_scale <= 0x1p60f)
+            return launch_act_reg(kRegStatic, A, s, nullptr, rows, K, q, scale, op, l1, nullptr,
+                                  fixed_scale, di, st);
         if (direction == kWeight)
             kern = small ? quantize_rows_reg<kWeight, 4> : quantize_rows_reg<kWeight, 8>;
         else

@@ -602,6 +602,28 @@ def test_static_saturation_and_ties(sq, golden_dir):
     np.testing.assert_array_equal(Xq.cpu().numpy()[1, :v.size], -want)
 
 
+# Smooth-Static scales on both sides of the register kernel's range
+# [2^-60, 2^60] (outside it the IEEE-division kernel codes), rows in registers
+# (1024, 4096) and unevenly filled (3072), codes across the whole range with
+# saturation far beyond it (products at and above 2^22 take the IEEE division)
+@pytest.mark.parametrize("K", [1024, 3072, 4096])
+def test_static_scale_range_and_saturation(sq, K):
+    rng = np.random.default_rng(K + 3)
+    s = rng.uniform(0.1, 10.0, K).astype(np.float32)
+    s[7] = np.float32(1e-7)                            # no reciprocal: IEEE divisions
+    for scale in (np.float32(2.0 ** -61), np.float32(2.0 ** -60), np.float32(0.37),
+                  np.float32(2.0 ** 60), np.float32(2.0 ** 61)):
+        u = rng.uniform(-200.0, 200.0, (64, K)).astype(np.float32)
+        u[3] *= np.float32(2.0 ** 30)                  # far beyond saturation
+        u[5, :16] = (np.arange(16) - 7.5).astype(np.float32)  # exact half-integers
+        X = (u.astype(np.float64) * s * np.float64(scale)).astype(np.float32)
+        q_ref = oracle.quantize_static(X, s, scale)
+        Xq, sx, Xop = sq.quantize_act_static(to_dev(X), to_dev(s), float(scale))
+        assert_codes_equal(Xq.cpu().numpy(), q_ref, f"static Xq, scale {scale}")
+        assert_codes_equal(op_as_int(Xop), q_ref, f"static Xop, scale {scale}")
+        assert np.all(sx.cpu().numpy() == scale)
+
+
 def test_static_linear_block(sq):
     """Static codes through the tcgen05 GEMM + epilogue against the oracle."""
     M, K, N = 256, 1024, 512
