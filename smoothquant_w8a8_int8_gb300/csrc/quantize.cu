@@ -121,6 +121,44 @@ __device__ __forceinline__ float group_sum(float v, int tpr, float *red) {
     return v;
 }
 
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float max2_nan(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+// Reductions across the tpr threads of row group g for the register and
+// LayerNorm kernels, synchronised on the group's own named barrier (1 + g, tpr threads)
+// instead of the block's, so that the groups of a block run their tiles
+// independently.  The caller alternates two slot arrays between consecutive
+// reductions: a slot is rewritten only after the group has passed the next
+// reduction's barrier, hence after every thread read it, so one barrier per
+// reduction is enough.
+__device__ __forceinline__ void row_group_sync(int g, int tpr) {
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(tpr) : "memory");
+}
+template <int OP>  // 0: max (NaN kept), 1: max, 2: sum
+__device__ __forceinline__ float row_group_reduce(float v, int tpr, int g, float *red) {
+    auto op = [](float a, float b) {
+        return OP == 0 ? max2_nan(a, b) : OP == 1 ? fmaxf(a, b) : a + b;
+    };
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (tpr > 32) {
+        const int wpg = tpr >> 5;
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+        row_group_sync(g, tpr);
+        v = red[g * wpg];
+        for (int w = 1; w < wpg; ++w) v = op(v, red[g * wpg + w]);
+    }
+    return v;
+}
+
 // Registers path: K4 = K/4 <= tpr * kVPT.
 template <int DIR, int kVPT>
 __global__ void __launch_bounds__(kThreads) quantize_rows_reg(
@@ -317,7 +355,8 @@ __global__ void __launch_bounds__(kThreads) layernorm_quant_kernel(
     __nv_bfloat16 *__restrict__ op, int32_t *__restrict__ l1, float fixed_scale) {
     pdl_launch_dependents();
     pdl_wait();
-    __shared__ float red[kThreads / 32];
+    __shared__ float red2[2][kThreads / 32];
+    int rb = 0;  // the slot array of the group's next reduction (see row_group_reduce)
     const int rpb = kThreads / tpr;
     const int g = threadIdx.x / tpr;
     const int t = threadIdx.x % tpr;
@@ -339,7 +378,8 @@ __global__ void __launch_bounds__(kThreads) layernorm_quant_kernel(
         float sum = 0.0f;
 #pragma unroll
         for (int i = 0; i < kVPT; ++i) sum += (v[i].x + v[i].y) + (v[i].z + v[i].w);
-        const float mean = __fdiv_rn(group_sum(sum, tpr, red), Kf);
+        const float mean = __fdiv_rn(row_group_reduce<2>(sum, tpr, g, red2[rb]), Kf);
+        rb ^= 1;
         float sq = 0.0f;
 #pragma unroll
         for (int i = 0; i < kVPT; ++i) {
@@ -349,7 +389,8 @@ __global__ void __launch_bounds__(kThreads) layernorm_quant_kernel(
                 sq += (v[i].x * v[i].x + v[i].y * v[i].y) + (v[i].z * v[i].z + v[i].w * v[i].w);
             }
         }
-        const float var = __fdiv_rn(group_sum(sq, tpr, red), Kf);
+        const float var = __fdiv_rn(row_group_reduce<2>(sq, tpr, g, red2[rb]), Kf);
+        rb ^= 1;
         const float rstd = __frsqrt_rn(__fadd_rn(var, eps));
         float m = 0.0f;
 #pragma unroll
@@ -372,7 +413,8 @@ __global__ void __launch_bounds__(kThreads) layernorm_quant_kernel(
         }
         float sc = fixed_scale;
         if (KIND == kActDynamic) {
-            m = group_max(m, tpr, red);
+            m = row_group_reduce<1>(m, tpr, g, red2[rb]);
+            rb ^= 1;
             sc = m == 0.0f ? 1.0f : __fdiv_rn(m, 127.0f);
         }
         const float rsc = __frcp_rn(sc);
@@ -386,7 +428,8 @@ __global__ void __launch_bounds__(kThreads) layernorm_quant_kernel(
             }
         }
         if (l1) {
-            a1 = group_sum(a1, tpr, red);
+            a1 = row_group_reduce<2>(a1, tpr, g, red2[rb]);
+            rb ^= 1;
             if (valid && t == 0) l1[row] = (int32_t)a1;
         }
     }
@@ -429,17 +472,6 @@ constexpr float kTieLimit = 0.49993896484375f;  // 0.5 - 2^-14
 constexpr unsigned long long kRingTimeoutNs = 2000000000ull;
 
 __device__ unsigned int g_quant_error;
-
-__device__ __forceinline__ float max3_nan(float a, float b, float c) {
-    float d;
-    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-__device__ __forceinline__ float max2_nan(float a, float b) {
-    float d;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
-    return d;
-}
 
 __device__ __forceinline__ uint32_t saddr(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -556,33 +588,6 @@ __device__ __noinline__ float exact_code(float x, float s, float scale) {
 
 // |fl(x / s)| (IEEE division), out of line for the rare exact path
 __device__ __noinline__ float abs_quotient(float x, float s) { return fabsf(__fdiv_rn(x, s)); }
-
-// Reductions across the tpr threads of row group g for the register kernel
-// below, synchronised on the group's own named barrier (1 + g, tpr threads)
-// instead of the block's, so that the groups of a block run their tiles
-// independently.  The caller alternates two slot arrays between consecutive
-// reductions: a slot is rewritten only after the group has passed the next
-// reduction's barrier, hence after every thread read it, so one barrier per
-// reduction is enough.
-__device__ __forceinline__ void row_group_sync(int g, int tpr) {
-    asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(tpr) : "memory");
-}
-template <int OP>  // 0: max (NaN kept), 1: max, 2: sum
-__device__ __forceinline__ float row_group_reduce(float v, int tpr, int g, float *red) {
-    auto op = [](float a, float b) {
-        return OP == 0 ? max2_nan(a, b) : OP == 1 ? fmaxf(a, b) : a + b;
-    };
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
-    if (tpr > 32) {
-        const int wpg = tpr >> 5;
-        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-        row_group_sync(g, tpr);
-        v = red[g * wpg];
-        for (int w = 1; w < wpg; ++w) v = op(v, red[g * wpg + w]);
-    }
-    return v;
-}
 
 // Smooth-Dynamic activations, the row in registers (K4 <= tpr * kVPT): the
 // arithmetic of the ring kernel below on the register kernel's layout (tpr
