@@ -131,6 +131,12 @@ __device__ __forceinline__ float max2_nan(float a, float b) {
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
     return d;
 }
+// RN(1/s) where the corrected reciprocal division is proven (|s| in
+// [2^-20, 2^20]), NaN elsewhere: the division tables' entry for s
+__device__ __forceinline__ float smooth_recip(float x) {
+    const float a = fabsf(x);
+    return (a >= 0x1p-20f && a <= 0x1p20f) ? __frcp_rn(x) : __int_as_float(0x7fffffff);
+}
 
 // Reductions across the tpr threads of row group g for the register and
 // LayerNorm kernels, synchronised on the group's own named barrier (1 + g, tpr threads)
@@ -339,102 +345,6 @@ int resident_blocks(Kern k) {
     return per_sm;
 }
 
-// LayerNorm with the next linear's quantiser fused in (the encoder's
-// normalisation, Table 3, emitting the smoothed int8 codes SmoothQuant's
-// folding implies).  A group of tpr threads owns a row, held in registers:
-//   mean = fl(sum / K), var = fl(sum (h - mean)^2 / K) (fp32 tree sums),
-//   y = fma((h - mean) * rstd, gamma, beta), rstd = RN(1 / sqrt(var + eps)),
-// then the quantiser of KIND on y: v = fl(y / s), per-token scale from the row
-// maximum (dynamic) or the given scale (static), codes as quantize_rows_reg.
-// y is also stored when Y is given.
-template <int KIND, int kVPT>
-__global__ void __launch_bounds__(kThreads) layernorm_quant_kernel(
-    const float *__restrict__ H, const float *__restrict__ gamma, const float *__restrict__ beta,
-    float eps, const float *__restrict__ s, int64_t rows, int K4, int tpr,
-    float *__restrict__ Y, int8_t *__restrict__ q, float *__restrict__ scale,
-    __nv_bfloat16 *__restrict__ op, int32_t *__restrict__ l1, float fixed_scale) {
-    pdl_launch_dependents();
-    pdl_wait();
-    __shared__ float red2[2][kThreads / 32];
-    int rb = 0;  // the slot array of the group's next reduction (see row_group_reduce)
-    const int rpb = kThreads / tpr;
-    const int g = threadIdx.x / tpr;
-    const int t = threadIdx.x % tpr;
-    const float4 *s4 = reinterpret_cast<const float4 *>(s);
-    const float4 *g4 = reinterpret_cast<const float4 *>(gamma);
-    const float4 *b4 = reinterpret_cast<const float4 *>(beta);
-    const float Kf = (float)(4 * K4);
-    const int64_t tiles = (rows + rpb - 1) / rpb;
-    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-        const int64_t row = tile * rpb + g;
-        const bool valid = row < rows;
-        const float4 *h4 = reinterpret_cast<const float4 *>(H) + (valid ? row : 0) * K4;
-        float4 v[kVPT];
-#pragma unroll
-        for (int i = 0; i < kVPT; ++i) {
-            const int j = t + i * tpr;
-            v[i] = (valid && j < K4) ? __ldcs(h4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        float sum = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kVPT; ++i) sum += (v[i].x + v[i].y) + (v[i].z + v[i].w);
-        const float mean = __fdiv_rn(row_group_reduce<2>(sum, tpr, g, red2[rb]), Kf);
-        rb ^= 1;
-        float sq = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kVPT; ++i) {
-            const int j = t + i * tpr;
-            if (j < K4) {
-                v[i] = make_float4(v[i].x - mean, v[i].y - mean, v[i].z - mean, v[i].w - mean);
-                sq += (v[i].x * v[i].x + v[i].y * v[i].y) + (v[i].z * v[i].z + v[i].w * v[i].w);
-            }
-        }
-        const float var = __fdiv_rn(row_group_reduce<2>(sq, tpr, g, red2[rb]), Kf);
-        rb ^= 1;
-        const float rstd = __frsqrt_rn(__fadd_rn(var, eps));
-        float m = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kVPT; ++i) {
-            const int j = t + i * tpr;
-            if (j < K4) {
-                const float4 gv = __ldg(g4 + j), bv = __ldg(b4 + j), sv = __ldg(s4 + j);
-                float4 y;
-                y.x = __fmaf_rn(__fmul_rn(v[i].x, rstd), gv.x, bv.x);
-                y.y = __fmaf_rn(__fmul_rn(v[i].y, rstd), gv.y, bv.y);
-                y.z = __fmaf_rn(__fmul_rn(v[i].z, rstd), gv.z, bv.z);
-                y.w = __fmaf_rn(__fmul_rn(v[i].w, rstd), gv.w, bv.w);
-                if (Y && valid) reinterpret_cast<float4 *>(Y)[row * K4 + j] = y;
-                v[i] = make_float4(__fdiv_rn(y.x, sv.x), __fdiv_rn(y.y, sv.y),
-                                   __fdiv_rn(y.z, sv.z), __fdiv_rn(y.w, sv.w));
-                if (KIND == kActDynamic)
-                    m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)),
-                                       fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
-            }
-        }
-        float sc = fixed_scale;
-        if (KIND == kActDynamic) {
-            m = row_group_reduce<1>(m, tpr, g, red2[rb]);
-            rb ^= 1;
-            sc = m == 0.0f ? 1.0f : __fdiv_rn(m, 127.0f);
-        }
-        const float rsc = __frcp_rn(sc);
-        float a1 = 0.0f;
-        if (valid) {
-            if (t == 0) scale[row] = sc;
-#pragma unroll
-            for (int i = 0; i < kVPT; ++i) {
-                const int j = t + i * tpr;
-                if (j < K4) a1 += store_codes<KIND>(v[i], sc, rsc, row * K4 + j, q, op);
-            }
-        }
-        if (l1) {
-            a1 = row_group_reduce<2>(a1, tpr, g, red2[rb]);
-            rb ^= 1;
-            if (valid && t == 0) l1[row] = (int32_t)a1;
-        }
-    }
-}
-
 
 // ---------------------------------------------------------------------------
 // Smooth-Dynamic activation quantiser (Table 10's run-time step).
@@ -630,10 +540,6 @@ __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
     pdl_wait();
     __shared__ float red2[2][kThreads / 32];
     int rb = 0;  // the slot array of the group's next reduction
-    auto recip = [](float x) {
-        const float a = fabsf(x);
-        return (a >= 0x1p-20f && a <= 0x1p20f) ? __frcp_rn(x) : __int_as_float(0x7fffffff);
-    };
     const int rpb = kThreads / tpr;
     const int g = threadIdx.x / tpr;
     const int t = threadIdx.x % tpr;
@@ -659,7 +565,8 @@ __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
         for (int j = threadIdx.x; j < K4; j += kThreads) {
             const float4 v = __ldg(s4 + j);
             nstab[j] = make_float4(-v.x, -v.y, -v.z, -v.w);
-            ytab[j] = make_float4(recip(v.x), recip(v.y), recip(v.z), recip(v.w));
+            ytab[j] = make_float4(smooth_recip(v.x), smooth_recip(v.y), smooth_recip(v.z),
+                                  smooth_recip(v.w));
         }
     }
     __syncthreads();
@@ -767,6 +674,188 @@ __global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) quantize_act_reg(
                         if (!(fabsf(d[3]) <= kTieLimit)) c[3] = exact_code(v[i].w, -ns.w, sc);
                     }
                     if (MODE != kRegDynamic) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) c[e] = fminf(127.0f, fmaxf(-127.0f, c[e]));
+                    }
+                    store4_codes(c[0], c[1], c[2], c[3], ((int64_t)row * K4 + j) * 4, q, op);
+                    a1 += (fabsf(c[0]) + fabsf(c[1])) + (fabsf(c[2]) + fabsf(c[3]));
+                }
+            }
+        }
+        if (l1) {
+            a1 = row_group_reduce<2>(a1, tpr, g, red2[rb]);  // exact: <= 127 * 8192 < 2^24
+            rb ^= 1;
+            if (valid && t == 0) l1[row] = (int32_t)a1;
+        }
+    }
+}
+
+// LayerNorm with the next linear's quantiser fused in (the encoder's
+// normalisation, Table 3, emitting the smoothed int8 codes SmoothQuant's
+// folding implies).  A group of tpr threads owns a row, held in registers:
+//   mean = fl(sum / K), var = fl(sum (h - mean)^2 / K) (fp32 tree sums),
+//   y = fma((h - mean) * rstd, gamma, beta), rstd = RN(1 / sqrt(var + eps)),
+// then the quantiser of KIND on y with the register kernel's arithmetic and
+// shared-memory division tables: the row maximum of |fl(y / s)| by the
+// corrected reciprocal division (dynamic) or the given scale (static), codes
+// from p = RN(RN(y RN(1/s)) RN(1/scale)) with the near-tie elements on IEEE
+// divisions.  A row whose maximum is NaN or outside [2^-60, 2^100], and every
+// row when a static scale lies outside [2^-60, 2^60] (fast == 0), takes IEEE
+// divisions throughout.  y is also stored when Y is given.  Row reductions
+// sync on each row group's named barrier.
+template <int KIND, int kVPT>
+__global__ void __launch_bounds__(kThreads, kVPT == 4 ? 4 : 2) layernorm_quant_kernel(
+    const float *__restrict__ H, const float *__restrict__ gamma, const float *__restrict__ beta,
+    float eps, const float *__restrict__ s, int64_t rows, int K4, int tpr,
+    float *__restrict__ Y, int8_t *__restrict__ q, float *__restrict__ scale,
+    __nv_bfloat16 *__restrict__ op, int32_t *__restrict__ l1, float fixed_scale, int fast) {
+    extern __shared__ float4 qtab[];
+    float4 *nstab = qtab;       // -s
+    float4 *ytab = qtab + K4;   // RN(1/s) or NaN
+    pdl_launch_dependents();
+    pdl_wait();
+    __shared__ float red2[2][kThreads / 32];
+    int rb = 0;  // the slot array of the group's next reduction (see row_group_reduce)
+    const int rpb = kThreads / tpr;
+    const int g = threadIdx.x / tpr;
+    const int t = threadIdx.x % tpr;
+    const float4 *s4 = reinterpret_cast<const float4 *>(s);
+    const float4 *g4 = reinterpret_cast<const float4 *>(gamma);
+    const float4 *b4 = reinterpret_cast<const float4 *>(beta);
+    for (int j = threadIdx.x; j < K4; j += kThreads) {
+        const float4 v = __ldg(s4 + j);
+        nstab[j] = make_float4(-v.x, -v.y, -v.z, -v.w);
+        ytab[j] = make_float4(smooth_recip(v.x), smooth_recip(v.y), smooth_recip(v.z),
+                              smooth_recip(v.w));
+    }
+    __syncthreads();
+    const unsigned long long magic2 = pk(kRoundMagic, kRoundMagic);
+    const float Kf = (float)(4 * K4);
+    const int64_t tiles = (rows + rpb - 1) / rpb;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const int64_t row = tile * rpb + g;
+        const bool valid = row < rows;
+        const float4 *h4 = reinterpret_cast<const float4 *>(H) + (valid ? row : 0) * K4;
+        float4 v[kVPT];
+#pragma unroll
+        for (int i = 0; i < kVPT; ++i) {
+            const int j = t + i * tpr;
+            v[i] = (valid && j < K4) ? __ldcs(h4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float sum = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kVPT; ++i) sum += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+        const float mean = __fdiv_rn(row_group_reduce<2>(sum, tpr, g, red2[rb]), Kf);
+        rb ^= 1;
+        float sq = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kVPT; ++i) {
+            const int j = t + i * tpr;
+            if (j < K4) {
+                v[i] = make_float4(v[i].x - mean, v[i].y - mean, v[i].z - mean, v[i].w - mean);
+                sq += (v[i].x * v[i].x + v[i].y * v[i].y) + (v[i].z * v[i].z + v[i].w * v[i].w);
+            }
+        }
+        const float var = __fdiv_rn(row_group_reduce<2>(sq, tpr, g, red2[rb]), Kf);
+        rb ^= 1;
+        const float rstd = __frsqrt_rn(__fadd_rn(var, eps));
+        // y = LayerNorm(h) (kept in v), and for Smooth-Dynamic the row maximum of
+        // |fl(y / s)| by the corrected reciprocal division on f32x2 pairs
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kVPT; ++i) {
+            const int j = t + i * tpr;
+            if (j >= K4) continue;
+            const float4 gv = __ldg(g4 + j), bv = __ldg(b4 + j);
+            float4 y;
+            y.x = __fmaf_rn(__fmul_rn(v[i].x, rstd), gv.x, bv.x);
+            y.y = __fmaf_rn(__fmul_rn(v[i].y, rstd), gv.y, bv.y);
+            y.z = __fmaf_rn(__fmul_rn(v[i].z, rstd), gv.z, bv.z);
+            y.w = __fmaf_rn(__fmul_rn(v[i].w, rstd), gv.w, bv.w);
+            if (Y && valid) reinterpret_cast<float4 *>(Y)[row * K4 + j] = y;
+            v[i] = y;
+            if (KIND == kActDynamic) {
+                const float4 ys = ytab[j], ns = nstab[j];
+                const unsigned long long x01 = pk(y.x, y.y), x23 = pk(y.z, y.w);
+                const unsigned long long y01 = pk(ys.x, ys.y), y23 = pk(ys.z, ys.w);
+                const unsigned long long q01 = mul2(x01, y01), q23 = mul2(x23, y23);
+                float d0, d1, d2, d3;
+                upk(fma2(fma2(q01, pk(ns.x, ns.y), x01), y01, q01), d0, d1);
+                upk(fma2(fma2(q23, pk(ns.z, ns.w), x23), y23, q23), d2, d3);
+                m = max3_nan(m, max2_nan(fabsf(d0), fabsf(d1)), max2_nan(fabsf(d2), fabsf(d3)));
+            }
+        }
+        bool exact;
+        if (KIND == kActDynamic) {
+            m = row_group_reduce<0>(m, tpr, g, red2[rb]);
+            rb ^= 1;
+            exact = !(m >= 0x1p-60f && m <= 0x1p100f);
+        } else {
+            exact = !fast;
+        }
+        float a1 = 0.0f;
+        if (exact) {
+            // IEEE divisions: v = fl(y / s), then the codes as the definition states
+            float me = 0.0f;
+#pragma unroll
+            for (int i = 0; i < kVPT; ++i) {
+                const int j = t + i * tpr;
+                if (j >= K4) continue;
+                const float4 sv = __ldg(s4 + j);
+                v[i] = make_float4(__fdiv_rn(v[i].x, sv.x), __fdiv_rn(v[i].y, sv.y),
+                                   __fdiv_rn(v[i].z, sv.z), __fdiv_rn(v[i].w, sv.w));
+                if (KIND == kActDynamic)
+                    me = fmaxf(me, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)),
+                                         fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+            }
+            float sc = fixed_scale;
+            if (KIND == kActDynamic) {
+                me = row_group_reduce<1>(me, tpr, g, red2[rb]);
+                rb ^= 1;
+                sc = me == 0.0f ? 1.0f : __fdiv_rn(me, 127.0f);
+            }
+            const float rsc = __frcp_rn(sc);
+            if (valid) {
+                if (t == 0) scale[row] = sc;
+#pragma unroll
+                for (int i = 0; i < kVPT; ++i) {
+                    const int j = t + i * tpr;
+                    if (j < K4) a1 += store_codes<KIND>(v[i], sc, rsc, row * K4 + j, q, op);
+                }
+            }
+        } else {
+            // p = RN(RN(y RN(1/s)) RN(1/scale)), rint where p is 2^-14 clear of a
+            // half-integer (NaN kept: a column without a reciprocal), else the
+            // IEEE divisions; Smooth-Static codes saturate at +-127
+            const float sc = KIND == kActDynamic ? __fdiv_rn(m, 127.0f) : fixed_scale;
+            const float rsc = __frcp_rn(sc);
+            const unsigned long long r2 = pk(rsc, rsc);
+            if (valid) {
+                if (t == 0) scale[row] = sc;
+#pragma unroll
+                for (int i = 0; i < kVPT; ++i) {
+                    const int j = t + i * tpr;
+                    if (j >= K4) continue;
+                    const float4 ys = ytab[j];
+                    const unsigned long long p01 = mul2(mul2(pk(v[i].x, v[i].y), pk(ys.x, ys.y)), r2);
+                    const unsigned long long p23 = mul2(mul2(pk(v[i].z, v[i].w), pk(ys.z, ys.w)), r2);
+                    const unsigned long long t01 = sub2(add2(p01, magic2), magic2);
+                    const unsigned long long t23 = sub2(add2(p23, magic2), magic2);
+                    float c[4], d[4];
+                    upk(t01, c[0], c[1]);
+                    upk(t23, c[2], c[3]);
+                    upk(sub2(p01, t01), d[0], d[1]);
+                    upk(sub2(p23, t23), d[2], d[3]);
+                    const float dm = max3_nan(fabsf(d[0]), fabsf(d[1]),
+                                              max2_nan(fabsf(d[2]), fabsf(d[3])));
+                    if (!(dm <= kTieLimit)) {
+                        const float4 ns = nstab[j];
+                        if (!(fabsf(d[0]) <= kTieLimit)) c[0] = exact_code(v[i].x, -ns.x, sc);
+                        if (!(fabsf(d[1]) <= kTieLimit)) c[1] = exact_code(v[i].y, -ns.y, sc);
+                        if (!(fabsf(d[2]) <= kTieLimit)) c[2] = exact_code(v[i].z, -ns.z, sc);
+                        if (!(fabsf(d[3]) <= kTieLimit)) c[3] = exact_code(v[i].w, -ns.w, sc);
+                    }
+                    if (KIND == kActStatic) {
 #pragma unroll
                         for (int e = 0; e < 4; ++e) c[e] = fminf(127.0f, fmaxf(-127.0f, c[e]));
                     }
@@ -1333,17 +1422,40 @@ sq_status launch_layernorm_quant(const float *H, const float *gamma, const float
     const int64_t tiles = (rows + rpb - 1) / rpb;
     using Kern = void (*)(const float *, const float *, const float *, float, const float *,
                           int64_t, int, int, float *, int8_t *, float *, __nv_bfloat16 *,
-                          int32_t *, float);
+                          int32_t *, float, int);
     static const Kern kerns[2][2] = {
         {layernorm_quant_kernel<kActDynamic, 4>, layernorm_quant_kernel<kActDynamic, 8>},
         {layernorm_quant_kernel<kActStatic, 4>, layernorm_quant_kernel<kActStatic, 8>}};
-    const Kern kern = kerns[static_scale > 0.0f ? 1 : 0][small ? 0 : 1];
-    static int per_sm[2][2] = {};
-    int &occ = per_sm[static_scale > 0.0f ? 1 : 0][small ? 0 : 1];
-    if (!occ) occ = resident_blocks(kern);
+    const int ki = static_scale > 0.0f ? 1 : 0, vi = small ? 0 : 1;
+    const Kern kern = kerns[ki][vi];
+    // the static shortcut's proven range of scales (as in launch_act_reg's static mode)
+    const int fast = static_scale >= 0x1p-60f && static_scale <= 0x1p60f;
+    const int smem = K4 * 32;
+    constexpr int kMaxTab = kThreads * kMaxVPT * 32;  // 64 KB at K = 8192
+    static std::mutex mu;
+    static bool opted[64][2][2] = {};
+    static int occ_dyn[64][2][2][8] = {};  // per device, kind, vpt, 256-float4 bucket of K4
+    int occ = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        const int dv = di.device & 63;
+        if (!opted[dv][ki][vi]) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kMaxTab) != cudaSuccess)
+                return SQ_ERR_CUDA;
+            opted[dv][ki][vi] = true;
+        }
+        const int bucket = (K4 - 1) / 256;
+        int &o = occ_dyn[dv][ki][vi][bucket];
+        if (!o && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                       &o, kern, kThreads, (bucket + 1) * 256 * 32) != cudaSuccess ||
+                   o < 1))
+            return SQ_ERR_CUDA;
+        occ = o;
+    }
     const int64_t grid = std::min<int64_t>(tiles, (int64_t)di.sms * occ);
-    return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), 0, st, 1, H, gamma, beta, eps, s,
-                      rows, K4, tpr, Y, q, scale, op, l1, static_scale);
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, 1, H, gamma, beta,
+                      eps, s, rows, K4, tpr, Y, q, scale, op, l1, static_scale, fast);
 }
 
 sq_status launch_act_absmax(const float *A, const float *s, int64_t rows, int64_t K,

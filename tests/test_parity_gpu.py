@@ -742,6 +742,43 @@ def test_layernorm_quant_parity(sq, M, K):
     assert np.all(sx3.cpu().numpy() == np.float32(scale))
 
 
+@pytest.mark.parametrize("K", [1024, 3072])
+def test_layernorm_quant_extreme_factors_and_scales(sq, K):
+    """Smoothing factors without a reciprocal in the division tables (|s|
+    outside [2^-20, 2^20]: IEEE divisions for those columns), beta alone in a
+    row of zeros (constant rows), and static scales on both sides of the fast
+    path's range [2^-60, 2^60]: codes and scales bit for bit against the
+    oracle's quantisers applied to the LayerNorm's own output."""
+    rng = np.random.default_rng(K + 17)
+    M = 70
+    H = (rng.standard_normal((M, K)) * 2.0).astype(np.float32)
+    H[4] = 0.0
+    gamma = (1.0 + 0.05 * rng.standard_normal(K)).astype(np.float32)
+    beta = (0.05 * rng.standard_normal(K)).astype(np.float32)
+    s = rng.uniform(0.3, 4.0, K).astype(np.float32)
+    s[[2, 9]] = np.float32(1e-7), np.float32(3e7)
+    eps = 1e-12
+    Xq, sx, Xop, Y, l1 = sq.layernorm_quant(to_dev(H), to_dev(gamma), to_dev(beta), eps,
+                                            to_dev(s), want_y=True, want_l1=True)
+    y = Y.cpu().numpy()
+    q_ref, sx_ref = oracle.quantize_rows(y, s, "act")
+    assert_codes_equal(Xq.cpu().numpy(), q_ref, "Xq")
+    assert_codes_equal(op_as_int(Xop), q_ref, "Xop")
+    assert_bits_equal(sx.cpu().numpy(), sx_ref, "x_scale")
+    np.testing.assert_array_equal(l1.cpu().numpy(), np.abs(q_ref.astype(np.int64)).sum(axis=1))
+    s2 = rng.uniform(0.3, 4.0, K).astype(np.float32)
+    for scale in (np.float32(2.0 ** -61), np.float32(2.0 ** -60), np.float32(0.01),
+                  np.float32(2.0 ** 60), np.float32(2.0 ** 61)):
+        H2 = (rng.standard_normal((M, K)) * 2.0).astype(np.float32)
+        g2 = (gamma * np.float32(scale) * 40.0).astype(np.float32)  # codes across the range
+        Xq2, sx2, _, Y2, _ = sq.layernorm_quant(to_dev(H2), to_dev(g2), to_dev(beta), eps,
+                                                to_dev(s2), static_scale=float(scale),
+                                                want_y=True, want_op=False)
+        q2 = oracle.quantize_static(Y2.cpu().numpy(), s2, scale)
+        assert_codes_equal(Xq2.cpu().numpy(), q2, f"static Xq, scale {scale}")
+        assert np.all(sx2.cpu().numpy() == scale)
+
+
 def test_layernorm_quant_constant_rows(sq):
     """Rows with no spread normalise to beta exactly (zero deviation)."""
     K = 256
