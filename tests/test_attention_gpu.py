@@ -40,6 +40,18 @@ def test_attention_parity(sq, B, S, H):
     assert_close_fp32(got, ref, f"attention B={B} S={S} H={H}")
 
 
+# More (sequence, head, query tile) units than a GB300 has SMs, so that each
+# persistent CTA takes several in turn: an odd number of 64-key chunks with a
+# partial last query tile (S = 192), and the longest sequence (S = 448)
+@pytest.mark.parametrize("B,S,H", [(4, 192, 40), (2, 448, 24)])
+def test_attention_several_units_per_cta(sq, B, S, H):
+    QKV = _qkv(B, S, H, seed=B + S + H)
+    ref = oracle.attention(QKV, B, S, H, 64)
+    got = sq.attention(to_dev(QKV), B, S, H).cpu().numpy()
+    assert sq.device_status() == sq.SQ_OK
+    assert_close_fp32(got, ref, f"attention B={B} S={S} H={H}")
+
+
 @pytest.mark.parametrize("spread", [0.05, 2.0, 4.0])
 def test_attention_logit_scales(sq, spread):
     """Nearly uniform weights (small logits) and peaked ones (large logits,
