@@ -20,12 +20,8 @@
 // most 448 (the logits of a query tile live in tensor memory: S columns, plus
 // 64 for O).  Persistent: one CTA per SM (the shared memory allows no second)
 // takes units blockIdx.x, + gridDim.x, ..., every barrier's phase running on
-// across them; a unit's copies start once the previous unit's P V products are
-// complete (pv_done: its P buffers are the next Q tile's and K chunks' space)
-// and its P V waits until the previous epilogue has read O (o_empty), so the
-// next unit's copies and logits overlap the previous unit's epilogue
-// (measured on GB300 at B = 32, S = 256, H = 16: 137.9 -> 135.8 us against one
-// CTA per unit).  Roles (448 threads):
+// across them; a unit's P V waits until the previous epilogue has read O
+// (o_empty).  Roles (448 threads):
 //   warps 0-3, 10-13  softmax and epilogue, two warps per tensor-memory lane
 //              quarter (query rows), each taking 32 of every chunk's 64 keys:
 //              the exact row maximum over all S logits (the two halves'
@@ -41,13 +37,23 @@
 //              128-byte swizzle): Q and K in place (hi over the raw value, lo
 //              beside it), V transposed so that keys run along K (every warp
 //              reads its share of the raw chunk before any writes);
-// K chunks cycle through four 32 KB slots (hi + lo): two of their own and the
-// two halves of the first P buffer (unused until the logits are complete), so
-// that up to four are in flight; V chunks go through the first two.  P is
-// double-buffered, the second buffer over the Q tile (dead once the logits are
-// complete), so that the softmax writes chunk c + 1 while the MMAs read c.
 //   warp 8     tensor memory, and lane 0 issues the MMAs:
 //              S[:, 64c..] = Q K_c^T, then O += P_c V_c.
+// Where P lives (the template's TP):
+//  * S <= 256 (TP): in tensor memory.  The softmax writes P's high part over
+//    the S chunk it has just read and its low part into one of two 64-column
+//    buffers (columns 320 and 384; O at 256), and the P V MMAs take A from
+//    tensor memory.  Shared memory then holds only Q and four 32 KB chunk slots
+//    that K and V chunks take in turn, so the next unit's Q tile is copied as
+//    soon as this unit's logits are complete and its K chunks as slots free up
+//    during this unit's P V: copies, splitting and logits of the next unit
+//    overlap this unit's softmax (measured on GB300 at B = 32, S = 256, H = 16:
+//    105 us, against 136 us with P in shared memory and 138 us with one CTA
+//    per unit).
+//  * S > 256: in shared memory, double-buffered: the first buffer over slots
+//    2-3 (which take K chunks only, so that four are in flight), the second
+//    over the Q tile (dead once the logits are complete); a unit's copies then
+//    wait until the previous unit's P V products are complete (pv_done).
 // A query tile that runs past its sequence (S % 128 == 64) copies the next
 // rows of the input (or zeros past its end) into its unused query rows; their
 // outputs are not stored and no other row reads them.
@@ -80,6 +86,10 @@ constexpr int SLOT_BYTES = 2 * KV_PART;  // hi + lo parts of one 64-row chunk
 static_assert(OFF_QL == OFF_QH + SLOT_BYTES && OFF_PL == OFF_PH + SLOT_BYTES, "slot layout");
 constexpr int A_SMEM = OFF_XCH + 2 * 2 * ABQ * 4 + 1024;  // + 1024-byte alignment slack
 constexpr int TMEM_COLS = 512;                // S (<= 448) + O (64)
+// P in tensor memory (sequences of at most 256): S in columns 0..S-1, P's tf32
+// high part written over each S chunk once it is read, O at 256, and P's low
+// part double-buffered at 320 and 384
+constexpr int TP_MAXS = 256, TP_O = 256, TP_PLO = 320;
 constexpr unsigned long long kAttnTimeoutNs = 4000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -180,6 +190,16 @@ __device__ __forceinline__ void mma_tf32(uint32_t d, uint64_t a, uint64_t b, uin
         "l"(a), "l"(b), "r"(IDESC_TF32), "r"(acc)
         : "memory");
 }
+// The same with A from tensor memory (lane = row of A, one 32-bit column per
+// K element: K = 8 columns from taddr).
+__device__ __forceinline__ void mma_tf32_ta(uint32_t d, uint32_t a_tmem, uint64_t b,
+                                            uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+        "r"(a_tmem), "l"(b), "r"(IDESC_TF32), "r"(acc)
+        : "memory");
+}
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -201,6 +221,30 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// 32 columns of this warp's 32 lanes into tensor memory from registers; the
+// caller waits (tmem_st_wait) before signalling that they are written.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
+        "%10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, "
+        "%27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Byte offset of element (row, k), k < 64, of an operand part of `rows` rows:
@@ -239,6 +283,7 @@ __device__ __forceinline__ float hi_part(float x) {
     return __uint_as_float(__float_as_uint(x) & 0xffffe000u);
 }
 
+template <bool TP>
 __global__ void __launch_bounds__(A_THREADS, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tmQKV, int S, int H, int units,
                      float scale, float *__restrict__ O) {
@@ -249,6 +294,10 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qtiles = (S + ABQ - 1) / ABQ;
     const int nch = S / ACH;
+    // the slot of chunk n (K chunks first, then V): with P in tensor memory all
+    // four slots take chunks in turn; otherwise slots 2-3 (the first P buffer)
+    // take K chunks only
+    auto slot_of = [&](int n) { return TP ? (n & 3) : chunk_slot(n, nch); };
     // unit u: query tile u % qtiles of head (u / qtiles) % H of sequence u / (qtiles H)
     auto unit_of = [&](int u, int &q0, int &h, int &row_b) {
         q0 = (u % qtiles) * ABQ;
@@ -305,9 +354,12 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                 int q0, h, row_b;
                 unit_of(u, q0, h, row_b);
                 const int xq = h * AD, xk = H * AD + h * AD, xv = 2 * H * AD + h * AD;
-                // the previous unit's P V products are complete: the Q region (its
-                // second P buffer) and slots 2-3 (its first) are free
-                if (it > 0 && !wait_bar(su32(&B.pv_done), (uint32_t)(it - 1) & 1u, abort)) break;
+                // the Q region is free: with P in tensor memory once the previous
+                // unit's logits are complete, otherwise once its P V products are
+                // (the Q region and slots 2-3 are its P buffers)
+                if (it > 0 && !wait_bar(su32(TP ? &B.s_full : &B.pv_done), (uint32_t)(it - 1) & 1u,
+                                        abort))
+                    break;
                 // the Q tile: four boxes (two 32-column K blocks x two 64-row halves)
                 arrive_expect(su32(&B.q_tma), Q_PART);
                 for (int kb = 0; kb < 2; ++kb)
@@ -355,7 +407,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                 }
                 bool ok = true;
                 for (int n = 0; n < 2 * nch; ++n) {
-                    const int sl = chunk_slot(n, nch);
+                    const int sl = slot_of(n);
                     const int use = uses[sl];
                     // the slot's previous chunk is done with
                     if (use > 0 &&
@@ -410,7 +462,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                 if (lane == 0) bar_arrive(su32(&B.q_full));
             }
             for (int n = 0; n < 2 * nch; ++n) {
-                const int sl = chunk_slot(n, nch);
+                const int sl = slot_of(n);
                 const uint32_t ph = (uint32_t)uses[sl]++ & 1u;
                 uint8_t *hi = smem + slot_off(sl);
                 uint8_t *lo = hi + KV_PART;
@@ -478,7 +530,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                 if (!wait_bar(su32(&B.q_full), (uint32_t)it & 1u, abort)) goto done_m;
                 tc_after();
                 for (int c = 0; c < nch; ++c) {
-                    const int sl = chunk_slot(c, nch);
+                    const int sl = slot_of(c);
                     if (!wait_bar(su32(&B.slot_full[sl]), (uint32_t)uses[sl]++ & 1u, abort))
                         goto done_m;
                     tc_after();
@@ -504,33 +556,55 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                 if (it > 0 && !wait_bar(su32(&B.o_empty), (uint32_t)(it - 1) & 1u, abort))
                     goto done_m;
                 for (int c = 0; c < nch; ++c) {
-                    const int sl = chunk_slot(nch + c, nch);
+                    const int sl = slot_of(nch + c);
                     if (!wait_bar(su32(&B.slot_full[sl]), (uint32_t)uses[sl]++ & 1u, abort))
                         goto done_m;
                     if (!wait_bar(su32(&B.p_full[c & 1]), (uint32_t)pfill[c & 1]++ & 1u, abort))
                         goto done_m;
                     tc_after();
                     const uint32_t vh = sbase + slot_off(sl), vl = vh + KV_PART;
-                    const uint32_t pa = sbase + p_off(c);
-                    const uint32_t d = tmem + (uint32_t)AMAXS;  // O after the logits' columns
+                    if (TP) {
+                        // A = P from tensor memory: its high part over S chunk c, its
+                        // low part in buffer c % 2
+                        const uint32_t d = tmem + (uint32_t)TP_O;
+                        const uint32_t phi = tmem + (uint32_t)(c * ACH);
+                        const uint32_t plo = tmem + (uint32_t)(TP_PLO + (c & 1) * ACH);
 #pragma unroll
-                    for (int p = 0; p < 3; ++p) {
-                        const uint32_t a = p == 2 ? pa + P_PART : pa;
-                        const uint32_t bb = p == 1 ? vl : vh;
+                        for (int p = 0; p < 3; ++p) {
+                            const uint32_t a = p == 2 ? plo : phi;
+                            const uint32_t bb = p == 1 ? vl : vh;
 #pragma unroll
-                        for (int kb = 0; kb < 2; ++kb) {
-                            const uint64_t ad = desc_sw128(a + kb * ABQ * 128);
-                            const uint64_t bd = desc_sw128(bb + kb * AD * 128);
+                            for (int kb = 0; kb < 2; ++kb) {
+                                const uint64_t bd = desc_sw128(bb + kb * AD * 128);
 #pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                mma_tf32(d, ad + 2 * k, bd + 2 * k, (c | p | kb | k) ? 1u : 0u);
+                                for (int k = 0; k < 4; ++k)
+                                    mma_tf32_ta(d, a + (uint32_t)(32 * kb + 8 * k), bd + 2 * k,
+                                                (c | p | kb | k) ? 1u : 0u);
+                            }
+                        }
+                    } else {
+                        const uint32_t pa = sbase + p_off(c);
+                        const uint32_t d = tmem + (uint32_t)AMAXS;  // O after the logits' columns
+#pragma unroll
+                        for (int p = 0; p < 3; ++p) {
+                            const uint32_t a = p == 2 ? pa + P_PART : pa;
+                            const uint32_t bb = p == 1 ? vl : vh;
+#pragma unroll
+                            for (int kb = 0; kb < 2; ++kb) {
+                                const uint64_t ad = desc_sw128(a + kb * ABQ * 128);
+                                const uint64_t bd = desc_sw128(bb + kb * AD * 128);
+#pragma unroll
+                                for (int k = 0; k < 4; ++k)
+                                    mma_tf32(d, ad + 2 * k, bd + 2 * k,
+                                             (c | p | kb | k) ? 1u : 0u);
+                            }
                         }
                     }
                     mma_commit(su32(&B.slot_empty[sl]));
                     mma_commit(su32(&B.p_empty[c & 1]));
                 }
                 mma_commit(su32(&B.o_full));
-                mma_commit(su32(&B.pv_done));
+                if (!TP) mma_commit(su32(&B.pv_done));
             }
         done_m:
             // every MMA issued above completes before tensor memory is freed
@@ -577,26 +651,42 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                 if (!warp_wait(su32(&B.p_empty[c & 1]), ((uint32_t)pfill[c & 1]++ & 1u) ^ 1u,
                                abort))
                     goto done_s;
-                uint8_t *pbuf = smem + p_off(c);
                 float v[32];
                 tmem_ld32(lane_addr + c * ACH + 32 * half, v);
+                if (TP) {
+                    // P's high part over the logits just read, its low part into
+                    // buffer c % 2
+                    float pl[32];
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    float pp[4], ph[4], pl[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        pp[e] = exp2f(__fmaf_rn(v[j + e], cl2e, -mc));
-                        sum += pp[e];
-                        ph[e] = hi_part(pp[e]);
-                        pl[e] = pp[e] - ph[e];
+                    for (int j = 0; j < 32; ++j) {
+                        const float pp = exp2f(__fmaf_rn(v[j], cl2e, -mc));
+                        sum += pp;
+                        v[j] = hi_part(pp);
+                        pl[j] = pp - v[j];
                     }
-                    const uint32_t off = sw_off(r, 32 * half + j, ABQ);
-                    *reinterpret_cast<float4 *>(pbuf + off) =
-                        make_float4(ph[0], ph[1], ph[2], ph[3]);
-                    *reinterpret_cast<float4 *>(pbuf + P_PART + off) =
-                        make_float4(pl[0], pl[1], pl[2], pl[3]);
+                    tmem_st32(lane_addr + c * ACH + 32 * half, v);
+                    tmem_st32(lane_addr + TP_PLO + (c & 1) * ACH + 32 * half, pl);
+                    tmem_st_wait();
+                } else {
+                    uint8_t *pbuf = smem + p_off(c);
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        float pp[4], ph[4], pl[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            pp[e] = exp2f(__fmaf_rn(v[j + e], cl2e, -mc));
+                            sum += pp[e];
+                            ph[e] = hi_part(pp[e]);
+                            pl[e] = pp[e] - ph[e];
+                        }
+                        const uint32_t off = sw_off(r, 32 * half + j, ABQ);
+                        *reinterpret_cast<float4 *>(pbuf + off) =
+                            make_float4(ph[0], ph[1], ph[2], ph[3]);
+                        *reinterpret_cast<float4 *>(pbuf + P_PART + off) =
+                            make_float4(pl[0], pl[1], pl[2], pl[3]);
+                    }
+                    fence_async_smem();
                 }
-                fence_async_smem();
                 tc_before();
                 __syncwarp();
                 if (lane == 0) bar_arrive(su32(&B.p_full[c & 1]));
@@ -612,7 +702,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
             tc_after();
             const float inv = __frcp_rn(sum);
             float o[32];
-            tmem_ld32(lane_addr + AMAXS + 32 * half, o);
+            tmem_ld32(lane_addr + (TP ? TP_O : AMAXS) + 32 * half, o);
             // O is in registers: the next unit's P V may overwrite it
             tc_before();
             __syncwarp();
@@ -651,7 +741,11 @@ sq_status launch_attention(const float *QKV, int64_t B, int64_t S, int64_t H, fl
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!attr[di.device & 63]) {
-            if (cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(attention_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     A_SMEM) != cudaSuccess ||
+                cudaFuncSetAttribute(attention_kernel<false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      A_SMEM) != cudaSuccess)
                 return SQ_ERR_CUDA;
             attr[di.device & 63] = true;
@@ -665,8 +759,9 @@ sq_status launch_attention(const float *QKV, int64_t B, int64_t S, int64_t H, fl
     // QKV as B*S rows of 3*H*64 floats, copied in boxes of 64 rows x 32 columns
     CUtensorMap map;
     if ((rc = make_map_f32(&map, QKV, B * S, 3 * H * AD, 64, 32)) != SQ_OK) return rc;
-    return launch_pdl(attention_kernel, dim3((unsigned)grid), dim3(A_THREADS), A_SMEM, st, 1, map,
-                      (int)S, (int)H, (int)units, scale, O);
+    return launch_pdl(S <= TP_MAXS ? attention_kernel<true> : attention_kernel<false>,
+                      dim3((unsigned)grid), dim3(A_THREADS), A_SMEM, st, 1, map, (int)S, (int)H,
+                      (int)units, scale, O);
 }
 
 sq_status attention_take_error(cudaStream_t st) {
