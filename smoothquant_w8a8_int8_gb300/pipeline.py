@@ -36,12 +36,15 @@ class LinearLayer:
 
 
 class HostLinearPipeline:
-    def __init__(self, M: int, max_K: int, max_N: int, device="cuda"):
+    def __init__(self, M: int, max_K: int, max_N: int, device="cuda", slots: int = 2):
         dev = torch.device(device)
         self.M = M
         self.dev = dev
-        self.x_slots = [torch.empty(M * max_K, dtype=torch.float32, device=dev) for _ in range(2)]
-        self.y_slots = [torch.empty(M * max_N, dtype=torch.float32, device=dev) for _ in range(2)]
+        self.nslots = slots
+        self.x_slots = [torch.empty(M * max_K, dtype=torch.float32, device=dev)
+                        for _ in range(slots)]
+        self.y_slots = [torch.empty(M * max_N, dtype=torch.float32, device=dev)
+                        for _ in range(slots)]
         self.xop = torch.empty(M * max_K, dtype=torch.bfloat16, device=dev)
         self.sx = torch.empty(M, dtype=torch.float32, device=dev)
         self.h2d = torch.cuda.Stream(device=dev)
@@ -58,15 +61,15 @@ class HostLinearPipeline:
         n = len(layers)
         x_ready = [torch.cuda.Event() for _ in range(n)]
         y_ready = [torch.cuda.Event() for _ in range(n)]
-        x_free = [None, None]
-        y_free = [None, None]
+        x_free = [None] * self.nslots
+        y_free = [None] * self.nslots
         cur = torch.cuda.current_stream(self.dev)
         for st in (self.h2d, self.comp, self.d2h):
             st.wait_stream(cur)
         for i, (L, Xh, Yh) in enumerate(zip(layers, X_host, Y_host)):
             K = Xh.shape[1]
             N = Yh.shape[1]
-            slot = i % 2
+            slot = i % self.nslots
             dX = self.x_slots[slot][: M * K].view(M, K)
             dY = self.y_slots[slot][: M * N].view(M, N)
             # host -> device
