@@ -2,7 +2,9 @@
 split-K on a caller workspace) captured in a CUDA graph: replays on new input
 data equal eager calls bit for bit.  Each entry point is called once eagerly
 first, so that the one-time per-device set-up (function attributes, cluster
-occupancy, tensor-map encoder) happens outside the capture."""
+occupancy, tensor-map encoder) happens outside the capture.  The step runs the
+quantiser from s's division table, both GEMM schedules and the attention
+kernel."""
 import pytest
 import torch
 
@@ -39,13 +41,17 @@ def test_step_captured_in_graph(sq):
     Xops = sq.empty_operand(Ms, Ks)
     Y = torch.empty(M, N, device=dev)
     Ys = torch.empty(Ms, Ns, device=dev)
+    table = sq.division_table(s)
+    QKV = torch.randn(2 * 128, 3 * 4 * 64, device=dev)
+    O = torch.empty(2 * 128, 4 * 64, device=dev)
 
     def step():
-        sq.quantize_act(X, s, out=(None, sx, Xop))
+        sq.quantize_act_table(X, s, table, out=(None, sx, Xop))
         sq.linear_i8(Xop, sx, Wop, sw, c.bias, None, wl.EPI_BIAS_GELU, out=Y)
         sq.quantize_act(Xs, ss, out=(None, sxs, Xops))
         sq.linear_i8_ws(Xops, sxs, Wops, sws, cs.bias, cs.residual, wl.EPI_BIAS_RESIDUAL, out=Ys,
                         workspace=ws)
+        sq.attention(QKV, 2, 128, 4, 64, out=O)
 
     step()  # eager, outside capture: one-time set-up
     torch.cuda.synchronize()
@@ -56,11 +62,13 @@ def test_step_captured_in_graph(sq):
         gen = torch.Generator(device=dev).manual_seed(seed)
         X.copy_(torch.randn(M, K, generator=gen, device=dev))
         Xs.copy_(torch.randn(Ms, Ks, generator=gen, device=dev))
+        QKV.copy_(torch.randn(QKV.shape, generator=gen, device=dev))
         g.replay()
         torch.cuda.synchronize()
-        Yg, Ysg = Y.clone(), Ys.clone()
+        Yg, Ysg, Og = Y.clone(), Ys.clone(), O.clone()
         step()
         torch.cuda.synchronize()
         assert torch.equal(Yg, Y), f"pair GEMM, seed {seed}"
         assert torch.equal(Ysg, Ys), f"split-K GEMM, seed {seed}"
+        assert torch.equal(Og, O), f"attention, seed {seed}"
     assert sq.device_status() == sq.SQ_OK
