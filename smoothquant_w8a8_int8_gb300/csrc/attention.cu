@@ -49,7 +49,9 @@
 //    during this unit's P V: copies, splitting and logits of the next unit
 //    overlap this unit's softmax (measured on GB300 at B = 32, S = 256, H = 16:
 //    105 us, against 136 us with P in shared memory and 138 us with one CTA
-//    per unit).
+//    per unit).  Slots 2p and 2p + 1 share a region in which their K chunks
+//    form one 128-row operand, so the logits of two chunks take one N = 128
+//    MMA group instead of two N = 64 ones (105 -> 97 us).
 //  * S > 256: in shared memory, double-buffered: the first buffer over slots
 //    2-3 (which take K chunks only, so that four are in flight), the second
 //    over the Q tile (dead once the logits are complete); a unit's copies then
@@ -96,6 +98,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 // instruction descriptor, kind::tf32: D fp32, A and B tf32, both K-major, N = 64, M = 128
 constexpr uint32_t IDESC_TF32 =
     (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(64 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+// the same with N = 128 (the logits of two K chunks at once)
+constexpr uint32_t IDESC_TF32_N128 =
+    (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(128 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 
 __device__ unsigned int g_attn_error;
 
@@ -183,11 +188,12 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
     d |= (uint64_t)2 << 61;
     return d;
 }
-__device__ __forceinline__ void mma_tf32(uint32_t d, uint64_t a, uint64_t b, uint32_t acc) {
+__device__ __forceinline__ void mma_tf32(uint32_t d, uint64_t a, uint64_t b, uint32_t acc,
+                                         uint32_t idesc = IDESC_TF32) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-        "l"(a), "l"(b), "r"(IDESC_TF32), "r"(acc)
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
 // The same with A from tensor memory (lane = row of A, one 32-bit column per
@@ -255,10 +261,19 @@ __device__ __forceinline__ uint32_t sw_off(int row, int k, int rows) {
                       ((k & 3) << 2));
 }
 
-// Shared-memory offset of slot s: 0, 1 of their own, 2, 3 the first P buffer;
+// With P in shared memory: slots 0, 1 of their own, 2, 3 the first P buffer;
 // chunk n (K chunks first, then V) and the slot it uses; P buffer c % 2.
-__device__ __forceinline__ int slot_off(int s) {
-    return s < 2 ? OFF_RING + s * SLOT_BYTES : OFF_PH + (s - 2) * SLOT_BYTES;
+static_assert(OFF_PH == OFF_RING + 2 * SLOT_BYTES, "slots 2-3 over the first P buffer");
+// Offset of K block kb (32 of the chunk's 64 columns) of part `part` (0: hi,
+// 1: lo) of slot s, 64 rows x 128 bytes.  With P in shared memory a slot is
+// [hi kb0 | hi kb1 | lo kb0 | lo kb1]; with P in tensor memory slots 2p and 2p + 1
+// share a 64 KB region [hi kb0 | hi kb1 | lo kb0 | lo kb1] of 128 rows each,
+// slot 2p in rows 0-63, so that two K chunks there form one 128-row operand.
+template <bool TP>
+__device__ __forceinline__ int piece_off(int s, int part, int kb) {
+    return TP ? OFF_RING + (s >> 1) * 2 * SLOT_BYTES + part * 2 * KV_PART + kb * KV_PART +
+                    (s & 1) * (KV_PART / 2)
+              : OFF_RING + s * SLOT_BYTES + part * KV_PART + kb * (KV_PART / 2);
 }
 __device__ __forceinline__ int chunk_slot(int n, int nch) {
     return n < nch ? (n & 3) : ((n - nch) & 1);
@@ -418,12 +433,11 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                     ++uses[sl];
                     // K chunk n raw into the slot's hi part, V chunk n - nch into its lo part
                     const bool kc = n < nch;
-                    const uint32_t dst = sbase + slot_off(sl) + (kc ? 0 : KV_PART);
                     const int x = kc ? xk : xv, y = row_b + (kc ? n : n - nch) * ACH;
                     arrive_expect(su32(&B.slot_tma[sl]), KV_PART);
                     for (int kb = 0; kb < 2; ++kb)
-                        tma_box(dst + kb * (ACH * 128), &tmQKV, su32(&B.slot_tma[sl]),
-                                x + 32 * kb, y);
+                        tma_box(sbase + piece_off<TP>(sl, kc ? 0 : 1, kb), &tmQKV,
+                                su32(&B.slot_tma[sl]), x + 32 * kb, y);
                 }
                 if (!ok) {
                     ++it;  // its Q copy was issued
@@ -464,21 +478,21 @@ __global__ void __launch_bounds__(A_THREADS, 1)
             for (int n = 0; n < 2 * nch; ++n) {
                 const int sl = slot_of(n);
                 const uint32_t ph = (uint32_t)uses[sl]++ & 1u;
-                uint8_t *hi = smem + slot_off(sl);
-                uint8_t *lo = hi + KV_PART;
                 if (!warp_wait(su32(&B.slot_tma[sl]), ph, abort)) goto done_l;
                 if (n < nch) {
                     // K chunk n, in place: hi over the copied value, lo beside it
-                    float4 *kh = reinterpret_cast<float4 *>(hi);
-                    float4 *kl = reinterpret_cast<float4 *>(lo);
 #pragma unroll
                     for (int i = 0; i < KV_PART / 16 / 128; ++i) {
-                        const int f = i * 128 + t;
-                        const float4 v = kh[f];
+                        const int f = i * 128 + t;  // 512 float4 per K block
+                        float4 *kh = reinterpret_cast<float4 *>(
+                                         smem + piece_off<TP>(sl, 0, f >> 9)) + (f & 511);
+                        float4 *kl = reinterpret_cast<float4 *>(
+                                         smem + piece_off<TP>(sl, 1, f >> 9)) + (f & 511);
+                        const float4 v = *kh;
                         const float4 vh = make_float4(hi_part(v.x), hi_part(v.y), hi_part(v.z),
                                                       hi_part(v.w));
-                        kh[f] = vh;
-                        kl[f] = make_float4(v.x - vh.x, v.y - vh.y, v.z - vh.z, v.w - vh.w);
+                        *kh = vh;
+                        *kl = make_float4(v.x - vh.x, v.y - vh.y, v.z - vh.z, v.w - vh.w);
                     }
                 } else {
                     // V chunk (copied into the lo part as [key][dimension]), transposed
@@ -494,7 +508,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                         const int c = w * 8 + k8;  // 32 (key block, dimension group) pairs
                         const int key = 32 * (c >> 4) + lane, d = 4 * (c & 15);
                         v[k8] = *reinterpret_cast<const float4 *>(
-                            lo + (d >> 5) * (ACH * 128) + key * 128 +
+                            smem + piece_off<TP>(sl, 1, d >> 5) + key * 128 +
                             ((((d & 31) >> 2) ^ (key & 7)) << 4));
                     }
                     __syncwarp();
@@ -508,9 +522,11 @@ __global__ void __launch_bounds__(A_THREADS, 1)
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const float eh = hi_part(e[q]);
-                            const uint32_t off = sw_off(d + q, key, AD);
-                            *reinterpret_cast<float *>(hi + off) = eh;
-                            *reinterpret_cast<float *>(lo + off) = e[q] - eh;
+                            const uint32_t off = sw_off(d + q, key & 31, AD);
+                            *reinterpret_cast<float *>(smem + piece_off<TP>(sl, 0, key >> 5) +
+                                                       off) = eh;
+                            *reinterpret_cast<float *>(smem + piece_off<TP>(sl, 1, key >> 5) +
+                                                       off) = e[q] - eh;
                         }
                     }
                 }
@@ -529,27 +545,35 @@ __global__ void __launch_bounds__(A_THREADS, 1)
             for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
                 if (!wait_bar(su32(&B.q_full), (uint32_t)it & 1u, abort)) goto done_m;
                 tc_after();
-                for (int c = 0; c < nch; ++c) {
+                for (int c = 0; c < nch;) {
+                    // with P in tensor memory two K chunks of one slot region form a
+                    // 128-row operand: their logits in one N = 128 MMA group
                     const int sl = slot_of(c);
+                    const bool two = TP && c + 1 < nch;
                     if (!wait_bar(su32(&B.slot_full[sl]), (uint32_t)uses[sl]++ & 1u, abort))
                         goto done_m;
+                    if (two && !wait_bar(su32(&B.slot_full[sl + 1]), (uint32_t)uses[sl + 1]++ & 1u,
+                                         abort))
+                        goto done_m;
                     tc_after();
-                    const uint32_t kh = sbase + slot_off(sl), kl = kh + KV_PART;
                     const uint32_t d = tmem + (uint32_t)(c * ACH);
 #pragma unroll
                     for (int p = 0; p < 3; ++p) {
                         const uint32_t a = p == 2 ? sbase + OFF_QL : sbase + OFF_QH;
-                        const uint32_t bb = p == 1 ? kl : kh;
 #pragma unroll
                         for (int kb = 0; kb < 2; ++kb) {
                             const uint64_t ad = desc_sw128(a + kb * ABQ * 128);
-                            const uint64_t bd = desc_sw128(bb + kb * ACH * 128);
+                            const uint64_t bd =
+                                desc_sw128(sbase + piece_off<TP>(sl, p == 1 ? 1 : 0, kb));
 #pragma unroll
                             for (int k = 0; k < 4; ++k)  // K = 8 tf32 = 32 bytes per MMA
-                                mma_tf32(d, ad + 2 * k, bd + 2 * k, (p | kb | k) ? 1u : 0u);
+                                mma_tf32(d, ad + 2 * k, bd + 2 * k, (p | kb | k) ? 1u : 0u,
+                                         two ? IDESC_TF32_N128 : IDESC_TF32);
                         }
                     }
                     mma_commit(su32(&B.slot_empty[sl]));
+                    if (two) mma_commit(su32(&B.slot_empty[sl + 1]));
+                    c += two ? 2 : 1;
                 }
                 mma_commit(su32(&B.s_full));
                 // the previous unit's epilogue has read O out of tensor memory
@@ -562,7 +586,6 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                     if (!wait_bar(su32(&B.p_full[c & 1]), (uint32_t)pfill[c & 1]++ & 1u, abort))
                         goto done_m;
                     tc_after();
-                    const uint32_t vh = sbase + slot_off(sl), vl = vh + KV_PART;
                     if (TP) {
                         // A = P from tensor memory: its high part over S chunk c, its
                         // low part in buffer c % 2
@@ -572,10 +595,10 @@ __global__ void __launch_bounds__(A_THREADS, 1)
 #pragma unroll
                         for (int p = 0; p < 3; ++p) {
                             const uint32_t a = p == 2 ? plo : phi;
-                            const uint32_t bb = p == 1 ? vl : vh;
 #pragma unroll
                             for (int kb = 0; kb < 2; ++kb) {
-                                const uint64_t bd = desc_sw128(bb + kb * AD * 128);
+                                const uint64_t bd =
+                                    desc_sw128(sbase + piece_off<TP>(sl, p == 1 ? 1 : 0, kb));
 #pragma unroll
                                 for (int k = 0; k < 4; ++k)
                                     mma_tf32_ta(d, a + (uint32_t)(32 * kb + 8 * k), bd + 2 * k,
@@ -588,11 +611,11 @@ __global__ void __launch_bounds__(A_THREADS, 1)
 #pragma unroll
                         for (int p = 0; p < 3; ++p) {
                             const uint32_t a = p == 2 ? pa + P_PART : pa;
-                            const uint32_t bb = p == 1 ? vl : vh;
 #pragma unroll
                             for (int kb = 0; kb < 2; ++kb) {
                                 const uint64_t ad = desc_sw128(a + kb * ABQ * 128);
-                                const uint64_t bd = desc_sw128(bb + kb * AD * 128);
+                                const uint64_t bd =
+                                    desc_sw128(sbase + piece_off<TP>(sl, p == 1 ? 1 : 0, kb));
 #pragma unroll
                                 for (int k = 0; k < 4; ++k)
                                     mma_tf32(d, ad + 2 * k, bd + 2 * k,
