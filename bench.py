@@ -506,9 +506,10 @@ def e2e_leg(args, layers, M, ops_per_step, world):
             "copies_only_gbs": round((h2d + d2h) / (copy_ms * 1e-3) / 1e9, 1),
             "outputs_match_device": bool(ok),
             "outputs_checked": "every element of every layer's Y",
-            "path": "pinned host X -> device, sq_quantize_act(_table) + sq_linear_i8, Y -> pinned "
-                    "host; copies overlapped with kernels on three streams "
-                    "(smoothquant_w8a8_int8_gb300.pipeline.HostLinearPipeline)"}
+            "path": "sq_linear_block_host (C ABI): pinned host X -> device, the layer's "
+                    "quantiser + sq_linear_i8, Y -> pinned host, copies overlapped with kernels "
+                    "on three streams (called through "
+                    "smoothquant_w8a8_int8_gb300.pipeline.HostLinearPipeline)"}
 
 
 def bench_ours(args, w: wl.Workload, rank: int, world: int, headline: bool = True):

@@ -419,6 +419,54 @@ sq_status sq_check_division(uint32_t b_first, uint32_t b_count, uint32_t a_first
                             uint32_t a_count, int corrected, unsigned long long *out,
                             void *stream);
 
+/* ---- The linear block on host buffers -------------------------------------- */
+
+/* One linear layer for sq_linear_block_host.  Device pointers as for
+ * sq_quantize_act / sq_quantize_act_table / sq_quantize_act_static and
+ * sq_linear_i8; static_scale > 0 selects Smooth-Static with that per-tensor
+ * scale, 0 Smooth-Dynamic (then s_table, if not NULL, is sq_division_table(s)). */
+typedef struct {
+    int64_t K, N;             /* input and output features (K a multiple of 16) */
+    int mode;                 /* epilogue: SQ_EPI_NONE .. SQ_EPI_BIAS_RESIDUAL */
+    float static_scale;       /* > 0: Smooth-Static scale; 0: Smooth-Dynamic */
+    const float *s;           /* smoothing factor [K] */
+    const float *s_table;     /* [K][2] division table of s, or NULL */
+    const void *Wop;          /* packed weight operand [N][K] (sq_pack_weight) */
+    const float *w_scale;     /* [N] */
+    const int32_t *w_row_l1;  /* [N] row L1 norms of the weight codes, or NULL */
+    const float *bias;        /* [N] or NULL */
+    const float *residual;    /* [M][N] or NULL (mode SQ_EPI_BIAS_RESIDUAL) */
+} sq_linear_layer;
+
+/* Device scratch that sq_linear_block_host needs for layers of at most max_K
+ * inputs and max_N outputs at M tokens: two input slots (M x max_K fp32), two
+ * output slots (M x max_N fp32), the operand (M x max_K bf16 codes) and the
+ * per-token scales, each 256-byte aligned. */
+sq_status sq_linear_block_host_scratch_bytes(int64_t M, int64_t max_K, int64_t max_N,
+                                             size_t *bytes);
+
+/* Y_host[i] = the linear block of layers[i] on X_host[i] for every i < count
+ * (fp32 [M][K_i] in, fp32 [M][N_i] out, host memory; pinned memory makes the
+ * copies asynchronous and lets them overlap): per layer the input is copied to
+ * the device on stream_h2d, quantised and multiplied (the layer's quantiser,
+ * then sq_linear_i8 with its epilogue) on stream_compute, and the output copied
+ * back on stream_d2h, through two device slots for inputs and two for outputs
+ * in `scratch` (sq_linear_block_host_scratch_bytes over the layers' largest K
+ * and N), so that layer i's kernels overlap the copies of layers i + 1 and
+ * i - 1.  The streams may coincide (no overlap then).  Returns once everything
+ * is enqueued; the outputs are complete when stream_d2h is (synchronise it
+ * before reading Y_host).  The call orders its own work through CUDA events
+ * it creates and releases; ordering with other work on the device (e.g. the
+ * producers of the weights) is the caller's.  scratch 256-byte aligned.
+ * Errors: SQ_ERR_INVALID_ARG (NULL arrays or pointers, count or M < 0, K or N
+ * <= 0, a mode outside 0..3, scratch too small), SQ_ERR_ALIGNMENT (K % 16,
+ * scratch), and the statuses of the calls it makes (checked for every layer
+ * before anything is enqueued). */
+sq_status sq_linear_block_host(const sq_linear_layer *layers, int64_t count, int64_t M,
+                               const float *const *X_host, float *const *Y_host, void *scratch,
+                               size_t scratch_bytes, void *stream_h2d, void *stream_compute,
+                               void *stream_d2h);
+
 /* ---- Device status --------------------------------------------------------- */
 
 /* Synchronises `stream`, then reports and clears the library's device error

@@ -28,8 +28,18 @@ EXPORTS = ("sq_status_string", "sq_version", "sq_operand_bytes", "sq_packed_weig
            "sq_linear_i8_requant", "sq_division_table", "sq_linear_i8_rowmax",
            "sq_quantize_act_rowmax", "sq_quantize_act_table", "sq_attention",
            "sq_linear_workspace_bytes", "sq_linear_i8_ws", "sq_linear_i8_requant_ws", "sq_linear_i8_static_ws", "sq_static_workspace_reset",
-           "sq_static_workspace", "sq_linear_i8_mma_sync",
+           "sq_static_workspace", "sq_linear_i8_mma_sync", "sq_linear_block_host_scratch_bytes",
+           "sq_linear_block_host",
            "sq_check_division", "sq_device_status", "sq_get_device_status")
+
+class LinearLayerC(ctypes.Structure):
+    """sq_linear_layer (include/sq.h): one layer of sq_linear_block_host."""
+    _fields_ = [("K", ctypes.c_int64), ("N", ctypes.c_int64), ("mode", ctypes.c_int),
+                ("static_scale", ctypes.c_float), ("s", ctypes.c_void_p),
+                ("s_table", ctypes.c_void_p), ("Wop", ctypes.c_void_p),
+                ("w_scale", ctypes.c_void_p), ("w_row_l1", ctypes.c_void_p),
+                ("bias", ctypes.c_void_p), ("residual", ctypes.c_void_p)]
+
 
 _lock = threading.Lock()
 _lib = None
@@ -89,6 +99,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                 "sq_static_workspace_reset": ([vp], i32),
                 "sq_static_workspace": ([ctypes.POINTER(vp), ctypes.POINTER(ctypes.c_size_t)], i32),
                 "sq_linear_i8_mma_sync": ([vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp], i32),
+                "sq_linear_block_host_scratch_bytes": ([i64, i64, i64,
+                                                        ctypes.POINTER(ctypes.c_size_t)], i32),
+                "sq_linear_block_host": ([ctypes.POINTER(LinearLayerC), i64, i64, vp, vp, vp,
+                                          ctypes.c_size_t, vp, vp, vp], i32),
                 "sq_check_division": ([ctypes.c_uint32] * 4 + [i32, vp, vp], i32),
                 "sq_device_status": ([vp], i32),
                 "sq_get_device_status": ([vp], i32),
@@ -535,6 +549,29 @@ def linear_i8_requant_ws(Xop, x_scale, Wop, w_scale, bias, residual, mode, s_nex
                                           _p(s_next), float(scale), _p(Yq), _p(Yop), _p(xs), wp,
                                           wn, _stream(stream)), "sq_linear_i8_requant_ws")
     return Yq, Yop, xs
+
+
+def linear_block_host_scratch_bytes(M: int, max_K: int, max_N: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().sq_linear_block_host_scratch_bytes(M, max_K, max_N, ctypes.byref(n)),
+           "sq_linear_block_host_scratch_bytes")
+    return n.value
+
+
+def linear_block_host(layers, M: int, X_host, Y_host, scratch: torch.Tensor, streams) -> None:
+    """sq_linear_block_host: `layers` a sequence of LinearLayerC, X_host / Y_host
+    pinned host tensors (one per layer), `scratch` a device uint8 tensor of at
+    least linear_block_host_scratch_bytes bytes, `streams` the (h2d, compute,
+    d2h) torch streams.  Returns once everything is enqueued."""
+    n = len(layers)
+    arr = (LinearLayerC * n)(*layers)
+    xs = (ctypes.c_void_p * n)(*[x.data_ptr() for x in X_host])
+    ys = (ctypes.c_void_p * n)(*[y.data_ptr() for y in Y_host])
+    h2d, comp, d2h = (st.cuda_stream for st in streams)
+    _check(load().sq_linear_block_host(arr, n, M, ctypes.cast(xs, ctypes.c_void_p),
+                                       ctypes.cast(ys, ctypes.c_void_p), _p(scratch),
+                                       scratch.numel(), h2d, comp, d2h),
+           "sq_linear_block_host")
 
 
 def linear_i8_mma_sync(Xq, x_scale, Wq, w_scale, bias=None, residual=None, mode=EPI_BIAS,

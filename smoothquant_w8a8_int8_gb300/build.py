@@ -22,7 +22,7 @@ LIB = os.path.join(HERE, "libsq_gb300.so")
 OBJ_DIR = os.path.join(HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["api.cu", "quantize.cu", "gemm_mma.cu", "gemm_tc.cu", "selfcheck.cu", "static_ws.cu",
-           "attention.cu"]
+           "attention.cu", "host_pipeline.cu"]
 
 
 def nvcc() -> str:

@@ -261,6 +261,38 @@ def test_workspace_entry_points_check_arguments_first(lib):
     assert qt(a, a, a, _fake(0x10002), 4, 32, a, a, None, None, None) == ALIGN  # maxima
     assert qt(a, a, a, None, 4, 40, a, a, None, None, None) == ALIGN        # K % 16
     assert qt(None, None, None, None, 0, 32, None, None, None, None, None) == 0
+    # the host-buffer pipeline: argument checks before anything is enqueued
+    from smoothquant_w8a8_int8_gb300.binding import LinearLayerC
+    hb = lib.sq_linear_block_host_scratch_bytes
+    hb.argtypes = [i64, i64, i64, ctypes.POINTER(ctypes.c_size_t)]
+    nb = ctypes.c_size_t(0)
+    assert hb(8, 32, 16, None) == INVALID
+    assert hb(8, 0, 16, ctypes.byref(nb)) == INVALID
+    assert hb(8, 32, 16, ctypes.byref(nb)) == 0
+    assert nb.value == 2 * 1024 + 2 * 512 + 512 + 256   # 256-byte parts: x, y slots, operand, scales
+    hp = lib.sq_linear_block_host
+    hp.argtypes = [ctypes.POINTER(LinearLayerC), i64, i64, vp, vp, vp, ctypes.c_size_t, vp, vp, vp]
+    lay = LinearLayerC(32, 16, 1, 0.0, 0x10000, None, 0x10000, 0x10000, None, 0x10000, None)
+    arr = (LinearLayerC * 1)(lay)
+    hx = (ctypes.c_void_p * 1)(0x20000)
+    hy = (ctypes.c_void_p * 1)(0x30000)
+    big = 1 << 20
+    assert hp(arr, 1, 8, hx, hy, None, big, None, None, None) == INVALID            # no scratch
+    assert hp(arr, 1, 8, hx, hy, _fake(0x10010), big, None, None, None) == ALIGN   # scratch
+    assert hp(arr, 1, 8, hx, hy, a, 100, None, None, None) == INVALID             # too small
+    assert hp(None, 1, 8, hx, hy, a, big, None, None, None) == INVALID
+    assert hp(arr, 1, 8, None, hy, a, big, None, None, None) == INVALID
+    assert hp(arr, -1, 8, hx, hy, a, big, None, None, None) == INVALID
+    assert hp(None, 0, 8, None, None, None, 0, None, None, None) == 0             # empty
+    bad = [LinearLayerC(40, 16, 1, 0.0, 0x10000, None, 0x10000, 0x10000, None, 0x10000, None),
+           LinearLayerC(32, 16, 7, 0.0, 0x10000, None, 0x10000, 0x10000, None, 0x10000, None),
+           LinearLayerC(32, 16, 1, 0.0, None, None, 0x10000, 0x10000, None, 0x10000, None),
+           LinearLayerC(32, 16, 1, 0.0, 0x10004, None, 0x10000, 0x10000, None, 0x10000, None),
+           LinearLayerC(32, 16, 1, -1.0, 0x10000, None, 0x10000, 0x10000, None, 0x10000, None),
+           LinearLayerC(32, 16, 1, 0.0, 0x10000, None, 0x10000, 0x10000, None, None, None)]
+    want = [ALIGN, INVALID, INVALID, ALIGN, INVALID, INVALID]   # K % 16, mode, s, s, scale, bias
+    for L, w in zip(bad, want):
+        assert hp((LinearLayerC * 1)(L), 1, 8, hx, hy, a, big, None, None, None) == w, (L.K, w)
     at = lib.sq_attention
     at.argtypes = [vp, i64, i64, i64, i64, ctypes.c_float, vp, vp]
     assert at(a, 2, 128, 4, 64, 0.125, None, None) == INVALID

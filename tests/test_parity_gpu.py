@@ -522,8 +522,10 @@ def test_large_workloads_sampled(sq, path, name, index):
 
 
 def test_host_pipeline_matches_direct_calls(sq):
-    """The host-streaming pipeline (copies overlapped with kernels on three
-    streams) returns exactly what the direct device calls return."""
+    """The host-buffer pipeline (sq_linear_block_host: copies overlapped with
+    kernels on three streams) returns exactly what the direct device calls
+    return, for Smooth-Dynamic (with and without s's division table) and
+    Smooth-Static layers."""
     from smoothquant_w8a8_int8_gb300.pipeline import HostLinearPipeline, LinearLayer
     M = 300
     shapes = [(256, 384, wl.EPI_BIAS), (384, 256, wl.EPI_BIAS_GELU), (256, 256, wl.EPI_BIAS_RESIDUAL),
@@ -536,10 +538,15 @@ def test_host_pipeline_matches_direct_calls(sq):
         _, sw, Wop, wl1 = sq.pack_weight(W, s, want_q=False, want_l1=True)
         b = c.bias.cuda() if c.bias is not None else None
         r = c.residual.cuda() if c.residual is not None else None
-        _, sx, Xop = sq.quantize_act(X, s, want_q=False)
+        # layer 2 Smooth-Static (a quarter of its calibrated scale: some codes
+        # saturate), odd layers with s's division table (sq_quantize_act_table)
+        static = float(sq.static_scale(sq.act_absmax(X, s))) * 0.25 if i == 2 else None
+        if static is None:
+            _, sx, Xop = sq.quantize_act(X, s, want_q=False)
+        else:
+            _, sx, Xop = sq.quantize_act_static(X, s, static, want_q=False)
         ref.append(sq.linear_i8(Xop, sx, Wop, sw, b, r, mode, w_l1=wl1).cpu())
-        # odd layers carry s's division table (sq_quantize_act_table)
-        layers.append(LinearLayer(s, Wop, sw, mode, b, r, wl1,
+        layers.append(LinearLayer(s, Wop, sw, mode, b, r, wl1, static_scale=static,
                                   s_table=sq.division_table(s) if i % 2 else None))
         xh.append(c.X.pin_memory())
         yh.append(torch.empty(M, N, dtype=torch.float32).pin_memory())
