@@ -283,8 +283,9 @@ sq_status sq_quantize_act_rowmax(const float *X, const float *s, const float *ro
                                  int64_t M, int64_t K, int8_t *Xq, float *x_scale, void *Xop,
                                  int32_t *x_row_l1, void *stream);
 
-/* sq_quantize_act (row_amax NULL) or sq_quantize_act_rowmax (row_amax given)
- * with s's division table beside s: s_table = sq_division_table(s), computed
+/* Table 10's Smooth-Dynamic run-time step again: sq_quantize_act (row_amax
+ * NULL) or sq_quantize_act_rowmax (row_amax given) with s's division table
+ * beside s: s_table = sq_division_table(s), computed
  * offline with the packed weights.  Outputs bit for bit those of the call
  * without the table; where the rows are held in registers the kernel reads -s
  * and RN(1/s) from the table instead of forming the reciprocals in every
@@ -445,7 +446,9 @@ typedef struct {
 sq_status sq_linear_block_host_scratch_bytes(int64_t M, int64_t max_K, int64_t max_N,
                                              size_t *bytes);
 
-/* Y_host[i] = the linear block of layers[i] on X_host[i] for every i < count
+/* The INT8 linear block (Table 3's "Linear-Block": quantise, GEMM, fused
+ * post-operations) on activations in host memory:
+ * Y_host[i] = the linear block of layers[i] on X_host[i] for every i < count
  * (fp32 [M][K_i] in, fp32 [M][N_i] out, host memory; pinned memory makes the
  * copies asynchronous and lets them overlap): per layer the input is copied to
  * the device on stream_h2d, quantised and multiplied (the layer's quantiser,
