@@ -446,7 +446,7 @@ typedef struct {
 sq_status sq_linear_block_host_scratch_bytes(int64_t M, int64_t max_K, int64_t max_N,
                                              size_t *bytes);
 
-/* The INT8 linear block (Table 3's "Linear-Block": quantise, GEMM, fused
+/* The INT8 linear block (Table 3's linear-block share: quantise, GEMM, fused
  * post-operations) on activations in host memory:
  * Y_host[i] = the linear block of layers[i] on X_host[i] for every i < count
  * (fp32 [M][K_i] in, fp32 [M][N_i] out, host memory; pinned memory makes the
