@@ -558,6 +558,23 @@ def test_host_pipeline_matches_direct_calls(sq):
         torch.cuda.synchronize()
         for y, r in zip(yh, ref):
             assert torch.equal(y, r)
+    # the three streams may be one: the same outputs, in order
+    cur = torch.cuda.current_stream()
+    table = []
+    for L, x, y in zip(layers, xh, yh):
+        y.zero_()
+        table.append(sq.LinearLayerC(
+            x.shape[1], y.shape[1], int(L.mode),
+            0.0 if L.static_scale is None else float(L.static_scale), L.s.data_ptr(),
+            None if L.s_table is None or L.static_scale is not None else L.s_table.data_ptr(),
+            L.Wop.data_ptr(), L.w_scale.data_ptr(), L.w_l1.data_ptr(),
+            None if L.bias is None else L.bias.data_ptr(),
+            None if L.residual is None else L.residual.data_ptr()))
+    sq.linear_block_host(table, M, xh, yh, pipe.scratch, (cur, cur, cur))
+    torch.cuda.synchronize()
+    for y, r in zip(yh, ref):
+        assert torch.equal(y, r)
+    assert sq.device_status() == sq.SQ_OK
 
 
 # ------------------------------------------------------------- Smooth-Static
